@@ -1,0 +1,157 @@
+"""MiTA forward oracle -- test infrastructure only.
+
+A slow, single-threaded fp64 CPU restatement of the Mixture-of-Top-k
+Attention forward operator (36Kr / 新智元 "注意力也是FFN？", section
+"用少量地标查询，同时构造全局概括与细节专家"; English version "Is Attention Also
+FFN?", section "Construct global generalization and detail experts ...").
+The arithmetic lives in ``mita_oracle.c``; this module compiles it with gcc
+and marshals numpy arrays to it.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library neither imports nor
+links it, and it shares no code with the CUDA library.
+
+Parity status per function: every function is pinned by a ``-m "not gpu"``
+test in ``tests/test_oracle_pins.py`` against something other than itself
+(library routines, brute force, closed forms, invariants).
+"""
+from __future__ import annotations
+
+import contextlib
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mita_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+IO_F64, IO_F32, IO_BF16 = 0, 1, 2
+_IO_NAMES = {"f64": IO_F64, "f32": IO_F32, "bf16": IO_BF16}
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``mita_oracle.c`` into ``liboracle.so`` next to it (IEEE fp64,
+    no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+                               "-ffp-contract=off", "-o", _LIB, _SRC, "-lm"])
+    return _LIB
+
+
+def _open(path):
+    lib = ctypes.CDLL(path)
+    dp = ctypes.POINTER(ctypes.c_double)
+    ip = ctypes.POINTER(ctypes.c_int32)
+    i = ctypes.c_int
+    lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+    lib.oracle_round_bf16.restype = ctypes.c_double
+    lib.oracle_bin.argtypes = [i, i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
+    lib.oracle_head.argtypes = [i, i, i, i, i, i, i, i, i, dp, dp, dp, i, ip,
+                                dp, ip, ip, dp, dp, dp, dp, dp]
+    lib.oracle_head.restype = i
+    lib.oracle_forward.argtypes = [i, i, i, i, i, i, i, i, i, i, dp, dp, dp, dp, ip, ip]
+    lib.oracle_forward.restype = i
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = _open(build())
+    return _lib
+
+
+@contextlib.contextmanager
+def swapped_library(path):
+    """Run the wrapper against another build of the oracle source (used by
+    the tests that plant mistakes in a copy of it)."""
+    global _lib
+    saved = _lib
+    _lib = _open(path)
+    try:
+        yield
+    finally:
+        _lib = saved
+
+
+def _dp(a):
+    return None if a is None else a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _ip(a):
+    return None if a is None else a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def round_bf16(x: float) -> float:
+    """Nearest bfloat16 value of ``x`` (ties to even)."""
+    return _load().oracle_round_bf16(float(x))
+
+
+def pool_bin(i: int, G: int, P: int) -> tuple[int, int]:
+    """Adaptive-average-pooling bin [lo, hi) of output cell ``i`` (G -> P)."""
+    lo, hi = ctypes.c_int(), ctypes.c_int()
+    _load().oracle_bin(i, G, P, ctypes.byref(lo), ctypes.byref(hi))
+    return lo.value, hi.value
+
+
+def _f64(x) -> np.ndarray:
+    if hasattr(x, "detach"):  # torch tensor: exact upcast of bf16 / fp32 values
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def head(Q, K, V, grid, m: int, k: int, io: str = "f64", queries=None, debug: bool = False):
+    """Run the oracle on one head.
+
+    Q, K, V: [N, d] arrays (values are taken exactly; bf16/fp32 torch tensors
+    are upcast exactly).  grid = (gh, gw, ph, pw).  ``io`` is the type that
+    Q_l, V_l and out are rounded to.  ``queries``: optional list of query
+    indices (default all).  Returns a dict with out [nq,d], idx [m,k],
+    route [nq] and, with ``debug``, Ql, Vl, R [m,N] (raw scores),
+    A [nq,m] (raw query-landmark scores) and W [nq, m+k] (attention weights).
+    """
+    lib = _load()
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    N, d = Q.shape
+    gh, gw, ph, pw = grid
+    qlist = None if queries is None else np.ascontiguousarray(queries, dtype=np.int32)
+    nq = N if qlist is None else len(qlist)
+    out = np.zeros((nq, d))
+    idx = np.zeros((m, k), dtype=np.int32)
+    route = np.zeros(nq, dtype=np.int32)
+    Ql = np.zeros((m, d)) if debug else None
+    Vl = np.zeros((m, d)) if debug else None
+    R = np.zeros((m, N)) if debug else None
+    A = np.zeros((nq, m)) if debug else None
+    W = np.zeros((nq, m + k)) if debug else None
+    rc = lib.oracle_head(N, d, gh, gw, ph, pw, m, k, _IO_NAMES[io], _dp(Q), _dp(K), _dp(V),
+                         nq, _ip(qlist), _dp(out), _ip(idx), _ip(route),
+                         _dp(Ql), _dp(Vl), _dp(R), _dp(A), _dp(W))
+    if rc != 0:
+        raise ValueError("oracle: invalid sizes")
+    res = {"out": out, "idx": idx, "route": route}
+    if debug:
+        res.update(Ql=Ql, Vl=Vl, R=R, A=A, W=W)
+    return res
+
+
+def forward(Q, K, V, grid, m: int, k: int, io: str = "f64"):
+    """Run the oracle on a [B, H, N, d] batch; returns out [B,H,N,d] (fp64,
+    holding values of the I/O type), idx [B,H,m,k] and route [B,H,N]."""
+    lib = _load()
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, H, N, d = Q.shape
+    gh, gw, ph, pw = grid
+    out = np.zeros((B, H, N, d))
+    idx = np.zeros((B, H, m, k), dtype=np.int32)
+    route = np.zeros((B, H, N), dtype=np.int32)
+    rc = lib.oracle_forward(B * H, N, d, gh, gw, ph, pw, m, k, _IO_NAMES[io],
+                            _dp(Q), _dp(K), _dp(V), _dp(out), _ip(idx), _ip(route))
+    if rc != 0:
+        raise ValueError("oracle: invalid sizes")
+    return {"out": out, "idx": idx, "route": route}

@@ -1,0 +1,260 @@
+/*
+ * MiTA forward oracle -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, single-threaded fp64 restatement of the Mixture-of-Top-k
+ * Attention forward operator, written from the method description in
+ * "NeurIPS'26：注意力也是FFN？从快权重出发，重新理解高效注意力" (36Kr / 新智元,
+ * section "用少量地标查询，同时构造全局概括与细节专家") and its English version
+ * "Is Attention Also FFN? ..." (section "Construct global generalization and
+ * detail experts at the same time with a small number of landmark queries").
+ *
+ * Only tests, the smoke check and the CPU-baseline leg of the benchmark may
+ * load this code.  The CUDA library never links, includes or calls it, and
+ * this file includes nothing from the CUDA library.
+ *
+ * Every step is the plain definition, one head at a time, no blocking and no
+ * fusion.  Accumulation is fp64.  The only rounding is the explicit rounding
+ * of the landmark queries, the landmark values and the output to the I/O type
+ * (the reading of the text for a bf16 pipeline, see round_io()).
+ *
+ * Steps (per head; Q, K, V are [N, d] row-major):
+ *   1. pool      Q_l[i] = mean of Q over adaptive-average-pooling bin i
+ *   2. scores    R[i, j] = Q_l[i] . K[j]            (raw, unscaled)
+ *   3. top-k     E_i = k largest R[i, .], ties to the lower key index,
+ *                stored in ascending key order
+ *   4. values    V_l[i] = sum_j softmax_j(R[i, .] / sqrt(d)) V[j]
+ *   5. route     A[q, i] = q . Q_l[i]; r(q) = first argmax_i A[q, i]
+ *   6. attend    out_q = softmax over the m shared logits A[q, .]/sqrt(d)
+ *                and the k routed logits q . K[j]/sqrt(d), j in E_r(q),
+ *                applied to [V_l ; V[E_r(q)]]
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* I/O types: the values the caller's tensors hold and the type the three
+ * rounded intermediates/outputs are rounded to. */
+enum { ORACLE_IO_F64 = 0, ORACLE_IO_F32 = 1, ORACLE_IO_BF16 = 2 };
+
+/* Round x to the nearest bfloat16 value, ties to even (8 significant bits).
+ * Written from the definition: scale x so that it has 8 integer bits, round
+ * to the nearest integer with ties to even, scale back.  Results below the
+ * bf16 normal range or above its largest finite value do not occur for the
+ * inputs this operator is checked on and are not treated specially. */
+double oracle_round_bf16(double x) {
+    if (x == 0.0 || !isfinite(x)) return x;
+    int e;
+    frexp(x, &e);                       /* |x| = f * 2^e, f in [0.5, 1) */
+    double y = ldexp(x, 8 - e);         /* |y| in [128, 256)            */
+    double r = nearbyint(y);            /* default mode: nearest, even  */
+    return ldexp(r, e - 8);
+}
+
+/* Round to the I/O type.  fp32: the C conversion rounds to nearest even. */
+static double round_io(double x, int io) {
+    if (io == ORACLE_IO_F32) return (double)(float)x;
+    if (io == ORACLE_IO_BF16) return oracle_round_bf16(x);
+    return x;
+}
+
+/* Adaptive average pooling bin of output cell i when G input cells are
+ * pooled to P output cells: [floor(i*G/P), ceil((i+1)*G/P)). */
+void oracle_bin(int i, int G, int P, int* lo, int* hi) {
+    *lo = (i * G) / P;
+    *hi = ((i + 1) * G + P - 1) / P;
+}
+
+/* Step 1: landmark queries by local average pooling of Q over the gh x gw
+ * token grid (token t = row * gw + col) into ph x pw landmarks (landmark
+ * i = r * pw + c).  Q_l is rounded to the I/O type. */
+void oracle_pool(int gh, int gw, int ph, int pw, int d, int io,
+                 const double* Q, double* Ql) {
+    for (int r = 0; r < ph; ++r) {
+        int r0, r1;
+        oracle_bin(r, gh, ph, &r0, &r1);
+        for (int c = 0; c < pw; ++c) {
+            int c0, c1;
+            oracle_bin(c, gw, pw, &c0, &c1);
+            double count = (double)((r1 - r0) * (c1 - c0));
+            double* dst = Ql + (size_t)(r * pw + c) * d;
+            for (int f = 0; f < d; ++f) {
+                double s = 0.0;
+                for (int y = r0; y < r1; ++y)
+                    for (int x = c0; x < c1; ++x)
+                        s += Q[(size_t)(y * gw + x) * d + f];
+                double mean = s / count;
+                /* A quotient that lands exactly on a bf16 rounding midpoint
+                 * is only a midpoint if s == count * mean exactly; otherwise
+                 * nudge it to the side the exact quotient lies on, so that
+                 * the bf16 result is the rounding of s / count itself. */
+                if (io == ORACLE_IO_BF16 && oracle_round_bf16(mean) != mean) {
+                    double lo_b = oracle_round_bf16(nextafter(mean, -INFINITY));
+                    double hi_b = oracle_round_bf16(nextafter(mean, INFINITY));
+                    if (lo_b != hi_b && fma(count, mean, -s) != 0.0)
+                        mean = (fma(count, mean, -s) > 0.0) ? nextafter(mean, -INFINITY)
+                                                           : nextafter(mean, INFINITY);
+                }
+                dst[f] = round_io(mean, io);
+            }
+        }
+    }
+}
+
+/* Step 2: raw landmark scores R[i, j] = Q_l[i] . K[j]  ([m, N]). */
+void oracle_scores(int N, int d, int m, const double* Ql, const double* K, double* R) {
+    for (int i = 0; i < m; ++i)
+        for (int j = 0; j < N; ++j) {
+            double s = 0.0;
+            for (int f = 0; f < d; ++f) s += Ql[(size_t)i * d + f] * K[(size_t)j * d + f];
+            R[(size_t)i * N + j] = s;
+        }
+}
+
+/* Order used by the top-k: higher score first, then lower index first.
+ * -0.0 and +0.0 compare equal in C, so they tie and the index decides. */
+static const double* g_sort_row;
+static int cmp_desc_then_index(const void* a, const void* b) {
+    int ia = *(const int32_t*)a, ib = *(const int32_t*)b;
+    double sa = g_sort_row[ia], sb = g_sort_row[ib];
+    if (sa > sb) return -1;
+    if (sa < sb) return 1;
+    return (ia > ib) - (ia < ib);
+}
+static int cmp_int(const void* a, const void* b) {
+    int32_t x = *(const int32_t*)a, y = *(const int32_t*)b;
+    return (x > y) - (x < y);
+}
+
+/* Step 3: routed expert i = the k key positions with the largest R[i, .],
+ * ties to the lower index, stored ascending.  idx is [m, k]. */
+void oracle_topk(int N, int m, int k, const double* R, int32_t* idx) {
+    int32_t* order = (int32_t*)malloc(sizeof(int32_t) * (size_t)N);
+    for (int i = 0; i < m; ++i) {
+        for (int j = 0; j < N; ++j) order[j] = j;
+        g_sort_row = R + (size_t)i * N;
+        qsort(order, (size_t)N, sizeof(int32_t), cmp_desc_then_index);
+        qsort(order, (size_t)k, sizeof(int32_t), cmp_int);
+        memcpy(idx + (size_t)i * k, order, sizeof(int32_t) * (size_t)k);
+    }
+    free(order);
+}
+
+/* Step 4: landmark values by cross-attention of the landmark queries over
+ * the whole sequence: V_l[i] = sum_j softmax_j(R[i, .] / sqrt(d)) V[j],
+ * rounded to the I/O type.  Together with Q_l as keys, these are the shared
+ * expert's key-value pairs. */
+void oracle_landmark_values(int N, int d, int m, int io, const double* R, const double* V,
+                            double* Vl) {
+    double scale = 1.0 / sqrt((double)d);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)d);
+    for (int i = 0; i < m; ++i) {
+        const double* row = R + (size_t)i * N;
+        double mx = -INFINITY;
+        for (int j = 0; j < N; ++j) if (row[j] * scale > mx) mx = row[j] * scale;
+        double den = 0.0;
+        for (int f = 0; f < d; ++f) acc[f] = 0.0;
+        for (int j = 0; j < N; ++j) {
+            double w = exp(row[j] * scale - mx);
+            den += w;
+            for (int f = 0; f < d; ++f) acc[f] += w * V[(size_t)j * d + f];
+        }
+        for (int f = 0; f < d; ++f) Vl[(size_t)i * d + f] = round_io(acc[f] / den, io);
+    }
+    free(acc);
+}
+
+/* Step 5 (one query): raw query-landmark scores A[i] = q . Q_l[i] and the
+ * route r(q) = the first i with the largest A[i] (s = 1). */
+int oracle_route_one(int d, int m, const double* q, const double* Ql, double* A) {
+    int best = 0;
+    for (int i = 0; i < m; ++i) {
+        double s = 0.0;
+        for (int f = 0; f < d; ++f) s += q[f] * Ql[(size_t)i * d + f];
+        A[i] = s;
+        if (s > A[best]) best = i;
+    }
+    return best;
+}
+
+/* Step 6 (one query): one softmax over the concatenation of the m shared
+ * logits (q . Q_l[i] / sqrt(d)) and the k routed logits (q . K[j] / sqrt(d),
+ * j in E_r), applied to [V_l ; V[E_r]].  W (if not NULL) receives the m + k
+ * weights in that order; out is rounded to the I/O type. */
+void oracle_attend_one(int d, int m, int k, int io, const double* q, const double* A,
+                       const int32_t* E, const double* K, const double* V,
+                       const double* Vl, double* out, double* W) {
+    double scale = 1.0 / sqrt((double)d);
+    int L = m + k;
+    double* logit = (double*)malloc(sizeof(double) * (size_t)L);
+    for (int i = 0; i < m; ++i) logit[i] = A[i] * scale;
+    for (int t = 0; t < k; ++t) {
+        const double* key = K + (size_t)E[t] * d;
+        double s = 0.0;
+        for (int f = 0; f < d; ++f) s += q[f] * key[f];
+        logit[m + t] = s * scale;
+    }
+    double mx = -INFINITY;
+    for (int l = 0; l < L; ++l) if (logit[l] > mx) mx = logit[l];
+    double den = 0.0;
+    for (int l = 0; l < L; ++l) { logit[l] = exp(logit[l] - mx); den += logit[l]; }
+    for (int f = 0; f < d; ++f) {
+        double s = 0.0;
+        for (int i = 0; i < m; ++i) s += logit[i] * Vl[(size_t)i * d + f];
+        for (int t = 0; t < k; ++t) s += logit[m + t] * V[(size_t)E[t] * d + f];
+        out[f] = round_io(s / den, io);
+    }
+    if (W) for (int l = 0; l < L; ++l) W[l] = logit[l] / den;
+    free(logit);
+}
+
+/* The whole operator for one head.  qlist (nq entries, NULL = all N queries
+ * in order) selects the queries whose route and output are produced; the
+ * landmarks, experts and landmark values always cover the whole head.
+ * Optional outputs (NULL to skip): Ql [m,d], Vl [m,d], R [m,N], A [nq,m],
+ * W [nq, m+k].  Returns 0, or -1 on invalid sizes. */
+int oracle_head(int N, int d, int gh, int gw, int ph, int pw, int m, int k, int io,
+                const double* Q, const double* K, const double* V,
+                int nq, const int32_t* qlist,
+                double* out, int32_t* idx, int32_t* route,
+                double* Ql_out, double* Vl_out, double* R_out, double* A_out, double* W_out) {
+    if (N < 1 || d < 1 || gh * gw != N || ph * pw != m || ph > gh || pw > gw || k < 1 || k > N)
+        return -1;
+    double* Ql = Ql_out ? Ql_out : (double*)malloc(sizeof(double) * (size_t)m * d);
+    double* Vl = Vl_out ? Vl_out : (double*)malloc(sizeof(double) * (size_t)m * d);
+    double* R = R_out ? R_out : (double*)malloc(sizeof(double) * (size_t)m * N);
+    double* A = (double*)malloc(sizeof(double) * (size_t)m);
+
+    oracle_pool(gh, gw, ph, pw, d, io, Q, Ql);
+    oracle_scores(N, d, m, Ql, K, R);
+    oracle_topk(N, m, k, R, idx);
+    oracle_landmark_values(N, d, m, io, R, V, Vl);
+    for (int n = 0; n < nq; ++n) {
+        int qi = qlist ? qlist[n] : n;
+        const double* q = Q + (size_t)qi * d;
+        int r = oracle_route_one(d, m, q, Ql, A);
+        route[n] = r;
+        if (A_out) memcpy(A_out + (size_t)n * m, A, sizeof(double) * (size_t)m);
+        oracle_attend_one(d, m, k, io, q, A, idx + (size_t)r * k, K, V, Vl,
+                          out + (size_t)n * d, W_out ? W_out + (size_t)n * (m + k) : NULL);
+    }
+    free(A);
+    if (!Ql_out) free(Ql);
+    if (!Vl_out) free(Vl);
+    if (!R_out) free(R);
+    return 0;
+}
+
+/* All heads of a [B*H, N, d] batch, every query. */
+int oracle_forward(int BH, int N, int d, int gh, int gw, int ph, int pw, int m, int k, int io,
+                   const double* Q, const double* K, const double* V,
+                   double* out, int32_t* idx, int32_t* route) {
+    for (int h = 0; h < BH; ++h) {
+        size_t o = (size_t)h * N * d;
+        int rc = oracle_head(N, d, gh, gw, ph, pw, m, k, io, Q + o, K + o, V + o, N, NULL,
+                             out + o, idx + (size_t)h * m * k, route + (size_t)h * N,
+                             NULL, NULL, NULL, NULL, NULL);
+        if (rc) return rc;
+    }
+    return 0;
+}

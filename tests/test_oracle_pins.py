@@ -1,0 +1,283 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each test checks one oracle function against a library routine, brute force,
+a closed form, an invariant or a value printed in the method description
+(36Kr / 新智元 "注意力也是FFN？" and its English version).  Planted-mistake
+tests at the end show that a plausible slip in the oracle fails a pin.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from mixture_top_attention_mita_b300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand(shape, seed, scale=1.0):
+    g = torch.Generator("cpu").manual_seed(seed)
+    return (scale * torch.randn(*shape, generator=g, dtype=torch.float64)).numpy()
+
+
+# ---------------------------------------------------------------- rounding
+def test_round_bf16_matches_torch_on_fp32_values():
+    # torch rounds fp32 -> bf16 to nearest, ties to even; on fp32-representable
+    # inputs (single rounding) the oracle must agree bit for bit.
+    g = torch.Generator("cpu").manual_seed(3)
+    x = torch.randn(20000, generator=g) * torch.exp2(torch.randint(-20, 20, (20000,), generator=g).float())
+    # include exact midpoints between bf16 neighbours
+    mids = (torch.randn(2000, generator=g).to(torch.bfloat16).float().view(torch.int32) + (1 << 15)).view(torch.float32)
+    x = torch.cat([x, mids])
+    ref = x.to(torch.bfloat16).double().numpy()
+    got = np.array([oracle.round_bf16(float(v)) for v in x.double().numpy()])
+    assert np.array_equal(ref, got)
+
+
+def test_round_bf16_hand_cases():
+    assert oracle.round_bf16(1 + 2 ** -8) == 1.0                 # tie -> even (down)
+    assert oracle.round_bf16(1 + 3 * 2 ** -8) == 1 + 2 ** -6     # tie -> even (up)
+    assert oracle.round_bf16(-(1 + 2 ** -8)) == -1.0
+    assert oracle.round_bf16(1 + 2 ** -8 + 2 ** -30) == 1 + 2 ** -7  # above the midpoint
+    assert oracle.round_bf16(0.0) == 0.0
+
+
+# ---------------------------------------------------------------- pooling
+@pytest.mark.parametrize("gh,gw,ph,pw", [(14, 14, 5, 5), (56, 56, 7, 7), (1, 512, 1, 8),
+                                         (7, 9, 3, 4), (5, 5, 5, 5), (6, 6, 1, 1)])
+def test_pool_matches_adaptive_avg_pool2d(gh, gw, ph, pw):
+    N, d, m = gh * gw, 8, ph * pw
+    Q = _rand((N, d), 11)
+    r = oracle.head(Q, Q, Q, (gh, gw, ph, pw), m, 1, io="f64", debug=True)
+    ref = F.adaptive_avg_pool2d(torch.from_numpy(Q).T.reshape(1, d, gh, gw), (ph, pw))
+    ref = ref.reshape(d, m).T.numpy()
+    np.testing.assert_allclose(r["Ql"], ref, rtol=0, atol=1e-13)
+
+
+def test_pool_bins_14_to_5_overlap():
+    # The 14 -> 5 adaptive bins overlap; their union covers every row once or twice.
+    bins = [oracle.pool_bin(i, 14, 5) for i in range(5)]
+    cover = np.zeros(14, int)
+    for lo, hi in bins:
+        cover[lo:hi] += 1
+    assert cover.min() == 1 and cover.max() == 2
+    assert bins[0][0] == 0 and bins[-1][1] == 14
+
+
+def test_pool_bf16_rounds_the_exact_mean():
+    # Q_l in the bf16 pipeline is the bf16 rounding of the exact fp64 mean.
+    Q = torch.randn(196, 16, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    f = oracle.head(Q, Q, Q, (14, 14, 5, 5), 25, 3, io="f64", debug=True)["Ql"]
+    b = oracle.head(Q, Q, Q, (14, 14, 5, 5), 25, 3, io="bf16", debug=True)["Ql"]
+    np.testing.assert_array_equal(b, np.vectorize(oracle.round_bf16)(f))
+
+
+# ---------------------------------------------------------------- top-k
+def _brute_topk(R, k):
+    # j is selected iff fewer than k keys beat it, where l beats j when
+    # R[l] > R[j], or R[l] == R[j] and l < j.
+    m, N = R.shape
+    out = []
+    for i in range(m):
+        sel = []
+        for j in range(N):
+            beat = sum(1 for l in range(N) if R[i, l] > R[i, j] or (R[i, l] == R[i, j] and l < j))
+            if beat < k:
+                sel.append(j)
+        out.append(sel)
+    return np.array(out, dtype=np.int32)
+
+
+@pytest.mark.parametrize("k", [1, 5, 17, 36])
+def test_topk_brute_force_with_ties(k):
+    g = torch.Generator().manual_seed(k)
+    Q = torch.randint(-2, 3, (36, 4), generator=g).double().numpy()
+    K = torch.randint(-1, 2, (36, 4), generator=g).double().numpy()   # many exact ties
+    r = oracle.head(Q, K, K, (6, 6, 2, 3), 6, k, io="f64", debug=True)
+    np.testing.assert_array_equal(r["idx"], _brute_topk(r["R"], k))
+
+
+def test_scores_match_matmul():
+    Q, K = _rand((49, 8), 1), _rand((49, 8), 2)
+    r = oracle.head(Q, K, K, (7, 7, 2, 2), 4, 5, io="f64", debug=True)
+    np.testing.assert_allclose(r["R"], r["Ql"] @ K.T, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r["A"], Q @ r["Ql"].T, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- route
+def test_route_is_first_argmax():
+    g = torch.Generator().manual_seed(9)
+    Q = torch.randint(-1, 2, (64, 4), generator=g).double().numpy()
+    r = oracle.head(Q, Q, Q, (8, 8, 4, 4), 16, 3, io="f64", debug=True)
+    A = Q @ r["Ql"].T
+    for q in range(64):
+        best = np.flatnonzero(A[q] == A[q].max())
+        assert r["route"][q] == best[0]
+    assert (np.sum(A == A.max(1, keepdims=True), 1) > 1).any()  # ties were exercised
+
+
+# ---------------------------------------------------------------- values and output
+def test_landmark_values_match_sdpa():
+    Q, K, V = _rand((196, 16), 1), _rand((196, 16), 2), _rand((196, 16), 3)
+    r = oracle.head(Q, K, V, (14, 14, 5, 5), 25, 25, io="f64", debug=True)
+    t = torch.from_numpy
+    ref = F.scaled_dot_product_attention(t(r["Ql"])[None], t(K)[None], t(V)[None])[0].numpy()
+    np.testing.assert_allclose(r["Vl"], ref, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("grid,m,k,d", [((14, 14, 5, 5), 25, 25, 16), ((8, 8, 2, 4), 8, 9, 8),
+                                        ((1, 96, 1, 6), 6, 40, 12)])
+def test_output_matches_masked_sdpa(grid, m, k, d):
+    N = grid[0] * grid[1]
+    Q, K, V = _rand((N, d), 4), _rand((N, d), 5), _rand((N, d), 6)
+    r = oracle.head(Q, K, V, grid, m, k, io="f64", debug=True)
+    keys = np.concatenate([r["Ql"], K])
+    vals = np.concatenate([r["Vl"], V])
+    mask = np.zeros((N, m + N), bool)
+    mask[:, :m] = True
+    for q in range(N):
+        mask[q, m + r["idx"][r["route"][q]]] = True
+    t = torch.from_numpy
+    ref = F.scaled_dot_product_attention(t(Q)[None], t(keys)[None], t(vals)[None],
+                                         attn_mask=t(mask)[None])[0].numpy()
+    np.testing.assert_allclose(r["out"], ref, rtol=0, atol=1e-12)
+
+
+def test_full_attention_special_case():
+    # k = N and m = 1: one landmark (the mean query) and every key routed, so
+    # the operator is textbook attention over N + 1 keys [Q_l ; K].
+    N, d = 48, 8
+    Q, K, V = _rand((N, d), 7), _rand((N, d), 8), _rand((N, d), 9)
+    r = oracle.head(Q, K, V, (6, 8, 1, 1), 1, N, io="f64", debug=True)
+    np.testing.assert_allclose(r["Ql"][0], Q.mean(0), rtol=0, atol=1e-14)
+    assert (r["route"] == 0).all() and (r["idx"][0] == np.arange(N)).all()
+    t = torch.from_numpy
+    vl = F.scaled_dot_product_attention(t(Q.mean(0, keepdims=True))[None], t(K)[None], t(V)[None])[0]
+    ref = F.scaled_dot_product_attention(t(Q)[None], torch.cat([t(Q.mean(0, keepdims=True)), t(K)])[None],
+                                         torch.cat([vl, t(V)])[None])[0].numpy()
+    np.testing.assert_allclose(r["out"], ref, rtol=0, atol=1e-12)
+
+
+def _golden_keys_per_query():
+    rows = []
+    with open(os.path.join(GOLDEN, "keys_per_query.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                m, k, total, _ = line.split()
+                rows.append((int(m), int(k), int(total)))
+    return rows
+
+
+@pytest.mark.parametrize("m,k,total", _golden_keys_per_query())
+def test_keys_per_query_printed_value(m, k, total):
+    # m shared + k routed entries per query (25+25=50, 49+49=98 as printed).
+    side = int(math.isqrt(m))
+    grid = (side * 4, side * 4, side, side)
+    N = grid[0] * grid[1]
+    Q, K, V = _rand((N, 8), 1), _rand((N, 8), 2), _rand((N, 8), 3)
+    r = oracle.head(Q, K, V, grid, m, k, io="f64", debug=True)
+    W = r["W"]
+    assert W.shape[1] == total
+    assert (W > 0).sum(1).min() == total        # every entry takes part
+    np.testing.assert_allclose(W.sum(1), 1.0, rtol=0, atol=1e-12)
+
+
+def test_weights_sum_to_one_and_shift_invariance():
+    Q, K, V = _rand((196, 8), 1), _rand((196, 8), 2), _rand((196, 8), 3)
+    g = (14, 14, 5, 5)
+    r0 = oracle.head(Q, K, V, g, 25, 25, io="f64", debug=True)
+    np.testing.assert_allclose(r0["W"].sum(1), 1.0, rtol=0, atol=1e-12)
+    c = np.linspace(-3, 3, 8)
+    r1 = oracle.head(Q, K, V + c, g, 25, 25, io="f64")
+    np.testing.assert_allclose(r1["out"], r0["out"] + c, rtol=0, atol=1e-12)
+
+
+def test_feature_permutation_equivariance():
+    Q, K, V = _rand((196, 8), 1), _rand((196, 8), 2), _rand((196, 8), 3)
+    p = np.random.default_rng(0).permutation(8)
+    g = (14, 14, 5, 5)
+    r0 = oracle.head(Q, K, V, g, 25, 25, io="f64")
+    r1 = oracle.head(Q[:, p], K[:, p], V[:, p], g, 25, 25, io="f64")
+    np.testing.assert_array_equal(r0["idx"], r1["idx"])
+    np.testing.assert_array_equal(r0["route"], r1["route"])
+    np.testing.assert_allclose(r1["out"], r0["out"][:, p], rtol=0, atol=1e-12)
+
+
+def test_experts_distinct_sorted_and_overlapping():
+    w = synth.WORKLOADS["deit_s"].scaled(B=1, H=1)
+    Q, K, V = synth.make_inputs(w)
+    r = oracle.head(Q[0, 0], K[0, 0], V[0, 0], w.grid, w.m, w.k, io="bf16")
+    idx = r["idx"]
+    assert (np.diff(idx, axis=1) > 0).all()
+    assert len(np.unique(idx)) < idx.size      # experts overlap on clustered tokens
+
+
+def test_query_subset_matches_full():
+    Q, K, V = _rand((196, 8), 1), _rand((196, 8), 2), _rand((196, 8), 3)
+    g = (14, 14, 5, 5)
+    full = oracle.head(Q, K, V, g, 25, 25, io="bf16")
+    qs = [195, 0, 77]
+    sub = oracle.head(Q, K, V, g, 25, 25, io="bf16", queries=qs)
+    np.testing.assert_array_equal(sub["out"], full["out"][qs])
+    np.testing.assert_array_equal(sub["route"], full["route"][qs])
+
+
+def test_batch_forward_matches_heads():
+    w = synth.WORKLOADS["deit_t"].scaled(B=2, H=2)
+    Q, K, V = synth.make_inputs(w)
+    r = oracle.forward(Q, K, V, w.grid, w.m, w.k, io="bf16")
+    h = oracle.head(Q[1, 0], K[1, 0], V[1, 0], w.grid, w.m, w.k, io="bf16")
+    np.testing.assert_array_equal(r["out"][1, 0], h["out"])
+    np.testing.assert_array_equal(r["idx"][1, 0], h["idx"])
+
+
+def test_integer_inputs_have_exact_bf16_means():
+    for name in ("deit_s", "hires56", "long1d"):
+        w = synth.WORKLOADS[name]
+        w = w.scaled(B=1, H=1, N=w.gh * w.gw if w.gh > 1 else 2048,
+                     gw=w.gw if w.gh > 1 else 2048, pw=w.pw if w.gh > 1 else 8, m=w.m if w.gh > 1 else 8)
+        Q, K, V = synth.make_integer_inputs(w)
+        f = oracle.head(Q[0, 0], K[0, 0], V[0, 0], w.grid, w.m, 3, io="f64", debug=True)["Ql"]
+        np.testing.assert_array_equal(f, np.vectorize(oracle.round_bf16)(f))
+
+
+# ---------------------------------------------------------------- planted mistakes
+_MUTANTS = {
+    "drop_shared_values": ("for (int i = 0; i < m; ++i) s += logit[i] * Vl[(size_t)i * d + f];", ""),
+    "unscaled_routed_logit": ("logit[m + t] = s * scale;", "logit[m + t] = s;"),
+    "ties_to_higher_index": ("return (ia > ib) - (ia < ib);", "return (ia < ib) - (ia > ib);"),
+    "pool_bins_floor_end": ("*hi = ((i + 1) * G + P - 1) / P;", "*hi = ((i + 1) * G) / P;"),
+    "route_last_argmax": ("if (s > A[best]) best = i;", "if (s >= A[best]) best = i;"),
+    "values_wrong_row": ("acc[f] += w * V[(size_t)j * d + f];", "acc[f] += w * V[(size_t)(N - 1 - j) * d + f];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(_MUTANTS))
+def test_planted_mistake_fails_a_pin(name, tmp_path):
+    """A copy of the oracle source with one plausible slip planted in it must
+    fail at least one of the pins above."""
+    import subprocess
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "mita_oracle.c")).read()
+    a, b = _MUTANTS[name]
+    assert a in src
+    c = tmp_path / "mutant.c"
+    c.write_text(src.replace(a, b))
+    so = tmp_path / "mutant.so"
+    subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-o", str(so), str(c), "-lm"])
+    pins = [lambda: test_output_matches_masked_sdpa((8, 8, 2, 4), 8, 9, 8),
+            lambda: test_landmark_values_match_sdpa(),
+            lambda: test_topk_brute_force_with_ties(17),
+            lambda: test_route_is_first_argmax(),
+            lambda: test_pool_matches_adaptive_avg_pool2d(14, 14, 5, 5)]
+    failures = 0
+    with oracle.swapped_library(str(so)):
+        for pin in pins:
+            try:
+                pin()
+            except AssertionError:
+                failures += 1
+    assert failures >= 1, name
