@@ -1,0 +1,397 @@
+"""Throughput benchmark of the MiTA forward operator on B300.
+
+One step = one ``mita_forward`` over the whole batch of the workload (all
+six steps of the operator).  Default workload: the DeiT-S-shaped layer
+(B=256, H=6, N=196 on a 14x14 grid, d=64, m=25 from 5x5 pooling, k=25,
+bf16, clustered tokens).  Metric: query-heads per second (B*H*N per step
+divided by the step time).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mita|reference]
+Under torchrun each rank runs its own copy of the workload (heads are
+independent, so the batch shards over ranks with no collective on the data
+path: weak scaling); the timing is the max over ranks.
+
+``--impl reference`` times the CPU oracle (the plain fp64 restatement the
+tests use) on the host cores over a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mixture_top_attention_mita_b300 import synth  # noqa: E402
+
+METRIC = "MiTA fwd query-heads/s at DeiT-S shape (m=k=25); % of HBM/tensor roofline"
+L2_BYTES = 126 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="mita", choices=["mita", "reference"])
+    ap.add_argument("--workload", default="deit_s", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--path", default="auto", choices=["auto", "staged", "fused"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def algorithmic(w):
+    """Compulsory HBM bytes and algorithmic FLOPs per step: read Q, K, V once,
+    write out, expert indices and routes; FLOPs of the six contractions
+    (landmark scores, landmark values, query-landmark scores reused for the
+    route, shared and routed QK and PV)."""
+    e = 2 if w.dtype == "bf16" else 4
+    per_head_bytes = 4 * w.N * w.d * e + 4 * w.m * w.k + 4 * w.N
+    per_head_flops = 4 * w.N * w.d * (2 * w.m + w.k)
+    return per_head_bytes * w.heads, per_head_flops * w.heads
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+def workload_desc(w):
+    grid = f"{w.gh}x{w.gw}" if w.gh > 1 else f"1-D {w.N}"
+    return (f"{w.name}: B={w.B} H={w.H} N={w.N} ({grid}) d={w.d} m={w.m} ({w.ph}x{w.pw}) k={w.k} "
+            f"s=1 {w.dtype} {w.gen}")
+
+
+def source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mixture_top_attention_mita_b300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel_tag, workload):
+    """DRAM bytes per launch recorded from an ncu capture of this kernel on
+    this workload, or None when none is recorded or the kernel sources have
+    changed since."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = source_hash()
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        f = dict(kv.split("=", 1) for kv in line.split())
+        if f.get("kernel") == kernel_tag and f.get("workload") == workload and f.get("src") == want:
+            return float(f["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(w, seconds, full=False):
+    """Time the CPU oracle (single thread, fp64) on whole heads of the
+    workload until about ``seconds`` of work; returns query-heads/s."""
+    import oracle
+    Q, K, V = synth.make_inputs(w.scaled(B=1, H=min(w.H, 4)) if not full else w)
+    Qf, Kf, Vf = Q.double().numpy(), K.double().numpy(), V.double().numpy()
+    heads, t0 = 0, time.perf_counter()
+    queries = None
+    if w.N > 16384:   # a long sequence: all landmark work, a slice of queries
+        queries = list(range(0, w.N, max(1, w.N // 512)))
+    nq = w.N if queries is None else len(queries)
+    while True:
+        h = heads % Q.shape[1]
+        oracle.head(Qf[0, h], Kf[0, h], Vf[0, h], w.grid, w.m, w.k, io=w.dtype, queries=queries)
+        heads += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or (queries is not None and heads >= 1):
+            break
+    if queries is not None:
+        sample = (f"{heads} head(s) of {w.name}: landmark stages on all {w.N} tokens, route+attend on "
+                  f"{nq} queries; time scaled to all {w.N} queries by the attend share")
+        # scale: landmark stages are per head, attend per query; measure attend share separately
+        t1 = time.perf_counter()
+        oracle.head(Qf[0, 0], Kf[0, 0], Vf[0, 0], w.grid, w.m, w.k, io=w.dtype, queries=queries[:1])
+        base = time.perf_counter() - t1
+        per_q = max(0.0, (el / heads - base) / max(1, nq - 1))
+        per_head = base + per_q * w.N
+        return {"value": w.N / per_head, "unit": "query-heads/s", "cores": 1, "kind": "oracle",
+                "sample": sample}
+    return {"value": heads * w.N / el, "unit": "query-heads/s", "cores": 1, "kind": "oracle",
+            "sample": f"{heads} whole heads of {w.name} ({heads * w.N} query-heads), {el:.1f} s, 1 thread"}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, w, ws, rank):
+    if rank != 0:
+        return 0
+    import oracle  # noqa: F401  (build happens in cpu_baseline)
+    times = []
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    for s in range(args.warmup + args.steps):
+        cb = cpu_baseline(w, per_step)
+        if s >= args.warmup:
+            times.append(cb)
+    v = sorted(c["value"] for c in times)[len(times) // 2]
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "query-heads/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * w.heads * w.N / v,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded generator, no dataset)",
+            "config": {"workload": workload_desc(w), "global_batch": w.B * ws, "seq_len": w.N,
+                       "parallelism": f"heads sharded, {ws} replica(s)"},
+            "cpu_baseline": {"value": v, "unit": "query-heads/s", "cores": 1, "kind": "oracle",
+                             "sample": times[0]["sample"] + " per step; median over steps"},
+            "e2e": {"value": v, "unit": "query-heads/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_setup()
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w, ws, rank)
+
+    import mixture_top_attention_mita_b300 as mita
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    plan = mita.Plan.for_workload(w)
+    plan.set_path(args.path)
+    path = plan.path
+    stream = torch.cuda.current_stream()
+
+    # inputs: enough rotating sets that consecutive steps never hit in L2
+    Qc, Kc, Vc = synth.make_inputs(w, seed=w.seed + 7919 * rank)
+    set_bytes = 4 * Qc.numel() * Qc.element_size()
+    nsets = max(2, math.ceil(3 * L2_BYTES / set_bytes) + 1)
+    nsets = min(nsets, 8)
+    sets = []
+    for s in range(nsets):
+        Q, K, V = Qc.to(dev), Kc.to(dev), Vc.to(dev)
+        out = torch.empty_like(Q)
+        idx = torch.empty(w.B, w.H, w.m, w.k, dtype=torch.int32, device=dev)
+        route = torch.empty(w.B, w.H, w.N, dtype=torch.int32, device=dev)
+        sets.append((Q, K, V, out, idx, route))
+
+    def step(i):
+        Q, K, V, out, idx, route = sets[i % nsets]
+        plan.forward(Q, K, V, out, idx, route, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    st = plan.status()
+    if st != mita.MITA_OK:
+        raise SystemExit(f"device status {mita.STATUS.get(st, st)}")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.2)
+    launches0 = plan.launch_count()
+    barrier(ws)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    launches = plan.launch_count() - launches0
+    ms = ev0.elapsed_time(ev1) / args.steps
+    # keep the same load running until the clock sampler has seen >= 1 s
+    t_end = time.time() + max(0.0, 1.0 - ms * args.steps / 1000.0)
+    i = 0
+    while time.time() < t_end:
+        step(i)
+        i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    st = plan.status()
+    if st != mita.MITA_OK:
+        raise SystemExit(f"device status {mita.STATUS.get(st, st)}")
+    ms = max_over_ranks(ms, ws, dev)
+
+    qh = w.heads * w.N
+    value = ws * qh / (ms / 1000.0)
+    nbytes, flops = algorithmic(w)
+    pk = peaks()
+    # dominant kernel: on the fused path the step is one launch; on the
+    # staged path the whole step is reported (kernel-level shares live in
+    # the ncu launch list under profiles/).
+    kernel_tag = "mita_fused" if path == "fused" else "mita_staged_step"
+    t_s = ms / 1000.0
+    bw = nbytes / t_s / 1e9
+    tf = flops / t_s / 1e12
+    hbm_frac = bw / pk["hbm_gbs"]
+    roof_t = max(nbytes / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12))
+    bound = "hbm" if nbytes / (pk["hbm_gbs"] * 1e9) >= flops / (pk["bf16_tflops"] * 1e12) else "tensor"
+    traffic = traffic_from_profiles(kernel_tag, w.name)
+    roofline = {"bound": bound, "achieved": round(bw if bound == "hbm" else tf, 2),
+                "peak": pk["hbm_gbs"] if bound == "hbm" else pk["bf16_tflops"],
+                "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+                "frac": round((bw / pk["hbm_gbs"]) if bound == "hbm" else tf / pk["bf16_tflops"], 4),
+                "traffic": traffic, "kernel": kernel_tag,
+                "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops,
+                "roofline_frac_of_step": round(roof_t / t_s, 4), "peak_source": pk["source"] + " (MEASURED_PEAKS.json)"}
+
+    # end to end through the public API: pinned host inputs -> device ->
+    # forward -> host results, every step
+    e2e = None
+    if not args.no_e2e:
+        hQ, hK, hV = Qc.pin_memory(), Kc.pin_memory(), Vc.pin_memory()
+        Q, K, V, out, idx, route = sets[0]
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hidx = torch.empty(idx.shape, dtype=idx.dtype).pin_memory()
+        hroute = torch.empty(route.shape, dtype=route.dtype).pin_memory()
+        e_steps = max(3, min(args.steps, 20))
+
+        def e2e_step():
+            Q.copy_(hQ, non_blocking=True)
+            K.copy_(hK, non_blocking=True)
+            V.copy_(hV, non_blocking=True)
+            plan.forward(Q, K, V, out, idx, route, stream)
+            hout.copy_(out, non_blocking=True)
+            hidx.copy_(idx, non_blocking=True)
+            hroute.copy_(route, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        barrier(ws)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        ems = max_over_ranks(e0.elapsed_time(e1) / e_steps, ws, dev)
+        h2d = 3 * Qc.numel() * Qc.element_size()
+        d2h = out.numel() * out.element_size() + idx.numel() * 4 + route.numel() * 4
+        e2e = {"value": ws * qh / (ems / 1000.0), "unit": "query-heads/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(ems, 4)}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "query-heads/s", "n_gpus": ws, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded generator, no dataset)",
+                "config": {"workload": workload_desc(w), "global_batch": w.B * ws, "seq_len": w.N,
+                           "parallelism": f"heads sharded over {ws} GPU(s), no collective",
+                           "path": path, "l2": f"inputs rotate over {nsets} buffer sets "
+                                               f"({nsets * set_bytes / 1e6:.0f} MB > 126 MB L2)"},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "clocks": clocks, "achieved_tflops": round(tf, 2), "achieved_hbm_gbs": round(bw, 1),
+                "hbm_frac": round(hbm_frac, 4)}
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

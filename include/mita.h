@@ -1,0 +1,139 @@
+/*
+ * mita.h -- C ABI of the B300 (sm_103a) Mixture-of-Top-k Attention forward
+ * operator.
+ *
+ * The operator (36Kr / 新智元 "注意力也是FFN？从快权重出发，重新理解高效注意力",
+ * section "用少量地标查询，同时构造全局概括与细节专家"; English version "Is
+ * Attention Also FFN? ...", section "Construct global generalization and
+ * detail experts at the same time with a small number of landmark queries"),
+ * per (batch, head), with Q, K, V of N tokens x d features:
+ *   1. m landmark queries Q_l by local average pooling of Q over the token
+ *      grid (adaptive bins [floor(i*G/P), ceil((i+1)*G/P)) per axis);
+ *   2. landmark scores Q_l . K^T / sqrt(d)   (m x N);
+ *   3. routed expert i = the k keys with the highest scores of landmark i
+ *      (ties to the lower key index);
+ *   4. landmark values V_l = softmax(scores) . V; (Q_l, V_l) is the shared
+ *      expert of m key-value pairs;
+ *   5. each query is routed (s = 1) to the landmark with the highest
+ *      q . Q_l / sqrt(d) (ties to the lower landmark index);
+ *   6. each query takes one softmax over the m shared pairs and the k raw
+ *      key-value pairs of its routed expert.
+ * The attention is non-causal and the scale is fixed at 1/sqrt(d).
+ *
+ * Precision contract: inputs and out are MITA_F32 or MITA_BF16.  All sums are
+ * fp32.  Q_l is the correctly rounded mean in the I/O type; V_l is rounded
+ * to the I/O type; out is rounded to nearest even.  Top-k and routing compare
+ * the unscaled fp32 dot products; -0.0 compares equal to +0.0.
+ *
+ * Every function returns a mita_status_t (0 = MITA_OK) unless noted.  No
+ * function synchronises the host with the device except mita_get_status()
+ * and mita_destroy().
+ */
+#ifndef MITA_H
+#define MITA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                       /* = cudaStream_t */
+typedef struct mita_plan_s* mita_plan_t;
+
+typedef enum { MITA_F32 = 0, MITA_BF16 = 1 } mita_dtype_t;
+
+typedef enum {
+    MITA_OK = 0,
+    MITA_ERR_INVALID_ARG = 1,   /* bad size, null or misaligned pointer     */
+    MITA_ERR_UNSUPPORTED = 2,   /* valid but outside the built kernels      */
+    MITA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed     */
+    MITA_ERR_TIMEOUT = 4,       /* a bounded device wait ran out            */
+    MITA_ERR_OOM = 5,           /* workspace allocation failed              */
+    MITA_ERR_DEVICE = 6         /* a kernel flagged bad data (status word)  */
+} mita_status_t;
+
+/* Token grid and landmark grid.  2-D: gh x gw tokens in row-major order
+ * pooled to ph x pw landmarks (landmark i = row * pw + col).  1-D sequence:
+ * gh = ph = 1, gw = N, pw = m. */
+typedef struct {
+    int gh, gw;
+    int ph, pw;
+} mita_grid_t;
+
+/* Create a plan for B x H heads of N tokens, head dim d, m landmarks and
+ * top-k width k, with inputs of type dtype.
+ * Requirements (else MITA_ERR_INVALID_ARG): B, H, N >= 1; gh*gw == N;
+ * ph*pw == m; 1 <= ph <= gh; 1 <= pw <= gw; 1 <= k <= N; plan != NULL.
+ * Supported (else MITA_ERR_UNSUPPORTED): d in {64, 128}; m <= 1024;
+ * k <= 4096; m + k <= 4096; B*H*N*d < 2^40.
+ * The plan owns a device workspace on the current device, allocated here
+ * (MITA_ERR_OOM if that fails) and freed by mita_destroy().  *plan is set to
+ * NULL on failure. */
+int mita_plan(mita_plan_t* plan, int B, int H, int N, int d, mita_grid_t grid,
+              int m, int k, mita_dtype_t dtype);
+
+/* Run the forward operator asynchronously on `stream` (NULL = legacy default
+ * stream).  Device pointers, all contiguous and 16-byte aligned:
+ *   Q, K, V     [B, H, N, d] of the plan's dtype (read only);
+ *   out         [B, H, N, d] of the plan's dtype (written);
+ *   expert_idx  [B, H, m, k] int32, each expert's key indices in ascending
+ *               order (written; may be NULL);
+ *   route       [B, H, N] int32, the landmark each query is routed to
+ *               (written; may be NULL).
+ * The caller owns every buffer; out must not alias Q, K or V.  Calls on one
+ * plan share its workspace: they must be ordered on one stream.  Returns
+ * MITA_ERR_INVALID_ARG for a null/misaligned pointer and MITA_ERR_CUDA if a
+ * launch fails; data errors found by kernels are reported by
+ * mita_get_status(). */
+int mita_forward(mita_plan_t plan, const void* Q, const void* K, const void* V, void* out,
+                 int32_t* expert_idx, int32_t* route, struct CUstream_st* stream);
+
+/* Synchronise the plan's device and return the device status word of the
+ * plan's kernels since the last call (MITA_OK or MITA_ERR_DEVICE /
+ * MITA_ERR_TIMEOUT), then clear it. */
+int mita_get_status(mita_plan_t plan);
+
+/* Free the workspace and the plan (NULL is a no-op).  Synchronises the
+ * plan's device first. */
+void mita_destroy(mita_plan_t plan);
+
+/* Static string for a status code (never NULL). */
+const char* mita_strerror(int code);
+
+/* Plan options (set before mita_forward; return MITA_ERR_INVALID_ARG for an
+ * unknown option or value):
+ *   MITA_OPT_PATH            MITA_PATH_AUTO (default) picks the fastest
+ *                            built path for the shape; MITA_PATH_STAGED
+ *                            forces the stage-by-stage kernels;
+ *                            MITA_PATH_FUSED forces the one-kernel path for
+ *                            short sequences (MITA_ERR_UNSUPPORTED at
+ *                            forward time if the shape does not fit it).
+ *   MITA_OPT_KEEP_LANDMARKS  1: mita_forward also stores Q_l and V_l in the
+ *                            workspace for mita_get_landmarks(). */
+typedef enum { MITA_OPT_PATH = 0, MITA_OPT_KEEP_LANDMARKS = 1 } mita_option_t;
+typedef enum { MITA_PATH_AUTO = 0, MITA_PATH_STAGED = 1, MITA_PATH_FUSED = 2 } mita_path_t;
+int mita_set_option(mita_plan_t plan, int option, int value);
+
+/* Path the next mita_forward() will take (a mita_path_t value other than
+ * AUTO), or a negative status on error. */
+int mita_get_path(mita_plan_t plan);
+
+/* Copy the landmark queries Q_l and landmark values V_l of the last forward
+ * ([B, H, m, d] each, plan dtype, device pointers) on `stream`.  Requires
+ * MITA_OPT_KEEP_LANDMARKS = 1 before that forward (else
+ * MITA_ERR_INVALID_ARG). */
+int mita_get_landmarks(mita_plan_t plan, void* Ql, void* Vl, struct CUstream_st* stream);
+
+/* Bytes of device workspace the plan holds. */
+int mita_workspace_bytes(mita_plan_t plan, uint64_t* bytes);
+
+/* Number of kernels this plan has launched since it was created (every
+ * mita_forward adds the launches of the path it took). */
+int mita_launch_count(mita_plan_t plan, uint64_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MITA_H */

@@ -1,0 +1,448 @@
+// Stage-by-stage MiTA forward kernels (any supported shape).
+//
+// One kernel per step of the operator (36Kr / 新智元 "注意力也是FFN？", section
+// "用少量地标查询，同时构造全局概括与细节专家"):
+//   pool_kernel      step 1, landmark queries by adaptive average pooling
+//   scores_kernel    step 2, raw landmark scores S = Q_l . K^T (fp32, [m, N])
+//   topk_kernel      step 3, per-landmark radix select of the k best keys
+//   values_kernel    step 4, landmark values V_l = softmax(S / sqrt d) . V
+//   route_kernel     step 5, first argmax of q . Q_l per query
+//   bucket_kernel    step 5, stable counting sort of the queries by route
+//   attend_kernel    step 6, one softmax over m shared + k routed keys
+// These kernels favour plain structure over speed; the fused and tensor-core
+// kernels handle the shapes they cover faster.
+#include "common.cuh"
+#include "staged.cuh"
+
+namespace mita {
+
+// ---------------------------------------------------------------- step 1
+// grid (m, BH), block d threads: thread f sums feature f over the bin's
+// tokens (coalesced row reads) and writes the correctly rounded mean.
+template <typename T>
+__global__ void pool_kernel(Shape s, const T* __restrict__ Q, T* __restrict__ Ql) {
+    const int i = blockIdx.x, bh = blockIdx.y, f = threadIdx.x;
+    const int r = i / s.pw, c = i % s.pw;
+    int r0, r1, c0, c1;
+    pool_bin(r, s.gh, s.ph, r0, r1);
+    pool_bin(c, s.gw, s.pw, c0, c1);
+    const T* q = Q + (size_t)bh * s.N * s.d;
+    float hi = 0.0f, lo = 0.0f;
+    for (int y = r0; y < r1; ++y)
+        for (int x = c0; x < c1; ++x) acc2(hi, lo, to_f32(q[(size_t)(y * s.gw + x) * s.d + f]));
+    const float cnt = (float)((r1 - r0) * (c1 - c0));
+    Ql[((size_t)bh * s.m + i) * s.d + f] = pooled_mean<T>(hi, lo, cnt);
+}
+
+// ---------------------------------------------------------------- step 2
+// S[bh, i, j] = sum_f Q_l[i, f] K[j, f] in fp32.  Block tile: 32 landmarks x
+// 128 keys, features staged through shared memory 32 at a time.
+template <typename T>
+__global__ void __launch_bounds__(256) scores_kernel(Shape s, const T* __restrict__ Ql,
+                                                     const T* __restrict__ K, float* __restrict__ S) {
+    __shared__ float a_s[32][33];
+    __shared__ float b_s[128][33];
+    const int bh = blockIdx.z, i0 = blockIdx.y * 32, j0 = blockIdx.x * 128;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 8 x 32
+    const T* a = Ql + (size_t)bh * s.m * s.d;
+    const T* b = K + (size_t)bh * s.N * s.d;
+    float acc[4][4] = {};
+    for (int f0 = 0; f0 < s.d; f0 += 32) {
+        for (int e = threadIdx.x; e < 32 * 32; e += 256) {
+            int r = e >> 5, f = e & 31;
+            a_s[r][f] = (i0 + r < s.m) ? to_f32(a[(size_t)(i0 + r) * s.d + f0 + f]) : 0.0f;
+        }
+        for (int e = threadIdx.x; e < 128 * 32; e += 256) {
+            int r = e >> 5, f = e & 31;
+            b_s[r][f] = (j0 + r < s.N) ? to_f32(b[(size_t)(j0 + r) * s.d + f0 + f]) : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int f = 0; f < 32; ++f) {
+            float av[4], bv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) av[u] = a_s[ty * 4 + u][f];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) bv[u] = b_s[tx + 32 * u][f];
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) acc[p][u] = fmaf(av[p], bv[u], acc[p][u]);
+        }
+        __syncthreads();
+    }
+    float* out = S + (size_t)bh * s.m * s.N;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        int i = i0 + ty * 4 + p;
+        if (i >= s.m) continue;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            int j = j0 + tx + 32 * u;
+            if (j < s.N) out[(size_t)i * s.N + j] = acc[p][u];
+        }
+    }
+}
+
+// ---------------------------------------------------------------- block scan helper
+// Exclusive prefix sum of one int per thread over a block of kThreads
+// threads; returns the block total through *total.
+template <int kThreads>
+__device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int t = lane < kThreads / 32 ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < kThreads / 32) warp_sums[lane] = t;   // inclusive
+    }
+    __syncthreads();
+    int base = w ? warp_sums[w - 1] : 0;
+    *total = warp_sums[kThreads / 32 - 1];
+    __syncthreads();
+    return base + x - v;
+}
+
+// ---------------------------------------------------------------- step 3
+// One block per (landmark, head).  Radix select, 8 bits per pass from the
+// top, finds the k-th largest order key T and how many keys equal to T are
+// needed; a final pass in index order emits keys > T plus the lowest-index
+// keys == T, which yields the expert in ascending index order with ties to
+// the lower index.
+constexpr int kTopkThreads = 512;
+
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(Shape s, const float* __restrict__ S,
+                                                           int32_t* __restrict__ idx) {
+    __shared__ int hist[256];
+    __shared__ int warp_sums[32];
+    __shared__ uint32_t sh_prefix;
+    __shared__ int sh_need;
+    const int i = blockIdx.x, bh = blockIdx.y;
+    const float* row = S + ((size_t)bh * s.m + i) * s.N;
+    uint32_t prefix = 0, mask = 0;
+    int need = s.k;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int e = threadIdx.x; e < 256; e += kTopkThreads) hist[e] = 0;
+        __syncthreads();
+        for (int j = threadIdx.x; j < s.N; j += kTopkThreads) {
+            uint32_t key = order_key(row[j]);
+            if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            // lane L holds digits 255-8L .. 248-8L (descending)
+            const int lane = threadIdx.x;
+            int c[8], tot = 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) { c[u] = hist[255 - 8 * lane - u]; tot += c[u]; }
+            int incl = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            int above = incl - tot;   // count in strictly higher digits
+            // the lane whose range crosses `need`
+            bool mine = above < need && incl >= need;
+            if (mine) {
+                int run = above, digit = 0, rem = need;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    if (run + c[u] >= need) { digit = 255 - 8 * lane - u; rem = need - run; break; }
+                    run += c[u];
+                }
+                sh_prefix = prefix | ((uint32_t)digit << shift);
+                sh_need = rem;
+            }
+        }
+        __syncthreads();
+        prefix = sh_prefix;
+        need = sh_need;
+        mask |= 255u << shift;
+        __syncthreads();
+    }
+    // prefix == T; `need` keys equal to T are taken, lowest index first.
+    int32_t* out = idx + ((size_t)bh * s.m + i) * s.k;
+    int taken = 0, eq_seen = 0;
+    for (int j0 = 0; j0 < s.N; j0 += kTopkThreads) {
+        int j = j0 + threadIdx.x;
+        uint32_t key = j < s.N ? order_key(row[j]) : 0u;
+        int is_eq = (j < s.N && key == prefix) ? 1 : 0;
+        int eq_tot;
+        int eq_rank = eq_seen + block_exclusive_scan<kTopkThreads>(is_eq, warp_sums, &eq_tot);
+        int sel = (j < s.N) && (key > prefix || (is_eq && eq_rank < need));
+        int sel_tot;
+        int pos = taken + block_exclusive_scan<kTopkThreads>(sel, warp_sums, &sel_tot);
+        if (sel) out[pos] = j;
+        taken += sel_tot;
+        eq_seen += eq_tot;
+    }
+}
+
+// ---------------------------------------------------------------- step 4
+// One block per (landmark, head).  V_l[i] = sum_j w_j V[j] / sum_j w_j with
+// w_j = exp((S_j - max S) / sqrt d); 256 / d groups of d threads each take
+// every (256/d)-th key of a 256-key chunk.
+template <typename T>
+__global__ void __launch_bounds__(256) values_kernel(Shape s, const float* __restrict__ S,
+                                                    const T* __restrict__ V, T* __restrict__ Vl) {
+    __shared__ float w_s[256];
+    __shared__ float red[256];
+    __shared__ float acc_s[256];
+    const int i = blockIdx.x, bh = blockIdx.y, t = threadIdx.x;
+    const float* row = S + ((size_t)bh * s.m + i) * s.N;
+    const T* v = V + (size_t)bh * s.N * s.d;
+    float mx = -INFINITY;
+    for (int j = t; j < s.N; j += 256) mx = fmaxf(mx, row[j]);
+    red[t] = mx;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+        if (t < o) red[t] = fmaxf(red[t], red[t + o]);
+        __syncthreads();
+    }
+    mx = red[0];
+    __syncthreads();
+    const float c = rsqrtf((float)s.d) * kLog2e;
+    const int groups = 256 / s.d, g = t / s.d, f = t % s.d;
+    float acc = 0.0f, den = 0.0f;
+    for (int j0 = 0; j0 < s.N; j0 += 256) {
+        int j = j0 + t;
+        float w = j < s.N ? exp2f((row[j] - mx) * c) : 0.0f;
+        w_s[t] = w;
+        den += w;
+        __syncthreads();
+        int jn = min(256, s.N - j0);
+        for (int u = g; u < jn; u += groups) acc = fmaf(w_s[u], to_f32(v[(size_t)(j0 + u) * s.d + f]), acc);
+        __syncthreads();
+    }
+    red[t] = den;
+    acc_s[t] = acc;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+        if (t < o) red[t] += red[t + o];
+        __syncthreads();
+    }
+    if (t < s.d) {
+        float a = 0.0f;
+        for (int u = 0; u < groups; ++u) a += acc_s[u * s.d + t];
+        Vl[((size_t)bh * s.m + i) * s.d + t] = from_f32<T>(a / red[0]);
+    }
+}
+
+// ---------------------------------------------------------------- step 5
+// One thread per query: raw scores q . Q_l[i] over all landmarks, first
+// argmax.  Landmarks are staged through shared memory 32 at a time.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) route_kernel(Shape s, const T* __restrict__ Q,
+                                                   const T* __restrict__ Ql, int32_t* __restrict__ route) {
+    __shared__ float l_s[32][D];
+    const int bh = blockIdx.y;
+    const int qi = blockIdx.x * 128 + threadIdx.x;
+    const bool live = qi < s.N;
+    float q[D];
+    const T* qp = Q + ((size_t)bh * s.N + (live ? qi : 0)) * D;
+#pragma unroll
+    for (int f = 0; f < D; ++f) q[f] = to_f32(qp[f]);
+    float best = -INFINITY;
+    int arg = 0;
+    const T* lp = Ql + (size_t)bh * s.m * D;
+    for (int i0 = 0; i0 < s.m; i0 += 32) {
+        const int n = min(32, s.m - i0);
+        __syncthreads();
+        for (int e = threadIdx.x; e < n * D; e += 128) l_s[e / D][e % D] = to_f32(lp[(size_t)i0 * D + e]);
+        __syncthreads();
+        for (int u = 0; u < n; ++u) {
+            float a = 0.0f;
+#pragma unroll
+            for (int f = 0; f < D; ++f) a = fmaf(q[f], l_s[u][f], a);
+            if (i0 + u == 0 || a > best) { best = a; arg = i0 + u; }
+        }
+    }
+    if (live) route[(size_t)bh * s.N + qi] = arg;
+}
+
+// One warp per head: per-landmark counts, exclusive offsets, and the
+// queries listed bucket by bucket in ascending query order (stable).
+__global__ void bucket_kernel(Shape s, const int32_t* __restrict__ route, int32_t* __restrict__ counts,
+                              int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                              int32_t* __restrict__ status) {
+    const int bh = blockIdx.x, lane = threadIdx.x;
+    const int32_t* r = route + (size_t)bh * s.N;
+    int32_t* cnt = counts + (size_t)bh * s.m;
+    int32_t* off = offsets + (size_t)bh * (s.m + 1);
+    int32_t* p = perm + (size_t)bh * s.N;
+    for (int i = lane; i < s.m; i += 32) cnt[i] = 0;
+    __syncwarp();
+    for (int q = lane; q < s.N; q += 32) {
+        int b = r[q];
+        if (b < 0 || b >= s.m) { atomicExch(status, (int)MITA_ERR_DEVICE); continue; }
+        atomicAdd(&cnt[b], 1);
+    }
+    __syncwarp();
+    __threadfence_block();
+    int carry = 0;
+    for (int i0 = 0; i0 < s.m; i0 += 32) {
+        int i = i0 + lane;
+        int v = i < s.m ? __ldcg(&cnt[i]) : 0, x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (i < s.m) off[i] = carry + x - v;
+        carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) off[s.m] = carry;
+    __syncwarp();
+    __threadfence_block();
+    // cursor per bucket reuses counts
+    for (int i = lane; i < s.m; i += 32) cnt[i] = off[i];
+    __syncwarp();
+    __threadfence_block();
+    for (int q0 = 0; q0 < s.N; q0 += 32) {
+        int q = q0 + lane;
+        int b = q < s.N ? r[q] : -1;
+        bool ok = b >= 0 && b < s.m;
+        unsigned peers = __match_any_sync(0xffffffffu, ok ? b : -1);
+        unsigned lower = peers & ((1u << lane) - 1u);
+        int leader = __ffs(peers) - 1;
+        int base = 0;
+        if (ok && lane == leader) base = atomicAdd(&cnt[b], __popc(peers));
+        base = __shfl_sync(peers, base, leader);
+        if (ok) p[base + __popc(lower)] = q;
+        __syncwarp();
+    }
+    // restore counts
+    for (int i = lane; i < s.m; i += 32) cnt[i] = off[i + 1] - off[i];
+}
+
+// ---------------------------------------------------------------- step 6
+// One warp per query, queries taken in bucket order so that neighbouring
+// warps share an expert.  Lane t computes logits t, t+32, ... of the m + k
+// concatenated keys; the softmax is exact (max, exp, sum) in fp32; lane f
+// accumulates output features f, f+32, ...
+constexpr int kAttendWarps = 4;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(32 * kAttendWarps)
+    attend_kernel(Shape s, const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
+                  const T* __restrict__ Ql, const T* __restrict__ Vl, const int32_t* __restrict__ idx,
+                  const int32_t* __restrict__ route, const int32_t* __restrict__ perm, T* __restrict__ out,
+                  int32_t* __restrict__ status) {
+    extern __shared__ float smem[];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int L = s.m + s.k;
+    float* q_s = smem + w * (D + L);
+    float* l_s = q_s + D;
+    const int bh = blockIdx.y;
+    const int slot = blockIdx.x * kAttendWarps + w;
+    if (slot >= s.N) return;
+    const int qi = perm[(size_t)bh * s.N + slot];
+    if (qi < 0 || qi >= s.N) { if (lane == 0) atomicExch(status, (int)MITA_ERR_DEVICE); return; }
+    const int r = route[(size_t)bh * s.N + qi];
+    if (r < 0 || r >= s.m) { if (lane == 0) atomicExch(status, (int)MITA_ERR_DEVICE); return; }
+    const size_t hoff = (size_t)bh * s.N * D;
+    for (int f = lane; f < D; f += 32) q_s[f] = to_f32(Q[hoff + (size_t)qi * D + f]);
+    __syncwarp();
+    const T* lq = Ql + (size_t)bh * s.m * D;
+    const int32_t* E = idx + ((size_t)bh * s.m + r) * s.k;
+    const float scale = rsqrtf((float)D);
+    float mx = -INFINITY;
+    for (int t = lane; t < L; t += 32) {
+        const T* key;
+        if (t < s.m) key = lq + (size_t)t * D;
+        else {
+            int j = E[t - s.m];
+            if (j < 0 || j >= s.N) { atomicExch(status, (int)MITA_ERR_DEVICE); j = 0; }
+            key = K + hoff + (size_t)j * D;
+        }
+        float a = 0.0f;
+#pragma unroll 8
+        for (int f = 0; f < D; ++f) a = fmaf(q_s[f], to_f32(key[f]), a);
+        a *= scale;
+        l_s[t] = a;
+        mx = fmaxf(mx, a);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    __syncwarp();
+    float den = 0.0f;
+    for (int t = lane; t < L; t += 32) {
+        float p = exp2f((l_s[t] - mx) * kLog2e);
+        l_s[t] = p;
+        den += p;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    __syncwarp();
+    const T* lv = Vl + (size_t)bh * s.m * D;
+    float acc[D / 32];
+#pragma unroll
+    for (int u = 0; u < D / 32; ++u) acc[u] = 0.0f;
+    for (int t = 0; t < s.m; ++t) {
+        float p = l_s[t];
+#pragma unroll
+        for (int u = 0; u < D / 32; ++u) acc[u] = fmaf(p, to_f32(lv[(size_t)t * D + lane + 32 * u]), acc[u]);
+    }
+    for (int t = 0; t < s.k; ++t) {
+        float p = l_s[s.m + t];
+        int j = E[t];
+        j = (j < 0 || j >= s.N) ? 0 : j;
+#pragma unroll
+        for (int u = 0; u < D / 32; ++u) acc[u] = fmaf(p, to_f32(V[hoff + (size_t)j * D + lane + 32 * u]), acc[u]);
+    }
+    const float inv = 1.0f / den;
+#pragma unroll
+    for (int u = 0; u < D / 32; ++u) out[hoff + (size_t)qi * D + lane + 32 * u] = from_f32<T>(acc[u] * inv);
+}
+
+size_t staged_attend_smem(const Shape& s) {
+    return (size_t)kAttendWarps * (s.d + s.m + s.k) * sizeof(float);
+}
+
+// ---------------------------------------------------------------- launcher
+template <typename T, int D>
+static cudaError_t run_staged_t(mita_plan_s* p, const T* Q, const T* K, const T* V, T* out, int32_t* idx,
+                                int32_t* route, cudaStream_t st) {
+    const Shape& s = p->s;
+    const int BH = s.BH();
+    T* Ql = (T*)p->Ql;
+    T* Vl = (T*)p->Vl;
+    pool_kernel<T><<<dim3(s.m, BH), D, 0, st>>>(s, Q, Ql);
+    scores_kernel<T><<<dim3((s.N + 127) / 128, (s.m + 31) / 32, BH), 256, 0, st>>>(s, Ql, K, p->S);
+    topk_kernel<<<dim3(s.m, BH), kTopkThreads, 0, st>>>(s, p->S, idx);
+    values_kernel<T><<<dim3(s.m, BH), 256, 0, st>>>(s, p->S, V, Vl);
+    route_kernel<T, D><<<dim3((s.N + 127) / 128, BH), 128, 0, st>>>(s, Q, Ql, route);
+    bucket_kernel<<<BH, 32, 0, st>>>(s, route, p->counts, p->offsets, p->perm, p->status);
+    const size_t smem = staged_attend_smem(s);
+    cudaFuncSetAttribute(attend_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    attend_kernel<T, D><<<dim3((s.N + kAttendWarps - 1) / kAttendWarps, BH), 32 * kAttendWarps, smem, st>>>(
+        s, Q, K, V, Ql, Vl, idx, route, p->perm, out, p->status);
+    p->launches += 7;
+    return cudaGetLastError();
+}
+
+cudaError_t run_staged(mita_plan_s* p, const void* Q, const void* K, const void* V, void* out, int32_t* idx,
+                       int32_t* route, cudaStream_t st) {
+    if (p->dtype == MITA_BF16) {
+        using T = __nv_bfloat16;
+        if (p->s.d == 64) return run_staged_t<T, 64>(p, (const T*)Q, (const T*)K, (const T*)V, (T*)out, idx, route, st);
+        return run_staged_t<T, 128>(p, (const T*)Q, (const T*)K, (const T*)V, (T*)out, idx, route, st);
+    }
+    using T = float;
+    if (p->s.d == 64) return run_staged_t<T, 64>(p, (const T*)Q, (const T*)K, (const T*)V, (T*)out, idx, route, st);
+    return run_staged_t<T, 128>(p, (const T*)Q, (const T*)K, (const T*)V, (T*)out, idx, route, st);
+}
+
+}  // namespace mita

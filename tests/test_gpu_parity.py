@@ -1,0 +1,207 @@
+"""Parity of the CUDA path with the CPU oracle (needs a CUDA device).
+
+Every call goes through the C ABI (``libmita.so``) via the thin binding.
+Sizes: reduced batches of every workload shape (several tiles and a ragged
+tail, the oracle checks all heads), small-integer inputs (indices and
+routes bit-exact), degenerate shapes, and the full-size workloads in the
+launch configuration the benchmark times (sampled heads / queries).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import mixture_top_attention_mita_b300 as mita
+from mixture_top_attention_mita_b300 import synth
+from parity_util import compare_batch
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+PATHS = ["staged", "fused"]
+
+
+def _run(w, Q, K, V, path="auto", keep=False):
+    plan = mita.Plan.for_workload(w)
+    plan.set_path(path)
+    if keep:
+        plan.set_option(mita.OPT_KEEP_LANDMARKS, 1)
+    dev = torch.device("cuda")
+    Qd, Kd, Vd = Q.to(dev), K.to(dev), V.to(dev)
+    out = torch.empty_like(Qd)
+    idx = torch.full((w.B, w.H, w.m, w.k), -1, dtype=torch.int32, device=dev)
+    route = torch.full((w.B, w.H, w.N), -1, dtype=torch.int32, device=dev)
+    plan.forward(Qd, Kd, Vd, out, idx, route)
+    st = plan.status()
+    assert st == mita.MITA_OK, mita.STATUS.get(st, st)
+    res = {"out": out, "idx": idx, "route": route, "plan": plan}
+    if keep:
+        Ql = torch.empty(w.B, w.H, w.m, w.d, dtype=Qd.dtype, device=dev)
+        Vl = torch.empty_like(Ql)
+        plan.landmarks(Ql, Vl)
+        torch.cuda.synchronize()
+        res.update(Ql=Ql, Vl=Vl)
+    return res
+
+
+def _fused_ok(w):
+    plan = mita.Plan.for_workload(w.scaled(B=1, H=1))
+    plan.set_path("auto")
+    return plan.path == "fused"
+
+
+def _skip_unbuilt(w, path):
+    if path == "fused" and not _fused_ok(w):
+        pytest.skip("no fused kernel for this shape")
+
+
+SMALL = {
+    "tiny_f32": W["tiny_f32"],
+    "deit_t": W["deit_t"].scaled(B=2, H=3),
+    "deit_s": W["deit_s"].scaled(B=2, H=4),
+    "hires56": W["hires56"].scaled(B=1, H=2),
+    "long1d_8k": W["long1d"].scaled(B=1, H=2, N=8192, gw=8192, pw=32, m=32),
+}
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_random(name, path):
+    w = SMALL[name]
+    _skip_unbuilt(w, path)
+    Q, K, V = synth.make_inputs(w)
+    r = _run(w, Q, K, V, path)
+    compare_batch(w, Q, K, V, r["out"], r["idx"], r["route"], exact=False)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_integer_exact(name, path):
+    w = SMALL[name]
+    _skip_unbuilt(w, path)
+    Q, K, V = synth.make_integer_inputs(w)
+    r = _run(w, Q, K, V, path)
+    compare_batch(w, Q, K, V, r["out"], r["idx"], r["route"], exact=True)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_landmarks_match_oracle(path):
+    import oracle
+    w = SMALL["deit_s"]
+    _skip_unbuilt(w, path)
+    Q, K, V = synth.make_inputs(w)
+    r = _run(w, Q, K, V, path, keep=True)
+    Ql, Vl = r["Ql"].cpu().double().numpy(), r["Vl"].cpu().double().numpy()
+    for b in range(w.B):
+        for h in range(w.H):
+            o = oracle.head(Q[b, h], K[b, h], V[b, h], w.grid, w.m, w.k, io=w.dtype, debug=True)
+            np.testing.assert_array_equal(Ql[b, h], o["Ql"])          # correctly rounded mean
+            np.testing.assert_allclose(Vl[b, h], o["Vl"], rtol=0, atol=2 ** -7)
+
+
+EDGE = [
+    # full attention + one pooled key: k = N, m = 1
+    W["deit_t"].scaled(B=1, H=2, m=1, ph=1, pw=1, k=196),
+    # every token its own landmark
+    W["deit_t"].scaled(B=1, H=1, m=196, ph=14, pw=14, k=3),
+    # k = 1
+    W["deit_t"].scaled(B=1, H=2, k=1),
+    # short 1-D sequences, odd sizes
+    W["long1d"].scaled(B=1, H=3, N=7, gw=7, pw=1, m=1, k=7, d=64, gen="iid"),
+    W["long1d"].scaled(B=2, H=1, N=1, gw=1, pw=1, m=1, k=1, gen="iid"),
+    W["long1d"].scaled(B=1, H=1, N=1000, gw=1000, pw=9, m=9, k=333, gen="iid"),
+    # d = 128 on a 2-D grid, fp32
+    W["tiny_f32"].scaled(B=1, H=2, d=128, gh=10, gw=13, N=130, ph=3, pw=4, m=12, k=40),
+]
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("i", range(len(EDGE)))
+def test_edge_shapes(i, path):
+    w = EDGE[i]
+    _skip_unbuilt(w, path)
+    Q, K, V = synth.make_inputs(w, seed=100 + i)
+    r = _run(w, Q, K, V, path)
+    compare_batch(w, Q, K, V, r["out"], r["idx"], r["route"], exact=False)
+    Q, K, V = synth.make_integer_inputs(w, seed=200 + i)
+    r = _run(w, Q, K, V, path)
+    compare_batch(w, Q, K, V, r["out"], r["idx"], r["route"], exact=_means_exact(w, Q))
+
+
+def _means_exact(w, Q):
+    """True when every pooled mean of these integer inputs is exactly
+    representable in the I/O type, so that all fp32 sums are exact."""
+    import oracle
+    for b in range(w.B):
+        for h in range(w.H):
+            f = oracle.head(Q[b, h], Q[b, h], Q[b, h], w.grid, w.m, 1, io="f64", debug=True)["Ql"]
+            t = torch.from_numpy(f).to(synth.torch_dtype(w)).double().numpy()
+            if not np.array_equal(t, f):
+                return False
+    return True
+
+
+def test_paths_agree_bitwise_on_integer_inputs():
+    w = SMALL["deit_s"]
+    if not _fused_ok(w):
+        pytest.skip("no fused kernel for this shape")
+    Q, K, V = synth.make_integer_inputs(w)
+    a, b = _run(w, Q, K, V, "staged"), _run(w, Q, K, V, "fused")
+    assert torch.equal(a["idx"], b["idx"]) and torch.equal(a["route"], b["route"])
+
+
+def test_deterministic():
+    w = SMALL["deit_s"]
+    Q, K, V = synth.make_inputs(w)
+    a, b = _run(w, Q, K, V), _run(w, Q, K, V)
+    assert torch.equal(a["out"], b["out"]) and torch.equal(a["idx"], b["idx"])
+
+
+def test_null_optional_outputs():
+    w = SMALL["deit_t"]
+    Q, K, V = synth.make_inputs(w)
+    plan = mita.Plan.for_workload(w)
+    dev = torch.device("cuda")
+    Qd, Kd, Vd = Q.to(dev), K.to(dev), V.to(dev)
+    out = torch.empty_like(Qd)
+    plan.forward(Qd, Kd, Vd, out)
+    assert plan.status() == mita.MITA_OK
+    ref = _run(w, Q, K, V)["out"]
+    assert torch.equal(out, ref)
+
+
+def test_misaligned_pointer_rejected():
+    w = SMALL["deit_t"]
+    plan = mita.Plan.for_workload(w)
+    buf = torch.empty(w.B * w.H * w.N * w.d + 8, dtype=torch.bfloat16, device="cuda")
+    bad = buf[1:1 + w.B * w.H * w.N * w.d]
+    with pytest.raises(mita.MitaError):
+        plan.forward(bad, bad, bad, buf[8:])
+
+
+# ------------------------------------------------------------- full size
+FULL_HEADS = {"tiny_f32": None, "deit_t": [(0, 0), (77, 2), (127, 1)],
+              "deit_s": [(0, 0), (131, 3), (255, 5)], "hires56": [(0, 0), (15, 5)],
+              "long1d": [(0, 0), (1, 7)]}
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", sorted(FULL_HEADS))
+def test_full_size_sampled(name):
+    w = W[name]
+    Q, K, V = synth.make_inputs(w)
+    r = _run(w, Q, K, V, "auto")
+    queries = None
+    if w.N > 4096:
+        queries = np.random.default_rng(0).choice(w.N, 384, replace=False)
+        queries.sort()
+    report = []
+    compare_batch(w, Q, K, V, r["out"], r["idx"], r["route"], exact=False, heads=FULL_HEADS[name],
+                  queries=queries, report=report)
+    print(name, report)
+    # every query of every head has a valid route; experts ascending
+    route, idx = r["route"], r["idx"]
+    assert int(route.min()) >= 0 and int(route.max()) < w.m
+    assert bool((idx[..., 1:] > idx[..., :-1]).all())
+    assert bool(torch.isfinite(r["out"].float()).all())
