@@ -132,6 +132,44 @@ int mita_workspace_bytes(mita_plan_t plan, uint64_t* bytes);
  * mita_forward adds the launches of the path it took). */
 int mita_launch_count(mita_plan_t plan, uint64_t* launches);
 
+/* ---------------------------------------------------------------------
+ * Allocation-free forward.  The method description has no counterpart of
+ * this entry point: it exists for callers that cannot call cudaMalloc --
+ * code embedded in a host framework that owns all device memory through its
+ * own pool and forbids raw device allocations, and latency-critical loops
+ * in which an allocation would implicitly synchronise the device.  Such
+ * callers cannot create a plan either, because mita_plan() allocates.
+ *
+ * mita_forward_noalloc() computes the same result as mita_forward() on the
+ * stage-by-stage path, with the same arguments as mita_plan() followed by
+ * those of mita_forward().  It allocates nothing: its scratch (landmark
+ * queries and values, landmark scores, query buckets, a status word) lives
+ * in one fixed device array of MITA_NOALLOC_SCRATCH_BYTES that the library
+ * declares statically; every GPU that loads the library holds that array
+ * until the process exits.  It calls no cudaMalloc, cudaFree or allocating
+ * library routine.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - A shape whose scratch does not fit (mita_noalloc_scratch_bytes())
+ *     returns MITA_ERR_UNSUPPORTED; argument errors are those of mita_plan()
+ *     and mita_forward().
+ *   - Every call shares the one array, and a call leaves its contents
+ *     behind.  Calls that overlap on the GPU (different streams, or
+ *     different host threads, on one device) race on it: order them on one
+ *     stream.
+ *   - Kernel data checks have no plan to report to: a call returns only
+ *     launch errors.
+ */
+#define MITA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+int mita_forward_noalloc(int B, int H, int N, int d, mita_grid_t grid, int m, int k,
+                         mita_dtype_t dtype, const void* Q, const void* K, const void* V, void* out,
+                         int32_t* expert_idx, int32_t* route, struct CUstream_st* stream);
+
+/* Size in bytes of the fixed scratch array used by mita_forward_noalloc(). */
+uint64_t mita_noalloc_scratch_bytes(void);
+
 #ifdef __cplusplus
 }
 #endif

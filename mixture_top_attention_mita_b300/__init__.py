@@ -24,7 +24,7 @@ PATH_NAMES = {PATH_STAGED: "staged", PATH_FUSED: "fused"}
 # Every entry point declared in include/mita.h.
 EXPORTS = ("mita_plan", "mita_forward", "mita_get_status", "mita_destroy", "mita_strerror",
            "mita_set_option", "mita_get_path", "mita_get_landmarks", "mita_workspace_bytes",
-           "mita_launch_count")
+           "mita_launch_count", "mita_forward_noalloc", "mita_noalloc_scratch_bytes")
 
 
 class MitaError(RuntimeError):
@@ -62,9 +62,12 @@ def load(path: str | None = None):
     lib.mita_get_landmarks.argtypes = [vp, vp, vp, vp]
     lib.mita_workspace_bytes.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64)]
     lib.mita_launch_count.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64)]
+    lib.mita_forward_noalloc.argtypes = [i, i, i, i, Grid, i, i, i, vp, vp, vp, vp, vp, vp, vp]
+    lib.mita_noalloc_scratch_bytes.argtypes = []
     for name in EXPORTS:
-        if name != "mita_destroy" and name != "mita_strerror":
+        if name not in ("mita_destroy", "mita_strerror", "mita_noalloc_scratch_bytes"):
             getattr(lib, name).restype = i
+    lib.mita_noalloc_scratch_bytes.restype = ctypes.c_uint64
     if path is None:
         _lib = lib
     return lib
@@ -158,6 +161,17 @@ class Plan:
             self.close()
         except Exception:
             pass
+
+
+def forward_noalloc(Q, K, V, out, grid, m, k, expert_idx=None, route=None, stream=None):
+    """``mita_forward_noalloc``: the forward without a plan and without any
+    device allocation (scratch in the library's fixed device array)."""
+    import torch
+    B, H, N, d = Q.shape
+    code = MITA_BF16 if Q.dtype == torch.bfloat16 else MITA_F32
+    rc = load().mita_forward_noalloc(B, H, N, d, Grid(*grid), m, k, code, _ptr(Q), _ptr(K), _ptr(V),
+                                     _ptr(out), _ptr(expert_idx), _ptr(route), _stream_ptr(stream))
+    _check(rc, "mita_forward_noalloc")
 
 
 def mita_forward(Q, K, V, grid, m, k, path="auto", return_all=True):
