@@ -90,7 +90,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct Shape {
     int B, H, N, d, m, k;
     int gh, gw, ph, pw;
-    int BH() const { return B * H; }
+    __host__ __device__ int BH() const { return B * H; }
 };
 
 }  // namespace mita
