@@ -2,25 +2,29 @@
 // m <= 32, k <= 32): the DeiT-T / DeiT-S layer shapes.
 //
 // The six steps of the operator (36Kr / 新智元 "注意力也是FFN？", section
-// "用少量地标查询，同时构造全局概括与细节专家") run per head inside one CTA, from
-// shared memory:
-//   phase 1  pool        Q_l = correctly rounded bin means of Q
-//   phase 2  contraction [K ; Q] . Q_l^T with mma.sync: raw landmark scores
-//                        (kept in shared memory) and each query's first
-//                        argmax landmark (the route)
-//   phase 3  select      per landmark, the k best keys (ties to the lower
-//                        index) by a monotone 128-bin histogram + exact
-//                        resolution of the boundary bin; softmax numerators
-//                        of the landmark row; bucket sort of the queries
-//   phase 4  values      V_l = P . V with mma.sync, normalised, bf16
-//   phase 5  attention   per (expert, 8 queries) tile: logits against the 32
-//                        shared slots (Q_l) and 32 routed slots (the
-//                        expert's keys, gathered row by row with ldmatrix),
-//                        one softmax over both, output = P . [V_l ; V_E]
-// The kernel is persistent (one CTA per SM, heads strided by the grid) and
-// loads the next head's Q, K, V with TMA (128-byte swizzle) into the second
-// half of a double buffer while it computes the current head, so the HBM
-// stream of inputs and outputs never waits for the arithmetic.
+// "用少量地标查询，同时构造全局概括与细节专家") run per head inside one CTA of
+// 8 warps, from shared memory:
+//   load      TMA (128-byte swizzle) of the head's Q, K and V tiles
+//   phase A   pool        Q_l = correctly rounded bin means of Q (warp per
+//                         landmark, two features per lane)
+//   phase B   contraction [K ; Q] . Q_l^T with mma.sync: raw landmark scores
+//                         (fp32, shared memory) and each query's first argmax
+//                         landmark (the route)
+//   phase C   select      per landmark (warp per landmark) the k best keys,
+//                         ties to the lower index, by a monotone 128-bin
+//                         histogram and an exact rank of the boundary bin;
+//                         the bf16 softmax numerators overwrite the scores;
+//                         one warp bucket-sorts the queries by route
+//   phase D   values      V_l = P . V with mma.sync, normalised, bf16
+//   phase E   attention   per (expert, 16 queries) tile: logits against the
+//                         32 shared slots (Q_l) and 32 routed slots (the
+//                         expert's keys, gathered row by row by ldmatrix), one
+//                         softmax over both, output = P . [V_l ; V_E]; the
+//                         output rows overwrite the tile's own query rows
+//   store     TMA store of the head's output tile, then the next head's load
+// Two CTAs share an SM (about 110 KB of shared memory each), so one CTA's
+// loads and stores overlap the other's arithmetic.  Heads are strided over a
+// persistent grid.
 #include <cuda.h>
 
 #include "fused.cuh"
@@ -28,51 +32,49 @@
 namespace mita {
 namespace fz {
 
-constexpr int kWarps = 16;
+constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kD = 64;
 constexpr int kSlots = 32;      // shared slots (m <= 32) and routed slots (k <= 32)
 constexpr int kMaxN = 256;
-constexpr int kBins = 128;
-constexpr int kCand = 32;       // boundary-bin candidates resolved by rank
+constexpr int kBins = 64;       // histogram bins of the select
+constexpr int kCand = 32;       // boundary-bin members resolved by exact rank
+constexpr int kTile = 16;       // queries per attention tile
 constexpr int kMaxSmem = 232448;
 
 struct Layout {
-    int N, np16, nk16, sstr, pstrB, qkv;
-    int oBuf0, oBuf1, oQl, oVl, oS, oP, oHist, oCand, oIdx, oRoute, oPerm, oCnt, oOff, oCur,
-        oTiles, oPsum, oCtl, oBar, total;
+    int N, np16, nk16, sstr, qkv;
+    int oQ, oK, oV, oQl, oVl, oS, oIdx, oRoute, oPerm, oCnt, oOff, oTiles, oCtl, oBar, oHist,
+        oCand, total;
 };
 
 static int align_to(int x, int a) { return (x + a - 1) / a * a; }
 
-static Layout make_layout(int N) {
+static Layout make_layout(int N, int m) {
     Layout L{};
     L.N = N;
     L.np16 = align_to(N, 16);
     L.nk16 = L.np16 / 16;
-    L.sstr = L.np16 + 4;                 // fp32 words per score row (conflict-free stores)
-    L.pstrB = 2 * (L.np16 + 8);          // bytes per numerator row (conflict-free ldmatrix)
+    L.sstr = L.np16 + 4;                 // fp32 words per score row: conflict-free ldmatrix rows
     L.qkv = align_to(N * 128, 1024);
     int o = 0;
     auto take = [&](int bytes, int al) { o = align_to(o, al); int r = o; o += bytes; return r; };
-    L.oBuf0 = take(3 * L.qkv, 1024);
-    L.oBuf1 = take(3 * L.qkv, 1024);
-    L.oQl = take(kSlots * 128, 1024);
-    L.oVl = take(kSlots * 128, 1024);
-    L.oS = take(kSlots * L.sstr * 4, 16);
-    L.oP = take(kSlots * L.pstrB, 16);
-    L.oHist = take(kWarps * kBins * 4, 16);
-    L.oCand = take(kWarps * kCand * 8, 16);
+    L.oQ = take(L.qkv, 1024);
+    L.oK = take(L.qkv, 1024);
+    L.oV = take(N * 128, 1024);
+    L.oQl = take(kSlots * 128, 128);
+    L.oVl = take(kSlots * 128, 128);
+    L.oS = take(m * L.sstr * 4, 128);
     L.oIdx = take(kSlots * kSlots, 16);
     L.oRoute = take(kMaxN, 16);
     L.oPerm = take(kMaxN, 16);
     L.oCnt = take((kSlots + 1) * 4, 16);
     L.oOff = take((kSlots + 1) * 4, 16);
-    L.oCur = take(kSlots * 4, 16);
-    L.oTiles = take((kMaxN / 8 + kSlots) * 4, 16);
-    L.oPsum = take(kSlots * 4, 16);
+    L.oTiles = take((kMaxN / kTile + kSlots) * 4, 16);
     L.oCtl = take(16, 16);
     L.oBar = take(16, 16);
+    L.oHist = take(kWarps * kBins * 4, 16);
+    L.oCand = take(kWarps * kCand * 8, 16);
     L.total = o + 1024;                  // slack to align the dynamic base to 1024
     return L;
 }
@@ -80,13 +82,16 @@ static Layout make_layout(int N) {
 struct Params {
     Shape s;
     Layout L;
-    __nv_bfloat16* out;
     int32_t* idx;
     int32_t* route;
     __nv_bfloat16* Ql_keep;   // nullptr unless landmarks are kept
     __nv_bfloat16* Vl_keep;
     int32_t* status;
     float scale_log2;         // log2(e) / sqrt(d)
+    uint32_t rows[kSlots];    // landmark i pools token rows [lo, hi): lo | hi << 16
+    uint32_t cols[kSlots];    // and token columns [lo, hi): lo | hi << 16
+    float rcnt[kSlots];       // 1 / (tokens in the bin of landmark i)
+    int win[kSlots];          // 16 - ceil(log2(tokens in the bin)): exact-sum exponent window
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -103,8 +108,9 @@ MITA_DEV void ldsm_x4_t(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2, ui
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a));
 }
-MITA_DEV void ldsm_x2_t(uint32_t a, uint32_t& r0, uint32_t& r1) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n" : "=r"(r0), "=r"(r1) : "r"(a));
+MITA_DEV void stsm_x4(uint32_t a, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};\n"
+                 ::"r"(a), "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
 }
 MITA_DEV void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                        uint32_t b1) {
@@ -114,17 +120,33 @@ MITA_DEV void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uin
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-MITA_DEV uint32_t movm_t(uint32_t x) {
-    uint32_t y;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
-    return y;
-}
 MITA_DEV uint32_t pack2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
 }
 MITA_DEV float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 MITA_DEV float bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+MITA_DEV float ex2(float x) {   // hardware 2^x (PTX ex2.approx), -inf -> 0
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+MITA_DEV float rcp(float x) {   // hardware reciprocal (PTX rcp.approx)
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+MITA_DEV float max3(float a, float b, float c) {
+    float y;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+    return y;
+}
+MITA_DEV float min3(float a, float b, float c) {
+    float y;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+    return y;
+}
 
 MITA_DEV void mbar_init(uint32_t bar, int count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
@@ -139,18 +161,73 @@ MITA_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
     return ok != 0;
 }
+// As mbar_try_wait, but the thread may sleep up to `ns` nanoseconds for the phase.
+MITA_DEV bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(bar), "r"(parity), "r"(ns) : "memory");
+    return ok != 0;
+}
 MITA_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
         "[%4];\n" ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar) : "memory");
 }
+MITA_DEV void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];\n" ::"l"(map),
+                 "r"(x), "r"(y), "r"(src) : "memory");
+}
+MITA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+MITA_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+MITA_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+MITA_DEV void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+
+// ---------------------------------------------------------------- pooled mean
+// bf16 nearest (ties to even) to (hi + lo) / c for the exact bin sum hi + lo
+// and a positive integer count c (rc ~ 1/c).  The fp32 quotient picks a
+// candidate b; the exact position of the sum against c times the midpoints
+// next to b (c * midpoint is exact, the fused multiply-add keeps the sign)
+// decides between b and its neighbours.
+MITA_DEV __nv_bfloat16 round_mean(float hi, float lo, float c, float rc) {
+    const bool neg = hi < 0.0f;
+    if (neg) { hi = -hi; lo = -lo; }
+    uint16_t b = __bfloat16_as_ushort(__float2bfloat16_rn((hi + lo) * rc));
+    const float v0 = __bfloat162float(__ushort_as_bfloat16(b));
+    const float v1 = __bfloat162float(__ushort_as_bfloat16((uint16_t)(b + 1)));
+    const float e_up = fmaf(-c, 0.5f * (v0 + v1), hi) + lo;
+    if (e_up > 0.0f || (e_up == 0.0f && (b & 1))) {
+        b = (uint16_t)(b + 1);
+    } else if (b > 0) {
+        const float vm = __bfloat162float(__ushort_as_bfloat16((uint16_t)(b - 1)));
+        const float e_dn = fmaf(-c, 0.5f * (vm + v0), hi) + lo;
+        if (e_dn < 0.0f || (e_dn == 0.0f && (b & 1))) b = (uint16_t)(b - 1);
+    }
+    const __nv_bfloat16 r = __ushort_as_bfloat16(b);
+    return neg ? __hneg(r) : r;
+}
+
+MITA_DEV uint32_t umax16x2(uint32_t a, uint32_t b) {
+    uint32_t y;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
+    return y;
+}
+MITA_DEV uint32_t umin16x2(uint32_t a, uint32_t b) {
+    uint32_t y;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
+    return y;
+}
 
 // ---------------------------------------------------------------- the kernel
-__global__ void __launch_bounds__(kThreads, 1)
+template <int NV>   // score values per lane in the select: ceil(N / 32)
+__global__ void __launch_bounds__(kThreads, 2)
     fused_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
-                 const __grid_constant__ CUtensorMap mapV, const __grid_constant__ Params P) {
+                 const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapO,
+                 const __grid_constant__ Params P) {
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned base (128-byte swizzle), derived from the shared array by
+    // pointer arithmetic so that every access below stays a shared-space access
+    unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const Shape& s = P.s;
     const Layout& L = P.L;
     const int N = s.N, m = s.m, k = s.k;
@@ -158,8 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = lane >> 2, t = lane & 3;
 
     const uint32_t sbase = smem_u32(sm);
-    const uint32_t uBuf[2] = {sbase + L.oBuf0, sbase + L.oBuf1};
-    const uint32_t uQl = sbase + L.oQl, uVl = sbase + L.oVl, uP = sbase + L.oP;
+    const uint32_t uQ = sbase + L.oQ, uK = sbase + L.oK, uV = sbase + L.oV;
+    const uint32_t uQl = sbase + L.oQl, uVl = sbase + L.oVl, uS = sbase + L.oS;
+    const uint32_t sstrB = (uint32_t)L.sstr * 4u;
+    const unsigned char* Qb = sm + L.oQ;
     float* S_s = (float*)(sm + L.oS);
     int* hist = (int*)(sm + L.oHist) + warp * kBins;
     float2* cand = (float2*)(sm + L.oCand) + warp * kCand;
@@ -168,22 +247,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* perm_s = sm + L.oPerm;
     int* cnt_s = (int*)(sm + L.oCnt);
     int* off_s = (int*)(sm + L.oOff);
-    int* cur_s = (int*)(sm + L.oCur);
     int* tiles_s = (int*)(sm + L.oTiles);
-    float* psum_s = (float*)(sm + L.oPsum);
     int* ctl = (int*)(sm + L.oCtl);     // [0] tile count, [1] abort flag
     const uint32_t uBar = sbase + L.oBar;
 
-    // one-time set-up: zero the padding that later phases rely on
+    // one-time set-up: landmark slots past m stay zero (finite) for the MMAs
     for (int e = tid; e < kSlots * 128 / 4; e += kThreads) {
         ((uint32_t*)(sm + L.oQl))[e] = 0u;
         ((uint32_t*)(sm + L.oVl))[e] = 0u;
     }
-    for (int e = tid; e < kSlots * L.pstrB / 4; e += kThreads) ((uint32_t*)(sm + L.oP))[e] = 0u;
     for (int e = tid; e < kWarps * kBins; e += kThreads) ((int*)(sm + L.oHist))[e] = 0;
     if (tid == 0) {
         mbar_init(uBar, 1);
-        mbar_init(uBar + 8, 1);
         ctl[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
@@ -191,30 +266,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int BH = s.BH();
     const uint32_t bytes_per_head = 3u * (uint32_t)N * 128u;
-    auto issue = [&](int head, int buf) {
-        const uint32_t bar = uBar + 8 * buf;
-        mbar_expect_tx(bar, bytes_per_head);
-        tma_load_2d(uBuf[buf], &mapQ, 0, head * N, bar);
-        tma_load_2d(uBuf[buf] + L.qkv, &mapK, 0, head * N, bar);
-        tma_load_2d(uBuf[buf] + 2 * L.qkv, &mapV, 0, head * N, bar);
-    };
-    if (tid == 0 && (int)blockIdx.x < BH) issue(blockIdx.x, 0);
+    if (tid == 0 && (int)blockIdx.x < BH) {
+        mbar_expect_tx(uBar, bytes_per_head);
+        tma_load_2d(uQ, &mapQ, 0, blockIdx.x * N, uBar);
+        tma_load_2d(uK, &mapK, 0, blockIdx.x * N, uBar);
+        tma_load_2d(uV, &mapV, 0, blockIdx.x * N, uBar);
+    }
 
     const float cs = P.scale_log2;
     int it = 0;
     for (int head = blockIdx.x; head < BH; head += gridDim.x, ++it) {
-        const int buf = it & 1;
-        const uint32_t parity = (it >> 1) & 1;
+        const uint32_t parity = it & 1;
         if (tid == 0) {
-            const int nxt = head + gridDim.x;
-            if (nxt < BH) {
-                asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-                issue(nxt, buf ^ 1);
-            }
             // bounded wait for this head's tiles (about one second)
             const long long t0 = clock64();
             bool ok = false;
-            while (!(ok = mbar_try_wait(uBar + 8 * buf, parity))) {
+            while (!(ok = mbar_try_wait_sleep(uBar, parity, 20000u))) {
                 if (clock64() - t0 > 2000000000LL) break;
             }
             if (!ok) {
@@ -223,36 +290,62 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncthreads();
-        if (ctl[1]) return;
-        while (!mbar_try_wait(uBar + 8 * buf, parity)) {}   // completes at once: acquire for every thread
-        const uint32_t uQ = uBuf[buf], uK = uBuf[buf] + L.qkv, uV = uBuf[buf] + 2 * L.qkv;
-        const unsigned char* Qb = sm + (uQ - sbase);
+        if (ctl[1]) break;
+        while (!mbar_try_wait(uBar, parity)) {}   // completes at once: acquire for every thread
 
-        // ---------------- phase 1: landmark queries
-        for (int task = tid; task < m * 32; task += kThreads) {
-            const int i = task >> 5, fp = task & 31;
-            const int r = i / s.pw, c = i - r * s.pw;
-            int r0, r1, c0, c1;
-            pool_bin(r, s.gh, s.ph, r0, r1);
-            pool_bin(c, s.gw, s.pw, c0, c1);
-            float a0 = 0.0f, a1 = 0.0f;
-            for (int y = r0; y < r1; ++y)
+        // ---------------- phase A: landmark queries (warp per landmark)
+        for (int i = warp; i < m; i += kWarps) {
+            const int r0 = P.rows[i] & 0xffff, r1 = P.rows[i] >> 16;
+            const int c0 = P.cols[i] & 0xffff, c1 = P.cols[i] >> 16;
+            const uint32_t lo_off = (uint32_t)(lane & 3) * 4u;
+            const int chunk = lane >> 2;
+            // fp32 sums of the bin (features 2*lane, 2*lane+1) and the largest and
+            // smallest bf16 magnitude of each feature (packed 16-bit halves)
+            float s0 = 0.0f, s1 = 0.0f;
+            uint32_t mag_hi = 0u, mag_lo = 0x7fff7fffu;
+            for (int y = r0; y < r1; ++y) {
+                const int rb = y * s.gw;
+#pragma unroll 4
                 for (int x = c0; x < c1; ++x) {
-                    const int tok = y * s.gw + x;
-                    const uint32_t v = *(const uint32_t*)(Qb + swz(tok, fp >> 2) + (fp & 3) * 4);
-                    a0 += bf_lo(v);
-                    a1 += bf_hi(v);
+                    const uint32_t v = *(const uint32_t*)(Qb + swz(rb + x, chunk) + lo_off);
+                    s0 += bf_lo(v);
+                    s1 += bf_hi(v);
+                    const uint32_t mag = v & 0x7fff7fffu;
+                    mag_hi = umax16x2(mag_hi, mag);
+                    mag_lo = umin16x2(mag_lo, mag);
                 }
-            const float cnt = (float)((r1 - r0) * (c1 - c0));
+            }
+            // The sums are exact when no value is zero and the exponents span at
+            // most P.win[i] binades (then every partial sum is a multiple of the
+            // smallest value's last bit below 2^24 of them); otherwise sum again
+            // error-free (rare for continuous data).
+            const int win = P.win[i];
+            const bool exact0 = (mag_lo & 0xffffu) != 0u &&
+                                (int)((mag_hi >> 7) & 0xffu) - (int)((mag_lo >> 7) & 0xffu) <= win;
+            const bool exact1 = (mag_lo >> 16) != 0u &&
+                                (int)((mag_hi >> 23) & 0xffu) - (int)((mag_lo >> 23) & 0xffu) <= win;
+            float h0 = s0, l0 = 0.0f, h1 = s1, l1 = 0.0f;
+            if (!exact0 || !exact1) {
+                h0 = l0 = h1 = l1 = 0.0f;
+                for (int y = r0; y < r1; ++y)
+                    for (int x = c0; x < c1; ++x) {
+                        const uint32_t v = *(const uint32_t*)(Qb + swz(y * s.gw + x, chunk) + lo_off);
+                        acc2(h0, l0, bf_lo(v));
+                        acc2(h1, l1, bf_hi(v));
+                    }
+            }
+            const float cnt = (float)((r1 - r0) * (c1 - c0)), rc = P.rcnt[i];
+            const __nv_bfloat16 q0 = round_mean(h0, l0, cnt, rc);
+            const __nv_bfloat16 q1 = round_mean(h1, l1, cnt, rc);
             __nv_bfloat162 q2;
-            q2.x = mean_to_bf16(a0, 0.0f, cnt);
-            q2.y = mean_to_bf16(a1, 0.0f, cnt);
-            *(__nv_bfloat162*)(sm + L.oQl + swz(i, fp >> 2) + (fp & 3) * 4) = q2;
-            if (P.Ql_keep) *(__nv_bfloat162*)(P.Ql_keep + ((size_t)head * m + i) * kD + 2 * fp) = q2;
+            q2.x = q0;
+            q2.y = q1;
+            *(__nv_bfloat162*)(sm + L.oQl + swz(i, chunk) + lo_off) = q2;
+            if (P.Ql_keep) *(__nv_bfloat162*)(P.Ql_keep + ((size_t)head * m + i) * kD + 2 * lane) = q2;
         }
         __syncthreads();
 
-        // ---------------- phase 2: [K ; Q] . Q_l^T  -> scores and routes
+        // ---------------- phase B: [K ; Q] . Q_l^T  -> scores and routes
         {
             uint32_t bq[4][4][2];   // Q_l as B operand: [n8 tile][k16 step][2]
 #pragma unroll
@@ -314,6 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int oa = __shfl_xor_sync(0xffffffffu, arg, o);
                             if (ob > best || (ob == best && oa < arg)) { best = ob; arg = oa; }
                         }
+                        if (arg >= m) arg = 0;   // no finite score (undefined inputs): keep the bucket valid
                         const int q = r0 + g + 8 * h;
                         if (t == 0 && q < N) {
                             route_s[q] = (uint8_t)arg;
@@ -325,16 +419,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
 
-        // ---------------- phase 3: experts, numerators, buckets
+        // ---------------- phase C: experts and numerators (warp per landmark)
         for (int i = warp; i < m; i += kWarps) {
-            const float* srow = S_s + i * L.sstr;
-            float v[8];
-            float mx = -INFINITY, mn = INFINITY;
+            float* srow = S_s + i * L.sstr;
+            float v[NV];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < NV; ++u) {
                 const int j = lane + 32 * u;
-                v[u] = j < N ? srow[j] : 0.0f;
-                if (j < N) { mx = fmaxf(mx, v[u]); mn = fminf(mn, v[u]); }
+                v[u] = srow[j < N ? j : 0];   // a slot past N repeats key 0: max / min unchanged
+            }
+            float mx = v[0], mn = v[0];
+#pragma unroll
+            for (int u = 1; u < NV; u += 2) {
+                const float b = u + 1 < NV ? v[u + 1] : v[u];
+                mx = max3(mx, v[u], b);
+                mn = min3(mn, v[u], b);
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
@@ -344,9 +443,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // monotone binning: a larger score never lands in a lower bin
             const float range = mx - mn;
             const float sc = range > 0.0f ? (float)kBins / range : 0.0f;
-            int bin[8];
+            int bin[NV];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < NV; ++u) {
                 const int j = lane + 32 * u;
                 bin[u] = -1;
                 if (j < N) {
@@ -355,85 +454,83 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             __syncwarp();
-            int hc[4], tot = 0;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) { hc[u] = hist[kBins - 1 - 4 * lane - u]; tot += hc[u]; }
-            int incl = tot;
+            // lane L holds bins 2L, 2L+1; suffix counts from the top bin down
+            const int2 hw = *(const int2*)(hist + 2 * lane);
+            *(int2*)(hist + 2 * lane) = make_int2(0, 0);   // each lane clears what it read
+            const int tot = hw.x + hw.y;
+            int suf = tot;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
+                const int y = __shfl_down_sync(0xffffffffu, suf, o);
+                if (lane + o < 32) suf += y;
             }
-            const int above = incl - tot;
-            const bool mine = above < k && incl >= k;
+            const int above = suf - tot;   // members of bins above 2L+1
+            const bool mine = above < k && suf >= k;
             int bstar = 0, need = 0, cstar = 0;
             if (mine) {
-                int run = above;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    if (run + hc[u] >= k && need == 0) {
-                        bstar = kBins - 1 - 4 * lane - u;
-                        need = k - run;
-                        cstar = hc[u];
-                    }
-                    run += hc[u];
+                if (above + hw.y >= k) {
+                    bstar = 2 * lane + 1;
+                    need = k - above;
+                    cstar = hw.y;
+                } else {
+                    bstar = 2 * lane;
+                    need = k - above - hw.y;
+                    cstar = hw.x;
                 }
             }
             const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
             bstar = __shfl_sync(0xffffffffu, bstar, src);
             need = __shfl_sync(0xffffffffu, need, src);
             cstar = __shfl_sync(0xffffffffu, cstar, src);
-            __syncwarp();
-#pragma unroll
-            for (int u = 0; u < 4; ++u) hist[4 * lane + u] = 0;   // ready for the next landmark
-            // boundary bin: pick the `need` best of its `cstar` members
+            // boundary bin: take the `need` best of its `cstar` members
             uint32_t bsel = 0;   // bit u: member lane + 32u is taken
             if (need < cstar) {
                 if (cstar <= kCand) {
-                    int base = 0;
+                    // members to lanes 0 .. cstar-1, exact rank by (score desc, index asc)
+                    int base = 0, slot[NV];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
+                    for (int u = 0; u < NV; ++u) {
                         const bool isb = bin[u] == bstar;
                         const unsigned bal = __ballot_sync(0xffffffffu, isb);
-                        if (isb) cand[base + __popc(bal & ((1u << lane) - 1u))] =
-                                     make_float2(v[u], __int_as_float(lane + 32 * u));
+                        slot[u] = base + __popc(bal & ((1u << lane) - 1u));
+                        if (isb) cand[slot[u]] = make_float2(v[u], __int_as_float(lane + 32 * u));
                         base += __popc(bal);
                     }
                     __syncwarp();
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        if (bin[u] != bstar) continue;
-                        const int j = lane + 32 * u;
-                        int rank = 0;
-                        for (int e = 0; e < cstar; ++e) {
-                            const float2 ce = cand[e];
-                            const int je = __float_as_int(ce.y);
-                            rank += (ce.x > v[u] || (ce.x == v[u] && je < j)) ? 1 : 0;
-                        }
-                        if (rank < need) bsel |= 1u << u;
+                    const float2 me = cand[lane < cstar ? lane : 0];
+                    const int jm = __float_as_int(me.y);
+                    int rank = 0;
+                    for (int e = 0; e < cstar; ++e) {
+                        const float ve = __shfl_sync(0xffffffffu, me.x, e);
+                        const int je = __shfl_sync(0xffffffffu, jm, e);
+                        rank += (ve > me.x || (ve == me.x && je < jm)) ? 1 : 0;
                     }
+                    const unsigned chosen = __ballot_sync(0xffffffffu, lane < cstar && rank < need);
+#pragma unroll
+                    for (int u = 0; u < NV; ++u)
+                        if (bin[u] == bstar && ((chosen >> slot[u]) & 1u)) bsel |= 1u << u;
                     __syncwarp();
                 } else {
                     // many members (degenerate scores): bisect the order key
-                    uint32_t key[8];
+                    uint32_t key[NV];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) key[u] = order_key(v[u]);
+                    for (int u = 0; u < NV; ++u) key[u] = order_key(v[u]);
                     uint32_t T = 0;
                     for (int b = 31; b >= 0; --b) {
                         const uint32_t cand_t = T | (1u << b);
                         int c = 0;
 #pragma unroll
-                        for (int u = 0; u < 8; ++u) c += (bin[u] == bstar && key[u] >= cand_t) ? 1 : 0;
+                        for (int u = 0; u < NV; ++u) c += (bin[u] == bstar && key[u] >= cand_t) ? 1 : 0;
                         c = __reduce_add_sync(0xffffffffu, c);
                         if (c >= need) T = cand_t;
                     }
                     int gt = 0;
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) gt += (bin[u] == bstar && key[u] > T) ? 1 : 0;
+                    for (int u = 0; u < NV; ++u) gt += (bin[u] == bstar && key[u] > T) ? 1 : 0;
                     gt = __reduce_add_sync(0xffffffffu, gt);
                     int eq_left = need - gt, base = 0;
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
+                    for (int u = 0; u < NV; ++u) {
                         const bool isb = bin[u] == bstar;
                         const bool eq = isb && key[u] == T;
                         const unsigned bal = __ballot_sync(0xffffffffu, eq);
@@ -444,49 +541,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
+                for (int u = 0; u < NV; ++u)
                     if (bin[u] == bstar) bsel |= 1u << u;
             }
-            // write the expert in ascending key order
+            // the expert in ascending key order
             int pos = 0;
             uint8_t* irow = idx_s + i * kSlots;
-            int32_t* grow = P.idx + ((size_t)head * m + i) * k;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < NV; ++u) {
                 const bool sel = bin[u] > bstar || (bsel >> u & 1u);
                 const unsigned bal = __ballot_sync(0xffffffffu, sel);
-                if (sel) {
-                    const int p = pos + __popc(bal & ((1u << lane) - 1u));
-                    irow[p] = (uint8_t)(lane + 32 * u);
-                    grow[p] = lane + 32 * u;
-                }
+                if (sel) irow[pos + __popc(bal & ((1u << lane) - 1u))] = (uint8_t)(lane + 32 * u);
                 pos += __popc(bal);
             }
-            // softmax numerators of the landmark row (bf16, as the MMA reads them)
-            __nv_bfloat16* prow = (__nv_bfloat16*)(sm + L.oP + i * L.pstrB);
-            float ps = 0.0f;
+            // softmax numerators of the landmark row, bf16 as the MMA reads them,
+            // written over the row's own scores (every lane has read them)
+            __nv_bfloat16* prow = (__nv_bfloat16*)srow;
+            const float mb = mx * cs;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < NV; ++u) {
                 const int j = lane + 32 * u;
-                if (j < N) {
-                    const __nv_bfloat16 pb = __float2bfloat16_rn(exp2f((v[u] - mx) * cs));
-                    prow[j] = pb;
-                    ps += __bfloat162float(pb);
-                }
+                if (j < L.np16) prow[j] = __float2bfloat16_rn(j < N ? ex2(fmaf(v[u], cs, -mb)) : 0.0f);
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-            if (lane == 0) psum_s[i] = ps;
-            __syncwarp();   // histogram and candidate list are reused by the next landmark
+            __syncwarp();
+            if (lane < k) P.idx[((size_t)head * m + i) * k + lane] = irow[lane];
         }
         if (warp == kWarps - 1) {
-            // bucket sort of the queries by route; tiles of up to 8 queries
+            // bucket sort of the queries by route; tiles of up to kTile queries
             for (int b = lane; b <= kSlots; b += 32) cnt_s[b] = 0;
             __syncwarp();
             for (int q = lane; q < N; q += 32) atomicAdd(&cnt_s[route_s[q]], 1);
             __syncwarp();
             const int c = lane < m ? cnt_s[lane] : 0;
-            int x = c, nt = (c + 7) >> 3, y = nt;
+            int x = c, nt = (c + kTile - 1) / kTile, y = nt;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int a = __shfl_up_sync(0xffffffffu, x, o);
@@ -494,161 +581,185 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane >= o) { x += a; y += b; }
             }
             const int excl = x - c, texcl = y - nt;
+            __syncwarp();
             if (lane < m) {
                 off_s[lane] = excl;
-                cur_s[lane] = excl;
-                for (int e = 0; e < nt; ++e) tiles_s[texcl + e] = (lane << 8) | (8 * e);
+                cnt_s[lane] = excl;        // cursor
+                for (int e = 0; e < nt; ++e) tiles_s[texcl + e] = (lane << 8) | (kTile * e);
             }
-            if (lane == 31) ctl[0] = y;
+            if (lane == 31) {
+                ctl[0] = y;
+                off_s[m] = N;
+            }
             __syncwarp();
             for (int q = lane; q < N; q += 32) {
                 const int b = route_s[q];
-                perm_s[atomicAdd(&cur_s[b], 1)] = (uint8_t)q;
+                perm_s[atomicAdd(&cnt_s[b], 1)] = (uint8_t)q;
             }
         }
         __syncthreads();
 
-        // ---------------- phase 4: landmark values V_l = P . V
+        // ---------------- phase D: landmark values V_l = P . V / (P . 1)
         {
-            const int mt = warp >> 3, n = warp & 7;   // 2 x 8 tiles over the 16 warps
-            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const int prow = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int mt = warp >> 2, np = warp & 3;   // 2 x 4 (two n8 tiles each) over the 8 warps
+            const uint32_t ones = 0x3F803F80u;         // bf16 pair (1, 1): B operand of the row sums
+            float acc[3][4] = {};
+            const int prow = min(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, m - 1);
+            const uint32_t pa = uS + (uint32_t)prow * sstrB + (uint32_t)(lane >> 4) * 16u;
             for (int kk = 0; kk < L.nk16; ++kk) {
-                uint32_t a0, a1, a2, a3, b0, b1;
-                ldsm_x4(uP + prow * L.pstrB + (kk * 16 + (lane >> 4) * 8) * 2, a0, a1, a2, a3);
+                uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+                ldsm_x4(pa + kk * 32, a0, a1, a2, a3);
                 const int vrow = min(kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, N - 1);
-                ldsm_x2_t(uV + swz(vrow, n), b0, b1);
-                mma16816(acc, a0, a1, a2, a3, b0, b1);
+                ldsm_x4_t(uV + swz(vrow, 2 * np + (lane >> 4)), b0, b1, b2, b3);
+                mma16816(acc[0], a0, a1, a2, a3, b0, b1);
+                mma16816(acc[1], a0, a1, a2, a3, b2, b3);
+                mma16816(acc[2], a0, a1, a2, a3, ones, ones);
             }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int i = mt * 16 + g + 8 * h;
                 if (i < m) {
-                    const float inv = 1.0f / psum_s[i];
-                    const uint32_t pk = pack2(acc[2 * h] * inv, acc[2 * h + 1] * inv);
-                    *(uint32_t*)(sm + L.oVl + swz(i, n) + 4 * t) = pk;
-                    if (P.Vl_keep) *(uint32_t*)(P.Vl_keep + ((size_t)head * m + i) * kD + 8 * n + 2 * t) = pk;
+                    const float inv = 1.0f / acc[2][2 * h];
+#pragma unroll
+                    for (int n = 0; n < 2; ++n) {
+                        const uint32_t pk = pack2(acc[n][2 * h] * inv, acc[n][2 * h + 1] * inv);
+                        *(uint32_t*)(sm + L.oVl + swz(i, 2 * np + n) + 4 * t) = pk;
+                        if (P.Vl_keep)
+                            *(uint32_t*)(P.Vl_keep + ((size_t)head * m + i) * kD + 16 * np + 8 * n + 2 * t) = pk;
+                    }
                 }
             }
         }
         __syncthreads();
 
-        // ---------------- phase 5: grouped attention, 8 queries per tile
+        // ---------------- phase E: grouped attention, kTile queries per tile
         const int ntiles = ctl[0];
         for (int tile = warp; tile < ntiles; tile += kWarps) {
             const int b = tiles_s[tile] >> 8, st = tiles_s[tile] & 255;
-            const int nq = min(8, (b + 1 < m ? off_s[b + 1] : N) - off_s[b] - st);
             const int qbase = off_s[b] + st;
+            const int nq = min(kTile, off_s[b + 1] - qbase);
             const uint8_t* E = idx_s + b * kSlots;
-            // B operand of the logits: the tile's queries (rows of Q)
-            uint32_t bq[4][2];
-            {
-                const int qc = perm_s[qbase + min(lane & 7, nq - 1)];
+            // A operand: the tile's query rows (row r of the tile = query perm[qbase + r])
+            const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int qa_row = perm_s[qbase + min(arow, nq - 1)];
+            uint32_t qa[4][4];
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t r0, r1, r2, r3;
-                    ldsm_x4(uQ + swz(qc, 4 * hh + (lane >> 3)), r0, r1, r2, r3);
-                    bq[2 * hh][0] = r0;
-                    bq[2 * hh][1] = r1;
-                    bq[2 * hh + 1][0] = r2;
-                    bq[2 * hh + 1][1] = r3;
-                }
-            }
-            // logits: 4 key tiles (2 shared + 2 routed) x 8 queries
-            float sc4[4][4];
-            const int lr = (lane & 7) + ((lane >> 3) & 1) * 8;   // A row of this lane
+            for (int kk = 0; kk < 4; ++kk)
+                ldsm_x4(uQ + swz(qa_row, 2 * kk + (lane >> 4)), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+            // logits: 8 n8 slot tiles (0-3 shared Q_l, 4-7 routed keys) x 16 queries
+            float sc[8][4];
 #pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-                sc4[mt][0] = sc4[mt][1] = sc4[mt][2] = sc4[mt][3] = 0.0f;
-                uint32_t rowaddr;
-                if (mt < 2) rowaddr = uQl + (uint32_t)((mt * 16 + lr) * 128);
-                else {
-                    const int slot = (mt - 2) * 16 + lr;
-                    rowaddr = uK + (uint32_t)(E[slot < k ? slot : 0] * 128);
-                }
-                const int rsw = mt < 2 ? (mt * 16 + lr) & 7 : E[((mt - 2) * 16 + lr) < k ? (mt - 2) * 16 + lr : 0] & 7;
+            for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.0f;
+            const int brow = (lane & 7) + (lane >> 4) * 8;   // slot of this lane within an n8 pair
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4(rowaddr + (((2 * kk + (lane >> 4)) ^ rsw) << 4), a0, a1, a2, a3);
-                    mma16816(sc4[mt], a0, a1, a2, a3, bq[kk][0], bq[kk][1]);
-                }
-            }
-            // one softmax per query column over the m + k valid slots
-            float cmax[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int slot = (mt & 1) * 16 + g + 8 * h;
-                    const bool valid = mt < 2 ? slot < m : slot < k;
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        float x = valid ? sc4[mt][2 * h + e] * cs : -INFINITY;
-                        sc4[mt][2 * h + e] = x;
-                        cmax[e] = fmaxf(cmax[e], x);
-                    }
-                }
-#pragma unroll
-            for (int e = 0; e < 2; ++e)
-#pragma unroll
-                for (int o = 4; o < 32; o <<= 1) cmax[e] = fmaxf(cmax[e], __shfl_xor_sync(0xffffffffu, cmax[e], o));
-            float csum[2] = {0.0f, 0.0f};
-            uint32_t pb[4][2];   // P^T as B operand per key k16 step
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const float p0 = exp2f(sc4[mt][2 * h] - cmax[0]);
-                    const float p1 = exp2f(sc4[mt][2 * h + 1] - cmax[1]);
-                    const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
-                    csum[0] += __low2float(pp);
-                    csum[1] += __high2float(pp);
-                    pb[mt][h] = movm_t(*reinterpret_cast<const uint32_t*>(&pp));
-                }
-            }
-#pragma unroll
-            for (int e = 0; e < 2; ++e)
-#pragma unroll
-                for (int o = 4; o < 32; o <<= 1) csum[e] += __shfl_xor_sync(0xffffffffu, csum[e], o);
-            const float inv0 = 1.0f / csum[0], inv1 = 1.0f / csum[1];
-            // out^T = [V_l ; V_E]^T . P^T : 4 feature tiles x 8 queries
-            const int vr = (lane & 7) + (lane >> 4) * 8;   // key row of this lane within a k16 step
-            uint32_t vaddr[4];
-            int vsw[4];
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                if (kk < 2) {
-                    vaddr[kk] = uVl + (uint32_t)((kk * 16 + vr) * 128);
-                    vsw[kk] = (kk * 16 + vr) & 7;
+            for (int np = 0; np < 4; ++np) {
+                uint32_t rowbase;
+                int rsw;
+                if (np < 2) {
+                    const int slot = 16 * np + brow;
+                    rowbase = uQl + (uint32_t)slot * 128u;
+                    rsw = slot & 7;
                 } else {
-                    const int slot = (kk - 2) * 16 + vr;
+                    const int slot = 16 * (np - 2) + brow;
                     const int j = E[slot < k ? slot : 0];
-                    vaddr[kk] = uV + (uint32_t)(j * 128);
-                    vsw[kk] = j & 7;
+                    rowbase = uK + (uint32_t)j * 128u;
+                    rsw = j & 7;
                 }
-            }
-            const int qg = perm_s[qbase + min(g, nq - 1)];
-            __nv_bfloat16* orow = P.out + ((size_t)head * N + qg) * kD;
-#pragma unroll
-            for (int fm = 0; fm < 4; ++fm) {
-                float o4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4_t(vaddr[kk] + (((2 * fm + ((lane >> 3) & 1)) ^ vsw[kk]) << 4), a0, a1, a2, a3);
-                    mma16816(o4, a0, a1, a2, a3, pb[kk][0], pb[kk][1]);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(rowbase + (uint32_t)(((2 * kk + ((lane >> 3) & 1)) ^ rsw) << 4), b0, b1, b2, b3);
+                    mma16816(sc[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+                    mma16816(sc[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
                 }
-                const uint32_t y0 = movm_t(pack2(o4[0] * inv0, o4[1] * inv1));
-                const uint32_t y1 = movm_t(pack2(o4[2] * inv0, o4[3] * inv1));
-                if (g < nq) {
-                    *(uint32_t*)(orow + 16 * fm + 2 * t) = y0;
-                    *(uint32_t*)(orow + 16 * fm + 8 + 2 * t) = y1;
+            }
+            // mask the padding slots, then one softmax per query row
+#pragma unroll
+            for (int n = 0; n < 8; ++n) {
+                const int lim = n < 4 ? m : k;
+                const int s0 = 8 * (n & 3);
+                if (s0 + 8 > lim) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (s0 + 2 * t + (e & 1) >= lim) sc[n][e] = -INFINITY;
                 }
+            }
+            float mx0 = fmaxf(sc[0][0], sc[0][1]), mx1 = fmaxf(sc[0][2], sc[0][3]);
+#pragma unroll
+            for (int n = 1; n < 8; ++n) {
+                mx0 = max3(mx0, sc[n][0], sc[n][1]);
+                mx1 = max3(mx1, sc[n][2], sc[n][3]);
+            }
+#pragma unroll
+            for (int o = 1; o <= 2; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float mb0 = mx0 * cs, mb1 = mx1 * cs;
+            uint32_t pa[4][4];   // P as A operand per k16 slot step
+#pragma unroll
+            for (int n = 0; n < 8; ++n) {
+                pa[n >> 1][(n & 1) * 2 + 0] = pack2(ex2(fmaf(sc[n][0], cs, -mb0)), ex2(fmaf(sc[n][1], cs, -mb0)));
+                pa[n >> 1][(n & 1) * 2 + 1] = pack2(ex2(fmaf(sc[n][2], cs, -mb1)), ex2(fmaf(sc[n][3], cs, -mb1)));
+            }
+            // out = P . [V_l ; V_E] : 8 n8 feature tiles x 16 queries
+            float o8[8][4], osum[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // osum: row sums of P (ones column)
+#pragma unroll
+            for (int n = 0; n < 8; ++n) o8[n][0] = o8[n][1] = o8[n][2] = o8[n][3] = 0.0f;
+            const int vslot = (lane & 7) + ((lane >> 3) & 1) * 8;   // slot of this lane within a k16 step
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                uint32_t rowbase;
+                int rsw;
+                if (ks < 2) {
+                    const int slot = 16 * ks + vslot;
+                    rowbase = uVl + (uint32_t)slot * 128u;
+                    rsw = slot & 7;
+                } else {
+                    const int slot = 16 * (ks - 2) + vslot;
+                    const int j = E[slot < k ? slot : 0];
+                    rowbase = uV + (uint32_t)j * 128u;
+                    rsw = j & 7;
+                }
+                const uint32_t a0 = pa[ks][0], a1 = pa[ks][1], a2 = pa[ks][2], a3 = pa[ks][3];
+                mma16816(osum, a0, a1, a2, a3, 0x3F803F80u, 0x3F803F80u);
+#pragma unroll
+                for (int np = 0; np < 4; ++np) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(rowbase + (uint32_t)(((2 * np + (lane >> 4)) ^ rsw) << 4), b0, b1, b2, b3);
+                    mma16816(o8[2 * np], a0, a1, a2, a3, b0, b1);
+                    mma16816(o8[2 * np + 1], a0, a1, a2, a3, b2, b3);
+                }
+            }
+            // normalise; write the rows over the tile's own query rows
+            const float inv0 = rcp(osum[0]), inv1 = rcp(osum[2]);
+            const int srow_t = (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int qs_row = perm_s[qbase + min(srow_t, nq - 1)];
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                const uint32_t r0 = pack2(o8[2 * np][0] * inv0, o8[2 * np][1] * inv0);
+                const uint32_t r1 = pack2(o8[2 * np][2] * inv1, o8[2 * np][3] * inv1);
+                const uint32_t r2 = pack2(o8[2 * np + 1][0] * inv0, o8[2 * np + 1][1] * inv0);
+                const uint32_t r3 = pack2(o8[2 * np + 1][2] * inv1, o8[2 * np + 1][3] * inv1);
+                stsm_x4(uQ + swz(qs_row, 2 * np + (lane >> 4)), r0, r1, r2, r3);
             }
         }
+        fence_async_smem();   // the output rows are read next by the TMA store
         __syncthreads();
+        if (tid == 0) {
+            tma_store_2d(&mapO, uQ, 0, head * N);
+            bulk_commit();
+            const int nxt = head + gridDim.x;
+            if (nxt < BH) {
+                mbar_expect_tx(uBar, bytes_per_head);
+                tma_load_2d(uK, &mapK, 0, nxt * N, uBar);
+                tma_load_2d(uV, &mapV, 0, nxt * N, uBar);
+                bulk_wait_read0();   // the output tile has left Q's buffer
+                tma_load_2d(uQ, &mapQ, 0, nxt * N, uBar);
+            }
+        }
     }
+    if (tid == 0) bulk_wait0();
 }
 
 }  // namespace fz
@@ -686,35 +797,69 @@ static bool make_map(CUtensorMap* map, const void* base, int rows, int box_rows)
 bool fused_supported(const Shape& s, mita_dtype_t dtype) {
     if (dtype != MITA_BF16 || s.d != fz::kD) return false;
     if (s.N > fz::kMaxN || s.m > fz::kSlots || s.k > fz::kSlots) return false;
-    return fz::make_layout(s.N).total <= fz::kMaxSmem;
+    return fz::make_layout(s.N, s.m).total <= fz::kMaxSmem;
+}
+
+template <int NV>
+static cudaError_t launch_nv(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                             const CUtensorMap& mo, const fz::Params& prm, int device, cudaStream_t st) {
+    auto kern = fz::fused_kernel<NV>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, prm.L.total);
+    if (e != cudaSuccess) return e;
+    int sms = 0, per_sm = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, fz::kThreads, prm.L.total);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    const int slots = sms * per_sm;
+    const int grid = prm.s.BH() < slots ? prm.s.BH() : slots;
+    kern<<<grid, fz::kThreads, prm.L.total, st>>>(mq, mk, mv, mo, prm);
+    return cudaGetLastError();
 }
 
 cudaError_t run_fused(mita_plan_s* p, const void* Q, const void* K, const void* V, void* out, int32_t* idx,
                       int32_t* route, int keep_landmarks, cudaStream_t st) {
     const Shape& s = p->s;
     const int rows = s.BH() * s.N;
-    CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, Q, rows, s.N) || !make_map(&mk, K, rows, s.N) || !make_map(&mv, V, rows, s.N))
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_map(&mq, Q, rows, s.N) || !make_map(&mk, K, rows, s.N) || !make_map(&mv, V, rows, s.N) ||
+        !make_map(&mo, out, rows, s.N))
         return cudaErrorInvalidValue;
     fz::Params prm{};
     prm.s = s;
-    prm.L = fz::make_layout(s.N);
-    prm.out = (__nv_bfloat16*)out;
+    prm.L = fz::make_layout(s.N, s.m);
     prm.idx = idx;
     prm.route = route;
     prm.Ql_keep = keep_landmarks ? (__nv_bfloat16*)p->Ql : nullptr;
     prm.Vl_keep = keep_landmarks ? (__nv_bfloat16*)p->Vl : nullptr;
     prm.status = p->status;
     prm.scale_log2 = kLog2e / sqrtf((float)s.d);
-    int sms = 0;
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
-    cudaError_t e = cudaFuncSetAttribute(fz::fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         prm.L.total);
-    if (e != cudaSuccess) return e;
-    const int grid = s.BH() < sms ? s.BH() : sms;
-    fz::fused_kernel<<<grid, fz::kThreads, prm.L.total, st>>>(mq, mk, mv, prm);
+    for (int i = 0; i < s.m; ++i) {
+        // adaptive average pooling bins [floor(r*G/P), ceil((r+1)*G/P)) per axis
+        const int r = i / s.pw, c = i % s.pw;
+        const int r0 = r * s.gh / s.ph, r1 = ((r + 1) * s.gh + s.ph - 1) / s.ph;
+        const int c0 = c * s.gw / s.pw, c1 = ((c + 1) * s.gw + s.pw - 1) / s.pw;
+        prm.rows[i] = (uint32_t)r0 | ((uint32_t)r1 << 16);
+        prm.cols[i] = (uint32_t)c0 | ((uint32_t)c1 << 16);
+        const int n = (r1 - r0) * (c1 - c0);
+        int lg = 0;
+        while ((1 << lg) < n) ++lg;
+        prm.rcnt[i] = 1.0f / (float)n;
+        prm.win[i] = 16 - lg;
+    }
+    cudaError_t e;
+    switch ((s.N + 31) / 32) {
+        case 1: e = launch_nv<1>(mq, mk, mv, mo, prm, p->device, st); break;
+        case 2: e = launch_nv<2>(mq, mk, mv, mo, prm, p->device, st); break;
+        case 3: e = launch_nv<3>(mq, mk, mv, mo, prm, p->device, st); break;
+        case 4: e = launch_nv<4>(mq, mk, mv, mo, prm, p->device, st); break;
+        case 5: e = launch_nv<5>(mq, mk, mv, mo, prm, p->device, st); break;
+        case 6: e = launch_nv<6>(mq, mk, mv, mo, prm, p->device, st); break;
+        case 7: e = launch_nv<7>(mq, mk, mv, mo, prm, p->device, st); break;
+        default: e = launch_nv<8>(mq, mk, mv, mo, prm, p->device, st); break;
+    }
     p->launches += 1;
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace mita
