@@ -107,16 +107,19 @@ const char* mita_strerror(int code);
  *                            built path for the shape; MITA_PATH_STAGED
  *                            forces the stage-by-stage kernels;
  *                            MITA_PATH_FUSED forces the one-kernel path for
- *                            short sequences (MITA_ERR_UNSUPPORTED at
- *                            forward time if the shape does not fit it).
+ *                            short sequences and MITA_PATH_TILED the
+ *                            tensor-core kernel chain for long ones
+ *                            (MITA_ERR_UNSUPPORTED at forward time if the
+ *                            shape does not fit the forced path).
  *   MITA_OPT_KEEP_LANDMARKS  1: mita_forward also stores Q_l and V_l in the
  *                            workspace for mita_get_landmarks(). */
 typedef enum { MITA_OPT_PATH = 0, MITA_OPT_KEEP_LANDMARKS = 1 } mita_option_t;
-typedef enum { MITA_PATH_AUTO = 0, MITA_PATH_STAGED = 1, MITA_PATH_FUSED = 2 } mita_path_t;
+typedef enum { MITA_PATH_AUTO = 0, MITA_PATH_STAGED = 1, MITA_PATH_FUSED = 2, MITA_PATH_TILED = 3 } mita_path_t;
 int mita_set_option(mita_plan_t plan, int option, int value);
 
 /* Path the next mita_forward() will take (a mita_path_t value other than
- * AUTO), or a negative status on error. */
+ * AUTO), or a negative status on error: -MITA_ERR_UNSUPPORTED when a forced
+ * path does not fit the plan's shape. */
 int mita_get_path(mita_plan_t plan);
 
 /* Copy the landmark queries Q_l and landmark values V_l of the last forward

@@ -18,8 +18,8 @@ MITA_OK = 0
 STATUS = {0: "MITA_OK", 1: "MITA_ERR_INVALID_ARG", 2: "MITA_ERR_UNSUPPORTED", 3: "MITA_ERR_CUDA",
           4: "MITA_ERR_TIMEOUT", 5: "MITA_ERR_OOM", 6: "MITA_ERR_DEVICE"}
 OPT_PATH, OPT_KEEP_LANDMARKS = 0, 1
-PATH_AUTO, PATH_STAGED, PATH_FUSED = 0, 1, 2
-PATH_NAMES = {PATH_STAGED: "staged", PATH_FUSED: "fused"}
+PATH_AUTO, PATH_STAGED, PATH_FUSED, PATH_TILED = 0, 1, 2, 3
+PATH_NAMES = {PATH_STAGED: "staged", PATH_FUSED: "fused", PATH_TILED: "tiled"}
 
 # Every entry point declared in include/mita.h.
 EXPORTS = ("mita_plan", "mita_forward", "mita_get_status", "mita_destroy", "mita_strerror",
@@ -118,7 +118,8 @@ class Plan:
         _check(self.lib.mita_set_option(self.handle, option, value), "mita_set_option")
 
     def set_path(self, path: str):
-        self.set_option(OPT_PATH, {"auto": PATH_AUTO, "staged": PATH_STAGED, "fused": PATH_FUSED}[path])
+        self.set_option(OPT_PATH, {"auto": PATH_AUTO, "staged": PATH_STAGED, "fused": PATH_FUSED,
+                                  "tiled": PATH_TILED}[path])
 
     @property
     def path(self) -> str:

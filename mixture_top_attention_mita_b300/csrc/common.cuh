@@ -114,5 +114,11 @@ struct mita_plan_s {
     int32_t* offsets;      // [BH, m + 1]
     int32_t* perm;         // [BH, N]
     int32_t* status;       // [1]
+    // tiled path only (null otherwise)
+    uint32_t* rowmax;      // [BH, m]   order key of each landmark's largest raw score
+    float* vpart;          // [BH, splits, m, d + 1] landmark-value partials
+    int32_t* cursor;       // [BH, m]   bucket scatter cursors
+    int32_t* tiles;        // [BH, max tiles] attention tiles (expert << 16 | chunk)
+    int32_t* ntiles;       // [BH]
     uint64_t launches;     // kernels launched so far
 };

@@ -37,7 +37,7 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kD = 64;
 constexpr int kSlots = 32;      // shared slots (m <= 32) and routed slots (k <= 32)
 constexpr int kMaxN = 256;
-constexpr int kBins = 64;       // histogram bins of the select
+constexpr int kBins = 128;      // histogram bins of the select
 constexpr int kCand = 32;       // boundary-bin members resolved by exact rank
 constexpr int kTile = 16;       // queries per attention tile
 constexpr int kMaxSmem = 232448;
@@ -207,6 +207,17 @@ MITA_DEV __nv_bfloat16 round_mean(float hi, float lo, float c, float rc) {
     return neg ? __hneg(r) : r;
 }
 
+// Exclusive prefix sum of one int per lane over the warp.
+MITA_DEV int warp_excl_scan(int x, int lane) {
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    return incl - x;
+}
+
 MITA_DEV uint32_t umax16x2(uint32_t a, uint32_t b) {
     uint32_t y;
     asm("max.u16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
@@ -324,19 +335,21 @@ __global__ void __launch_bounds__(kThreads, 2)
                                 (int)((mag_hi >> 7) & 0xffu) - (int)((mag_lo >> 7) & 0xffu) <= win;
             const bool exact1 = (mag_lo >> 16) != 0u &&
                                 (int)((mag_hi >> 23) & 0xffu) - (int)((mag_lo >> 23) & 0xffu) <= win;
-            float h0 = s0, l0 = 0.0f, h1 = s1, l1 = 0.0f;
+            const float cnt = (float)((r1 - r0) * (c1 - c0)), rc = P.rcnt[i];
+            __nv_bfloat16 q0 = round_mean(s0, 0.0f, cnt, rc);
+            __nv_bfloat16 q1 = round_mean(s1, 0.0f, cnt, rc);
             if (!exact0 || !exact1) {
-                h0 = l0 = h1 = l1 = 0.0f;
+                // rare: sum the bin again error-free (TwoSum pairs)
+                float h0 = 0.0f, l0 = 0.0f, h1 = 0.0f, l1 = 0.0f;
                 for (int y = r0; y < r1; ++y)
                     for (int x = c0; x < c1; ++x) {
                         const uint32_t v = *(const uint32_t*)(Qb + swz(y * s.gw + x, chunk) + lo_off);
                         acc2(h0, l0, bf_lo(v));
                         acc2(h1, l1, bf_hi(v));
                     }
+                if (!exact0) q0 = round_mean(h0, l0, cnt, rc);
+                if (!exact1) q1 = round_mean(h1, l1, cnt, rc);
             }
-            const float cnt = (float)((r1 - r0) * (c1 - c0)), rc = P.rcnt[i];
-            const __nv_bfloat16 q0 = round_mean(h0, l0, cnt, rc);
-            const __nv_bfloat16 q1 = round_mean(h1, l1, cnt, rc);
             __nv_bfloat162 q2;
             q2.x = q0;
             q2.y = q1;
@@ -419,15 +432,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         __syncthreads();
 
-        // ---------------- phase C: experts and numerators (warp per landmark)
+        // ---------------- phase C: experts and numerators (warp per landmark;
+        // lane L owns keys [NV*L, NV*L + NV) of the landmark's row)
         for (int i = warp; i < m; i += kWarps) {
             float* srow = S_s + i * L.sstr;
+            const int j0 = NV * lane;
+            const int nval = max(0, min(NV, N - j0));   // valid keys of this lane
             float v[NV];
 #pragma unroll
-            for (int u = 0; u < NV; ++u) {
-                const int j = lane + 32 * u;
-                v[u] = srow[j < N ? j : 0];   // a slot past N repeats key 0: max / min unchanged
-            }
+            for (int u = 0; u < NV; ++u) v[u] = srow[u < nval ? j0 + u : 0];   // key 0 pads: max / min unchanged
             float mx = v[0], mn = v[0];
 #pragma unroll
             for (int u = 1; u < NV; u += 2) {
@@ -446,69 +459,72 @@ __global__ void __launch_bounds__(kThreads, 2)
             int bin[NV];
 #pragma unroll
             for (int u = 0; u < NV; ++u) {
-                const int j = lane + 32 * u;
-                bin[u] = -1;
-                if (j < N) {
-                    bin[u] = min(kBins - 1, (int)((v[u] - mn) * sc));
-                    atomicAdd(&hist[bin[u]], 1);
-                }
+                bin[u] = min(kBins - 1, (int)((v[u] - mn) * sc));
+                if (u < nval) atomicAdd(&hist[bin[u]], 1);
+                else bin[u] = -1;
             }
             __syncwarp();
-            // lane L holds bins 2L, 2L+1; suffix counts from the top bin down
-            const int2 hw = *(const int2*)(hist + 2 * lane);
-            *(int2*)(hist + 2 * lane) = make_int2(0, 0);   // each lane clears what it read
-            const int tot = hw.x + hw.y;
+            // lane L holds bins 4L .. 4L+3; suffix counts from the top bin down
+            const int4 hw = *(const int4*)(hist + 4 * lane);
+            *(int4*)(hist + 4 * lane) = make_int4(0, 0, 0, 0);   // each lane clears what it read
+            const int hc[4] = {hw.x, hw.y, hw.z, hw.w};
+            const int tot = hw.x + hw.y + hw.z + hw.w;
             int suf = tot;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_down_sync(0xffffffffu, suf, o);
                 if (lane + o < 32) suf += y;
             }
-            const int above = suf - tot;   // members of bins above 2L+1
+            const int above = suf - tot;   // members of bins above 4L+3
             const bool mine = above < k && suf >= k;
             int bstar = 0, need = 0, cstar = 0;
             if (mine) {
-                if (above + hw.y >= k) {
-                    bstar = 2 * lane + 1;
-                    need = k - above;
-                    cstar = hw.y;
-                } else {
-                    bstar = 2 * lane;
-                    need = k - above - hw.y;
-                    cstar = hw.x;
+                int run = above;
+#pragma unroll
+                for (int u = 3; u >= 0; --u) {
+                    if (need == 0 && run + hc[u] >= k) {
+                        bstar = 4 * lane + u;
+                        need = k - run;
+                        cstar = hc[u];
+                    }
+                    run += hc[u];
                 }
             }
             const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
             bstar = __shfl_sync(0xffffffffu, bstar, src);
             need = __shfl_sync(0xffffffffu, need, src);
             cstar = __shfl_sync(0xffffffffu, cstar, src);
-            // boundary bin: take the `need` best of its `cstar` members
-            uint32_t bsel = 0;   // bit u: member lane + 32u is taken
-            if (need < cstar) {
-                if (cstar <= kCand) {
-                    // members to lanes 0 .. cstar-1, exact rank by (score desc, index asc)
-                    int base = 0, slot[NV];
+            uint32_t selm = 0, bmem = 0;   // bit u: key j0+u selected / in the boundary bin
 #pragma unroll
-                    for (int u = 0; u < NV; ++u) {
-                        const bool isb = bin[u] == bstar;
-                        const unsigned bal = __ballot_sync(0xffffffffu, isb);
-                        slot[u] = base + __popc(bal & ((1u << lane) - 1u));
-                        if (isb) cand[slot[u]] = make_float2(v[u], __int_as_float(lane + 32 * u));
-                        base += __popc(bal);
-                    }
-                    __syncwarp();
-                    const float2 me = cand[lane < cstar ? lane : 0];
-                    const int jm = __float_as_int(me.y);
-                    int rank = 0;
-                    for (int e = 0; e < cstar; ++e) {
-                        const float ve = __shfl_sync(0xffffffffu, me.x, e);
-                        const int je = __shfl_sync(0xffffffffu, jm, e);
-                        rank += (ve > me.x || (ve == me.x && je < jm)) ? 1 : 0;
-                    }
-                    const unsigned chosen = __ballot_sync(0xffffffffu, lane < cstar && rank < need);
+            for (int u = 0; u < NV; ++u) {
+                selm |= (bin[u] > bstar ? 1u : 0u) << u;
+                bmem |= (bin[u] == bstar ? 1u : 0u) << u;
+            }
+            // boundary bin: take the `need` best of its `cstar` members
+            if (need < cstar) {
+                // members in ascending key order: lane L's members follow those of lanes < L
+                const int bbase = warp_excl_scan(__popc(bmem), lane);
+                if (cstar <= kCand) {
+                    int r = bbase;
 #pragma unroll
                     for (int u = 0; u < NV; ++u)
-                        if (bin[u] == bstar && ((chosen >> slot[u]) & 1u)) bsel |= 1u << u;
+                        if ((bmem >> u) & 1u) cand[r++] = make_float2(v[u], 0.0f);
+                    __syncwarp();
+                    // exact rank by (score desc, key asc); member order is key order
+                    const float me = cand[lane < cstar ? lane : 0].x;
+                    int rank = 0;
+                    for (int e = 0; e < cstar; ++e) {
+                        const float ve = __shfl_sync(0xffffffffu, me, e);
+                        rank += (ve > me || (ve == me && e < lane)) ? 1 : 0;
+                    }
+                    const unsigned chosen = __ballot_sync(0xffffffffu, lane < cstar && rank < need);
+                    r = bbase;
+#pragma unroll
+                    for (int u = 0; u < NV; ++u)
+                        if ((bmem >> u) & 1u) {
+                            selm |= ((chosen >> r) & 1u) << u;
+                            ++r;
+                        }
                     __syncwarp();
                 } else {
                     // many members (degenerate scores): bisect the order key
@@ -520,48 +536,47 @@ __global__ void __launch_bounds__(kThreads, 2)
                         const uint32_t cand_t = T | (1u << b);
                         int c = 0;
 #pragma unroll
-                        for (int u = 0; u < NV; ++u) c += (bin[u] == bstar && key[u] >= cand_t) ? 1 : 0;
+                        for (int u = 0; u < NV; ++u) c += (((bmem >> u) & 1u) && key[u] >= cand_t) ? 1 : 0;
                         c = __reduce_add_sync(0xffffffffu, c);
                         if (c >= need) T = cand_t;
                     }
-                    int gt = 0;
-#pragma unroll
-                    for (int u = 0; u < NV; ++u) gt += (bin[u] == bstar && key[u] > T) ? 1 : 0;
-                    gt = __reduce_add_sync(0xffffffffu, gt);
-                    int eq_left = need - gt, base = 0;
+                    int gt = 0, eq = 0;
 #pragma unroll
                     for (int u = 0; u < NV; ++u) {
-                        const bool isb = bin[u] == bstar;
-                        const bool eq = isb && key[u] == T;
-                        const unsigned bal = __ballot_sync(0xffffffffu, eq);
-                        const int r = base + __popc(bal & ((1u << lane) - 1u));
-                        if ((isb && key[u] > T) || (eq && r < eq_left)) bsel |= 1u << u;
-                        base += __popc(bal);
+                        const bool isb = (bmem >> u) & 1u;
+                        gt += (isb && key[u] > T) ? 1 : 0;
+                        eq += (isb && key[u] == T) ? 1 : 0;
+                    }
+                    gt = __reduce_add_sync(0xffffffffu, gt);
+                    int r = warp_excl_scan(eq, lane);   // ties at T: lower keys first
+                    const int eq_left = need - gt;
+#pragma unroll
+                    for (int u = 0; u < NV; ++u) {
+                        const bool isb = (bmem >> u) & 1u;
+                        if (isb && key[u] > T) selm |= 1u << u;
+                        if (isb && key[u] == T) {
+                            if (r < eq_left) selm |= 1u << u;
+                            ++r;
+                        }
                     }
                 }
             } else {
-#pragma unroll
-                for (int u = 0; u < NV; ++u)
-                    if (bin[u] == bstar) bsel |= 1u << u;
+                selm |= bmem;
             }
             // the expert in ascending key order
-            int pos = 0;
+            int pos = warp_excl_scan(__popc(selm), lane);
             uint8_t* irow = idx_s + i * kSlots;
 #pragma unroll
-            for (int u = 0; u < NV; ++u) {
-                const bool sel = bin[u] > bstar || (bsel >> u & 1u);
-                const unsigned bal = __ballot_sync(0xffffffffu, sel);
-                if (sel) irow[pos + __popc(bal & ((1u << lane) - 1u))] = (uint8_t)(lane + 32 * u);
-                pos += __popc(bal);
-            }
+            for (int u = 0; u < NV; ++u)
+                if ((selm >> u) & 1u) irow[pos++] = (uint8_t)(j0 + u);
             // softmax numerators of the landmark row, bf16 as the MMA reads them,
             // written over the row's own scores (every lane has read them)
             __nv_bfloat16* prow = (__nv_bfloat16*)srow;
             const float mb = mx * cs;
 #pragma unroll
             for (int u = 0; u < NV; ++u) {
-                const int j = lane + 32 * u;
-                if (j < L.np16) prow[j] = __float2bfloat16_rn(j < N ? ex2(fmaf(v[u], cs, -mb)) : 0.0f);
+                const int j = j0 + u;
+                if (j < L.np16) prow[j] = __float2bfloat16_rn(u < nval ? ex2(fmaf(v[u], cs, -mb)) : 0.0f);
             }
             __syncwarp();
             if (lane < k) P.idx[((size_t)head * m + i) * k + lane] = irow[lane];

@@ -7,6 +7,7 @@
 #include "common.cuh"
 #include "fused.cuh"
 #include "staged.cuh"
+#include "tiled.cuh"
 
 using mita::Shape;
 
@@ -17,9 +18,10 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 int resolve_path(const mita_plan_s* p) {
-    if (p->path_opt == MITA_PATH_STAGED) return MITA_PATH_STAGED;
-    if (p->path_opt == MITA_PATH_FUSED) return MITA_PATH_FUSED;
-    return mita::fused_supported(p->s, p->dtype) ? MITA_PATH_FUSED : MITA_PATH_STAGED;
+    if (p->path_opt != MITA_PATH_AUTO) return p->path_opt;
+    if (mita::fused_supported(p->s, p->dtype)) return MITA_PATH_FUSED;
+    if (mita::tiled_supported(p->s, p->dtype)) return MITA_PATH_TILED;
+    return MITA_PATH_STAGED;
 }
 
 }  // namespace
@@ -68,6 +70,12 @@ int mita_plan(mita_plan_t* plan, int B, int H, int N, int d, mita_grid_t grid, i
     const size_t oIdx = take(BH * m * (size_t)k * 4), oRoute = take(BH * (size_t)N * 4);
     const size_t oCnt = take(BH * m * 4), oOff = take(BH * (m + 1) * 4), oPerm = take(BH * (size_t)N * 4);
     const size_t oStatus = take(256);
+    const bool tiled = mita::tiled_supported(p->s, dtype);
+    const size_t oRowmax = take(tiled ? BH * m * 4 : 0);
+    const size_t oVpart = take(tiled ? mita::tiled_part_bytes(p->s) : 0);
+    const size_t oCursor = take(tiled ? BH * m * 4 : 0);
+    const size_t oTiles = take(tiled ? BH * (size_t)mita::tiled_max_tiles(p->s) * 4 : 0);
+    const size_t oNtiles = take(tiled ? BH * 4 : 0);
     p->ws_bytes = off;
     if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -84,6 +92,13 @@ int mita_plan(mita_plan_t* plan, int B, int H, int N, int d, mita_grid_t grid, i
     p->offsets = (int32_t*)(b + oOff);
     p->perm = (int32_t*)(b + oPerm);
     p->status = (int32_t*)(b + oStatus);
+    if (tiled) {
+        p->rowmax = (uint32_t*)(b + oRowmax);
+        p->vpart = (float*)(b + oVpart);
+        p->cursor = (int32_t*)(b + oCursor);
+        p->tiles = (int32_t*)(b + oTiles);
+        p->ntiles = (int32_t*)(b + oNtiles);
+    }
     if (cudaMemset(p->status, 0, 256) != cudaSuccess) {
         cudaFree(p->ws);
         free(p);
@@ -96,7 +111,8 @@ int mita_plan(mita_plan_t* plan, int B, int H, int N, int d, mita_grid_t grid, i
 int mita_set_option(mita_plan_t p, int option, int value) {
     if (!p) return MITA_ERR_INVALID_ARG;
     if (option == MITA_OPT_PATH) {
-        if (value != MITA_PATH_AUTO && value != MITA_PATH_STAGED && value != MITA_PATH_FUSED)
+        if (value != MITA_PATH_AUTO && value != MITA_PATH_STAGED && value != MITA_PATH_FUSED &&
+            value != MITA_PATH_TILED)
             return MITA_ERR_INVALID_ARG;
         p->path_opt = value;
         return MITA_OK;
@@ -111,7 +127,10 @@ int mita_set_option(mita_plan_t p, int option, int value) {
 
 int mita_get_path(mita_plan_t p) {
     if (!p) return -MITA_ERR_INVALID_ARG;
-    return resolve_path(p);
+    const int path = resolve_path(p);
+    if (path == MITA_PATH_FUSED && !mita::fused_supported(p->s, p->dtype)) return -MITA_ERR_UNSUPPORTED;
+    if (path == MITA_PATH_TILED && !p->rowmax) return -MITA_ERR_UNSUPPORTED;
+    return path;
 }
 
 int mita_forward(mita_plan_t p, const void* Q, const void* K, const void* V, void* out, int32_t* expert_idx,
@@ -127,11 +146,14 @@ int mita_forward(mita_plan_t p, const void* Q, const void* K, const void* V, voi
     if (path == MITA_PATH_FUSED) {
         if (!mita::fused_supported(p->s, p->dtype)) return MITA_ERR_UNSUPPORTED;
         err = mita::run_fused(p, Q, K, V, out, idx, rt, p->keep_landmarks, st);
+    } else if (path == MITA_PATH_TILED) {
+        if (!p->rowmax) return MITA_ERR_UNSUPPORTED;
+        err = mita::run_tiled(p, Q, K, V, out, idx, rt, st);
     } else {
         err = mita::run_staged(p, Q, K, V, out, idx, rt, st);
     }
     if (err != cudaSuccess) return MITA_ERR_CUDA;
-    p->landmarks_valid = p->keep_landmarks || path == MITA_PATH_STAGED;
+    p->landmarks_valid = p->keep_landmarks || path != MITA_PATH_FUSED;
     return MITA_OK;
 }
 

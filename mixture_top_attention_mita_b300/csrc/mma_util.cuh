@@ -1,0 +1,71 @@
+// Warp-level tensor-core and shared-memory helpers (inline PTX) used by the
+// tiled kernels: ldmatrix / stmatrix, bf16 m16n8k16 MMA with fp32
+// accumulation, cp.async copies and a few single-instruction math helpers.
+#pragma once
+
+#include "common.cuh"
+
+namespace mita {
+namespace mx {
+
+MITA_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// Byte offset of 16-byte chunk c of row r in a tile of RB-byte rows whose
+// chunks are XOR-swizzled by the row's low three bits: every 8 x 16-byte
+// ldmatrix / stmatrix access over 8 consecutive rows is bank-conflict free.
+template <int RB>
+MITA_DEV uint32_t swz(int r, int c) { return (uint32_t)(r * RB + ((c ^ (r & 7)) << 4)); }
+
+MITA_DEV void ldsm_x4(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a));
+}
+MITA_DEV void ldsm_x4_t(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a));
+}
+MITA_DEV void stsm_x4(uint32_t a, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};\n"
+                 ::"r"(a), "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
+}
+// D += A . B for a 16x16 (row) bf16 A, a 16x8 (column) bf16 B and fp32 D.
+MITA_DEV void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                       uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+constexpr uint32_t kOnes2 = 0x3F803F80u;   // bf16 pair (1, 1)
+
+MITA_DEV uint32_t pack2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+MITA_DEV float ex2(float x) {   // hardware 2^x (PTX ex2.approx), -inf -> 0
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+MITA_DEV float rcp(float x) {   // hardware reciprocal (PTX rcp.approx)
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// Inverse of order_key().
+MITA_DEV float key_to_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// 16-byte global -> shared copy; src_bytes = 0 fills the destination with zeros.
+MITA_DEV void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+MITA_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+MITA_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+}  // namespace mx
+}  // namespace mita

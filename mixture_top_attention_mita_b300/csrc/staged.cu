@@ -433,6 +433,19 @@ static cudaError_t run_staged_t(mita_plan_s* p, const T* Q, const T* K, const T*
     return cudaGetLastError();
 }
 
+cudaError_t staged_pool(const Shape& s, mita_dtype_t dtype, const void* Q, void* Ql, cudaStream_t st) {
+    if (dtype == MITA_BF16)
+        pool_kernel<__nv_bfloat16><<<dim3(s.m, s.BH()), s.d, 0, st>>>(s, (const __nv_bfloat16*)Q, (__nv_bfloat16*)Ql);
+    else
+        pool_kernel<float><<<dim3(s.m, s.BH()), s.d, 0, st>>>(s, (const float*)Q, (float*)Ql);
+    return cudaGetLastError();
+}
+
+cudaError_t staged_topk(const Shape& s, const float* S, int32_t* idx, cudaStream_t st) {
+    topk_kernel<<<dim3(s.m, s.BH()), kTopkThreads, 0, st>>>(s, S, idx);
+    return cudaGetLastError();
+}
+
 cudaError_t run_staged(mita_plan_s* p, const void* Q, const void* K, const void* V, void* out, int32_t* idx,
                        int32_t* route, cudaStream_t st) {
     if (p->dtype == MITA_BF16) {

@@ -1,0 +1,552 @@
+// Tensor-core tiled MiTA forward for long sequences (bf16, d in {64, 128},
+// m <= 256, k <= 512): the 56x56 vision layer and the 64K-token sequence.
+//
+// The steps of the operator (36Kr / 新智元 "注意力也是FFN？", section
+// "用少量地标查询，同时构造全局概括与细节专家") as a chain of kernels on one
+// stream, every contraction on bf16 mma.sync with fp32 accumulation:
+//   pool            Q_l, correctly rounded bin means (shared with the staged path)
+//   tl_scores       S = Q_l . K^T (fp32, workspace) and each landmark's row max
+//   topk            per landmark the k best keys, exact radix select over S
+//                   (shared with the staged path)
+//   tl_values       split-K partial sums of exp(S / sqrt d - max) . V and of
+//                   the row sums, per 1024-key split
+//   tl_values_fin   V_l = sum of partials / sum of row sums, bf16
+//   tl_route        q . Q_l^T per query tile, first argmax (the route), and
+//                   per-landmark query counts
+//   tl_bucket_off   per head: bucket offsets, cursors and the list of
+//                   (expert, 64-query chunk) attention tiles
+//   tl_bucket_put   queries scattered to their bucket
+//   tl_attend       per tile: the 64 queries of one expert against the m
+//                   shared slots (Q_l, V_l) and the k routed slots (the
+//                   expert's K, V rows), streamed through shared memory in
+//                   64-slot blocks with an online softmax
+#include "mma_util.cuh"
+#include "staged.cuh"
+#include "tiled.cuh"
+
+namespace mita {
+namespace tl {
+
+using bf16 = __nv_bfloat16;
+using namespace mx;
+
+constexpr int kKC = 1024;   // keys per tl_values split
+constexpr int kQT = 64;     // queries per attention tile (4 warps x 16)
+
+int nsplit(const Shape& s) { return (s.N + kKC - 1) / kKC; }
+int max_tiles(const Shape& s) { return (s.N + kQT - 1) / kQT + s.m; }
+
+// ---------------------------------------------------------------- scores
+// Block: 64 landmarks x 128 keys, 8 warps of 16 x 64.
+template <int D>
+__global__ void __launch_bounds__(256) tl_scores(Shape s, const bf16* __restrict__ Ql, const bf16* __restrict__ K,
+                                                 float* __restrict__ S, uint32_t* __restrict__ rowmax) {
+    constexpr int RB = 2 * D, CH = D / 8;
+    extern __shared__ __align__(128) unsigned char sm[];
+    const int n0 = blockIdx.x * 128, i0 = blockIdx.y * 64, bh = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const uint32_t uq = smem_u32(sm), uk = uq + 64 * RB;
+    const bf16* qsrc = Ql + (size_t)bh * s.m * D;
+    const bf16* ksrc = K + (size_t)bh * s.N * D;
+    for (int e = tid; e < 64 * CH; e += 256) {
+        const int r = e / CH, c = e % CH;
+        const bool ok = i0 + r < s.m;
+        cp_async16(uq + swz<RB>(r, c), qsrc + (size_t)(ok ? i0 + r : 0) * D + 8 * c, ok ? 16u : 0u);
+    }
+    for (int e = tid; e < 128 * CH; e += 256) {
+        const int r = e / CH, c = e % CH;
+        const bool ok = n0 + r < s.N;
+        cp_async16(uk + swz<RB>(r, c), ksrc + (size_t)(ok ? n0 + r : 0) * D + 8 * c, ok ? 16u : 0u);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+
+    const int mt = warp & 3, kh = warp >> 2;
+    const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, brow = (lane & 7) + (lane >> 4) * 8;
+    float acc[8][4];
+#pragma unroll
+    for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(uq + swz<RB>(mt * 16 + arow, 2 * kk + (lane >> 4)), a0, a1, a2, a3);
+#pragma unroll
+        for (int np = 0; np < 4; ++np) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(uk + swz<RB>(kh * 64 + np * 16 + brow, 2 * kk + ((lane >> 3) & 1)), b0, b1, b2, b3);
+            mma16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
+            mma16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int i = i0 + mt * 16 + g + 8 * h;
+        float mx = -INFINITY;
+        if (i < s.m) {
+            float* row = S + ((size_t)bh * s.m + i) * s.N;
+#pragma unroll
+            for (int n = 0; n < 8; ++n) {
+                const int j = n0 + kh * 64 + 8 * n + 2 * t;
+                if (j < s.N) {
+                    row[j] = acc[n][2 * h];
+                    mx = fmaxf(mx, acc[n][2 * h]);
+                }
+                if (j + 1 < s.N) {
+                    row[j + 1] = acc[n][2 * h + 1];
+                    mx = fmaxf(mx, acc[n][2 * h + 1]);
+                }
+            }
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        if (t == 0 && i < s.m && mx > -INFINITY) atomicMax(&rowmax[(size_t)bh * s.m + i], order_key(mx));
+    }
+}
+
+// ---------------------------------------------------------------- landmark values
+// Block: 64 landmarks x one split of kKC keys, in 64-key steps; 8 warps =
+// 4 landmark tiles x 2 feature halves.  Partials: [BH, nsplit, m, D + 1]
+// (the last column holds the row sum of the bf16 numerators).
+template <int D>
+__global__ void __launch_bounds__(256) tl_values(Shape s, const float* __restrict__ S,
+                                                 const uint32_t* __restrict__ rowmax, const bf16* __restrict__ V,
+                                                 float* __restrict__ part, float cs) {
+    constexpr int RB = 2 * D, CH = D / 8, NT = D / 16;   // NT: n8 feature tiles per warp
+    __shared__ __align__(128) unsigned char p_s[64 * 128];
+    __shared__ __align__(128) unsigned char v_s[64 * RB];
+    __shared__ float mb_s[64];
+    const int split = blockIdx.x, i0 = blockIdx.y * 64, bh = blockIdx.z, ns = gridDim.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const int jb0 = split * kKC, je = min(s.N, jb0 + kKC);
+    if (tid < 64) {
+        const int i = i0 + tid;
+        mb_s[tid] = i < s.m ? key_to_float(rowmax[(size_t)bh * s.m + i]) * cs : 0.0f;
+    }
+    const uint32_t up = smem_u32(p_s), uv = smem_u32(v_s);
+    const int mt = warp & 3, fh = warp >> 2;
+    const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, vrow = (lane & 7) + ((lane >> 3) & 1) * 8;
+    float o[NT][4], osum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
+    const bf16* vsrc = V + (size_t)bh * s.N * D;
+    for (int jb = jb0; jb < je; jb += 64) {
+        __syncthreads();   // the previous step's tiles are consumed (and mb_s is visible)
+        for (int e = tid; e < 64 * CH; e += 256) {
+            const int r = e / CH, c = e % CH;
+            const bool ok = jb + r < je;
+            cp_async16(uv + swz<RB>(r, c), vsrc + (size_t)(ok ? jb + r : 0) * D + 8 * c, ok ? 16u : 0u);
+        }
+        cp_async_commit();
+        // numerators: 64 rows x 64 keys, 4 consecutive keys per item
+        for (int e = tid; e < 64 * 16; e += 256) {
+            const int r = e >> 4, c4 = e & 15, i = i0 + r, j = jb + 4 * c4;
+            float p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (i < s.m) {
+                const float* row = S + ((size_t)bh * s.m + i) * s.N;
+                const float mb = mb_s[r];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (j + u < je) p[u] = ex2(fmaf(row[j + u], cs, -mb));
+            }
+            const uint2 pk = make_uint2(pack2(p[0], p[1]), pack2(p[2], p[3]));
+            *(uint2*)(p_s + swz<128>(r, c4 >> 1) + (c4 & 1) * 8) = pk;
+        }
+        cp_async_wait<0>();
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(up + swz<128>(mt * 16 + arow, 2 * kk + (lane >> 4)), a0, a1, a2, a3);
+            if (fh == 0) mma16816(osum, a0, a1, a2, a3, kOnes2, kOnes2);
+#pragma unroll
+            for (int np = 0; np < NT / 2; ++np) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(uv + swz<RB>(kk * 16 + vrow, fh * NT + 2 * np + (lane >> 4)), b0, b1, b2, b3);
+                mma16816(o[2 * np], a0, a1, a2, a3, b0, b1);
+                mma16816(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
+            }
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int i = i0 + mt * 16 + g + 8 * h;
+        if (i >= s.m) continue;
+        float* dst = part + (((size_t)bh * ns + split) * s.m + i) * (D + 1);
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const int f = fh * (D / 2) + 8 * n + 2 * t;
+            dst[f] = o[n][2 * h];
+            dst[f + 1] = o[n][2 * h + 1];
+        }
+        if (fh == 0 && t == 0) dst[D] = osum[2 * h];
+    }
+}
+
+// V_l[i] = (sum over splits of the partial row) / (sum of the partial row sums).
+template <int D>
+__global__ void tl_values_fin(Shape s, const float* __restrict__ part, int ns, bf16* __restrict__ Vl) {
+    const int i = blockIdx.x, bh = blockIdx.y, f = threadIdx.x;
+    const float* src = part + ((size_t)bh * ns * s.m + i) * (D + 1);
+    float num = 0.0f, den = 0.0f;
+    for (int sp = 0; sp < ns; ++sp) {
+        num += src[(size_t)sp * s.m * (D + 1) + f];
+        den += src[(size_t)sp * s.m * (D + 1) + D];
+    }
+    Vl[((size_t)bh * s.m + i) * D + f] = __float2bfloat16_rn(num / den);
+}
+
+// ---------------------------------------------------------------- route
+// Block: 128 queries (8 warps x 16) against all landmarks in groups of 64.
+template <int D>
+__global__ void __launch_bounds__(256) tl_route(Shape s, const bf16* __restrict__ Q, const bf16* __restrict__ Ql,
+                                                int32_t* __restrict__ route, int32_t* __restrict__ counts) {
+    constexpr int RB = 2 * D, CH = D / 8;
+    extern __shared__ __align__(128) unsigned char sm[];
+    __shared__ int hist[256];
+    const int q0 = blockIdx.x * 128, bh = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const int mp = (s.m + 63) / 64 * 64;   // landmark rows staged (zero past m)
+    const uint32_t uq = smem_u32(sm), ul = uq + 128 * RB;
+    const bf16* qsrc = Q + (size_t)bh * s.N * D;
+    const bf16* lsrc = Ql + (size_t)bh * s.m * D;
+    for (int e = tid; e < 128 * CH; e += 256) {
+        const int r = e / CH, c = e % CH;
+        const bool ok = q0 + r < s.N;
+        cp_async16(uq + swz<RB>(r, c), qsrc + (size_t)(ok ? q0 + r : 0) * D + 8 * c, ok ? 16u : 0u);
+    }
+    for (int e = tid; e < mp * CH; e += 256) {
+        const int r = e / CH, c = e % CH;
+        const bool ok = r < s.m;
+        cp_async16(ul + swz<RB>(r, c), lsrc + (size_t)(ok ? r : 0) * D + 8 * c, ok ? 16u : 0u);
+    }
+    cp_async_commit();
+    for (int e = tid; e < 256; e += 256) hist[e] = 0;
+    cp_async_wait<0>();
+    __syncthreads();
+
+    const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, brow = (lane & 7) + (lane >> 4) * 8;
+    uint32_t qa[D / 16][4];
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+        ldsm_x4(uq + swz<RB>(warp * 16 + arow, 2 * kk + (lane >> 4)), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+    float best[2] = {-INFINITY, -INFINITY};
+    int arg[2] = {0, 0};
+    for (int lg = 0; lg < mp; lg += 64) {
+        float acc[8][4];
+#pragma unroll
+        for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(ul + swz<RB>(lg + np * 16 + brow, 2 * kk + ((lane >> 3) & 1)), b0, b1, b2, b3);
+                mma16816(acc[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+                mma16816(acc[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+            }
+#pragma unroll
+        for (int n = 0; n < 8; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = lg + 8 * n + 2 * t + (e & 1);
+                const float v = acc[n][e];
+                if (i < s.m && v > best[e >> 1]) { best[e >> 1] = v; arg[e >> 1] = i; }
+            }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+            const float ob = __shfl_xor_sync(0xffffffffu, best[h], o);
+            const int oa = __shfl_xor_sync(0xffffffffu, arg[h], o);
+            if (ob > best[h] || (ob == best[h] && oa < arg[h])) { best[h] = ob; arg[h] = oa; }
+        }
+        const int q = q0 + warp * 16 + g + 8 * h;
+        if (t == 0 && q < s.N) {
+            route[(size_t)bh * s.N + q] = arg[h];
+            atomicAdd(&hist[arg[h]], 1);
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < s.m; i += 256)
+        if (hist[i]) atomicAdd(&counts[(size_t)bh * s.m + i], hist[i]);
+}
+
+// ---------------------------------------------------------------- buckets
+// One warp per head: bucket offsets (exclusive scan of the counts), the
+// scatter cursors and the attention tile list (expert << 16 | chunk).
+__global__ void tl_bucket_off(Shape s, const int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                              int32_t* __restrict__ cursor, int32_t* __restrict__ tiles,
+                              int32_t* __restrict__ ntiles, int maxt) {
+    const int bh = blockIdx.x, lane = threadIdx.x;
+    const int32_t* cnt = counts + (size_t)bh * s.m;
+    int carry = 0, tcarry = 0;
+    for (int i0 = 0; i0 < s.m; i0 += 32) {
+        const int i = i0 + lane;
+        const int c = i < s.m ? cnt[i] : 0, nt = (c + kQT - 1) / kQT;
+        int x = c, y = nt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int a = __shfl_up_sync(0xffffffffu, x, o), b = __shfl_up_sync(0xffffffffu, y, o);
+            if (lane >= o) { x += a; y += b; }
+        }
+        if (i < s.m) {
+            offsets[(size_t)bh * (s.m + 1) + i] = carry + x - c;
+            cursor[(size_t)bh * s.m + i] = carry + x - c;
+            for (int e = 0; e < nt; ++e) {
+                const int tt = tcarry + y - nt + e;
+                if (tt < maxt) tiles[(size_t)bh * maxt + tt] = (i << 16) | e;
+            }
+        }
+        carry += __shfl_sync(0xffffffffu, x, 31);
+        tcarry += __shfl_sync(0xffffffffu, y, 31);
+    }
+    if (lane == 0) {
+        offsets[(size_t)bh * (s.m + 1) + s.m] = carry;
+        ntiles[bh] = min(tcarry, maxt);
+    }
+}
+
+__global__ void tl_bucket_put(Shape s, const int32_t* __restrict__ route, int32_t* __restrict__ cursor,
+                              int32_t* __restrict__ perm, int32_t* __restrict__ status) {
+    const int bh = blockIdx.y, q = blockIdx.x * blockDim.x + threadIdx.x;
+    if (q >= s.N) return;
+    const int r = route[(size_t)bh * s.N + q];
+    if (r < 0 || r >= s.m) {
+        atomicExch(status, (int)MITA_ERR_DEVICE);
+        return;
+    }
+    const int pos = atomicAdd(&cursor[(size_t)bh * s.m + r], 1);
+    perm[(size_t)bh * s.N + pos] = q;
+}
+
+// ---------------------------------------------------------------- attention
+// Block: one tile = up to 64 queries of one expert (4 warps x 16 rows).
+// Slots 0..m-1 are the shared pairs (Q_l, V_l), slots m..m+k-1 the routed
+// pairs (K, V rows of the expert's keys); 64-slot blocks are staged by
+// cp.async into a double buffer and folded in by an online softmax.
+template <int D>
+__global__ void __launch_bounds__(128, 2)
+    tl_attend(Shape s, const bf16* __restrict__ Q, const bf16* __restrict__ K, const bf16* __restrict__ V,
+              const bf16* __restrict__ Ql, const bf16* __restrict__ Vl, const int32_t* __restrict__ idx,
+              const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm,
+              const int32_t* __restrict__ tiles, const int32_t* __restrict__ ntiles, int maxt,
+              bf16* __restrict__ out, float cs, int32_t* __restrict__ status) {
+    constexpr int RB = 2 * D, CH = D / 8, KS = D / 16, NT = D / 8;
+    extern __shared__ __align__(128) unsigned char sm[];
+    __shared__ int rows_s[kQT];
+    const int bh = blockIdx.y, tile = blockIdx.x;
+    if (tile >= ntiles[bh]) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, t = lane & 3;
+    const int e = tiles[(size_t)bh * maxt + tile] >> 16, chunk = tiles[(size_t)bh * maxt + tile] & 0xffff;
+    const int qstart = offsets[(size_t)bh * (s.m + 1) + e] + chunk * kQT;
+    const int nq = min(kQT, offsets[(size_t)bh * (s.m + 1) + e + 1] - qstart);
+    const int L = s.m + s.k, nblk = (L + 63) / 64;
+    const int32_t* E = idx + ((size_t)bh * s.m + e) * s.k;
+    const uint32_t uq = smem_u32(sm), ukv = uq + kQT * RB;   // kv buffer b: K at ukv + b*2*64*RB, V after it
+    const size_t hoff = (size_t)bh * s.N * D;
+    if (tid < kQT) {
+        int q = perm[(size_t)bh * s.N + qstart + min(tid, nq - 1)];
+        if (q < 0 || q >= s.N) { atomicExch(status, (int)MITA_ERR_DEVICE); q = 0; }
+        rows_s[tid] = q;
+    }
+    __syncthreads();
+    for (int x = tid; x < kQT * CH; x += 128) {
+        const int r = x / CH, c = x % CH;
+        cp_async16(uq + swz<RB>(r, c), Q + hoff + (size_t)rows_s[r] * D + 8 * c, 16u);
+    }
+    auto stage = [&](int b) {
+        const uint32_t kb = ukv + (uint32_t)(b & 1) * 2u * 64u * RB, vb = kb + 64u * RB;
+        for (int x = tid; x < 64 * CH; x += 128) {
+            const int r = x / CH, c = x % CH, slot = b * 64 + r;
+            const bf16 *ks, *vs;
+            uint32_t nbytes = 16u;
+            if (slot < s.m) {
+                ks = Ql + ((size_t)bh * s.m + slot) * D;
+                vs = Vl + ((size_t)bh * s.m + slot) * D;
+            } else if (slot < L) {
+                int j = E[slot - s.m];
+                if (j < 0 || j >= s.N) { atomicExch(status, (int)MITA_ERR_DEVICE); j = 0; }
+                ks = K + hoff + (size_t)j * D;
+                vs = V + hoff + (size_t)j * D;
+            } else {
+                ks = Ql;
+                vs = Vl;
+                nbytes = 0u;   // zero rows past the last slot
+            }
+            cp_async16(kb + swz<RB>(r, c), ks + 8 * c, nbytes);
+            cp_async16(vb + swz<RB>(r, c), vs + 8 * c, nbytes);
+        }
+        cp_async_commit();
+    };
+    stage(0);
+
+    const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, brow = (lane & 7) + (lane >> 4) * 8;
+    uint32_t qa[KS][4];
+    float o[NT][4], osum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
+    float m0 = -INFINITY, m1 = -INFINITY;   // running max (raw logits) of rows g, g+8
+    for (int b = 0; b < nblk; ++b) {
+        if (b + 1 < nblk) {
+            stage(b + 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        if (b == 0) {
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk)
+                ldsm_x4(uq + swz<RB>(warp * 16 + arow, 2 * kk + (lane >> 4)), qa[kk][0], qa[kk][1], qa[kk][2],
+                        qa[kk][3]);
+        }
+        const uint32_t kb = ukv + (uint32_t)(b & 1) * 2u * 64u * RB, vb = kb + 64u * RB;
+        float sc[8][4];
+#pragma unroll
+        for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.0f;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk)
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(kb + swz<RB>(np * 16 + brow, 2 * kk + ((lane >> 3) & 1)), b0, b1, b2, b3);
+                mma16816(sc[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+                mma16816(sc[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+            }
+        if (b * 64 + 64 > L) {   // padding slots of the last block
+#pragma unroll
+            for (int n = 0; n < 8; ++n)
+#pragma unroll
+                for (int x = 0; x < 4; ++x)
+                    if (b * 64 + 8 * n + 2 * t + (x & 1) >= L) sc[n][x] = -INFINITY;
+        }
+        float bm0 = -INFINITY, bm1 = -INFINITY;
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+            bm0 = fmaxf(bm0, fmaxf(sc[n][0], sc[n][1]));
+            bm1 = fmaxf(bm1, fmaxf(sc[n][2], sc[n][3]));
+        }
+#pragma unroll
+        for (int x = 1; x <= 2; x <<= 1) {
+            bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, x));
+            bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
+        }
+        const float n0 = fmaxf(m0, bm0), n1 = fmaxf(m1, bm1);
+        const float f0 = ex2((m0 - n0) * cs), f1 = ex2((m1 - n1) * cs);   // 0 on the first block
+        m0 = n0;
+        m1 = n1;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            o[n][0] *= f0;
+            o[n][1] *= f0;
+            o[n][2] *= f1;
+            o[n][3] *= f1;
+        }
+        osum[0] *= f0;
+        osum[1] *= f0;
+        osum[2] *= f1;
+        osum[3] *= f1;
+        const float mb0 = n0 * cs, mb1 = n1 * cs;
+        uint32_t pa[4][4];
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+            pa[n >> 1][(n & 1) * 2 + 0] = pack2(ex2(fmaf(sc[n][0], cs, -mb0)), ex2(fmaf(sc[n][1], cs, -mb0)));
+            pa[n >> 1][(n & 1) * 2 + 1] = pack2(ex2(fmaf(sc[n][2], cs, -mb1)), ex2(fmaf(sc[n][3], cs, -mb1)));
+        }
+        const int vrow = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            mma16816(osum, pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], kOnes2, kOnes2);
+#pragma unroll
+            for (int np = 0; np < NT / 2; ++np) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(vb + swz<RB>(ks * 16 + vrow, 2 * np + (lane >> 4)), b0, b1, b2, b3);
+                mma16816(o[2 * np], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], b0, b1);
+                mma16816(o[2 * np + 1], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], b2, b3);
+            }
+        }
+        __syncthreads();   // this buffer is restaged two blocks later
+    }
+    // normalise; the rows go over the warp's own query rows, then out
+    const float inv0 = rcp(osum[0]), inv1 = rcp(osum[2]);
+    const int srow = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+    for (int np = 0; np < NT / 2; ++np) {
+        const uint32_t r0 = pack2(o[2 * np][0] * inv0, o[2 * np][1] * inv0);
+        const uint32_t r1 = pack2(o[2 * np][2] * inv1, o[2 * np][3] * inv1);
+        const uint32_t r2 = pack2(o[2 * np + 1][0] * inv0, o[2 * np + 1][1] * inv0);
+        const uint32_t r3 = pack2(o[2 * np + 1][2] * inv1, o[2 * np + 1][3] * inv1);
+        stsm_x4(uq + swz<RB>(srow, 2 * np + (lane >> 4)), r0, r1, r2, r3);
+    }
+    __syncthreads();
+    for (int x = tid; x < nq * CH; x += 128) {
+        const int r = x / CH, c = x % CH;
+        *(uint4*)(out + hoff + (size_t)rows_s[r] * D + 8 * c) = *(const uint4*)(sm + swz<RB>(r, c));
+    }
+}
+
+template <int D>
+cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, bf16* out, int32_t* idx,
+                  int32_t* route, cudaStream_t st) {
+    const Shape& s = p->s;
+    const int BH = s.BH();
+    constexpr int RB = 2 * D;
+    const float cs = kLog2e / sqrtf((float)D);
+    bf16* Ql = (bf16*)p->Ql;
+    bf16* Vl = (bf16*)p->Vl;
+    cudaError_t err;
+    if ((err = cudaMemsetAsync(p->rowmax, 0, (size_t)BH * s.m * 4, st)) != cudaSuccess) return err;
+    if ((err = cudaMemsetAsync(p->counts, 0, (size_t)BH * s.m * 4, st)) != cudaSuccess) return err;
+    if ((err = staged_pool(s, MITA_BF16, Q, Ql, st)) != cudaSuccess) return err;
+    {
+        const int smem = (64 + 128) * RB;
+        auto kern = tl_scores<D>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        kern<<<dim3((s.N + 127) / 128, (s.m + 63) / 64, BH), 256, smem, st>>>(s, Ql, K, p->S, p->rowmax);
+    }
+    if ((err = staged_topk(s, p->S, idx, st)) != cudaSuccess) return err;
+    const int ns = nsplit(s);
+    tl_values<D><<<dim3(ns, (s.m + 63) / 64, BH), 256, 0, st>>>(s, p->S, p->rowmax, V, p->vpart, cs);
+    tl_values_fin<D><<<dim3(s.m, BH), D, 0, st>>>(s, p->vpart, ns, Vl);
+    {
+        const int smem = (128 + (s.m + 63) / 64 * 64) * RB;
+        auto kern = tl_route<D>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        kern<<<dim3((s.N + 127) / 128, BH), 256, smem, st>>>(s, Q, Ql, route, p->counts);
+    }
+    const int maxt = max_tiles(s);
+    tl_bucket_off<<<BH, 32, 0, st>>>(s, p->counts, p->offsets, p->cursor, p->tiles, p->ntiles, maxt);
+    tl_bucket_put<<<dim3((s.N + 255) / 256, BH), 256, 0, st>>>(s, route, p->cursor, p->perm, p->status);
+    {
+        const int smem = (kQT + 4 * 64) * RB;
+        auto kern = tl_attend<D>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        kern<<<dim3(maxt, BH), 128, smem, st>>>(s, Q, K, V, Ql, Vl, idx, p->offsets, p->perm, p->tiles, p->ntiles,
+                                                  maxt, out, cs, p->status);
+    }
+    p->launches += 9;
+    return cudaGetLastError();
+}
+
+}  // namespace tl
+
+bool tiled_supported(const Shape& s, mita_dtype_t dtype) {
+    return dtype == MITA_BF16 && (s.d == 64 || s.d == 128) && s.m <= 256 && s.k <= 512 && s.N < (1 << 24);
+}
+
+size_t tiled_part_bytes(const Shape& s) {
+    return (size_t)s.BH() * tl::nsplit(s) * s.m * (s.d + 1) * sizeof(float);
+}
+
+int tiled_max_tiles(const Shape& s) { return tl::max_tiles(s); }
+
+cudaError_t run_tiled(mita_plan_s* p, const void* Q, const void* K, const void* V, void* out, int32_t* idx,
+                      int32_t* route, cudaStream_t st) {
+    using T = __nv_bfloat16;
+    if (p->s.d == 64) return tl::run_t<64>(p, (const T*)Q, (const T*)K, (const T*)V, (T*)out, idx, route, st);
+    return tl::run_t<128>(p, (const T*)Q, (const T*)K, (const T*)V, (T*)out, idx, route, st);
+}
+
+}  // namespace mita

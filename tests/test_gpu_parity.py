@@ -19,7 +19,7 @@ from parity_util import compare_batch
 pytestmark = pytest.mark.gpu
 
 W = synth.WORKLOADS
-PATHS = ["staged", "fused"]
+PATHS = ["staged", "fused", "tiled"]
 
 
 def _run(w, Q, K, V, path="auto", keep=False):
@@ -45,15 +45,19 @@ def _run(w, Q, K, V, path="auto", keep=False):
     return res
 
 
-def _fused_ok(w):
+def _path_ok(w, path):
     plan = mita.Plan.for_workload(w.scaled(B=1, H=1))
-    plan.set_path("auto")
-    return plan.path == "fused"
+    plan.set_path(path)
+    return plan.lib.mita_get_path(plan.handle) >= 0
+
+
+def _fused_ok(w):
+    return _path_ok(w, "fused")
 
 
 def _skip_unbuilt(w, path):
-    if path == "fused" and not _fused_ok(w):
-        pytest.skip("no fused kernel for this shape")
+    if path != "staged" and not _path_ok(w, path):
+        pytest.skip(f"no {path} kernels for this shape")
 
 
 SMALL = {
