@@ -115,8 +115,8 @@ struct mita_plan_s {
     int32_t* perm;         // [BH, N]
     int32_t* status;       // [1]
     // tiled path only (null otherwise)
-    uint32_t* rowmax;      // [BH, m]   order key of each landmark's largest raw score
-    float* vpart;          // [BH, splits, m, d + 1] landmark-value partials
+    uint32_t* rowmax;      // [2, BH, m] order keys of each landmark's largest, then smallest, raw score
+    float* vpart;          // [head group, splits, m, d + 1] landmark-value partials
     int32_t* cursor;       // [BH, m]   bucket scatter cursors
     int32_t* tiles;        // [BH, max tiles] attention tiles (expert << 16 | chunk)
     int32_t* ntiles;       // [BH]

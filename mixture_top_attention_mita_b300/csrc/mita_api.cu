@@ -71,7 +71,7 @@ int mita_plan(mita_plan_t* plan, int B, int H, int N, int d, mita_grid_t grid, i
     const size_t oCnt = take(BH * m * 4), oOff = take(BH * (m + 1) * 4), oPerm = take(BH * (size_t)N * 4);
     const size_t oStatus = take(256);
     const bool tiled = mita::tiled_supported(p->s, dtype);
-    const size_t oRowmax = take(tiled ? BH * m * 4 : 0);
+    const size_t oRowmax = take(tiled ? 2 * BH * m * 4 : 0);   // row max, then row min
     const size_t oVpart = take(tiled ? mita::tiled_part_bytes(p->s) : 0);
     const size_t oCursor = take(tiled ? BH * m * 4 : 0);
     const size_t oTiles = take(tiled ? BH * (size_t)mita::tiled_max_tiles(p->s) * 4 : 0);

@@ -5,9 +5,12 @@
 // "用少量地标查询，同时构造全局概括与细节专家") as a chain of kernels on one
 // stream, every contraction on bf16 mma.sync with fp32 accumulation:
 //   pool            Q_l, correctly rounded bin means (shared with the staged path)
-//   tl_scores       S = Q_l . K^T (fp32, workspace) and each landmark's row max
-//   topk            per landmark the k best keys, exact radix select over S
-//                   (shared with the staged path)
+//   tl_scores       S = Q_l . K^T (fp32, workspace) and each landmark's row
+//                   max and min
+//   tl_topk         per landmark the k best keys (ties to the lower index):
+//                   a 2048-bin histogram over [min, max], an exact rank of the
+//                   boundary bin's members, an ordered emit (rows up to 16K
+//                   keys; longer rows use the staged path's radix select)
 //   tl_values       split-K partial sums of exp(S / sqrt d - max) . V and of
 //                   the row sums, per 1024-key split
 //   tl_values_fin   V_l = sum of partials / sum of row sums, bf16
@@ -40,7 +43,8 @@ int max_tiles(const Shape& s) { return (s.N + kQT - 1) / kQT + s.m; }
 // Block: 64 landmarks x 128 keys, 8 warps of 16 x 64.
 template <int D>
 __global__ void __launch_bounds__(256) tl_scores(Shape s, const bf16* __restrict__ Ql, const bf16* __restrict__ K,
-                                                 float* __restrict__ S, uint32_t* __restrict__ rowmax) {
+                                                 float* __restrict__ S, uint32_t* __restrict__ rowmax,
+                                                 uint32_t* __restrict__ rowmin) {
     constexpr int RB = 2 * D, CH = D / 8;
     extern __shared__ __align__(128) unsigned char sm[];
     const int n0 = blockIdx.x * 128, i0 = blockIdx.y * 64, bh = blockIdx.z;
@@ -82,7 +86,7 @@ __global__ void __launch_bounds__(256) tl_scores(Shape s, const bf16* __restrict
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int i = i0 + mt * 16 + g + 8 * h;
-        float mx = -INFINITY;
+        float mx = -INFINITY, mn = INFINITY;
         if (i < s.m) {
             float* row = S + ((size_t)bh * s.m + i) * s.N;
 #pragma unroll
@@ -91,30 +95,210 @@ __global__ void __launch_bounds__(256) tl_scores(Shape s, const bf16* __restrict
                 if (j < s.N) {
                     row[j] = acc[n][2 * h];
                     mx = fmaxf(mx, acc[n][2 * h]);
+                    mn = fminf(mn, acc[n][2 * h]);
                 }
                 if (j + 1 < s.N) {
                     row[j + 1] = acc[n][2 * h + 1];
                     mx = fmaxf(mx, acc[n][2 * h + 1]);
+                    mn = fminf(mn, acc[n][2 * h + 1]);
                 }
             }
         }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        if (t == 0 && i < s.m && mx > -INFINITY) atomicMax(&rowmax[(size_t)bh * s.m + i], order_key(mx));
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        }
+        if (t == 0 && i < s.m && mx >= mn) {
+            atomicMax(&rowmax[(size_t)bh * s.m + i], order_key(mx));
+            atomicMin(&rowmin[(size_t)bh * s.m + i], order_key(mn));
+        }
+    }
+}
+
+// ---------------------------------------------------------------- top-k
+constexpr int kTB = 256;          // threads per top-k block
+constexpr int kNB = 2048;         // histogram bins
+constexpr int kCandMax = 1024;    // boundary members ranked exactly
+constexpr int kHistTopkMaxN = 16384;   // longer rows use the radix select of the staged path
+
+// Block-wide exclusive prefix sum of one int per thread (kTB threads);
+// *total receives the block total.
+MITA_DEV int block_excl_scan(int x, int* wsum, int* total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    __syncthreads();
+    if (lane == 31) wsum[w] = incl;
+    __syncthreads();
+    int base = 0, tot = 0;
+#pragma unroll
+    for (int u = 0; u < kTB / 32; ++u) {
+        const int v = wsum[u];
+        base += u < w ? v : 0;
+        tot += v;
+    }
+    *total = tot;
+    return base + incl - x;
+}
+
+// Block per (landmark i, head bh): the k keys with the largest raw scores
+// S[bh, i, :], ties to the lower key index, written in ascending order.
+// Bins of equal width over [row min, row max] find the bin holding the k-th
+// largest score; bins above it are taken whole, and the boundary bin's
+// members are ranked exactly by (score desc, index asc).  Thread t owns the
+// contiguous key segment [t * seg, (t + 1) * seg), so per-thread counts and
+// one block scan give every emitted key its place in index order.
+__global__ void __launch_bounds__(kTB) tl_topk(Shape s, const float* __restrict__ S,
+                                               const uint32_t* __restrict__ rowmax,
+                                               const uint32_t* __restrict__ rowmin, int32_t* __restrict__ idx) {
+    __shared__ int hist[kNB];
+    __shared__ int wsum[kTB / 32];
+    __shared__ int sh[3];
+    __shared__ float cval[kCandMax];
+    __shared__ uint8_t chosen[kCandMax];
+    const int i = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x, N = s.N, k = s.k;
+    const float* row = S + ((size_t)bh * s.m + i) * N;
+    const float mx = key_to_float(rowmax[(size_t)bh * s.m + i]);
+    const float mn = key_to_float(rowmin[(size_t)bh * s.m + i]);
+    const float range = mx - mn;
+    const float sc = range > 0.0f ? (float)kNB / range : 0.0f;
+    auto bin_of = [&](float v) { return min(kNB - 1, (int)((v - mn) * sc)); };
+    for (int b = tid; b < kNB; b += kTB) hist[b] = 0;
+    __syncthreads();
+    for (int j = tid; j < N; j += kTB) atomicAdd(&hist[bin_of(row[j])], 1);
+    __syncthreads();
+    // thread t holds bins [8t, 8t + 8); counts of bins above, from the top down
+    int c[8], tot = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) { c[u] = hist[8 * tid + u]; tot += c[u]; }
+    int all;
+    const int below = block_excl_scan(tot, wsum, &all);   // members of bins under 8t
+    const int above = all - below - tot;                    // members of bins over 8t + 7
+    if (above < k && above + tot >= k) {
+        int run = above;
+#pragma unroll
+        for (int u = 7; u >= 0; --u) {
+            if (run < k && run + c[u] >= k) {
+                sh[0] = 8 * tid + u;
+                sh[1] = k - run;
+                sh[2] = c[u];
+            }
+            run += c[u];
+        }
+    }
+    __syncthreads();
+    const int bstar = sh[0], need = sh[1], cstar = sh[2];
+    const int seg = (N + kTB - 1) / kTB, j0 = min(N, tid * seg), j1 = min(N, j0 + seg);
+    int ngt = 0, nb = 0;
+    for (int j = j0; j < j1; ++j) {
+        const int b = bin_of(row[j]);
+        ngt += b > bstar;
+        nb += b == bstar;
+    }
+    int dummy;
+    const int pb = block_excl_scan(nb, wsum, &dummy);   // first boundary member of this thread
+    int nsel = ngt + nb;
+    if (need < cstar) {
+        if (cstar <= kCandMax) {
+            int r = pb;
+            for (int j = j0; j < j1; ++j) {
+                const float v = row[j];
+                if (bin_of(v) == bstar) cval[r++] = v;
+            }
+            __syncthreads();
+            for (int p = tid; p < cstar; p += kTB) {
+                const float v = cval[p];
+                int rank = 0;
+                for (int q = 0; q < cstar; ++q) {
+                    const float w = cval[q];
+                    rank += (w > v || (w == v && q < p)) ? 1 : 0;
+                }
+                chosen[p] = rank < need ? 1 : 0;
+            }
+            __syncthreads();
+            nsel = ngt;
+            for (int p = pb; p < pb + nb; ++p) nsel += chosen[p];
+        } else {
+            // many members (degenerate scores): bisect the order key T of the
+            // need-th best member; members above T are taken, and members equal
+            // to T in index order until need is met
+            uint32_t T = 0;
+            for (int b = 31; b >= 0; --b) {
+                const uint32_t ct = T | (1u << b);
+                int cnt = 0;
+                for (int j = j0; j < j1; ++j) {
+                    const float v = row[j];
+                    cnt += (bin_of(v) == bstar && order_key(v) >= ct) ? 1 : 0;
+                }
+                int total;
+                block_excl_scan(cnt, wsum, &total);
+                if (total >= need) T = ct;
+            }
+            int gt = 0, eq = 0;
+            for (int j = j0; j < j1; ++j) {
+                const float v = row[j];
+                if (bin_of(v) == bstar) {
+                    const uint32_t kv = order_key(v);
+                    gt += kv > T;
+                    eq += kv == T;
+                }
+            }
+            int gt_all;
+            block_excl_scan(gt, wsum, &gt_all);
+            int eq_all;
+            const int eq_before = block_excl_scan(eq, wsum, &eq_all);
+            const int eq_take = need - gt_all;
+            const int mine_eq = max(0, min(eq, eq_take - eq_before));
+            nsel = ngt + gt + mine_eq;
+            // emit directly: this thread's selection is known
+            int total_sel;
+            int pos = block_excl_scan(nsel, wsum, &total_sel);
+            int32_t* out = idx + ((size_t)bh * s.m + i) * k;
+            int eq_seen = 0;
+            for (int j = j0; j < j1; ++j) {
+                const float v = row[j];
+                const int b = bin_of(v);
+                bool sel = b > bstar;
+                if (b == bstar) {
+                    const uint32_t kv = order_key(v);
+                    if (kv > T) sel = true;
+                    else if (kv == T) sel = eq_seen++ < mine_eq;
+                }
+                if (sel) out[pos++] = j;
+            }
+            return;
+        }
+    }
+    int total_sel;
+    int pos = block_excl_scan(nsel, wsum, &total_sel);
+    int32_t* out = idx + ((size_t)bh * s.m + i) * k;
+    int r = pb;
+    for (int j = j0; j < j1; ++j) {
+        const int b = bin_of(row[j]);
+        bool sel = b > bstar;
+        if (b == bstar) sel = need >= cstar || chosen[r++];
+        if (sel) out[pos++] = j;
     }
 }
 
 // ---------------------------------------------------------------- landmark values
 // Block: 64 landmarks x one split of kKC keys, in 64-key steps; 8 warps =
 // 4 landmark tiles x 2 feature halves.  Partials: [BH, nsplit, m, D + 1]
-// (the last column holds the row sum of the bf16 numerators).
-template <int D>
+// (the last column holds the row sum of the bf16 numerators).  The next
+// step's scores are loaded into registers and its V rows copied into the
+// other half of a double buffer while the current step's MMAs run.
+template <int D, bool VEC>
 __global__ void __launch_bounds__(256) tl_values(Shape s, const float* __restrict__ S,
                                                  const uint32_t* __restrict__ rowmax, const bf16* __restrict__ V,
                                                  float* __restrict__ part, float cs) {
     constexpr int RB = 2 * D, CH = D / 8, NT = D / 16;   // NT: n8 feature tiles per warp
     __shared__ __align__(128) unsigned char p_s[64 * 128];
-    __shared__ __align__(128) unsigned char v_s[64 * RB];
+    __shared__ __align__(128) unsigned char v_s[2][64 * RB];
     __shared__ float mb_s[64];
     const int split = blockIdx.x, i0 = blockIdx.y * 64, bh = blockIdx.z, ns = gridDim.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
@@ -123,37 +307,63 @@ __global__ void __launch_bounds__(256) tl_values(Shape s, const float* __restric
         const int i = i0 + tid;
         mb_s[tid] = i < s.m ? key_to_float(rowmax[(size_t)bh * s.m + i]) * cs : 0.0f;
     }
-    const uint32_t up = smem_u32(p_s), uv = smem_u32(v_s);
+    const uint32_t up = smem_u32(p_s), uv0 = smem_u32(v_s[0]);
     const int mt = warp & 3, fh = warp >> 2;
     const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, vrow = (lane & 7) + ((lane >> 3) & 1) * 8;
     float o[NT][4], osum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
     const bf16* vsrc = V + (size_t)bh * s.N * D;
-    for (int jb = jb0; jb < je; jb += 64) {
-        __syncthreads();   // the previous step's tiles are consumed (and mb_s is visible)
+    // item q of this thread (q < 4): row r = (tid >> 4) + 16 q, keys 4 * (tid & 15) .. + 3
+    const int c4 = tid & 15;
+    auto load_s = [&](int jb, float (&sv)[4][4]) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int r = (tid >> 4) + 16 * q, i = i0 + r, j = jb + 4 * c4;
+            const float* row = S + ((size_t)bh * s.m + (i < s.m ? i : 0)) * s.N;
+            if (VEC && i < s.m && j + 3 < je) {
+                const float4 x = __ldg((const float4*)(row + j));
+                sv[q][0] = x.x; sv[q][1] = x.y; sv[q][2] = x.z; sv[q][3] = x.w;
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) sv[q][u] = (i < s.m && j + u < je) ? __ldg(row + j + u) : -INFINITY;
+            }
+        }
+    };
+    auto stage_v = [&](int jb, int buf) {
+        const uint32_t uv = uv0 + (uint32_t)buf * 64u * RB;
         for (int e = tid; e < 64 * CH; e += 256) {
             const int r = e / CH, c = e % CH;
             const bool ok = jb + r < je;
             cp_async16(uv + swz<RB>(r, c), vsrc + (size_t)(ok ? jb + r : 0) * D + 8 * c, ok ? 16u : 0u);
         }
         cp_async_commit();
-        // numerators: 64 rows x 64 keys, 4 consecutive keys per item
-        for (int e = tid; e < 64 * 16; e += 256) {
-            const int r = e >> 4, c4 = e & 15, i = i0 + r, j = jb + 4 * c4;
-            float p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if (i < s.m) {
-                const float* row = S + ((size_t)bh * s.m + i) * s.N;
-                const float mb = mb_s[r];
+    };
+    float sv[4][4];
+    load_s(jb0, sv);
+    stage_v(jb0, 0);
+    __syncthreads();   // mb_s
+    int buf = 0;
+    for (int jb = jb0; jb < je; jb += 64, buf ^= 1) {
+        // numerators of this step (padding keys and rows past m give 0)
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (j + u < je) p[u] = ex2(fmaf(row[j + u], cs, -mb));
-            }
-            const uint2 pk = make_uint2(pack2(p[0], p[1]), pack2(p[2], p[3]));
+        for (int q = 0; q < 4; ++q) {
+            const int r = (tid >> 4) + 16 * q;
+            const float mb = mb_s[r];
+            const uint2 pk = make_uint2(pack2(ex2(fmaf(sv[q][0], cs, -mb)), ex2(fmaf(sv[q][1], cs, -mb))),
+                                        pack2(ex2(fmaf(sv[q][2], cs, -mb)), ex2(fmaf(sv[q][3], cs, -mb))));
             *(uint2*)(p_s + swz<128>(r, c4 >> 1) + (c4 & 1) * 8) = pk;
         }
-        cp_async_wait<0>();
+        const bool more = jb + 64 < je;
+        if (more) {
+            load_s(jb + 64, sv);
+            stage_v(jb + 64, buf ^ 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
         __syncthreads();
+        const uint32_t uv = uv0 + (uint32_t)buf * 64u * RB;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
             uint32_t a0, a1, a2, a3;
@@ -167,6 +377,7 @@ __global__ void __launch_bounds__(256) tl_values(Shape s, const float* __restric
                 mma16816(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
             }
         }
+        __syncthreads();   // P and this V buffer are rewritten next
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -327,7 +538,7 @@ __global__ void tl_bucket_put(Shape s, const int32_t* __restrict__ route, int32_
 // pairs (K, V rows of the expert's keys); 64-slot blocks are staged by
 // cp.async into a double buffer and folded in by an online softmax.
 template <int D>
-__global__ void __launch_bounds__(128, 2)
+__global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
     tl_attend(Shape s, const bf16* __restrict__ Q, const bf16* __restrict__ K, const bf16* __restrict__ V,
               const bf16* __restrict__ Ql, const bf16* __restrict__ Vl, const int32_t* __restrict__ idx,
               const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm,
@@ -487,6 +698,11 @@ __global__ void __launch_bounds__(128, 2)
     }
 }
 
+// Heads per landmark-stage launch.  All heads at once: grouping heads so
+// that a group's raw scores stay in L2 starves the launches of blocks at
+// these head counts (measured slower at both long shapes).
+int head_group(const Shape& s) { return s.BH(); }
+
 template <int D>
 cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, bf16* out, int32_t* idx,
                   int32_t* route, cudaStream_t st) {
@@ -496,20 +712,36 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
     const float cs = kLog2e / sqrtf((float)D);
     bf16* Ql = (bf16*)p->Ql;
     bf16* Vl = (bf16*)p->Vl;
+    uint32_t* rowmin = p->rowmax + (size_t)BH * s.m;
     cudaError_t err;
     if ((err = cudaMemsetAsync(p->rowmax, 0, (size_t)BH * s.m * 4, st)) != cudaSuccess) return err;
+    if ((err = cudaMemsetAsync(rowmin, 0xff, (size_t)BH * s.m * 4, st)) != cudaSuccess) return err;
     if ((err = cudaMemsetAsync(p->counts, 0, (size_t)BH * s.m * 4, st)) != cudaSuccess) return err;
     if ((err = staged_pool(s, MITA_BF16, Q, Ql, st)) != cudaSuccess) return err;
-    {
-        const int smem = (64 + 128) * RB;
-        auto kern = tl_scores<D>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        kern<<<dim3((s.N + 127) / 128, (s.m + 63) / 64, BH), 256, smem, st>>>(s, Ql, K, p->S, p->rowmax);
+    const int smem_sc = (64 + 128) * RB;
+    cudaFuncSetAttribute(tl_scores<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_sc);
+    const int ns = nsplit(s), G = head_group(s);
+    for (int h0 = 0; h0 < BH; h0 += G) {
+        Shape sg = s;
+        sg.B = 1;
+        sg.H = min(G, BH - h0);
+        const size_t mo = (size_t)h0 * s.m, no = (size_t)h0 * s.N;
+        tl_scores<D><<<dim3((s.N + 127) / 128, (s.m + 63) / 64, sg.H), 256, smem_sc, st>>>(
+            sg, Ql + mo * D, K + no * D, p->S, p->rowmax + mo, rowmin + mo);
+        if (s.N <= kHistTopkMaxN) {
+            tl_topk<<<dim3(s.m, sg.H), kTB, 0, st>>>(sg, p->S, p->rowmax + mo, rowmin + mo, idx + mo * s.k);
+        } else {   // long rows: one block per row is too little parallelism for the histogram select
+            if ((err = staged_topk(sg, p->S, idx + mo * s.k, st)) != cudaSuccess) return err;
+        }
+        if (s.N % 4 == 0)
+            tl_values<D, true><<<dim3(ns, (s.m + 63) / 64, sg.H), 256, 0, st>>>(sg, p->S, p->rowmax + mo,
+                                                                                 V + no * D, p->vpart, cs);
+        else
+            tl_values<D, false><<<dim3(ns, (s.m + 63) / 64, sg.H), 256, 0, st>>>(sg, p->S, p->rowmax + mo,
+                                                                                  V + no * D, p->vpart, cs);
+        tl_values_fin<D><<<dim3(s.m, sg.H), D, 0, st>>>(sg, p->vpart, ns, Vl + mo * D);
+        p->launches += 4;
     }
-    if ((err = staged_topk(s, p->S, idx, st)) != cudaSuccess) return err;
-    const int ns = nsplit(s);
-    tl_values<D><<<dim3(ns, (s.m + 63) / 64, BH), 256, 0, st>>>(s, p->S, p->rowmax, V, p->vpart, cs);
-    tl_values_fin<D><<<dim3(s.m, BH), D, 0, st>>>(s, p->vpart, ns, Vl);
     {
         const int smem = (128 + (s.m + 63) / 64 * 64) * RB;
         auto kern = tl_route<D>;
@@ -526,7 +758,7 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
         kern<<<dim3(maxt, BH), 128, smem, st>>>(s, Q, K, V, Ql, Vl, idx, p->offsets, p->perm, p->tiles, p->ntiles,
                                                   maxt, out, cs, p->status);
     }
-    p->launches += 9;
+    p->launches += 5;
     return cudaGetLastError();
 }
 
@@ -537,7 +769,7 @@ bool tiled_supported(const Shape& s, mita_dtype_t dtype) {
 }
 
 size_t tiled_part_bytes(const Shape& s) {
-    return (size_t)s.BH() * tl::nsplit(s) * s.m * (s.d + 1) * sizeof(float);
+    return (size_t)tl::head_group(s) * tl::nsplit(s) * s.m * (s.d + 1) * sizeof(float);
 }
 
 int tiled_max_tiles(const Shape& s) { return tl::max_tiles(s); }
