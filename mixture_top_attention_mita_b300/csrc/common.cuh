@@ -84,6 +84,11 @@ MITA_DEV uint32_t order_key(float x) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Inverse of order_key().
+MITA_DEV float key_to_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- plan
@@ -120,5 +125,7 @@ struct mita_plan_s {
     int32_t* cursor;       // [BH, m]   bucket scatter cursors
     int32_t* tiles;        // [BH, max tiles] attention tiles (expert << 16 | chunk)
     int32_t* ntiles;       // [BH]
+    // one-kernel path only (null otherwise)
+    void* pool_mat;        // pooling matrix (see fused_pool_matrix)
     uint64_t launches;     // kernels launched so far
 };

@@ -53,10 +53,6 @@ MITA_DEV float rcp(float x) {   // hardware reciprocal (PTX rcp.approx)
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-// Inverse of order_key().
-MITA_DEV float key_to_float(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
 
 // 16-byte global -> shared copy; src_bytes = 0 fills the destination with zeros.
 MITA_DEV void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {

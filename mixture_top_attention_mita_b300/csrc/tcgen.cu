@@ -1,0 +1,442 @@
+// tcgen05 kernels of the tiled MiTA path (sm_103a): the dense contractions
+// run on the fifth-generation tensor cores with operands staged by TMA and
+// fp32 accumulators in tensor memory.
+//   tc_scores  S = Q_l . K^T per (128 landmarks x 128 keys) tile; each thread
+//              of the epilogue owns one landmark row: it stores the row's
+//              scores and folds them into the row max and min.
+//   tc_values  split-K partials of V_l: numerators exp(S / sqrt d - max) are
+//              computed from S straight into a 128-byte swizzled K-major A
+//              tile, V comes by TMA as an M/N-major B tile, and the MMAs of a
+//              1024-key split accumulate in tensor memory (two stages: the
+//              next tile's numerators and V copy overlap the current MMAs).
+//   tc_route   q . Q_l^T for 128 queries against all landmarks; each thread
+//              owns one query and takes the first argmax (the route).
+// Step numbers refer to the operator of 36Kr / 新智元 "注意力也是FFN？",
+// section "用少量地标查询，同时构造全局概括与细节专家": scores are step 2,
+// landmark values step 4, routes step 5.
+#include "tc_util.cuh"
+#include "tcgen.cuh"
+
+namespace mita {
+namespace tcg {
+
+using bf16 = __nv_bfloat16;
+using namespace tc;
+
+constexpr uint32_t kChunk = 128 * 128;   // one 128-row x 64-column bf16 tile, bytes
+constexpr int kKCV = 1024;               // keys per tc_values split
+
+// ---------------------------------------------------------------- scores
+template <int D, bool VEC>
+__global__ void __launch_bounds__(128) tc_scores(const __grid_constant__ CUtensorMap mQl,
+                                                 const __grid_constant__ CUtensorMap mK, Shape s,
+                                                 float* __restrict__ S, uint32_t* __restrict__ rowmax,
+                                                 uint32_t* __restrict__ rowmin, int32_t* __restrict__ status) {
+    constexpr int KC = D / 64;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ uint32_t tslot;
+    __shared__ __align__(8) uint64_t bars[2];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (smem_u32(smem) & 1023u) {   // the swizzled tiles need a 1024-byte aligned base
+        if (tid == 0) atomicExch(status, (int)MITA_ERR_DEVICE);
+        return;
+    }
+    const int n0 = blockIdx.x * 128, i0 = blockIdx.y * 128, bh = blockIdx.z;
+    const uint32_t sA = smem_u32(smem), sB = sA + KC * kChunk;
+    const uint32_t bar_ld = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[1]);
+    if (tid == 0) {
+        mbar_init(bar_ld, 1);
+        mbar_init(bar_mma, 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc(smem_u32(&tslot), 128);
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = tslot;
+    if (tid == 0) {
+        mbar_expect_tx(bar_ld, 2u * KC * kChunk);
+        for (int kc = 0; kc < KC; ++kc) {
+            tma_load_2d(sA + kc * kChunk, &mQl, kc * 64, bh * s.m + i0, bar_ld);
+            tma_load_2d(sB + kc * kChunk, &mK, kc * 64, bh * s.N + n0, bar_ld);
+        }
+        if (mbar_wait_bounded(bar_ld, 0)) {
+            fence_after();
+            constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
+                mma_bf16(tmem, desc_kmajor(sA + off), desc_kmajor(sB + off), idesc, kk > 0);
+            }
+            mma_commit(bar_mma);
+        }
+    }
+    if (!mbar_wait_bounded(bar_mma, 0)) {
+        if (lane == 0) atomicExch(status, (int)MITA_ERR_TIMEOUT);
+    } else {
+        fence_after();
+        const int i = i0 + warp * 32 + lane, nv = min(128, s.N - n0);
+        const bool live = i < s.m;
+        float* row = S + ((size_t)bh * s.m + (live ? i : 0)) * s.N + n0;
+        float mx = -INFINITY, mn = INFINITY;
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+            float v[32];
+            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+            if (live) {
+                if (VEC && c0 + 32 <= nv) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        *(float4*)(row + c0 + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        mx = fmaxf(mx, v[j]);
+                        mn = fminf(mn, v[j]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (c0 + j < nv) {
+                            row[c0 + j] = v[j];
+                            mx = fmaxf(mx, v[j]);
+                            mn = fminf(mn, v[j]);
+                        }
+                }
+            }
+        }
+        if (live && mx >= mn) {
+            atomicMax(&rowmax[(size_t)bh * s.m + i], order_key(mx));
+            atomicMin(&rowmin[(size_t)bh * s.m + i], order_key(mn));
+        }
+    }
+    fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_free(tmem, 128);
+}
+
+// ---------------------------------------------------------------- landmark values
+// 512 threads: thread t builds the numerators of landmark row t % 128 for
+// keys [32 (t / 128), + 32) of each 128-key tile, with the next tile's scores
+// already loaded into registers; warps w, w + 4 (w < 4) read the same
+// tensor-memory lanes and split the D output columns.
+template <int D, bool VEC>
+__global__ void __launch_bounds__(512) tc_values(const __grid_constant__ CUtensorMap mV, Shape s,
+                                                 const float* __restrict__ S, const uint32_t* __restrict__ rowmax,
+                                                 float* __restrict__ part, float cs, int32_t* __restrict__ status) {
+    constexpr int KC = D / 64;                       // 64-wide feature chunks of a V tile
+    constexpr uint32_t PBYTES = 2 * kChunk;          // numerators: 128 rows x 128 keys
+    constexpr uint32_t VBYTES = KC * kChunk;         // V: 128 keys x D
+    constexpr uint32_t STAGE = PBYTES + VBYTES;
+    constexpr uint32_t TCOLS = D;                    // fp32 accumulator columns
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ uint32_t tslot;
+    __shared__ __align__(8) uint64_t bars[5];        // v_full[2], mma_done[2], final
+    __shared__ float rsum[512];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (smem_u32(smem) & 1023u) {
+        if (tid == 0) atomicExch(status, (int)MITA_ERR_DEVICE);
+        return;
+    }
+    const int split = blockIdx.x, i0 = blockIdx.y * 128, bh = blockIdx.z, ns = gridDim.x;
+    const int jb0 = split * kKCV, je = min(s.N, jb0 + kKCV), ntile = (je - jb0 + 127) / 128;
+    const uint32_t base = smem_u32(smem);
+    const uint32_t bar0 = smem_u32(&bars[0]);
+    auto v_full = [&](int st) { return bar0 + 8u * st; };
+    auto mma_done = [&](int st) { return bar0 + 16u + 8u * st; };
+    const uint32_t bar_fin = bar0 + 32u;
+    if (tid == 0) {
+        for (int b = 0; b < 5; ++b) mbar_init(bar0 + 8u * b, 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc(smem_u32(&tslot), TCOLS);
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = tslot;
+    const int r = tid & 127, q = tid >> 7, i = i0 + r;
+    const bool live = i < s.m;
+    const float mb = live ? key_to_float(rowmax[(size_t)bh * s.m + i]) * cs : 0.0f;
+    const float* srow = S + ((size_t)bh * s.m + (live ? i : 0)) * s.N;
+    float psum = 0.0f;
+    bool ok = true;
+    auto issue_v = [&](int t) {
+        const int st = t & 1;
+        mbar_expect_tx(v_full(st), VBYTES);
+        for (int kc = 0; kc < KC; ++kc)
+            tma_load_2d(base + st * STAGE + PBYTES + kc * kChunk, &mV, kc * 64, bh * s.N + jb0 + 128 * t, v_full(st));
+    };
+    // this thread's 32 scores of tile t
+    auto load_s = [&](int t, float (&x)[32]) {
+        const int j = jb0 + 128 * t + 32 * q;
+        if (VEC && live && j + 32 <= je) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float4 a = __ldg((const float4*)(srow + j + 4 * c));
+                x[4 * c] = a.x; x[4 * c + 1] = a.y; x[4 * c + 2] = a.z; x[4 * c + 3] = a.w;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) x[u] = (live && j + u < je) ? __ldg(srow + j + u) : -INFINITY;
+        }
+    };
+    if (tid == 0) {
+        issue_v(0);
+        if (ntile > 1) issue_v(1);
+    }
+    if (!live) {   // padding rows: zero numerators in both stages, written once
+        for (int st = 0; st < 2; ++st) {
+            unsigned char* prow = smem + st * STAGE + (q >> 1) * kChunk + r * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) *(uint4*)(prow + ((4 * (q & 1) + c) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    float x[32];
+    if (live) load_s(0, x);
+    for (int t = 0; t < ntile; ++t) {
+        const int st = t & 1;
+        const uint32_t sP = base + st * STAGE, sV = sP + PBYTES;
+        if (t >= 2) {   // the stage is free again once the MMAs of tile t - 2 are done
+            if (!mbar_wait_bounded(mma_done(st), ((t - 2) >> 1) & 1)) ok = false;
+            if (tid == 0 && ok) issue_v(t);
+        }
+        // numerators of row r, keys 32 q .. 32 q + 31 of the tile: 16-byte pieces
+        // 4 (q & 1) .. + 3 of row r in chunk q / 2 of the A tile
+        if (live) {
+        uint32_t w[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            float p0, p1;
+            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(p0) : "f"(fmaf(x[2 * u], cs, -mb)));
+            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(p1) : "f"(fmaf(x[2 * u + 1], cs, -mb)));
+            const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
+            psum += __low2float(pp) + __high2float(pp);
+            w[u] = *reinterpret_cast<const uint32_t*>(&pp);
+        }
+        if (t + 1 < ntile) load_s(t + 1, x);   // in flight while the stores and the MMAs proceed
+        unsigned char* prow = smem + st * STAGE + (q >> 1) * kChunk + r * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int piece = 4 * (q & 1) + c;
+            *(uint4*)(prow + ((piece ^ (r & 7)) << 4)) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        }
+        }
+        fence_async_smem();   // the numerators are read next by the tensor core
+        __syncthreads();
+        if (tid == 0 && ok) {
+            if (!mbar_wait_bounded(v_full(st), (t >> 1) & 1)) ok = false;
+            if (ok) {
+                fence_after();
+                constexpr uint32_t idesc = idesc_bf16(128, D, 0, 1);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t da = desc_kmajor(sP + (kk >> 2) * kChunk + (kk & 3) * 32);
+                    const uint64_t db = desc_mnmajor(sV + kk * 16 * 128, kChunk);
+                    mma_bf16(tmem, da, db, idesc, t > 0 || kk > 0);
+                }
+                mma_commit(mma_done(st));
+            }
+        }
+    }
+    if (tid == 0) mma_commit(bar_fin);
+    rsum[tid] = psum;
+    __syncthreads();
+    const bool fin = mbar_wait_bounded(bar_fin, 0);
+    if (!fin || !ok) {
+        if (lane == 0) atomicExch(status, (int)MITA_ERR_TIMEOUT);
+    } else if (warp < 8) {
+        fence_after();
+        const int lr = (warp & 3) * 32 + lane, li = i0 + lr, cbase = (warp >> 2) * (D / 2);
+        float* dst = part + (((size_t)bh * ns + split) * s.m + (li < s.m ? li : 0)) * (D + 1);
+#pragma unroll
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+            float v[32];
+            tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + cbase + c0, v);
+            if (li < s.m)
+#pragma unroll
+                for (int j = 0; j < 32; ++j) dst[cbase + c0 + j] = v[j];
+        }
+        if (warp < 4 && li < s.m) dst[D] = rsum[lr] + rsum[lr + 128] + rsum[lr + 256] + rsum[lr + 384];
+    }
+    fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_free(tmem, TCOLS);
+}
+
+// ---------------------------------------------------------------- routes
+template <int D>
+__global__ void __launch_bounds__(128) tc_route(const __grid_constant__ CUtensorMap mQ,
+                                                const __grid_constant__ CUtensorMap mQl, Shape s, int nb, int tcols,
+                                                int32_t* __restrict__ route, int32_t* __restrict__ counts,
+                                                int32_t* __restrict__ status) {
+    constexpr int KC = D / 64;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ uint32_t tslot;
+    __shared__ __align__(8) uint64_t bars[2];
+    __shared__ int hist[256];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (smem_u32(smem) & 1023u) {
+        if (tid == 0) atomicExch(status, (int)MITA_ERR_DEVICE);
+        return;
+    }
+    const int q0 = blockIdx.x * 128, bh = blockIdx.y;
+    const uint32_t sA = smem_u32(smem), sB = sA + KC * kChunk;
+    const uint32_t bchunk = (uint32_t)nb * 128u;   // bytes per 64-column chunk of the landmark tile
+    const uint32_t bar_ld = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[1]);
+    for (int e = tid; e < 256; e += 128) hist[e] = 0;
+    if (tid == 0) {
+        mbar_init(bar_ld, 1);
+        mbar_init(bar_mma, 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc(smem_u32(&tslot), (uint32_t)tcols);
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = tslot;
+    if (tid == 0) {
+        mbar_expect_tx(bar_ld, KC * (kChunk + bchunk));
+        for (int kc = 0; kc < KC; ++kc) {
+            tma_load_2d(sA + kc * kChunk, &mQ, kc * 64, bh * s.N + q0, bar_ld);
+            tma_load_2d(sB + kc * bchunk, &mQl, kc * 64, bh * s.m, bar_ld);
+        }
+        if (mbar_wait_bounded(bar_ld, 0)) {
+            fence_after();
+            const uint32_t idesc = idesc_bf16(128, nb, 0, 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t da = desc_kmajor(sA + (kk >> 2) * kChunk + (kk & 3) * 32);
+                const uint64_t db = desc_kmajor(sB + (kk >> 2) * bchunk + (kk & 3) * 32);
+                mma_bf16(tmem, da, db, idesc, kk > 0);
+            }
+            mma_commit(bar_mma);
+        }
+    }
+    if (!mbar_wait_bounded(bar_mma, 0)) {
+        if (lane == 0) atomicExch(status, (int)MITA_ERR_TIMEOUT);
+    } else {
+        fence_after();
+        const int q = q0 + warp * 32 + lane;
+        float best = -INFINITY;
+        int arg = 0;
+        for (int c0 = 0; c0 < nb; c0 += 32) {
+            float v[32];
+            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (c0 + j < s.m && v[j] > best) {   // ascending landmarks, strict: first argmax
+                    best = v[j];
+                    arg = c0 + j;
+                }
+        }
+        if (q < s.N) {
+            route[(size_t)bh * s.N + q] = arg;
+            atomicAdd(&hist[arg], 1);
+        }
+    }
+    fence_before();
+    __syncthreads();
+    for (int e = tid; e < s.m; e += 128)
+        if (hist[e]) atomicAdd(&counts[(size_t)bh * s.m + e], hist[e]);
+    if (warp == 0) tmem_free(tmem, (uint32_t)tcols);
+}
+
+}  // namespace tcg
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn tc_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)p;
+    }
+    return fn;
+}
+
+// 2-D map over `rows` rows of `d` bf16, boxes of 64 columns x box_rows rows,
+// 128-byte swizzle (rows past the end read as zero).
+static bool map_rows(CUtensorMap* map, const void* base, int d, size_t rows, int box_rows) {
+    EncodeTiledFn fn = tc_encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+static cudaError_t tc_scores_t(const Shape& s, const void* Ql, const void* K, float* S, uint32_t* rowmax,
+                               uint32_t* rowmin, int32_t* status, cudaStream_t st) {
+    CUtensorMap mq, mk;
+    if (!map_rows(&mq, Ql, D, (size_t)s.BH() * s.m, 128) || !map_rows(&mk, K, D, (size_t)s.BH() * s.N, 128))
+        return cudaErrorInvalidValue;
+    const int smem = 2 * (D / 64) * (int)tcg::kChunk + 1024;
+    const dim3 grid((s.N + 127) / 128, (s.m + 127) / 128, s.BH());
+    if (s.N % 4 == 0) {
+        cudaFuncSetAttribute(tcg::tc_scores<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        tcg::tc_scores<D, true><<<grid, 128, smem, st>>>(mq, mk, s, S, rowmax, rowmin, status);
+    } else {
+        cudaFuncSetAttribute(tcg::tc_scores<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        tcg::tc_scores<D, false><<<grid, 128, smem, st>>>(mq, mk, s, S, rowmax, rowmin, status);
+    }
+    return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t tc_values_t(const Shape& s, const float* S, const uint32_t* rowmax, const void* V, float* part,
+                               float cs, int32_t* status, cudaStream_t st) {
+    CUtensorMap mv;
+    if (!map_rows(&mv, V, D, (size_t)s.BH() * s.N, 128)) return cudaErrorInvalidValue;
+    const int smem = 2 * (2 * (int)tcg::kChunk + (D / 64) * (int)tcg::kChunk) + 1024;
+    const dim3 grid((s.N + tcg::kKCV - 1) / tcg::kKCV, (s.m + 127) / 128, s.BH());
+    if (s.N % 4 == 0) {
+        cudaFuncSetAttribute(tcg::tc_values<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        tcg::tc_values<D, true><<<grid, 512, smem, st>>>(mv, s, S, rowmax, part, cs, status);
+    } else {
+        cudaFuncSetAttribute(tcg::tc_values<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        tcg::tc_values<D, false><<<grid, 512, smem, st>>>(mv, s, S, rowmax, part, cs, status);
+    }
+    return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t tc_route_t(const Shape& s, const void* Q, const void* Ql, int32_t* route, int32_t* counts,
+                              int32_t* status, cudaStream_t st) {
+    const int nb = (s.m + 15) / 16 * 16;
+    int tcols = 32;
+    while (tcols < nb) tcols <<= 1;
+    CUtensorMap mq, ml;
+    if (!map_rows(&mq, Q, D, (size_t)s.BH() * s.N, 128) || !map_rows(&ml, Ql, D, (size_t)s.BH() * s.m, nb))
+        return cudaErrorInvalidValue;
+    const int smem = (D / 64) * ((int)tcg::kChunk + nb * 128) + 1024;
+    cudaFuncSetAttribute(tcg::tc_route<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    tcg::tc_route<D><<<dim3((s.N + 127) / 128, s.BH()), 128, smem, st>>>(mq, ml, s, nb, tcols, route, counts, status);
+    return cudaGetLastError();
+}
+
+int tc_value_splits(const Shape& s) { return (s.N + tcg::kKCV - 1) / tcg::kKCV; }
+
+cudaError_t tc_scores(const Shape& s, const void* Ql, const void* K, float* S, uint32_t* rowmax, uint32_t* rowmin,
+                      int32_t* status, cudaStream_t st) {
+    return s.d == 64 ? tc_scores_t<64>(s, Ql, K, S, rowmax, rowmin, status, st)
+                     : tc_scores_t<128>(s, Ql, K, S, rowmax, rowmin, status, st);
+}
+cudaError_t tc_values(const Shape& s, const float* S, const uint32_t* rowmax, const void* V, float* part, float cs,
+                      int32_t* status, cudaStream_t st) {
+    return s.d == 64 ? tc_values_t<64>(s, S, rowmax, V, part, cs, status, st)
+                     : tc_values_t<128>(s, S, rowmax, V, part, cs, status, st);
+}
+cudaError_t tc_route(const Shape& s, const void* Q, const void* Ql, int32_t* route, int32_t* counts, int32_t* status,
+                     cudaStream_t st) {
+    return s.d == 64 ? tc_route_t<64>(s, Q, Ql, route, counts, status, st)
+                     : tc_route_t<128>(s, Q, Ql, route, counts, status, st);
+}
+
+}  // namespace mita

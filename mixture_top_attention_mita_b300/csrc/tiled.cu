@@ -3,18 +3,19 @@
 //
 // The steps of the operator (36Kr / 新智元 "注意力也是FFN？", section
 // "用少量地标查询，同时构造全局概括与细节专家") as a chain of kernels on one
-// stream, every contraction on bf16 mma.sync with fp32 accumulation:
+// stream; the landmark scores, landmark values and routes run on tcgen05
+// (tcgen.cu), the grouped attention on bf16 mma.sync:
 //   pool            Q_l, correctly rounded bin means (shared with the staged path)
-//   tl_scores       S = Q_l . K^T (fp32, workspace) and each landmark's row
+//   tc_scores       S = Q_l . K^T (fp32, workspace) and each landmark's row
 //                   max and min
 //   tl_topk         per landmark the k best keys (ties to the lower index):
 //                   a 2048-bin histogram over [min, max], an exact rank of the
 //                   boundary bin's members, an ordered emit (rows up to 16K
 //                   keys; longer rows use the staged path's radix select)
-//   tl_values       split-K partial sums of exp(S / sqrt d - max) . V and of
+//   tc_values       split-K partial sums of exp(S / sqrt d - max) . V and of
 //                   the row sums, per 1024-key split
 //   tl_values_fin   V_l = sum of partials / sum of row sums, bf16
-//   tl_route        q . Q_l^T per query tile, first argmax (the route), and
+//   tc_route        q . Q_l^T per query tile, first argmax (the route), and
 //                   per-landmark query counts
 //   tl_bucket_off   per head: bucket offsets, cursors and the list of
 //                   (expert, 64-query chunk) attention tiles
@@ -25,6 +26,7 @@
 //                   64-slot blocks with an online softmax
 #include "mma_util.cuh"
 #include "staged.cuh"
+#include "tcgen.cuh"
 #include "tiled.cuh"
 
 namespace mita {
@@ -33,88 +35,11 @@ namespace tl {
 using bf16 = __nv_bfloat16;
 using namespace mx;
 
-constexpr int kKC = 1024;   // keys per tl_values split
 constexpr int kQT = 64;     // queries per attention tile (4 warps x 16)
 
-int nsplit(const Shape& s) { return (s.N + kKC - 1) / kKC; }
+int nsplit(const Shape& s) { return tc_value_splits(s); }
 int max_tiles(const Shape& s) { return (s.N + kQT - 1) / kQT + s.m; }
 
-// ---------------------------------------------------------------- scores
-// Block: 64 landmarks x 128 keys, 8 warps of 16 x 64.
-template <int D>
-__global__ void __launch_bounds__(256) tl_scores(Shape s, const bf16* __restrict__ Ql, const bf16* __restrict__ K,
-                                                 float* __restrict__ S, uint32_t* __restrict__ rowmax,
-                                                 uint32_t* __restrict__ rowmin) {
-    constexpr int RB = 2 * D, CH = D / 8;
-    extern __shared__ __align__(128) unsigned char sm[];
-    const int n0 = blockIdx.x * 128, i0 = blockIdx.y * 64, bh = blockIdx.z;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-    const uint32_t uq = smem_u32(sm), uk = uq + 64 * RB;
-    const bf16* qsrc = Ql + (size_t)bh * s.m * D;
-    const bf16* ksrc = K + (size_t)bh * s.N * D;
-    for (int e = tid; e < 64 * CH; e += 256) {
-        const int r = e / CH, c = e % CH;
-        const bool ok = i0 + r < s.m;
-        cp_async16(uq + swz<RB>(r, c), qsrc + (size_t)(ok ? i0 + r : 0) * D + 8 * c, ok ? 16u : 0u);
-    }
-    for (int e = tid; e < 128 * CH; e += 256) {
-        const int r = e / CH, c = e % CH;
-        const bool ok = n0 + r < s.N;
-        cp_async16(uk + swz<RB>(r, c), ksrc + (size_t)(ok ? n0 + r : 0) * D + 8 * c, ok ? 16u : 0u);
-    }
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
-
-    const int mt = warp & 3, kh = warp >> 2;
-    const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, brow = (lane & 7) + (lane >> 4) * 8;
-    float acc[8][4];
-#pragma unroll
-    for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(uq + swz<RB>(mt * 16 + arow, 2 * kk + (lane >> 4)), a0, a1, a2, a3);
-#pragma unroll
-        for (int np = 0; np < 4; ++np) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(uk + swz<RB>(kh * 64 + np * 16 + brow, 2 * kk + ((lane >> 3) & 1)), b0, b1, b2, b3);
-            mma16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
-            mma16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
-        }
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int i = i0 + mt * 16 + g + 8 * h;
-        float mx = -INFINITY, mn = INFINITY;
-        if (i < s.m) {
-            float* row = S + ((size_t)bh * s.m + i) * s.N;
-#pragma unroll
-            for (int n = 0; n < 8; ++n) {
-                const int j = n0 + kh * 64 + 8 * n + 2 * t;
-                if (j < s.N) {
-                    row[j] = acc[n][2 * h];
-                    mx = fmaxf(mx, acc[n][2 * h]);
-                    mn = fminf(mn, acc[n][2 * h]);
-                }
-                if (j + 1 < s.N) {
-                    row[j + 1] = acc[n][2 * h + 1];
-                    mx = fmaxf(mx, acc[n][2 * h + 1]);
-                    mn = fminf(mn, acc[n][2 * h + 1]);
-                }
-            }
-        }
-#pragma unroll
-        for (int o = 1; o <= 2; o <<= 1) {
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        }
-        if (t == 0 && i < s.m && mx >= mn) {
-            atomicMax(&rowmax[(size_t)bh * s.m + i], order_key(mx));
-            atomicMin(&rowmin[(size_t)bh * s.m + i], order_key(mn));
-        }
-    }
-}
 
 // ---------------------------------------------------------------- top-k
 constexpr int kTB = 256;          // threads per top-k block
@@ -286,114 +211,6 @@ __global__ void __launch_bounds__(kTB) tl_topk(Shape s, const float* __restrict_
     }
 }
 
-// ---------------------------------------------------------------- landmark values
-// Block: 64 landmarks x one split of kKC keys, in 64-key steps; 8 warps =
-// 4 landmark tiles x 2 feature halves.  Partials: [BH, nsplit, m, D + 1]
-// (the last column holds the row sum of the bf16 numerators).  The next
-// step's scores are loaded into registers and its V rows copied into the
-// other half of a double buffer while the current step's MMAs run.
-template <int D, bool VEC>
-__global__ void __launch_bounds__(256) tl_values(Shape s, const float* __restrict__ S,
-                                                 const uint32_t* __restrict__ rowmax, const bf16* __restrict__ V,
-                                                 float* __restrict__ part, float cs) {
-    constexpr int RB = 2 * D, CH = D / 8, NT = D / 16;   // NT: n8 feature tiles per warp
-    __shared__ __align__(128) unsigned char p_s[64 * 128];
-    __shared__ __align__(128) unsigned char v_s[2][64 * RB];
-    __shared__ float mb_s[64];
-    const int split = blockIdx.x, i0 = blockIdx.y * 64, bh = blockIdx.z, ns = gridDim.x;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-    const int jb0 = split * kKC, je = min(s.N, jb0 + kKC);
-    if (tid < 64) {
-        const int i = i0 + tid;
-        mb_s[tid] = i < s.m ? key_to_float(rowmax[(size_t)bh * s.m + i]) * cs : 0.0f;
-    }
-    const uint32_t up = smem_u32(p_s), uv0 = smem_u32(v_s[0]);
-    const int mt = warp & 3, fh = warp >> 2;
-    const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, vrow = (lane & 7) + ((lane >> 3) & 1) * 8;
-    float o[NT][4], osum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
-    const bf16* vsrc = V + (size_t)bh * s.N * D;
-    // item q of this thread (q < 4): row r = (tid >> 4) + 16 q, keys 4 * (tid & 15) .. + 3
-    const int c4 = tid & 15;
-    auto load_s = [&](int jb, float (&sv)[4][4]) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int r = (tid >> 4) + 16 * q, i = i0 + r, j = jb + 4 * c4;
-            const float* row = S + ((size_t)bh * s.m + (i < s.m ? i : 0)) * s.N;
-            if (VEC && i < s.m && j + 3 < je) {
-                const float4 x = __ldg((const float4*)(row + j));
-                sv[q][0] = x.x; sv[q][1] = x.y; sv[q][2] = x.z; sv[q][3] = x.w;
-            } else {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) sv[q][u] = (i < s.m && j + u < je) ? __ldg(row + j + u) : -INFINITY;
-            }
-        }
-    };
-    auto stage_v = [&](int jb, int buf) {
-        const uint32_t uv = uv0 + (uint32_t)buf * 64u * RB;
-        for (int e = tid; e < 64 * CH; e += 256) {
-            const int r = e / CH, c = e % CH;
-            const bool ok = jb + r < je;
-            cp_async16(uv + swz<RB>(r, c), vsrc + (size_t)(ok ? jb + r : 0) * D + 8 * c, ok ? 16u : 0u);
-        }
-        cp_async_commit();
-    };
-    float sv[4][4];
-    load_s(jb0, sv);
-    stage_v(jb0, 0);
-    __syncthreads();   // mb_s
-    int buf = 0;
-    for (int jb = jb0; jb < je; jb += 64, buf ^= 1) {
-        // numerators of this step (padding keys and rows past m give 0)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int r = (tid >> 4) + 16 * q;
-            const float mb = mb_s[r];
-            const uint2 pk = make_uint2(pack2(ex2(fmaf(sv[q][0], cs, -mb)), ex2(fmaf(sv[q][1], cs, -mb))),
-                                        pack2(ex2(fmaf(sv[q][2], cs, -mb)), ex2(fmaf(sv[q][3], cs, -mb))));
-            *(uint2*)(p_s + swz<128>(r, c4 >> 1) + (c4 & 1) * 8) = pk;
-        }
-        const bool more = jb + 64 < je;
-        if (more) {
-            load_s(jb + 64, sv);
-            stage_v(jb + 64, buf ^ 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
-        const uint32_t uv = uv0 + (uint32_t)buf * 64u * RB;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(up + swz<128>(mt * 16 + arow, 2 * kk + (lane >> 4)), a0, a1, a2, a3);
-            if (fh == 0) mma16816(osum, a0, a1, a2, a3, kOnes2, kOnes2);
-#pragma unroll
-            for (int np = 0; np < NT / 2; ++np) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(uv + swz<RB>(kk * 16 + vrow, fh * NT + 2 * np + (lane >> 4)), b0, b1, b2, b3);
-                mma16816(o[2 * np], a0, a1, a2, a3, b0, b1);
-                mma16816(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
-            }
-        }
-        __syncthreads();   // P and this V buffer are rewritten next
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int i = i0 + mt * 16 + g + 8 * h;
-        if (i >= s.m) continue;
-        float* dst = part + (((size_t)bh * ns + split) * s.m + i) * (D + 1);
-#pragma unroll
-        for (int n = 0; n < NT; ++n) {
-            const int f = fh * (D / 2) + 8 * n + 2 * t;
-            dst[f] = o[n][2 * h];
-            dst[f + 1] = o[n][2 * h + 1];
-        }
-        if (fh == 0 && t == 0) dst[D] = osum[2 * h];
-    }
-}
-
 // V_l[i] = (sum over splits of the partial row) / (sum of the partial row sums).
 template <int D>
 __global__ void tl_values_fin(Shape s, const float* __restrict__ part, int ns, bf16* __restrict__ Vl) {
@@ -405,83 +222,6 @@ __global__ void tl_values_fin(Shape s, const float* __restrict__ part, int ns, b
         den += src[(size_t)sp * s.m * (D + 1) + D];
     }
     Vl[((size_t)bh * s.m + i) * D + f] = __float2bfloat16_rn(num / den);
-}
-
-// ---------------------------------------------------------------- route
-// Block: 128 queries (8 warps x 16) against all landmarks in groups of 64.
-template <int D>
-__global__ void __launch_bounds__(256) tl_route(Shape s, const bf16* __restrict__ Q, const bf16* __restrict__ Ql,
-                                                int32_t* __restrict__ route, int32_t* __restrict__ counts) {
-    constexpr int RB = 2 * D, CH = D / 8;
-    extern __shared__ __align__(128) unsigned char sm[];
-    __shared__ int hist[256];
-    const int q0 = blockIdx.x * 128, bh = blockIdx.y;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-    const int mp = (s.m + 63) / 64 * 64;   // landmark rows staged (zero past m)
-    const uint32_t uq = smem_u32(sm), ul = uq + 128 * RB;
-    const bf16* qsrc = Q + (size_t)bh * s.N * D;
-    const bf16* lsrc = Ql + (size_t)bh * s.m * D;
-    for (int e = tid; e < 128 * CH; e += 256) {
-        const int r = e / CH, c = e % CH;
-        const bool ok = q0 + r < s.N;
-        cp_async16(uq + swz<RB>(r, c), qsrc + (size_t)(ok ? q0 + r : 0) * D + 8 * c, ok ? 16u : 0u);
-    }
-    for (int e = tid; e < mp * CH; e += 256) {
-        const int r = e / CH, c = e % CH;
-        const bool ok = r < s.m;
-        cp_async16(ul + swz<RB>(r, c), lsrc + (size_t)(ok ? r : 0) * D + 8 * c, ok ? 16u : 0u);
-    }
-    cp_async_commit();
-    for (int e = tid; e < 256; e += 256) hist[e] = 0;
-    cp_async_wait<0>();
-    __syncthreads();
-
-    const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, brow = (lane & 7) + (lane >> 4) * 8;
-    uint32_t qa[D / 16][4];
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk)
-        ldsm_x4(uq + swz<RB>(warp * 16 + arow, 2 * kk + (lane >> 4)), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
-    float best[2] = {-INFINITY, -INFINITY};
-    int arg[2] = {0, 0};
-    for (int lg = 0; lg < mp; lg += 64) {
-        float acc[8][4];
-#pragma unroll
-        for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(ul + swz<RB>(lg + np * 16 + brow, 2 * kk + ((lane >> 3) & 1)), b0, b1, b2, b3);
-                mma16816(acc[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-                mma16816(acc[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
-            }
-#pragma unroll
-        for (int n = 0; n < 8; ++n)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int i = lg + 8 * n + 2 * t + (e & 1);
-                const float v = acc[n][e];
-                if (i < s.m && v > best[e >> 1]) { best[e >> 1] = v; arg[e >> 1] = i; }
-            }
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-#pragma unroll
-        for (int o = 1; o <= 2; o <<= 1) {
-            const float ob = __shfl_xor_sync(0xffffffffu, best[h], o);
-            const int oa = __shfl_xor_sync(0xffffffffu, arg[h], o);
-            if (ob > best[h] || (ob == best[h] && oa < arg[h])) { best[h] = ob; arg[h] = oa; }
-        }
-        const int q = q0 + warp * 16 + g + 8 * h;
-        if (t == 0 && q < s.N) {
-            route[(size_t)bh * s.N + q] = arg[h];
-            atomicAdd(&hist[arg[h]], 1);
-        }
-    }
-    __syncthreads();
-    for (int i = tid; i < s.m; i += 256)
-        if (hist[i]) atomicAdd(&counts[(size_t)bh * s.m + i], hist[i]);
 }
 
 // ---------------------------------------------------------------- buckets
@@ -718,36 +458,26 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
     if ((err = cudaMemsetAsync(rowmin, 0xff, (size_t)BH * s.m * 4, st)) != cudaSuccess) return err;
     if ((err = cudaMemsetAsync(p->counts, 0, (size_t)BH * s.m * 4, st)) != cudaSuccess) return err;
     if ((err = staged_pool(s, MITA_BF16, Q, Ql, st)) != cudaSuccess) return err;
-    const int smem_sc = (64 + 128) * RB;
-    cudaFuncSetAttribute(tl_scores<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_sc);
     const int ns = nsplit(s), G = head_group(s);
     for (int h0 = 0; h0 < BH; h0 += G) {
         Shape sg = s;
         sg.B = 1;
         sg.H = min(G, BH - h0);
         const size_t mo = (size_t)h0 * s.m, no = (size_t)h0 * s.N;
-        tl_scores<D><<<dim3((s.N + 127) / 128, (s.m + 63) / 64, sg.H), 256, smem_sc, st>>>(
-            sg, Ql + mo * D, K + no * D, p->S, p->rowmax + mo, rowmin + mo);
+        if ((err = tc_scores(sg, Ql + mo * D, K + no * D, p->S, p->rowmax + mo, rowmin + mo, p->status, st)) !=
+            cudaSuccess)
+            return err;
         if (s.N <= kHistTopkMaxN) {
             tl_topk<<<dim3(s.m, sg.H), kTB, 0, st>>>(sg, p->S, p->rowmax + mo, rowmin + mo, idx + mo * s.k);
         } else {   // long rows: one block per row is too little parallelism for the histogram select
             if ((err = staged_topk(sg, p->S, idx + mo * s.k, st)) != cudaSuccess) return err;
         }
-        if (s.N % 4 == 0)
-            tl_values<D, true><<<dim3(ns, (s.m + 63) / 64, sg.H), 256, 0, st>>>(sg, p->S, p->rowmax + mo,
-                                                                                 V + no * D, p->vpart, cs);
-        else
-            tl_values<D, false><<<dim3(ns, (s.m + 63) / 64, sg.H), 256, 0, st>>>(sg, p->S, p->rowmax + mo,
-                                                                                  V + no * D, p->vpart, cs);
+        if ((err = tc_values(sg, p->S, p->rowmax + mo, V + no * D, p->vpart, cs, p->status, st)) != cudaSuccess)
+            return err;
         tl_values_fin<D><<<dim3(s.m, sg.H), D, 0, st>>>(sg, p->vpart, ns, Vl + mo * D);
         p->launches += 4;
     }
-    {
-        const int smem = (128 + (s.m + 63) / 64 * 64) * RB;
-        auto kern = tl_route<D>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        kern<<<dim3((s.N + 127) / 128, BH), 256, smem, st>>>(s, Q, Ql, route, p->counts);
-    }
+    if ((err = tc_route(s, Q, Ql, route, p->counts, p->status, st)) != cudaSuccess) return err;
     const int maxt = max_tiles(s);
     tl_bucket_off<<<BH, 32, 0, st>>>(s, p->counts, p->offsets, p->cursor, p->tiles, p->ntiles, maxt);
     tl_bucket_put<<<dim3((s.N + 255) / 256, BH), 256, 0, st>>>(s, route, p->cursor, p->perm, p->status);
