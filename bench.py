@@ -218,6 +218,13 @@ def max_over_ranks(x, ws, device):
     return float(t.item())
 
 
+def whole_job_rate(units_per_rank, ms_per_rank, ws, device):
+    """Whole-job throughput: every rank processes units_per_rank units; the
+    job takes as long as its slowest rank (max over ranks)."""
+    ms = max_over_ranks(ms_per_rank, ws, device)
+    return ws * units_per_rank / (ms / 1000.0), ms
+
+
 def run_reference(args, w, ws, rank):
     if rank != 0:
         return 0
@@ -310,10 +317,8 @@ def main():
     st = plan.status()
     if st != mita.MITA_OK:
         raise SystemExit(f"device status {mita.STATUS.get(st, st)}")
-    ms = max_over_ranks(ms, ws, dev)
-
     qh = w.heads * w.N
-    value = ws * qh / (ms / 1000.0)
+    value, ms = whole_job_rate(qh, ms, ws, dev)
     nbytes, flops = algorithmic(w)
     pk = peaks()
     # dominant kernel: on the fused path the step is one launch; on the
