@@ -66,6 +66,8 @@ SMALL = {
     "deit_s": W["deit_s"].scaled(B=2, H=4),
     "hires56": W["hires56"].scaled(B=1, H=2),
     "long1d_8k": W["long1d"].scaled(B=1, H=2, N=8192, gw=8192, pw=32, m=32),
+    # rows longer than 16K keys: the two-pass long-row top-k (and its fallback)
+    "long1d_32k": W["long1d"].scaled(B=1, H=1, N=32768, gw=32768, pw=128, m=128, k=128),
 }
 
 
