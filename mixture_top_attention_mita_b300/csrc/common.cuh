@@ -125,7 +125,5 @@ struct mita_plan_s {
     int32_t* cursor;       // [BH, m]   bucket scatter cursors
     int32_t* tiles;        // [BH, max tiles] attention tiles (expert << 16 | chunk)
     int32_t* ntiles;       // [BH]
-    // one-kernel path only (null otherwise)
-    void* pool_mat;        // pooling matrix (see fused_pool_matrix)
     uint64_t launches;     // kernels launched so far
 };

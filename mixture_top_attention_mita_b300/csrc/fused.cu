@@ -11,7 +11,7 @@
 //                         (fp32, shared memory) and each query's first argmax
 //                         landmark (the route)
 //   phase C   select      per landmark (warp per landmark) the k best keys,
-//                         ties to the lower index, by a monotone 128-bin
+//                         ties to the lower index, by a monotone 64-bin
 //                         histogram and an exact rank of the boundary bin;
 //                         the bf16 softmax numerators overwrite the scores;
 //                         one warp bucket-sorts the queries by route
@@ -27,9 +27,6 @@
 // persistent grid.
 #include <cuda.h>
 
-#include <algorithm>
-#include <vector>
-
 #include "fused.cuh"
 
 namespace mita {
@@ -40,13 +37,13 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kD = 64;
 constexpr int kSlots = 32;      // shared slots (m <= 32) and routed slots (k <= 32)
 constexpr int kMaxN = 256;
-constexpr int kBins = 128;      // histogram bins of the select
+constexpr int kBins = 64;       // histogram bins of the select
 constexpr int kCand = 32;       // boundary-bin members resolved by exact rank
 constexpr int kTile = 16;       // queries per attention tile
 constexpr int kMaxSmem = 232448;
 
 struct Layout {
-    int N, np16, nk16, sstr, qkv, apB, m16;
+    int N, np16, nk16, sstr, qkv;
     int oQ, oK, oV, oQl, oVl, oS, oIdx, oRoute, oPerm, oCnt, oOff, oTiles, oCtl, oBar, oHist,
         oCand, total;
 };
@@ -59,8 +56,6 @@ static Layout make_layout(int N, int m) {
     L.np16 = align_to(N, 16);
     L.nk16 = L.np16 / 16;
     L.sstr = L.np16 + 4;                 // fp32 words per score row: conflict-free ldmatrix rows
-    L.apB = 2 * (L.np16 + 8);            // bytes per pooling-matrix row (conflict-free ldmatrix rows)
-    L.m16 = align_to(m, 16);             // pooling-matrix rows (MMA row tiles)
     L.qkv = align_to(N * 128, 1024);
     int o = 0;
     auto take = [&](int bytes, int al) { o = align_to(o, al); int r = o; o += bytes; return r; };
@@ -69,7 +64,7 @@ static Layout make_layout(int N, int m) {
     L.oV = take(N * 128, 1024);
     L.oQl = take(kSlots * 128, 128);
     L.oVl = take(kSlots * 128, 128);
-    L.oS = take(std::max(m * L.sstr * 4, L.m16 * L.apB), 128);   // scores / numerators, or the pooling matrix
+    L.oS = take(m * L.sstr * 4, 128);
     L.oIdx = take(kSlots * kSlots, 16);
     L.oRoute = take(kMaxN, 16);
     L.oPerm = take(kMaxN, 16);
@@ -96,8 +91,7 @@ struct Params {
     uint32_t rows[kSlots];    // landmark i pools token rows [lo, hi): lo | hi << 16
     uint32_t cols[kSlots];    // and token columns [lo, hi): lo | hi << 16
     float rcnt[kSlots];       // 1 / (tokens in the bin of landmark i)
-    float cnt[kSlots];        // tokens in the bin of landmark i
-    const __nv_bfloat16* pool_mat;   // [m16, apB / 2] bf16 0/1: token t pooled into landmark i
+    int win[kSlots];          // 16 - ceil(log2(tokens in the bin)): exact-sum exponent window
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -190,48 +184,39 @@ MITA_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "m
 MITA_DEV void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
 // ---------------------------------------------------------------- pooled mean
-// bf16 nearest to S / c when the sum s is within err of the exact bin sum S:
-// the candidate from the fp32 quotient is kept or moved to a neighbour by the
-// position of s against c times the midpoints next to it, trusted only when
-// that position clears err.  Returns false when it does not (a tie or a near
-// tie); the caller then sums the bin again error-free.
-MITA_DEV bool round_mean_bounded(float s, float err, float c, float rc, __nv_bfloat16& out) {
-    const bool neg = s < 0.0f;
-    const float a = fabsf(s);
-    uint16_t b = __bfloat16_as_ushort(__float2bfloat16_rn(a * rc));
+// bf16 nearest (ties to even) to (hi + lo) / c for the exact bin sum hi + lo
+// and a positive integer count c (rc ~ 1/c).  The fp32 quotient picks a
+// candidate b; the exact position of the sum against c times the midpoints
+// next to b (c * midpoint is exact, the fused multiply-add keeps the sign)
+// decides between b and its neighbours.
+MITA_DEV __nv_bfloat16 round_mean(float hi, float lo, float c, float rc) {
+    const bool neg = hi < 0.0f;
+    if (neg) { hi = -hi; lo = -lo; }
+    uint16_t b = __bfloat16_as_ushort(__float2bfloat16_rn((hi + lo) * rc));
     const float v0 = __bfloat162float(__ushort_as_bfloat16(b));
     const float v1 = __bfloat162float(__ushort_as_bfloat16((uint16_t)(b + 1)));
-    const float e_up = fmaf(-c, 0.5f * (v0 + v1), a);
-    if (fabsf(e_up) <= err) return false;
-    if (e_up > 0.0f) {
+    const float e_up = fmaf(-c, 0.5f * (v0 + v1), hi) + lo;
+    if (e_up > 0.0f || (e_up == 0.0f && (b & 1))) {
         b = (uint16_t)(b + 1);
     } else if (b > 0) {
         const float vm = __bfloat162float(__ushort_as_bfloat16((uint16_t)(b - 1)));
-        const float e_dn = fmaf(-c, 0.5f * (vm + v0), a);
-        if (fabsf(e_dn) <= err) return false;
-        if (e_dn < 0.0f) b = (uint16_t)(b - 1);
+        const float e_dn = fmaf(-c, 0.5f * (vm + v0), hi) + lo;
+        if (e_dn < 0.0f || (e_dn == 0.0f && (b & 1))) b = (uint16_t)(b - 1);
     }
     const __nv_bfloat16 r = __ushort_as_bfloat16(b);
-    out = neg ? __hneg(r) : r;
-    return true;
+    return neg ? __hneg(r) : r;
 }
 
-// Exclusive prefix sum of one int per lane over the warp.
-MITA_DEV int warp_excl_scan(int x, int lane) {
-    int incl = x;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    return incl - x;
+MITA_DEV uint32_t umax16x2(uint32_t a, uint32_t b) {
+    uint32_t y;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
+    return y;
 }
-
-// Accumulation-error bound of the tensor-core bin sums, relative to the sum of
-// magnitudes: 2^-17, sixty-four times the unit roundoff of fp32, a generous
-// margin over the few roundings (or truncations) of a 13-step MMA chain.
-constexpr float kPoolErrRel = 7.62939453125e-6f;
-
+MITA_DEV uint32_t umin16x2(uint32_t a, uint32_t b) {
+    uint32_t y;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
+    return y;
+}
 
 // ---------------------------------------------------------------- the kernel
 template <int NV>   // score values per lane in the select: ceil(N / 32)
@@ -288,19 +273,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_load_2d(uV, &mapV, 0, blockIdx.x * N, uBar);
     }
 
-    // the pooling matrix for phase A goes into the score region, which is idle
-    // from the end of phase D until phase B of the next head
-    const int pool_chunks = L.m16 * L.apB / 16;
-    auto copy_pool = [&]() {
-        for (int e = tid; e < pool_chunks; e += kThreads)
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(uS + 16u * (uint32_t)e),
-                         "l"((const unsigned char*)P.pool_mat + 16 * e)
-                         : "memory");
-        asm volatile("cp.async.commit_group;\n" ::: "memory");
-    };
-    copy_pool();
-    if (tid == 0) ctl[2] = 0;
-
     const float cs = P.scale_log2;
     int it = 0;
     for (int head = blockIdx.x; head < BH; head += gridDim.x, ++it) {
@@ -317,82 +289,59 @@ __global__ void __launch_bounds__(kThreads, 2)
                 ctl[1] = 1;
             }
         }
-        asm volatile("cp.async.wait_group 0;\n" ::: "memory");   // this thread's pooling-matrix copy
         __syncthreads();
         if (ctl[1]) break;
         while (!mbar_try_wait(uBar, parity)) {}   // completes at once: acquire for every thread
 
-        // ---------------- phase A: landmark queries
-        // Bin sums on the tensor pipe: Pool^T (m16 x tokens, 0/1) . Q and the
-        // same over |Q| (for the error bound); 8 warps = 2 landmark tiles x 4
-        // feature pairs of n8 tiles.  Elements whose rounding the bound cannot
-        // decide are listed and summed again error-free, one per thread.
-        {
-            uint16_t* fb_list = (uint16_t*)(sm + L.oHist);   // the select's histograms, idle here
-            const int mt = warp >> 2, np = warp & 3;
-            if (mt * 16 < m) {
-                float sa[2][4] = {}, ta[2][4] = {};
-                const int prow = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                const uint32_t pa = uS + (uint32_t)prow * (uint32_t)L.apB + (uint32_t)(lane >> 4) * 16u;
-                for (int kk = 0; kk < L.nk16; ++kk) {
-                    uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-                    ldsm_x4(pa + kk * 32, a0, a1, a2, a3);
-                    const int qrow = min(kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, N - 1);
-                    ldsm_x4_t(uQ + swz(qrow, 2 * np + (lane >> 4)), b0, b1, b2, b3);
-                    mma16816(sa[0], a0, a1, a2, a3, b0, b1);
-                    mma16816(sa[1], a0, a1, a2, a3, b2, b3);
-                    mma16816(ta[0], a0, a1, a2, a3, b0 & 0x7fff7fffu, b1 & 0x7fff7fffu);
-                    mma16816(ta[1], a0, a1, a2, a3, b2 & 0x7fff7fffu, b3 & 0x7fff7fffu);
-                }
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int i = mt * 16 + g + 8 * h;
-                    if (i >= m) continue;
-                    const float cnt = P.cnt[i], rc = P.rcnt[i];
-#pragma unroll
-                    for (int n = 0; n < 2; ++n) {
-                        const int f = 16 * np + 8 * n + 2 * t;
-                        __nv_bfloat16 q0, q1;
-                        const bool ok0 = round_mean_bounded(sa[n][2 * h], ta[n][2 * h] * kPoolErrRel, cnt, rc, q0);
-                        const bool ok1 = round_mean_bounded(sa[n][2 * h + 1], ta[n][2 * h + 1] * kPoolErrRel, cnt, rc, q1);
-                        unsigned char* dst = sm + L.oQl + swz(i, f >> 3) + (f & 7) * 2;
-                        if (ok0 && ok1) {
-                            __nv_bfloat162 q2;
-                            q2.x = q0;
-                            q2.y = q1;
-                            *(__nv_bfloat162*)dst = q2;
-                        } else {
-                            if (ok0) *(__nv_bfloat16*)dst = q0;
-                            else fb_list[atomicAdd(&ctl[2], 1)] = (uint16_t)((i << 6) | f);
-                            if (ok1) *(__nv_bfloat16*)(dst + 2) = q1;
-                            else fb_list[atomicAdd(&ctl[2], 1)] = (uint16_t)((i << 6) | (f + 1));
-                        }
-                    }
+        // ---------------- phase A: landmark queries (warp per landmark)
+        for (int i = warp; i < m; i += kWarps) {
+            const int r0 = P.rows[i] & 0xffff, r1 = P.rows[i] >> 16;
+            const int c0 = P.cols[i] & 0xffff, c1 = P.cols[i] >> 16;
+            const uint32_t lo_off = (uint32_t)(lane & 3) * 4u;
+            const int chunk = lane >> 2;
+            // fp32 sums of the bin (features 2*lane, 2*lane+1) and the largest and
+            // smallest bf16 magnitude of each feature (packed 16-bit halves)
+            float s0 = 0.0f, s1 = 0.0f;
+            uint32_t mag_hi = 0u, mag_lo = 0x7fff7fffu;
+            for (int y = r0; y < r1; ++y) {
+                const int rb = y * s.gw;
+#pragma unroll 4
+                for (int x = c0; x < c1; ++x) {
+                    const uint32_t v = *(const uint32_t*)(Qb + swz(rb + x, chunk) + lo_off);
+                    s0 += bf_lo(v);
+                    s1 += bf_hi(v);
+                    const uint32_t mag = v & 0x7fff7fffu;
+                    mag_hi = umax16x2(mag_hi, mag);
+                    mag_lo = umin16x2(mag_lo, mag);
                 }
             }
-            __syncthreads();
-            const int nfb = ctl[2];
-            for (int e = tid; e < nfb; e += kThreads) {
-                const int i = fb_list[e] >> 6, f = fb_list[e] & 63;
-                const int r0 = P.rows[i] & 0xffff, r1 = P.rows[i] >> 16;
-                const int c0 = P.cols[i] & 0xffff, c1 = P.cols[i] >> 16;
-                float hi = 0.0f, lo = 0.0f;
+            // The sums are exact when no value is zero and the exponents span at
+            // most P.win[i] binades (then every partial sum is a multiple of the
+            // smallest value's last bit below 2^24 of them); otherwise sum again
+            // error-free (rare for continuous data).
+            const int win = P.win[i];
+            const bool exact0 = (mag_lo & 0xffffu) != 0u &&
+                                (int)((mag_hi >> 7) & 0xffu) - (int)((mag_lo >> 7) & 0xffu) <= win;
+            const bool exact1 = (mag_lo >> 16) != 0u &&
+                                (int)((mag_hi >> 23) & 0xffu) - (int)((mag_lo >> 23) & 0xffu) <= win;
+            float h0 = s0, l0 = 0.0f, h1 = s1, l1 = 0.0f;
+            if (!exact0 || !exact1) {
+                h0 = l0 = h1 = l1 = 0.0f;
                 for (int y = r0; y < r1; ++y)
                     for (int x = c0; x < c1; ++x) {
-                        const uint32_t v = *(const uint16_t*)(Qb + swz(y * s.gw + x, f >> 3) + (f & 7) * 2);
-                        acc2(hi, lo, __uint_as_float(v << 16));
+                        const uint32_t v = *(const uint32_t*)(Qb + swz(y * s.gw + x, chunk) + lo_off);
+                        acc2(h0, l0, bf_lo(v));
+                        acc2(h1, l1, bf_hi(v));
                     }
-                *(__nv_bfloat16*)(sm + L.oQl + swz(i, f >> 3) + (f & 7) * 2) = mean_to_bf16(hi, lo, P.cnt[i]);
             }
-            __syncthreads();
-            if (tid == 0) ctl[2] = 0;
-            for (int e = tid; e < kWarps * kBins; e += kThreads) ((int*)(sm + L.oHist))[e] = 0;
-            if (P.Ql_keep)
-                for (int e = tid; e < m * 32; e += kThreads) {
-                    const int i = e >> 5, fp = e & 31;
-                    *(uint32_t*)(P.Ql_keep + ((size_t)head * m + i) * kD + 2 * fp) =
-                        *(const uint32_t*)(sm + L.oQl + swz(i, fp >> 2) + (fp & 3) * 4);
-                }
+            const float cnt = (float)((r1 - r0) * (c1 - c0)), rc = P.rcnt[i];
+            const __nv_bfloat16 q0 = round_mean(h0, l0, cnt, rc);
+            const __nv_bfloat16 q1 = round_mean(h1, l1, cnt, rc);
+            __nv_bfloat162 q2;
+            q2.x = q0;
+            q2.y = q1;
+            *(__nv_bfloat162*)(sm + L.oQl + swz(i, chunk) + lo_off) = q2;
+            if (P.Ql_keep) *(__nv_bfloat162*)(P.Ql_keep + ((size_t)head * m + i) * kD + 2 * lane) = q2;
         }
         __syncthreads();
 
@@ -470,15 +419,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         __syncthreads();
 
-        // ---------------- phase C: experts and numerators (warp per landmark;
-        // lane L owns keys [NV*L, NV*L + NV) of the landmark's row)
+        // ---------------- phase C: experts and numerators (warp per landmark)
         for (int i = warp; i < m; i += kWarps) {
             float* srow = S_s + i * L.sstr;
-            const int j0 = NV * lane;
-            const int nval = max(0, min(NV, N - j0));   // valid keys of this lane
             float v[NV];
 #pragma unroll
-            for (int u = 0; u < NV; ++u) v[u] = srow[u < nval ? j0 + u : 0];   // key 0 pads: max / min unchanged
+            for (int u = 0; u < NV; ++u) {
+                const int j = lane + 32 * u;
+                v[u] = srow[j < N ? j : 0];   // a slot past N repeats key 0: max / min unchanged
+            }
             float mx = v[0], mn = v[0];
 #pragma unroll
             for (int u = 1; u < NV; u += 2) {
@@ -497,72 +446,69 @@ __global__ void __launch_bounds__(kThreads, 2)
             int bin[NV];
 #pragma unroll
             for (int u = 0; u < NV; ++u) {
-                bin[u] = min(kBins - 1, (int)((v[u] - mn) * sc));
-                if (u < nval) atomicAdd(&hist[bin[u]], 1);
-                else bin[u] = -1;
+                const int j = lane + 32 * u;
+                bin[u] = -1;
+                if (j < N) {
+                    bin[u] = min(kBins - 1, (int)((v[u] - mn) * sc));
+                    atomicAdd(&hist[bin[u]], 1);
+                }
             }
             __syncwarp();
-            // lane L holds bins 4L .. 4L+3; suffix counts from the top bin down
-            const int4 hw = *(const int4*)(hist + 4 * lane);
-            *(int4*)(hist + 4 * lane) = make_int4(0, 0, 0, 0);   // each lane clears what it read
-            const int hc[4] = {hw.x, hw.y, hw.z, hw.w};
-            const int tot = hw.x + hw.y + hw.z + hw.w;
+            // lane L holds bins 2L, 2L+1; suffix counts from the top bin down
+            const int2 hw = *(const int2*)(hist + 2 * lane);
+            *(int2*)(hist + 2 * lane) = make_int2(0, 0);   // each lane clears what it read
+            const int tot = hw.x + hw.y;
             int suf = tot;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_down_sync(0xffffffffu, suf, o);
                 if (lane + o < 32) suf += y;
             }
-            const int above = suf - tot;   // members of bins above 4L+3
+            const int above = suf - tot;   // members of bins above 2L+1
             const bool mine = above < k && suf >= k;
             int bstar = 0, need = 0, cstar = 0;
             if (mine) {
-                int run = above;
-#pragma unroll
-                for (int u = 3; u >= 0; --u) {
-                    if (need == 0 && run + hc[u] >= k) {
-                        bstar = 4 * lane + u;
-                        need = k - run;
-                        cstar = hc[u];
-                    }
-                    run += hc[u];
+                if (above + hw.y >= k) {
+                    bstar = 2 * lane + 1;
+                    need = k - above;
+                    cstar = hw.y;
+                } else {
+                    bstar = 2 * lane;
+                    need = k - above - hw.y;
+                    cstar = hw.x;
                 }
             }
             const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
             bstar = __shfl_sync(0xffffffffu, bstar, src);
             need = __shfl_sync(0xffffffffu, need, src);
             cstar = __shfl_sync(0xffffffffu, cstar, src);
-            uint32_t selm = 0, bmem = 0;   // bit u: key j0+u selected / in the boundary bin
-#pragma unroll
-            for (int u = 0; u < NV; ++u) {
-                selm |= (bin[u] > bstar ? 1u : 0u) << u;
-                bmem |= (bin[u] == bstar ? 1u : 0u) << u;
-            }
             // boundary bin: take the `need` best of its `cstar` members
+            uint32_t bsel = 0;   // bit u: member lane + 32u is taken
             if (need < cstar) {
-                // members in ascending key order: lane L's members follow those of lanes < L
-                const int bbase = warp_excl_scan(__popc(bmem), lane);
                 if (cstar <= kCand) {
-                    int r = bbase;
+                    // members to lanes 0 .. cstar-1, exact rank by (score desc, index asc)
+                    int base = 0, slot[NV];
 #pragma unroll
-                    for (int u = 0; u < NV; ++u)
-                        if ((bmem >> u) & 1u) cand[r++] = make_float2(v[u], 0.0f);
+                    for (int u = 0; u < NV; ++u) {
+                        const bool isb = bin[u] == bstar;
+                        const unsigned bal = __ballot_sync(0xffffffffu, isb);
+                        slot[u] = base + __popc(bal & ((1u << lane) - 1u));
+                        if (isb) cand[slot[u]] = make_float2(v[u], __int_as_float(lane + 32 * u));
+                        base += __popc(bal);
+                    }
                     __syncwarp();
-                    // exact rank by (score desc, key asc); member order is key order
-                    const float me = cand[lane < cstar ? lane : 0].x;
+                    const float2 me = cand[lane < cstar ? lane : 0];
+                    const int jm = __float_as_int(me.y);
                     int rank = 0;
                     for (int e = 0; e < cstar; ++e) {
-                        const float ve = __shfl_sync(0xffffffffu, me, e);
-                        rank += (ve > me || (ve == me && e < lane)) ? 1 : 0;
+                        const float ve = __shfl_sync(0xffffffffu, me.x, e);
+                        const int je = __shfl_sync(0xffffffffu, jm, e);
+                        rank += (ve > me.x || (ve == me.x && je < jm)) ? 1 : 0;
                     }
                     const unsigned chosen = __ballot_sync(0xffffffffu, lane < cstar && rank < need);
-                    r = bbase;
 #pragma unroll
                     for (int u = 0; u < NV; ++u)
-                        if ((bmem >> u) & 1u) {
-                            selm |= ((chosen >> r) & 1u) << u;
-                            ++r;
-                        }
+                        if (bin[u] == bstar && ((chosen >> slot[u]) & 1u)) bsel |= 1u << u;
                     __syncwarp();
                 } else {
                     // many members (degenerate scores): bisect the order key
@@ -574,47 +520,48 @@ __global__ void __launch_bounds__(kThreads, 2)
                         const uint32_t cand_t = T | (1u << b);
                         int c = 0;
 #pragma unroll
-                        for (int u = 0; u < NV; ++u) c += (((bmem >> u) & 1u) && key[u] >= cand_t) ? 1 : 0;
+                        for (int u = 0; u < NV; ++u) c += (bin[u] == bstar && key[u] >= cand_t) ? 1 : 0;
                         c = __reduce_add_sync(0xffffffffu, c);
                         if (c >= need) T = cand_t;
                     }
-                    int gt = 0, eq = 0;
+                    int gt = 0;
 #pragma unroll
-                    for (int u = 0; u < NV; ++u) {
-                        const bool isb = (bmem >> u) & 1u;
-                        gt += (isb && key[u] > T) ? 1 : 0;
-                        eq += (isb && key[u] == T) ? 1 : 0;
-                    }
+                    for (int u = 0; u < NV; ++u) gt += (bin[u] == bstar && key[u] > T) ? 1 : 0;
                     gt = __reduce_add_sync(0xffffffffu, gt);
-                    int r = warp_excl_scan(eq, lane);   // ties at T: lower keys first
-                    const int eq_left = need - gt;
+                    int eq_left = need - gt, base = 0;
 #pragma unroll
                     for (int u = 0; u < NV; ++u) {
-                        const bool isb = (bmem >> u) & 1u;
-                        if (isb && key[u] > T) selm |= 1u << u;
-                        if (isb && key[u] == T) {
-                            if (r < eq_left) selm |= 1u << u;
-                            ++r;
-                        }
+                        const bool isb = bin[u] == bstar;
+                        const bool eq = isb && key[u] == T;
+                        const unsigned bal = __ballot_sync(0xffffffffu, eq);
+                        const int r = base + __popc(bal & ((1u << lane) - 1u));
+                        if ((isb && key[u] > T) || (eq && r < eq_left)) bsel |= 1u << u;
+                        base += __popc(bal);
                     }
                 }
             } else {
-                selm |= bmem;
+#pragma unroll
+                for (int u = 0; u < NV; ++u)
+                    if (bin[u] == bstar) bsel |= 1u << u;
             }
             // the expert in ascending key order
-            int pos = warp_excl_scan(__popc(selm), lane);
+            int pos = 0;
             uint8_t* irow = idx_s + i * kSlots;
 #pragma unroll
-            for (int u = 0; u < NV; ++u)
-                if ((selm >> u) & 1u) irow[pos++] = (uint8_t)(j0 + u);
+            for (int u = 0; u < NV; ++u) {
+                const bool sel = bin[u] > bstar || (bsel >> u & 1u);
+                const unsigned bal = __ballot_sync(0xffffffffu, sel);
+                if (sel) irow[pos + __popc(bal & ((1u << lane) - 1u))] = (uint8_t)(lane + 32 * u);
+                pos += __popc(bal);
+            }
             // softmax numerators of the landmark row, bf16 as the MMA reads them,
             // written over the row's own scores (every lane has read them)
             __nv_bfloat16* prow = (__nv_bfloat16*)srow;
             const float mb = mx * cs;
 #pragma unroll
             for (int u = 0; u < NV; ++u) {
-                const int j = j0 + u;
-                if (j < L.np16) prow[j] = __float2bfloat16_rn(u < nval ? ex2(fmaf(v[u], cs, -mb)) : 0.0f);
+                const int j = lane + 32 * u;
+                if (j < L.np16) prow[j] = __float2bfloat16_rn(j < N ? ex2(fmaf(v[u], cs, -mb)) : 0.0f);
             }
             __syncwarp();
             if (lane < k) P.idx[((size_t)head * m + i) * k + lane] = irow[lane];
@@ -686,7 +633,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncthreads();
 
         // ---------------- phase E: grouped attention, kTile queries per tile
-        if (head + (int)gridDim.x < BH) copy_pool();   // for the next head (the score region is idle now)
         const int ntiles = ctl[0];
         for (int tile = warp; tile < ntiles; tile += kWarps) {
             const int b = tiles_s[tile] >> 8, st = tiles_s[tile] & 255;
@@ -848,27 +794,6 @@ static bool make_map(CUtensorMap* map, const void* base, int rows, int box_rows)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t fused_pool_bytes(const Shape& s) {
-    const fz::Layout L = fz::make_layout(s.N, s.m);
-    return (size_t)L.m16 * L.apB;
-}
-
-void fused_pool_matrix(const Shape& s, uint16_t* dst) {
-    // row i (landmark), column t (token): bf16 1.0 when token t lies in the
-    // adaptive average pooling bin [floor(r*G/P), ceil((r+1)*G/P)) x (same for
-    // columns) of landmark i = r * pw + c; zero elsewhere and in padding
-    const fz::Layout L = fz::make_layout(s.N, s.m);
-    const int stride = L.apB / 2;
-    std::fill(dst, dst + (size_t)L.m16 * stride, (uint16_t)0);
-    for (int i = 0; i < s.m; ++i) {
-        const int r = i / s.pw, c = i % s.pw;
-        const int r0 = r * s.gh / s.ph, r1 = ((r + 1) * s.gh + s.ph - 1) / s.ph;
-        const int c0 = c * s.gw / s.pw, c1 = ((c + 1) * s.gw + s.pw - 1) / s.pw;
-        for (int y = r0; y < r1; ++y)
-            for (int x = c0; x < c1; ++x) dst[(size_t)i * stride + y * s.gw + x] = 0x3F80u;
-    }
-}
-
 bool fused_supported(const Shape& s, mita_dtype_t dtype) {
     if (dtype != MITA_BF16 || s.d != fz::kD) return false;
     if (s.N > fz::kMaxN || s.m > fz::kSlots || s.k > fz::kSlots) return false;
@@ -908,8 +833,6 @@ cudaError_t run_fused(mita_plan_s* p, const void* Q, const void* K, const void* 
     prm.Ql_keep = keep_landmarks ? (__nv_bfloat16*)p->Ql : nullptr;
     prm.Vl_keep = keep_landmarks ? (__nv_bfloat16*)p->Vl : nullptr;
     prm.status = p->status;
-    prm.pool_mat = (const __nv_bfloat16*)p->pool_mat;
-    if (!prm.pool_mat) return cudaErrorInvalidValue;
     prm.scale_log2 = kLog2e / sqrtf((float)s.d);
     for (int i = 0; i < s.m; ++i) {
         // adaptive average pooling bins [floor(r*G/P), ceil((r+1)*G/P)) per axis
@@ -919,8 +842,10 @@ cudaError_t run_fused(mita_plan_s* p, const void* Q, const void* K, const void* 
         prm.rows[i] = (uint32_t)r0 | ((uint32_t)r1 << 16);
         prm.cols[i] = (uint32_t)c0 | ((uint32_t)c1 << 16);
         const int n = (r1 - r0) * (c1 - c0);
+        int lg = 0;
+        while ((1 << lg) < n) ++lg;
         prm.rcnt[i] = 1.0f / (float)n;
-        prm.cnt[i] = (float)n;
+        prm.win[i] = 16 - lg;
     }
     cudaError_t e;
     switch ((s.N + 31) / 32) {

@@ -76,8 +76,7 @@ int mita_plan(mita_plan_t* plan, int B, int H, int N, int d, mita_grid_t grid, i
     const size_t oCursor = take(tiled ? BH * m * 4 : 0);
     const size_t oTiles = take(tiled ? BH * (size_t)mita::tiled_max_tiles(p->s) * 4 : 0);
     const size_t oNtiles = take(tiled ? BH * 4 : 0);
-    const bool fused = mita::fused_supported(p->s, dtype);
-    const size_t oPool = take(fused ? mita::fused_pool_bytes(p->s) : 0);
+
     p->ws_bytes = off;
     if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -100,22 +99,6 @@ int mita_plan(mita_plan_t* plan, int B, int H, int N, int d, mita_grid_t grid, i
         p->cursor = (int32_t*)(b + oCursor);
         p->tiles = (int32_t*)(b + oTiles);
         p->ntiles = (int32_t*)(b + oNtiles);
-    }
-    if (fused) {
-        p->pool_mat = b + oPool;
-        const size_t nb = mita::fused_pool_bytes(p->s);
-        uint16_t* host = (uint16_t*)malloc(nb);
-        bool ok = host != nullptr;
-        if (ok) {
-            mita::fused_pool_matrix(p->s, host);
-            ok = cudaMemcpy(p->pool_mat, host, nb, cudaMemcpyHostToDevice) == cudaSuccess;
-        }
-        free(host);
-        if (!ok) {
-            cudaFree(p->ws);
-            free(p);
-            return MITA_ERR_CUDA;
-        }
     }
     if (cudaMemset(p->status, 0, 256) != cudaSuccess) {
         cudaFree(p->ws);
