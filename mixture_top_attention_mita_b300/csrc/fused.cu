@@ -82,6 +82,9 @@ static Layout make_layout(int N, int m) {
 struct Params {
     Shape s;
     Layout L;
+    const unsigned char* Qg;  // inputs, for the L2 prefetch of the next head
+    const unsigned char* Kg;
+    const unsigned char* Vg;
     int32_t* idx;
     int32_t* route;
     __nv_bfloat16* Ql_keep;   // nullptr unless landmarks are kept
@@ -177,6 +180,9 @@ MITA_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, ui
 MITA_DEV void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];\n" ::"l"(map),
                  "r"(x), "r"(y), "r"(src) : "memory");
+}
+MITA_DEV void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
 }
 MITA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 MITA_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
@@ -292,6 +298,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncthreads();
         if (ctl[1]) break;
         while (!mbar_try_wait(uBar, parity)) {}   // completes at once: acquire for every thread
+
+        if (tid == 0 && head + (int)gridDim.x < BH) {
+            // the next head's tiles into L2 now, so that their TMA load at the end of
+            // this head is short
+            const size_t off = (size_t)(head + gridDim.x) * N * 128;
+            prefetch_l2(P.Qg + off, (uint32_t)N * 128u);
+            prefetch_l2(P.Kg + off, (uint32_t)N * 128u);
+            prefetch_l2(P.Vg + off, (uint32_t)N * 128u);
+        }
 
         // ---------------- phase A: landmark queries (warp per landmark)
         for (int i = warp; i < m; i += kWarps) {
@@ -828,6 +843,9 @@ cudaError_t run_fused(mita_plan_s* p, const void* Q, const void* K, const void* 
     fz::Params prm{};
     prm.s = s;
     prm.L = fz::make_layout(s.N, s.m);
+    prm.Qg = (const unsigned char*)Q;
+    prm.Kg = (const unsigned char*)K;
+    prm.Vg = (const unsigned char*)V;
     prm.idx = idx;
     prm.route = route;
     prm.Ql_keep = keep_landmarks ? (__nv_bfloat16*)p->Ql : nullptr;

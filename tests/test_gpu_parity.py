@@ -135,6 +135,25 @@ def test_edge_shapes(i, path):
     compare_batch(w, Q, K, V, r["out"], r["idx"], r["route"], exact=_means_exact(w, Q))
 
 
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("kind", ["flat", "two_values"])
+def test_flat_and_tied_rows(kind, path):
+    """Rows whose scores are all equal (every key ties: the expert is the first
+    k keys) or take two values (the boundary holds far more tied keys than a
+    rank list keeps): the selects' many-ties fallbacks."""
+    w = SMALL["deit_s"]
+    _skip_unbuilt(w, path)
+    Q, K, V = synth.make_integer_inputs(w, seed=31)
+    if kind == "flat":
+        Q, K = torch.ones_like(Q), torch.ones_like(K)
+    else:
+        g = torch.Generator("cpu").manual_seed(5)
+        pick = torch.randint(0, 2, (w.B, w.H, w.N), generator=g)
+        K = torch.where(pick[..., None].bool(), K[:, :, :1, :], K[:, :, 1:2, :]).contiguous()
+    r = _run(w, Q, K, V, path)
+    compare_batch(w, Q, K, V, r["out"], r["idx"], r["route"], exact=True)
+
+
 def _means_exact(w, Q):
     """True when every pooled mean of these integer inputs is exactly
     representable in the I/O type, so that all fp32 sums are exact."""
