@@ -27,6 +27,8 @@
 // persistent grid.
 #include <cuda.h>
 
+#include <algorithm>
+
 #include "fused.cuh"
 
 namespace mita {
@@ -41,6 +43,7 @@ constexpr int kBins = 64;       // histogram bins of the select
 constexpr int kCand = 32;       // boundary-bin members resolved by exact rank
 constexpr int kTile = 16;       // queries per attention tile
 constexpr int kMaxSmem = 232448;
+constexpr int kTokMax = 1024;   // bin memberships of all landmarks (the pool's token table)
 
 struct Layout {
     int N, np16, nk16, sstr, qkv;
@@ -64,7 +67,7 @@ static Layout make_layout(int N, int m) {
     L.oV = take(N * 128, 1024);
     L.oQl = take(kSlots * 128, 128);
     L.oVl = take(kSlots * 128, 128);
-    L.oS = take(m * L.sstr * 4, 128);
+    L.oS = take(std::max(m * L.sstr * 4, m * 128), 128);   // scores / numerators, or the pool's fallback list
     L.oIdx = take(kSlots * kSlots, 16);
     L.oRoute = take(kMaxN, 16);
     L.oPerm = take(kMaxN, 16);
@@ -91,10 +94,11 @@ struct Params {
     __nv_bfloat16* Vl_keep;
     int32_t* status;
     float scale_log2;         // log2(e) / sqrt(d)
-    uint32_t rows[kSlots];    // landmark i pools token rows [lo, hi): lo | hi << 16
-    uint32_t cols[kSlots];    // and token columns [lo, hi): lo | hi << 16
     float rcnt[kSlots];       // 1 / (tokens in the bin of landmark i)
+    float cnt[kSlots];        // tokens in the bin of landmark i
     int win[kSlots];          // 16 - ceil(log2(tokens in the bin)): exact-sum exponent window
+    uint16_t tstart[kSlots + 1];   // landmark i pools tokens toff[tstart[i] .. tstart[i + 1])
+    uint16_t toff[kTokMax];        // byte offset of a token's row in the swizzled Q tile, r*128 + (r%8)*16
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -266,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (tid == 0) {
         mbar_init(uBar, 1);
         ctl[1] = 0;
+        ctl[2] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     __syncthreads();
@@ -309,54 +314,58 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
 
         // ---------------- phase A: landmark queries (warp per landmark)
-        for (int i = warp; i < m; i += kWarps) {
-            const int r0 = P.rows[i] & 0xffff, r1 = P.rows[i] >> 16;
-            const int c0 = P.cols[i] & 0xffff, c1 = P.cols[i] >> 16;
-            const uint32_t lo_off = (uint32_t)(lane & 3) * 4u;
-            const int chunk = lane >> 2;
-            // fp32 sums of the bin (features 2*lane, 2*lane+1) and the largest and
-            // smallest bf16 magnitude of each feature (packed 16-bit halves)
-            float s0 = 0.0f, s1 = 0.0f;
-            uint32_t mag_hi = 0u, mag_lo = 0x7fff7fffu;
-            for (int y = r0; y < r1; ++y) {
-                const int rb = y * s.gw;
+        // Lane L sums features 2L, 2L+1 over the bin's tokens (a flat list of
+        // row offsets; a lane's 4 bytes of a swizzled row sit at offset ^ lx).
+        // The fp32 sums are exact when no value is zero and the exponents span
+        // at most P.win[i] binades (then every partial sum is a multiple of the
+        // smallest value's last bit below 2^24 of them); features without that
+        // certificate are listed and summed again error-free after the loop.
+        {
+            uint16_t* fb_list = (uint16_t*)S_s;   // the scores' region is idle until phase B
+            const uint32_t lx = ((uint32_t)(lane >> 2) << 4) | ((uint32_t)(lane & 3) * 4u);
+            for (int i = warp; i < m; i += kWarps) {
+                const int e0 = P.tstart[i], e1 = P.tstart[i + 1];
+                float s0 = 0.0f, s1 = 0.0f;
+                uint32_t mag_hi = 0u, mag_lo = 0x7fff7fffu;
 #pragma unroll 4
-                for (int x = c0; x < c1; ++x) {
-                    const uint32_t v = *(const uint32_t*)(Qb + swz(rb + x, chunk) + lo_off);
-                    s0 += bf_lo(v);
-                    s1 += bf_hi(v);
+                for (int e = e0; e < e1; ++e) {
+                    const uint32_t v = *(const uint32_t*)(Qb + ((uint32_t)P.toff[e] ^ lx));
+                    s0 += __uint_as_float(v << 16);
+                    s1 += __uint_as_float(v & 0xffff0000u);
                     const uint32_t mag = v & 0x7fff7fffu;
                     mag_hi = umax16x2(mag_hi, mag);
                     mag_lo = umin16x2(mag_lo, mag);
                 }
+                const int win = P.win[i];
+                const bool exact0 = (mag_lo & 0xffffu) != 0u &&
+                                    (int)((mag_hi >> 7) & 0xffu) - (int)((mag_lo >> 7) & 0xffu) <= win;
+                const bool exact1 = (mag_lo >> 16) != 0u &&
+                                    (int)((mag_hi >> 23) & 0xffu) - (int)((mag_lo >> 23) & 0xffu) <= win;
+                const float cnt = P.cnt[i], rc = P.rcnt[i];
+                unsigned char* dst = sm + L.oQl + ((uint32_t)(i * 128 + (i & 7) * 16) ^ lx);
+                if (exact0) *(__nv_bfloat16*)dst = round_mean(s0, 0.0f, cnt, rc);
+                else fb_list[atomicAdd(&ctl[2], 1)] = (uint16_t)((i << 6) | (2 * lane));
+                if (exact1) *(__nv_bfloat16*)(dst + 2) = round_mean(s1, 0.0f, cnt, rc);
+                else fb_list[atomicAdd(&ctl[2], 1)] = (uint16_t)((i << 6) | (2 * lane + 1));
             }
-            // The sums are exact when no value is zero and the exponents span at
-            // most P.win[i] binades (then every partial sum is a multiple of the
-            // smallest value's last bit below 2^24 of them); otherwise sum again
-            // error-free (rare for continuous data).
-            const int win = P.win[i];
-            const bool exact0 = (mag_lo & 0xffffu) != 0u &&
-                                (int)((mag_hi >> 7) & 0xffu) - (int)((mag_lo >> 7) & 0xffu) <= win;
-            const bool exact1 = (mag_lo >> 16) != 0u &&
-                                (int)((mag_hi >> 23) & 0xffu) - (int)((mag_lo >> 23) & 0xffu) <= win;
-            float h0 = s0, l0 = 0.0f, h1 = s1, l1 = 0.0f;
-            if (!exact0 || !exact1) {
-                h0 = l0 = h1 = l1 = 0.0f;
-                for (int y = r0; y < r1; ++y)
-                    for (int x = c0; x < c1; ++x) {
-                        const uint32_t v = *(const uint32_t*)(Qb + swz(y * s.gw + x, chunk) + lo_off);
-                        acc2(h0, l0, bf_lo(v));
-                        acc2(h1, l1, bf_hi(v));
-                    }
+            __syncthreads();
+            const int nfb = ctl[2];
+            for (int x = tid; x < nfb; x += kThreads) {
+                const int i = fb_list[x] >> 6, f = fb_list[x] & 63;
+                const uint32_t fx = ((uint32_t)(f >> 3) << 4) | ((uint32_t)(f & 7) * 2u);
+                float hi = 0.0f, lo = 0.0f;
+                for (int e = P.tstart[i]; e < P.tstart[i + 1]; ++e)
+                    acc2(hi, lo, __uint_as_float((uint32_t)*(const uint16_t*)(Qb + ((uint32_t)P.toff[e] ^ fx)) << 16));
+                *(__nv_bfloat16*)(sm + L.oQl + ((uint32_t)(i * 128 + (i & 7) * 16) ^ fx)) = mean_to_bf16(hi, lo, P.cnt[i]);
             }
-            const float cnt = (float)((r1 - r0) * (c1 - c0)), rc = P.rcnt[i];
-            const __nv_bfloat16 q0 = round_mean(h0, l0, cnt, rc);
-            const __nv_bfloat16 q1 = round_mean(h1, l1, cnt, rc);
-            __nv_bfloat162 q2;
-            q2.x = q0;
-            q2.y = q1;
-            *(__nv_bfloat162*)(sm + L.oQl + swz(i, chunk) + lo_off) = q2;
-            if (P.Ql_keep) *(__nv_bfloat162*)(P.Ql_keep + ((size_t)head * m + i) * kD + 2 * lane) = q2;
+            __syncthreads();
+            if (tid == 0) ctl[2] = 0;
+            if (P.Ql_keep)
+                for (int x = tid; x < m * 32; x += kThreads) {
+                    const int i = x >> 5, fp = x & 31;
+                    *(uint32_t*)(P.Ql_keep + ((size_t)head * m + i) * kD + 2 * fp) =
+                        *(const uint32_t*)(sm + L.oQl + swz(i, fp >> 2) + (fp & 3) * 4);
+                }
         }
         __syncthreads();
 
@@ -852,19 +861,27 @@ cudaError_t run_fused(mita_plan_s* p, const void* Q, const void* K, const void* 
     prm.Vl_keep = keep_landmarks ? (__nv_bfloat16*)p->Vl : nullptr;
     prm.status = p->status;
     prm.scale_log2 = kLog2e / sqrtf((float)s.d);
+    int ntok = 0;
     for (int i = 0; i < s.m; ++i) {
         // adaptive average pooling bins [floor(r*G/P), ceil((r+1)*G/P)) per axis
         const int r = i / s.pw, c = i % s.pw;
         const int r0 = r * s.gh / s.ph, r1 = ((r + 1) * s.gh + s.ph - 1) / s.ph;
         const int c0 = c * s.gw / s.pw, c1 = ((c + 1) * s.gw + s.pw - 1) / s.pw;
-        prm.rows[i] = (uint32_t)r0 | ((uint32_t)r1 << 16);
-        prm.cols[i] = (uint32_t)c0 | ((uint32_t)c1 << 16);
+        prm.tstart[i] = (uint16_t)ntok;
+        for (int y = r0; y < r1; ++y)
+            for (int x = c0; x < c1; ++x) {
+                const int t = y * s.gw + x;
+                if (ntok >= fz::kTokMax) return cudaErrorInvalidValue;
+                prm.toff[ntok++] = (uint16_t)(t * 128 + (t & 7) * 16);
+            }
         const int n = (r1 - r0) * (c1 - c0);
+        prm.cnt[i] = (float)n;
         int lg = 0;
         while ((1 << lg) < n) ++lg;
         prm.rcnt[i] = 1.0f / (float)n;
         prm.win[i] = 16 - lg;
     }
+    prm.tstart[s.m] = (uint16_t)ntok;
     cudaError_t e;
     switch ((s.N + 31) / 32) {
         case 1: e = launch_nv<1>(mq, mk, mv, mo, prm, p->device, st); break;
