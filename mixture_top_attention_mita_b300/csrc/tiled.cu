@@ -36,6 +36,7 @@ using bf16 = __nv_bfloat16;
 using namespace mx;
 
 constexpr int kQT = 64;     // queries per attention tile (4 warps x 16)
+constexpr int kMaxK = 512;  // routed keys per expert
 
 int nsplit(const Shape& s) { return tc_value_splits(s); }
 int max_tiles(const Shape& s) { return (s.N + kQT - 1) / kQT + s.m; }
@@ -287,6 +288,7 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
     constexpr int RB = 2 * D, CH = D / 8, KS = D / 16, NT = D / 8;
     extern __shared__ __align__(128) unsigned char sm[];
     __shared__ int rows_s[kQT];
+    __shared__ int E_s[kMaxK];   // the expert's key indices (read once per tile, not per staged row)
     const int bh = blockIdx.y, tile = blockIdx.x;
     if (tile >= ntiles[bh]) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, t = lane & 3;
@@ -301,6 +303,11 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
         int q = perm[(size_t)bh * s.N + qstart + min(tid, nq - 1)];
         if (q < 0 || q >= s.N) { atomicExch(status, (int)MITA_ERR_DEVICE); q = 0; }
         rows_s[tid] = q;
+    }
+    for (int x = tid; x < s.k; x += 128) {
+        int j = E[x];
+        if (j < 0 || j >= s.N) { atomicExch(status, (int)MITA_ERR_DEVICE); j = 0; }
+        E_s[x] = j;
     }
     __syncthreads();
     for (int x = tid; x < kQT * CH; x += 128) {
@@ -317,8 +324,7 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
                 ks = Ql + ((size_t)bh * s.m + slot) * D;
                 vs = Vl + ((size_t)bh * s.m + slot) * D;
             } else if (slot < L) {
-                int j = E[slot - s.m];
-                if (j < 0 || j >= s.N) { atomicExch(status, (int)MITA_ERR_DEVICE); j = 0; }
+                const int j = E_s[slot - s.m];
                 ks = K + hoff + (size_t)j * D;
                 vs = V + hoff + (size_t)j * D;
             } else {
@@ -495,7 +501,7 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
 }  // namespace tl
 
 bool tiled_supported(const Shape& s, mita_dtype_t dtype) {
-    return dtype == MITA_BF16 && (s.d == 64 || s.d == 128) && s.m <= 256 && s.k <= 512 && s.N < (1 << 24);
+    return dtype == MITA_BF16 && (s.d == 64 || s.d == 128) && s.m <= 256 && s.k <= tl::kMaxK && s.N < (1 << 24);
 }
 
 size_t tiled_part_bytes(const Shape& s) {
