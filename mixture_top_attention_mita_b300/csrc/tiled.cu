@@ -8,10 +8,11 @@
 //   pool            Q_l, correctly rounded bin means (shared with the staged path)
 //   tc_scores       S = Q_l . K^T (fp32, workspace) and each landmark's row
 //                   max and min
-//   tl_topk         per landmark the k best keys (ties to the lower index):
+//   tl_topk_bits    per landmark the k best keys (ties to the lower index):
 //                   a 2048-bin histogram over [min, max], an exact rank of the
-//                   boundary bin's members, an ordered emit (rows up to 16K
-//                   keys; longer rows use the staged path's radix select)
+//                   boundary bin's members, the expert as a bitmap over the
+//                   row read out in key order (rows up to 64K keys; longer
+//                   rows use the staged path's radix select)
 //   tc_values       split-K partial sums of exp(S / sqrt d - max) . V and of
 //                   the row sums, per 1024-key split
 //   tl_values_fin   V_l = sum of partials / sum of row sums, bf16
@@ -46,7 +47,6 @@ int max_tiles(const Shape& s) { return (s.N + kQT - 1) / kQT + s.m; }
 constexpr int kTB = 256;          // threads per top-k block
 constexpr int kNB = 2048;         // histogram bins
 constexpr int kCandMax = 1024;    // boundary members ranked exactly
-constexpr int kHistTopkMaxN = 16384;   // longer rows use the radix select of the staged path
 
 // Block-wide exclusive prefix sum of one int per thread (kTB threads);
 // *total receives the block total.
@@ -72,22 +72,30 @@ MITA_DEV int block_excl_scan(int x, int* wsum, int* total) {
     return base + incl - x;
 }
 
-// Block per (landmark i, head bh): the k keys with the largest raw scores
-// S[bh, i, :], ties to the lower key index, written in ascending order.
-// Bins of equal width over [row min, row max] find the bin holding the k-th
-// largest score; bins above it are taken whole, and the boundary bin's
-// members are ranked exactly by (score desc, index asc).  Thread t owns the
-// contiguous key segment [t * seg, (t + 1) * seg), so per-thread counts and
-// one block scan give every emitted key its place in index order.
-__global__ void __launch_bounds__(kTB) tl_topk(Shape s, const float* __restrict__ S,
-                                               const uint32_t* __restrict__ rowmax,
-                                               const uint32_t* __restrict__ rowmin, int32_t* __restrict__ idx) {
+// Block per (landmark i, head bh), rows up to kBitsMaxN keys: the k keys
+// with the largest raw scores S[bh, i, :], ties to the lower key index, in
+// ascending order.  Bins of equal width over [row min, row max] find the bin
+// bin* holding the k-th largest score; every pass over the row is coalesced.
+// Pass 1 builds the histogram; pass 2 marks the keys of the bins above bin* in a bitmap
+// over the row (one ballot word per 32 keys) and lists bin*'s members with
+// their indices; the listed members are ranked exactly (score desc, index
+// asc) and the chosen ones join the bitmap; the bitmap, read word by word
+// with one block scan, gives the expert in ascending key order.  A bin* with
+// more than kCandMax members (ties, flat rows) is resolved by bisecting the
+// order key of its need-th best member.
+constexpr int kBitsMaxN = 65536;
+
+__global__ void __launch_bounds__(kTB) tl_topk_bits(Shape s, const float* __restrict__ S,
+                                                    const uint32_t* __restrict__ rowmax,
+                                                    const uint32_t* __restrict__ rowmin, int32_t* __restrict__ idx) {
     __shared__ int hist[kNB];
-    __shared__ int wsum[kTB / 32];
-    __shared__ int sh[3];
+    __shared__ uint32_t bits[kBitsMaxN / 32];
     __shared__ float cval[kCandMax];
-    __shared__ uint8_t chosen[kCandMax];
-    const int i = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x, N = s.N, k = s.k;
+    __shared__ int cidx[kCandMax];
+    __shared__ int wsum[kTB / 32];
+    __shared__ int sh[4];
+    const int i = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int N = s.N, k = s.k, nw = (N + 31) >> 5;
     const float* row = S + ((size_t)bh * s.m + i) * N;
     const float mx = key_to_float(rowmax[(size_t)bh * s.m + i]);
     const float mn = key_to_float(rowmin[(size_t)bh * s.m + i]);
@@ -95,120 +103,120 @@ __global__ void __launch_bounds__(kTB) tl_topk(Shape s, const float* __restrict_
     const float sc = range > 0.0f ? (float)kNB / range : 0.0f;
     auto bin_of = [&](float v) { return min(kNB - 1, (int)((v - mn) * sc)); };
     for (int b = tid; b < kNB; b += kTB) hist[b] = 0;
+    for (int w = tid; w < nw; w += kTB) bits[w] = 0u;
+    if (tid == 0) sh[3] = 0;
     __syncthreads();
     for (int j = tid; j < N; j += kTB) atomicAdd(&hist[bin_of(row[j])], 1);
     __syncthreads();
     // thread t holds bins [8t, 8t + 8); counts of bins above, from the top down
-    int c[8], tot = 0;
+    {
+        int c[8], tot = 0;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) { c[u] = hist[8 * tid + u]; tot += c[u]; }
-    int all;
-    const int below = block_excl_scan(tot, wsum, &all);   // members of bins under 8t
-    const int above = all - below - tot;                    // members of bins over 8t + 7
-    if (above < k && above + tot >= k) {
-        int run = above;
+        for (int u = 0; u < 8; ++u) { c[u] = hist[8 * tid + u]; tot += c[u]; }
+        int all;
+        const int below = block_excl_scan(tot, wsum, &all);
+        const int above = all - below - tot;
+        if (above < k && above + tot >= k) {
+            int run = above;
 #pragma unroll
-        for (int u = 7; u >= 0; --u) {
-            if (run < k && run + c[u] >= k) {
-                sh[0] = 8 * tid + u;
-                sh[1] = k - run;
-                sh[2] = c[u];
+            for (int u = 7; u >= 0; --u) {
+                if (run < k && run + c[u] >= k) {
+                    sh[0] = 8 * tid + u;
+                    sh[1] = k - run;
+                    sh[2] = c[u];
+                }
+                run += c[u];
             }
-            run += c[u];
         }
     }
     __syncthreads();
     const int bstar = sh[0], need = sh[1], cstar = sh[2];
-    const int seg = (N + kTB - 1) / kTB, j0 = min(N, tid * seg), j1 = min(N, j0 + seg);
-    int ngt = 0, nb = 0;
-    for (int j = j0; j < j1; ++j) {
-        const int b = bin_of(row[j]);
-        ngt += b > bstar;
-        nb += b == bstar;
-    }
-    int dummy;
-    const int pb = block_excl_scan(nb, wsum, &dummy);   // first boundary member of this thread
-    int nsel = ngt + nb;
-    if (need < cstar) {
-        if (cstar <= kCandMax) {
-            int r = pb;
-            for (int j = j0; j < j1; ++j) {
-                const float v = row[j];
-                if (bin_of(v) == bstar) cval[r++] = v;
-            }
-            __syncthreads();
-            for (int p = tid; p < cstar; p += kTB) {
-                const float v = cval[p];
-                int rank = 0;
-                for (int q = 0; q < cstar; ++q) {
-                    const float w = cval[q];
-                    rank += (w > v || (w == v && q < p)) ? 1 : 0;
-                }
-                chosen[p] = rank < need ? 1 : 0;
-            }
-            __syncthreads();
-            nsel = ngt;
-            for (int p = pb; p < pb + nb; ++p) nsel += chosen[p];
-        } else {
-            // many members (degenerate scores): bisect the order key T of the
-            // need-th best member; members above T are taken, and members equal
-            // to T in index order until need is met
-            uint32_t T = 0;
-            for (int b = 31; b >= 0; --b) {
-                const uint32_t ct = T | (1u << b);
-                int cnt = 0;
-                for (int j = j0; j < j1; ++j) {
-                    const float v = row[j];
-                    cnt += (bin_of(v) == bstar && order_key(v) >= ct) ? 1 : 0;
-                }
-                int total;
-                block_excl_scan(cnt, wsum, &total);
-                if (total >= need) T = ct;
-            }
-            int gt = 0, eq = 0;
-            for (int j = j0; j < j1; ++j) {
-                const float v = row[j];
-                if (bin_of(v) == bstar) {
-                    const uint32_t kv = order_key(v);
-                    gt += kv > T;
-                    eq += kv == T;
-                }
-            }
-            int gt_all;
-            block_excl_scan(gt, wsum, &gt_all);
-            int eq_all;
-            const int eq_before = block_excl_scan(eq, wsum, &eq_all);
-            const int eq_take = need - gt_all;
-            const int mine_eq = max(0, min(eq, eq_take - eq_before));
-            nsel = ngt + gt + mine_eq;
-            // emit directly: this thread's selection is known
-            int total_sel;
-            int pos = block_excl_scan(nsel, wsum, &total_sel);
-            int32_t* out = idx + ((size_t)bh * s.m + i) * k;
-            int eq_seen = 0;
-            for (int j = j0; j < j1; ++j) {
-                const float v = row[j];
-                const int b = bin_of(v);
-                bool sel = b > bstar;
-                if (b == bstar) {
-                    const uint32_t kv = order_key(v);
-                    if (kv > T) sel = true;
-                    else if (kv == T) sel = eq_seen++ < mine_eq;
-                }
-                if (sel) out[pos++] = j;
-            }
-            return;
+    const bool take_all = need >= cstar;            // every member of bin* is in the expert
+    const bool listed = !take_all && cstar <= kCandMax;
+    // pass 2: warp w walks words w, w + 8, ... (32 consecutive keys per step)
+    for (int w = warp; w < nw; w += kTB / 32) {
+        const int j = 32 * w + lane;
+        const int b = j < N ? bin_of(row[j]) : -1;
+        const uint32_t sel = __ballot_sync(0xffffffffu, b > bstar || (take_all && b == bstar));
+        if (lane == 0) bits[w] = sel;
+        if (listed && b == bstar) {
+            const int p = atomicAdd(&sh[3], 1);
+            cval[p] = row[j];
+            cidx[p] = j;
         }
     }
-    int total_sel;
-    int pos = block_excl_scan(nsel, wsum, &total_sel);
+    __syncthreads();
+    if (listed) {
+        for (int p = tid; p < cstar; p += kTB) {
+            const float v = cval[p];
+            const int jp = cidx[p];
+            int rank = 0;
+            for (int q = 0; q < cstar; ++q) {
+                const float w = cval[q];
+                rank += (w > v || (w == v && cidx[q] < jp)) ? 1 : 0;
+            }
+            if (rank < need) atomicOr(&bits[jp >> 5], 1u << (jp & 31));
+        }
+        __syncthreads();
+    } else if (!take_all) {
+        // many members: the need-th best member's order key T by bisection, then
+        // members above T and, in key order, those equal to T until need is met
+        uint32_t T = 0u;
+        for (int bb = 31; bb >= 0; --bb) {
+            const uint32_t ct = T | (1u << bb);
+            int cnt = 0;
+            for (int j = tid; j < N; j += kTB) {
+                const float v = row[j];
+                cnt += (bin_of(v) == bstar && order_key(v) >= ct) ? 1 : 0;
+            }
+            int total;
+            block_excl_scan(cnt, wsum, &total);
+            if (total >= need) T = ct;
+        }
+        int gt = 0;
+        for (int j = tid; j < N; j += kTB) {
+            const float v = row[j];
+            gt += (bin_of(v) == bstar && order_key(v) > T) ? 1 : 0;
+        }
+        int gt_all;
+        block_excl_scan(gt, wsum, &gt_all);
+        if (warp == 0) {   // one warp, in key order: members above T, and the first ones equal to T
+            int eq_left = need - gt_all;
+            for (int w = 0; w < nw; ++w) {
+                const int j = 32 * w + lane;
+                bool above = false, eq = false;
+                if (j < N) {
+                    const float v = row[j];
+                    if (bin_of(v) == bstar) {
+                        const uint32_t kv = order_key(v);
+                        above = kv > T;
+                        eq = kv == T;
+                    }
+                }
+                const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
+                const int r = __popc(eqm & ((1u << lane) - 1u));
+                const uint32_t add = __ballot_sync(0xffffffffu, above || (eq && r < eq_left));
+                eq_left -= min(eq_left, __popc(eqm));
+                if (lane == 0) bits[w] |= add;
+            }
+        }
+        __syncthreads();
+    }
+    // the expert in ascending key order: thread t reads words [t*wpt, (t+1)*wpt)
+    const int wpt = (nw + kTB - 1) / kTB, w0 = min(nw, tid * wpt), w1 = min(nw, w0 + wpt);
+    int cnt = 0;
+    for (int w = w0; w < w1; ++w) cnt += __popc(bits[w]);
+    int total;
+    int pos = block_excl_scan(cnt, wsum, &total);
     int32_t* out = idx + ((size_t)bh * s.m + i) * k;
-    int r = pb;
-    for (int j = j0; j < j1; ++j) {
-        const int b = bin_of(row[j]);
-        bool sel = b > bstar;
-        if (b == bstar) sel = need >= cstar || chosen[r++];
-        if (sel) out[pos++] = j;
+    for (int w = w0; w < w1; ++w) {
+        uint32_t b = bits[w];
+        while (b) {
+            const int x = __ffs(b) - 1;
+            b &= b - 1u;
+            if (pos < k) out[pos] = 32 * w + x;
+            ++pos;
+        }
     }
 }
 
@@ -473,9 +481,9 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
         if ((err = tc_scores(sg, Ql + mo * D, K + no * D, p->S, p->rowmax + mo, rowmin + mo, p->status, st)) !=
             cudaSuccess)
             return err;
-        if (s.N <= kHistTopkMaxN) {
-            tl_topk<<<dim3(s.m, sg.H), kTB, 0, st>>>(sg, p->S, p->rowmax + mo, rowmin + mo, idx + mo * s.k);
-        } else {   // long rows: one block per row is too little parallelism for the histogram select
+        if (s.N <= kBitsMaxN) {
+            tl_topk_bits<<<dim3(s.m, sg.H), kTB, 0, st>>>(sg, p->S, p->rowmax + mo, rowmin + mo, idx + mo * s.k);
+        } else {   // rows past the bitmap: the staged path's radix select
             if ((err = staged_topk(sg, p->S, idx + mo * s.k, st)) != cudaSuccess) return err;
         }
         if ((err = tc_values(sg, p->S, p->rowmax + mo, V + no * D, p->vpart, cs, p->status, st)) != cudaSuccess)

@@ -137,11 +137,12 @@ def test_edge_shapes(i, path):
 
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("kind", ["flat", "two_values"])
-def test_flat_and_tied_rows(kind, path):
+@pytest.mark.parametrize("name", ["deit_s", "long1d_8k"])
+def test_flat_and_tied_rows(name, kind, path):
     """Rows whose scores are all equal (every key ties: the expert is the first
     k keys) or take two values (the boundary holds far more tied keys than a
     rank list keeps): the selects' many-ties fallbacks."""
-    w = SMALL["deit_s"]
+    w = SMALL[name]
     _skip_unbuilt(w, path)
     Q, K, V = synth.make_integer_inputs(w, seed=31)
     if kind == "flat":
