@@ -36,11 +36,14 @@ namespace tl {
 using bf16 = __nv_bfloat16;
 using namespace mx;
 
-constexpr int kQT = 64;     // queries per attention tile (4 warps x 16)
+// Queries per attention tile (16 per warp): 128 at d = 128, where the routed
+// keys are many and their K, V rows are gathered once for twice the queries;
+// 64 at d = 64, where most experts hold fewer queries than that.
+constexpr int qt_of(int d) { return d == 128 ? 128 : 64; }
 constexpr int kMaxK = 512;  // routed keys per expert
 
 int nsplit(const Shape& s) { return tc_value_splits(s); }
-int max_tiles(const Shape& s) { return (s.N + kQT - 1) / kQT + s.m; }
+int max_tiles(const Shape& s) { return (s.N + qt_of(s.d) - 1) / qt_of(s.d) + s.m; }
 
 
 // ---------------------------------------------------------------- top-k
@@ -106,7 +109,31 @@ __global__ void __launch_bounds__(kTB) tl_topk_bits(Shape s, const float* __rest
     for (int w = tid; w < nw; w += kTB) bits[w] = 0u;
     if (tid == 0) sh[3] = 0;
     __syncthreads();
-    for (int j = tid; j < N; j += kTB) atomicAdd(&hist[bin_of(row[j])], 1);
+    if ((N & 3) == 0) {   // 16-byte loads, two in flight per thread
+        const float4* row4 = (const float4*)row;
+        const int n4 = N >> 2;
+        int j = tid;
+        for (; j + kTB < n4; j += 2 * kTB) {
+            const float4 a = row4[j], b = row4[j + kTB];
+            atomicAdd(&hist[bin_of(a.x)], 1);
+            atomicAdd(&hist[bin_of(a.y)], 1);
+            atomicAdd(&hist[bin_of(a.z)], 1);
+            atomicAdd(&hist[bin_of(a.w)], 1);
+            atomicAdd(&hist[bin_of(b.x)], 1);
+            atomicAdd(&hist[bin_of(b.y)], 1);
+            atomicAdd(&hist[bin_of(b.z)], 1);
+            atomicAdd(&hist[bin_of(b.w)], 1);
+        }
+        for (; j < n4; j += kTB) {
+            const float4 a = row4[j];
+            atomicAdd(&hist[bin_of(a.x)], 1);
+            atomicAdd(&hist[bin_of(a.y)], 1);
+            atomicAdd(&hist[bin_of(a.z)], 1);
+            atomicAdd(&hist[bin_of(a.w)], 1);
+        }
+    } else {
+        for (int j = tid; j < N; j += kTB) atomicAdd(&hist[bin_of(row[j])], 1);
+    }
     __syncthreads();
     // thread t holds bins [8t, 8t + 8); counts of bins above, from the top down
     {
@@ -133,16 +160,30 @@ __global__ void __launch_bounds__(kTB) tl_topk_bits(Shape s, const float* __rest
     const int bstar = sh[0], need = sh[1], cstar = sh[2];
     const bool take_all = need >= cstar;            // every member of bin* is in the expert
     const bool listed = !take_all && cstar <= kCandMax;
-    // pass 2: warp w walks words w, w + 8, ... (32 consecutive keys per step)
-    for (int w = warp; w < nw; w += kTB / 32) {
-        const int j = 32 * w + lane;
-        const int b = j < N ? bin_of(row[j]) : -1;
-        const uint32_t sel = __ballot_sync(0xffffffffu, b > bstar || (take_all && b == bstar));
-        if (lane == 0) bits[w] = sel;
-        if (listed && b == bstar) {
-            const int p = atomicAdd(&sh[3], 1);
-            cval[p] = row[j];
-            cidx[p] = j;
+    // pass 2: warp w walks words w, w + 8, ... (32 consecutive keys per word),
+    // four words per step with their loads in flight together
+    constexpr int kWS = kTB / 32;
+    for (int w = warp; w < nw; w += 4 * kWS) {
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int j = 32 * (w + u * kWS) + lane;
+            v[u] = j < N ? row[j] : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int wu = w + u * kWS;
+            if (wu < nw) {   // warp-uniform
+                const int j = 32 * wu + lane;
+                const int b = j < N ? bin_of(v[u]) : -1;
+                const uint32_t sel = __ballot_sync(0xffffffffu, b > bstar || (take_all && b == bstar));
+                if (lane == 0) bits[wu] = sel;
+                if (listed && b == bstar) {
+                    const int p = atomicAdd(&sh[3], 1);
+                    cval[p] = v[u];
+                    cidx[p] = j;
+                }
+            }
         }
     }
     __syncthreads();
@@ -238,13 +279,13 @@ __global__ void tl_values_fin(Shape s, const float* __restrict__ part, int ns, b
 // scatter cursors and the attention tile list (expert << 16 | chunk).
 __global__ void tl_bucket_off(Shape s, const int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                               int32_t* __restrict__ cursor, int32_t* __restrict__ tiles,
-                              int32_t* __restrict__ ntiles, int maxt) {
+                              int32_t* __restrict__ ntiles, int maxt, int qt) {
     const int bh = blockIdx.x, lane = threadIdx.x;
     const int32_t* cnt = counts + (size_t)bh * s.m;
     int carry = 0, tcarry = 0;
     for (int i0 = 0; i0 < s.m; i0 += 32) {
         const int i = i0 + lane;
-        const int c = i < s.m ? cnt[i] : 0, nt = (c + kQT - 1) / kQT;
+        const int c = i < s.m ? cnt[i] : 0, nt = (c + qt - 1) / qt;
         int x = c, y = nt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -282,12 +323,12 @@ __global__ void tl_bucket_put(Shape s, const int32_t* __restrict__ route, int32_
 }
 
 // ---------------------------------------------------------------- attention
-// Block: one tile = up to 64 queries of one expert (4 warps x 16 rows).
+// Block: one tile = up to QT queries of one expert (QT / 16 warps x 16 rows).
 // Slots 0..m-1 are the shared pairs (Q_l, V_l), slots m..m+k-1 the routed
 // pairs (K, V rows of the expert's keys); 64-slot blocks are staged by
 // cp.async into a double buffer and folded in by an online softmax.
-template <int D>
-__global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
+template <int D, int QT>
+__global__ void __launch_bounds__(2 * QT, D == 64 ? 4 : 1)
     tl_attend(Shape s, const bf16* __restrict__ Q, const bf16* __restrict__ K, const bf16* __restrict__ V,
               const bf16* __restrict__ Ql, const bf16* __restrict__ Vl, const int32_t* __restrict__ idx,
               const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm,
@@ -295,36 +336,37 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
               bf16* __restrict__ out, float cs, int32_t* __restrict__ status) {
     constexpr int RB = 2 * D, CH = D / 8, KS = D / 16, NT = D / 8;
     extern __shared__ __align__(128) unsigned char sm[];
-    __shared__ int rows_s[kQT];
+    constexpr int NTH = 2 * QT;   // threads
+    __shared__ int rows_s[QT];
     __shared__ int E_s[kMaxK];   // the expert's key indices (read once per tile, not per staged row)
     const int bh = blockIdx.y, tile = blockIdx.x;
     if (tile >= ntiles[bh]) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, t = lane & 3;
     const int e = tiles[(size_t)bh * maxt + tile] >> 16, chunk = tiles[(size_t)bh * maxt + tile] & 0xffff;
-    const int qstart = offsets[(size_t)bh * (s.m + 1) + e] + chunk * kQT;
-    const int nq = min(kQT, offsets[(size_t)bh * (s.m + 1) + e + 1] - qstart);
+    const int qstart = offsets[(size_t)bh * (s.m + 1) + e] + chunk * QT;
+    const int nq = min(QT, offsets[(size_t)bh * (s.m + 1) + e + 1] - qstart);
     const int L = s.m + s.k, nblk = (L + 63) / 64;
     const int32_t* E = idx + ((size_t)bh * s.m + e) * s.k;
-    const uint32_t uq = smem_u32(sm), ukv = uq + kQT * RB;   // kv buffer b: K at ukv + b*2*64*RB, V after it
+    const uint32_t uq = smem_u32(sm), ukv = uq + QT * RB;   // kv buffer b: K at ukv + b*2*64*RB, V after it
     const size_t hoff = (size_t)bh * s.N * D;
-    if (tid < kQT) {
+    if (tid < QT) {
         int q = perm[(size_t)bh * s.N + qstart + min(tid, nq - 1)];
         if (q < 0 || q >= s.N) { atomicExch(status, (int)MITA_ERR_DEVICE); q = 0; }
         rows_s[tid] = q;
     }
-    for (int x = tid; x < s.k; x += 128) {
+    for (int x = tid; x < s.k; x += NTH) {
         int j = E[x];
         if (j < 0 || j >= s.N) { atomicExch(status, (int)MITA_ERR_DEVICE); j = 0; }
         E_s[x] = j;
     }
     __syncthreads();
-    for (int x = tid; x < kQT * CH; x += 128) {
+    for (int x = tid; x < QT * CH; x += NTH) {
         const int r = x / CH, c = x % CH;
         cp_async16(uq + swz<RB>(r, c), Q + hoff + (size_t)rows_s[r] * D + 8 * c, 16u);
     }
     auto stage = [&](int b) {
         const uint32_t kb = ukv + (uint32_t)(b & 1) * 2u * 64u * RB, vb = kb + 64u * RB;
-        for (int x = tid; x < 64 * CH; x += 128) {
+        for (int x = tid; x < 64 * CH; x += NTH) {
             const int r = x / CH, c = x % CH, slot = b * 64 + r;
             const bf16 *ks, *vs;
             uint32_t nbytes = 16u;
@@ -446,7 +488,7 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
         stsm_x4(uq + swz<RB>(srow, 2 * np + (lane >> 4)), r0, r1, r2, r3);
     }
     __syncthreads();
-    for (int x = tid; x < nq * CH; x += 128) {
+    for (int x = tid; x < nq * CH; x += NTH) {
         const int r = x / CH, c = x % CH;
         *(uint4*)(out + hoff + (size_t)rows_s[r] * D + 8 * c) = *(const uint4*)(sm + swz<RB>(r, c));
     }
@@ -493,13 +535,14 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
     }
     if ((err = tc_route(s, Q, Ql, route, p->counts, p->status, st)) != cudaSuccess) return err;
     const int maxt = max_tiles(s);
-    tl_bucket_off<<<BH, 32, 0, st>>>(s, p->counts, p->offsets, p->cursor, p->tiles, p->ntiles, maxt);
+    constexpr int QT = qt_of(D);
+    tl_bucket_off<<<BH, 32, 0, st>>>(s, p->counts, p->offsets, p->cursor, p->tiles, p->ntiles, maxt, QT);
     tl_bucket_put<<<dim3((s.N + 255) / 256, BH), 256, 0, st>>>(s, route, p->cursor, p->perm, p->status);
     {
-        const int smem = (kQT + 4 * 64) * RB;
-        auto kern = tl_attend<D>;
+        const int smem = (QT + 4 * 64) * RB;
+        auto kern = tl_attend<D, QT>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        kern<<<dim3(maxt, BH), 128, smem, st>>>(s, Q, K, V, Ql, Vl, idx, p->offsets, p->perm, p->tiles, p->ntiles,
+        kern<<<dim3(maxt, BH), 2 * QT, smem, st>>>(s, Q, K, V, Ql, Vl, idx, p->offsets, p->perm, p->tiles, p->ntiles,
                                                   maxt, out, cs, p->status);
     }
     p->launches += 5;
