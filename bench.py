@@ -43,10 +43,11 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="mita", choices=["mita", "reference"])
     ap.add_argument("--workload", default="deit_s", choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--path", default="auto", choices=["auto", "staged", "fused"])
+    ap.add_argument("--path", default="auto", choices=["auto", "staged", "fused", "tiled"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--no-soak", action="store_true", help="skip the untimed repeats that extend clock sampling")
     return ap.parse_args()
 
@@ -324,7 +325,7 @@ def main():
     # dominant kernel: on the fused path the step is one launch; on the
     # staged path the whole step is reported (kernel-level shares live in
     # the ncu launch list under profiles/).
-    kernel_tag = "mita_fused" if path == "fused" else "mita_staged_step"
+    kernel_tag = "mita_fused" if path == "fused" else f"mita_{path}_step"
     t_s = ms / 1000.0
     bw = nbytes / t_s / 1e9
     tf = flops / t_s / 1e12
@@ -377,6 +378,41 @@ def main():
         e2e = {"value": ws * qh / (ems / 1000.0), "unit": "query-heads/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": round(ems, 4)}
 
+    # the same forwards replayed from one CUDA graph (one forward per buffer
+    # set, so replays keep rotating the inputs): launch overhead removed
+    graph = None
+    if not args.no_graph:
+        try:
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
+                cs = torch.cuda.current_stream()
+                for i in range(nsets):
+                    Q, K, V, out, idx, route = sets[i]
+                    plan.forward(Q, K, V, out, idx, route, cs)
+            reps = max(3, args.steps // nsets)
+            for _ in range(3):
+                g.replay()
+            barrier(ws)
+            torch.cuda.synchronize()
+            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            g0.record()
+            for _ in range(reps):
+                g.replay()
+            g1.record()
+            torch.cuda.synchronize()
+            barrier(ws)
+            gms = max_over_ranks(g0.elapsed_time(g1) / (reps * nsets), ws, dev)
+            st = plan.status()
+            if st != mita.MITA_OK:
+                raise RuntimeError(f"device status {mita.STATUS.get(st, st)}")
+            graph = {"ms_per_step": round(gms, 5), "value": ws * qh / (gms / 1000.0), "unit": "query-heads/s",
+                     "forwards_per_graph": nsets}
+            del g
+        except Exception as exc:   # reported, not fatal: the line above stands without it
+            graph = {"error": str(exc).splitlines()[0][:200]}
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.cpu_seconds)
@@ -389,7 +425,7 @@ def main():
                            "parallelism": f"heads sharded over {ws} GPU(s), no collective",
                            "path": path, "l2": f"inputs rotate over {nsets} buffer sets "
                                                f"({nsets * set_bytes / 1e6:.0f} MB > 126 MB L2)"},
-                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "graph": graph, "gpu_launches": launches,
                 "clocks": clocks, "achieved_tflops": round(tf, 2), "achieved_hbm_gbs": round(bw, 1),
                 "hbm_frac": round(hbm_frac, 4)}
         print(json.dumps(line))
