@@ -30,6 +30,7 @@
 #include <algorithm>
 
 #include "fused.cuh"
+#include "host_cache.cuh"
 
 namespace mita {
 namespace fz {
@@ -789,33 +790,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 }  // namespace fz
 
 // ---------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = (EncodeTiledFn)p;
-    }
-    return fn;
-}
-
 static bool make_map(CUtensorMap* map, const void* base, int rows, int box_rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)fz::kD, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)fz::kD * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)fz::kD, (cuuint32_t)box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return tma_map_bf16(map, base, fz::kD, (size_t)rows, fz::kD, box_rows);
 }
 
 bool fused_supported(const Shape& s, mita_dtype_t dtype) {
@@ -828,12 +804,11 @@ template <int NV>
 static cudaError_t launch_nv(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                              const CUtensorMap& mo, const fz::Params& prm, int device, cudaStream_t st) {
     auto kern = fz::fused_kernel<NV>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, prm.L.total);
+    cudaError_t e = ensure_smem_attr((const void*)kern, prm.L.total);
     if (e != cudaSuccess) return e;
-    int sms = 0, per_sm = 0;
+    int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, fz::kThreads, prm.L.total);
-    if (e != cudaSuccess) return e;
+    const int per_sm = blocks_per_sm((const void*)kern, fz::kThreads, prm.L.total);
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int slots = sms * per_sm;
     const int grid = prm.s.BH() < slots ? prm.s.BH() : slots;

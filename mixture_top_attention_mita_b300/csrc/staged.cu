@@ -13,6 +13,7 @@
 // kernels handle the shapes they cover faster.
 #include "common.cuh"
 #include "staged.cuh"
+#include "host_cache.cuh"
 
 namespace mita {
 
@@ -426,7 +427,7 @@ static cudaError_t run_staged_t(mita_plan_s* p, const T* Q, const T* K, const T*
     route_kernel<T, D><<<dim3((s.N + 127) / 128, BH), 128, 0, st>>>(s, Q, Ql, route);
     bucket_kernel<<<BH, 32, 0, st>>>(s, route, p->counts, p->offsets, p->perm, p->status);
     const size_t smem = staged_attend_smem(s);
-    cudaFuncSetAttribute(attend_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    ensure_smem_attr((const void*)attend_kernel<T, D>, (int)smem);
     attend_kernel<T, D><<<dim3((s.N + kAttendWarps - 1) / kAttendWarps, BH), 32 * kAttendWarps, smem, st>>>(
         s, Q, K, V, Ql, Vl, idx, route, p->perm, out, p->status);
     p->launches += 7;

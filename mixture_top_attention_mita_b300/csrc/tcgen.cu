@@ -16,6 +16,7 @@
 // landmark values step 4, routes step 5.
 #include "tc_util.cuh"
 #include "tcgen.cuh"
+#include "host_cache.cuh"
 
 namespace mita {
 namespace tcg {
@@ -340,35 +341,10 @@ __global__ void __launch_bounds__(128) tc_route(const __grid_constant__ CUtensor
 }  // namespace tcg
 
 // ---------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn tc_encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = (EncodeTiledFn)p;
-    }
-    return fn;
-}
-
 // 2-D map over `rows` rows of `d` bf16, boxes of 64 columns x box_rows rows,
 // 128-byte swizzle (rows past the end read as zero).
 static bool map_rows(CUtensorMap* map, const void* base, int d, size_t rows, int box_rows) {
-    EncodeTiledFn fn = tc_encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
-    const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return tma_map_bf16(map, base, d, rows, 64, box_rows);
 }
 
 template <int D>
@@ -380,10 +356,10 @@ static cudaError_t tc_scores_t(const Shape& s, const void* Ql, const void* K, fl
     const int smem = 2 * (D / 64) * (int)tcg::kChunk + 1024;
     const dim3 grid((s.N + 127) / 128, (s.m + 127) / 128, s.BH());
     if (s.N % 4 == 0) {
-        cudaFuncSetAttribute(tcg::tc_scores<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        ensure_smem_attr((const void*)tcg::tc_scores<D, true>, smem);
         tcg::tc_scores<D, true><<<grid, 128, smem, st>>>(mq, mk, s, S, rowmax, rowmin, status);
     } else {
-        cudaFuncSetAttribute(tcg::tc_scores<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        ensure_smem_attr((const void*)tcg::tc_scores<D, false>, smem);
         tcg::tc_scores<D, false><<<grid, 128, smem, st>>>(mq, mk, s, S, rowmax, rowmin, status);
     }
     return cudaGetLastError();
@@ -397,10 +373,10 @@ static cudaError_t tc_values_t(const Shape& s, const float* S, const uint32_t* r
     const int smem = 2 * (2 * (int)tcg::kChunk + (D / 64) * (int)tcg::kChunk) + 1024;
     const dim3 grid((s.N + tcg::kKCV - 1) / tcg::kKCV, (s.m + 127) / 128, s.BH());
     if (s.N % 4 == 0) {
-        cudaFuncSetAttribute(tcg::tc_values<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        ensure_smem_attr((const void*)tcg::tc_values<D, true>, smem);
         tcg::tc_values<D, true><<<grid, 512, smem, st>>>(mv, s, S, rowmax, part, cs, status);
     } else {
-        cudaFuncSetAttribute(tcg::tc_values<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        ensure_smem_attr((const void*)tcg::tc_values<D, false>, smem);
         tcg::tc_values<D, false><<<grid, 512, smem, st>>>(mv, s, S, rowmax, part, cs, status);
     }
     return cudaGetLastError();
@@ -416,7 +392,7 @@ static cudaError_t tc_route_t(const Shape& s, const void* Q, const void* Ql, int
     if (!map_rows(&mq, Q, D, (size_t)s.BH() * s.N, 128) || !map_rows(&ml, Ql, D, (size_t)s.BH() * s.m, nb))
         return cudaErrorInvalidValue;
     const int smem = (D / 64) * ((int)tcg::kChunk + nb * 128) + 1024;
-    cudaFuncSetAttribute(tcg::tc_route<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    ensure_smem_attr((const void*)tcg::tc_route<D>, smem);
     tcg::tc_route<D><<<dim3((s.N + 127) / 128, s.BH()), 128, smem, st>>>(mq, ml, s, nb, tcols, route, counts, status);
     return cudaGetLastError();
 }

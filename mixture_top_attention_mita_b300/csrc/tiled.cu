@@ -29,6 +29,7 @@
 #include "staged.cuh"
 #include "tcgen.cuh"
 #include "tiled.cuh"
+#include "host_cache.cuh"
 
 namespace mita {
 namespace tl {
@@ -541,7 +542,7 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
     {
         const int smem = (QT + 4 * 64) * RB;
         auto kern = tl_attend<D, QT>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        ensure_smem_attr((const void*)kern, smem);
         kern<<<dim3(maxt, BH), 2 * QT, smem, st>>>(s, Q, K, V, Ql, Vl, idx, p->offsets, p->perm, p->tiles, p->ntiles,
                                                   maxt, out, cs, p->status);
     }
