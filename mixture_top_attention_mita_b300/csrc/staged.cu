@@ -14,6 +14,7 @@
 #include "common.cuh"
 #include "staged.cuh"
 #include "host_cache.cuh"
+#include "launch.cuh"
 
 namespace mita {
 
@@ -22,6 +23,7 @@ namespace mita {
 // tokens (coalesced row reads) and writes the correctly rounded mean.
 template <typename T>
 __global__ void pool_kernel(Shape s, const T* __restrict__ Q, T* __restrict__ Ql) {
+    chain_wait_and_trigger();
     const int i = blockIdx.x, bh = blockIdx.y, f = threadIdx.x;
     const int r = i / s.pw, c = i % s.pw;
     int r0, r1, c0, c1;
@@ -125,6 +127,7 @@ constexpr int kTopkThreads = 512;
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(Shape s, const float* __restrict__ S,
                                                            int32_t* __restrict__ idx) {
+    chain_wait_and_trigger();
     __shared__ int hist[256];
     __shared__ int warp_sums[32];
     __shared__ uint32_t sh_prefix;
@@ -434,17 +437,16 @@ static cudaError_t run_staged_t(mita_plan_s* p, const T* Q, const T* K, const T*
     return cudaGetLastError();
 }
 
-cudaError_t staged_pool(const Shape& s, mita_dtype_t dtype, const void* Q, void* Ql, cudaStream_t st) {
+cudaError_t staged_pool(const Shape& s, mita_dtype_t dtype, const void* Q, void* Ql, cudaStream_t st, bool chained) {
+    const dim3 grid(s.m, s.BH());
     if (dtype == MITA_BF16)
-        pool_kernel<__nv_bfloat16><<<dim3(s.m, s.BH()), s.d, 0, st>>>(s, (const __nv_bfloat16*)Q, (__nv_bfloat16*)Ql);
-    else
-        pool_kernel<float><<<dim3(s.m, s.BH()), s.d, 0, st>>>(s, (const float*)Q, (float*)Ql);
-    return cudaGetLastError();
+        return launch_chained(chained, pool_kernel<__nv_bfloat16>, grid, dim3(s.d), 0, st, s, (const __nv_bfloat16*)Q,
+                              (__nv_bfloat16*)Ql);
+    return launch_chained(chained, pool_kernel<float>, grid, dim3(s.d), 0, st, s, (const float*)Q, (float*)Ql);
 }
 
-cudaError_t staged_topk(const Shape& s, const float* S, int32_t* idx, cudaStream_t st) {
-    topk_kernel<<<dim3(s.m, s.BH()), kTopkThreads, 0, st>>>(s, S, idx);
-    return cudaGetLastError();
+cudaError_t staged_topk(const Shape& s, const float* S, int32_t* idx, cudaStream_t st, bool chained) {
+    return launch_chained(chained, topk_kernel, dim3(s.m, s.BH()), dim3(kTopkThreads), 0, st, s, S, idx);
 }
 
 cudaError_t run_staged(mita_plan_s* p, const void* Q, const void* K, const void* V, void* out, int32_t* idx,

@@ -17,6 +17,7 @@
 #include "tc_util.cuh"
 #include "tcgen.cuh"
 #include "host_cache.cuh"
+#include "launch.cuh"
 
 namespace mita {
 namespace tcg {
@@ -33,6 +34,7 @@ __global__ void __launch_bounds__(128) tc_scores(const __grid_constant__ CUtenso
                                                  const __grid_constant__ CUtensorMap mK, Shape s,
                                                  float* __restrict__ S, uint32_t* __restrict__ rowmax,
                                                  uint32_t* __restrict__ rowmin, int32_t* __restrict__ status) {
+    chain_wait_and_trigger();
     constexpr int KC = D / 64;
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ uint32_t tslot;
@@ -123,6 +125,7 @@ template <int D, bool VEC>
 __global__ void __launch_bounds__(512) tc_values(const __grid_constant__ CUtensorMap mV, Shape s,
                                                  const float* __restrict__ S, const uint32_t* __restrict__ rowmax,
                                                  float* __restrict__ part, float cs, int32_t* __restrict__ status) {
+    chain_wait_and_trigger();
     constexpr int KC = D / 64;                       // 64-wide feature chunks of a V tile
     constexpr uint32_t PBYTES = 2 * kChunk;          // numerators: 128 rows x 128 keys
     constexpr uint32_t VBYTES = KC * kChunk;         // V: 128 keys x D
@@ -267,6 +270,7 @@ __global__ void __launch_bounds__(128) tc_route(const __grid_constant__ CUtensor
                                                 const __grid_constant__ CUtensorMap mQl, Shape s, int nb, int tcols,
                                                 int32_t* __restrict__ route, int32_t* __restrict__ counts,
                                                 int32_t* __restrict__ status) {
+    chain_wait_and_trigger();
     constexpr int KC = D / 64;
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ uint32_t tslot;
@@ -349,7 +353,7 @@ static bool map_rows(CUtensorMap* map, const void* base, int d, size_t rows, int
 
 template <int D>
 static cudaError_t tc_scores_t(const Shape& s, const void* Ql, const void* K, float* S, uint32_t* rowmax,
-                               uint32_t* rowmin, int32_t* status, cudaStream_t st) {
+                               uint32_t* rowmin, int32_t* status, cudaStream_t st, bool chain) {
     CUtensorMap mq, mk;
     if (!map_rows(&mq, Ql, D, (size_t)s.BH() * s.m, 128) || !map_rows(&mk, K, D, (size_t)s.BH() * s.N, 128))
         return cudaErrorInvalidValue;
@@ -357,34 +361,38 @@ static cudaError_t tc_scores_t(const Shape& s, const void* Ql, const void* K, fl
     const dim3 grid((s.N + 127) / 128, (s.m + 127) / 128, s.BH());
     if (s.N % 4 == 0) {
         ensure_smem_attr((const void*)tcg::tc_scores<D, true>, smem);
-        tcg::tc_scores<D, true><<<grid, 128, smem, st>>>(mq, mk, s, S, rowmax, rowmin, status);
+        cudaError_t le = launch_chained(chain, tcg::tc_scores<D, true>, grid, dim3(128), smem, st, mq, mk, s, S, rowmax, rowmin, status);
+        if (le != cudaSuccess) return le;
     } else {
         ensure_smem_attr((const void*)tcg::tc_scores<D, false>, smem);
-        tcg::tc_scores<D, false><<<grid, 128, smem, st>>>(mq, mk, s, S, rowmax, rowmin, status);
+        cudaError_t le = launch_chained(chain, tcg::tc_scores<D, false>, grid, dim3(128), smem, st, mq, mk, s, S, rowmax, rowmin, status);
+        if (le != cudaSuccess) return le;
     }
     return cudaGetLastError();
 }
 
 template <int D>
 static cudaError_t tc_values_t(const Shape& s, const float* S, const uint32_t* rowmax, const void* V, float* part,
-                               float cs, int32_t* status, cudaStream_t st) {
+                               float cs, int32_t* status, cudaStream_t st, bool chain) {
     CUtensorMap mv;
     if (!map_rows(&mv, V, D, (size_t)s.BH() * s.N, 128)) return cudaErrorInvalidValue;
     const int smem = 2 * (2 * (int)tcg::kChunk + (D / 64) * (int)tcg::kChunk) + 1024;
     const dim3 grid((s.N + tcg::kKCV - 1) / tcg::kKCV, (s.m + 127) / 128, s.BH());
     if (s.N % 4 == 0) {
         ensure_smem_attr((const void*)tcg::tc_values<D, true>, smem);
-        tcg::tc_values<D, true><<<grid, 512, smem, st>>>(mv, s, S, rowmax, part, cs, status);
+        cudaError_t le = launch_chained(chain, tcg::tc_values<D, true>, grid, dim3(512), smem, st, mv, s, S, rowmax, part, cs, status);
+        if (le != cudaSuccess) return le;
     } else {
         ensure_smem_attr((const void*)tcg::tc_values<D, false>, smem);
-        tcg::tc_values<D, false><<<grid, 512, smem, st>>>(mv, s, S, rowmax, part, cs, status);
+        cudaError_t le = launch_chained(chain, tcg::tc_values<D, false>, grid, dim3(512), smem, st, mv, s, S, rowmax, part, cs, status);
+        if (le != cudaSuccess) return le;
     }
     return cudaGetLastError();
 }
 
 template <int D>
 static cudaError_t tc_route_t(const Shape& s, const void* Q, const void* Ql, int32_t* route, int32_t* counts,
-                              int32_t* status, cudaStream_t st) {
+                              int32_t* status, cudaStream_t st, bool chain) {
     const int nb = (s.m + 15) / 16 * 16;
     int tcols = 32;
     while (tcols < nb) tcols <<= 1;
@@ -393,26 +401,28 @@ static cudaError_t tc_route_t(const Shape& s, const void* Q, const void* Ql, int
         return cudaErrorInvalidValue;
     const int smem = (D / 64) * ((int)tcg::kChunk + nb * 128) + 1024;
     ensure_smem_attr((const void*)tcg::tc_route<D>, smem);
-    tcg::tc_route<D><<<dim3((s.N + 127) / 128, s.BH()), 128, smem, st>>>(mq, ml, s, nb, tcols, route, counts, status);
+    cudaError_t le = launch_chained(chain, tcg::tc_route<D>, dim3((s.N + 127) / 128, s.BH()), dim3(128), smem, st, mq, ml, s,
+                                    nb, tcols, route, counts, status);
+    if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
 
 int tc_value_splits(const Shape& s) { return (s.N + tcg::kKCV - 1) / tcg::kKCV; }
 
 cudaError_t tc_scores(const Shape& s, const void* Ql, const void* K, float* S, uint32_t* rowmax, uint32_t* rowmin,
-                      int32_t* status, cudaStream_t st) {
-    return s.d == 64 ? tc_scores_t<64>(s, Ql, K, S, rowmax, rowmin, status, st)
-                     : tc_scores_t<128>(s, Ql, K, S, rowmax, rowmin, status, st);
+                      int32_t* status, cudaStream_t st, bool chain) {
+    return s.d == 64 ? tc_scores_t<64>(s, Ql, K, S, rowmax, rowmin, status, st, chain)
+                     : tc_scores_t<128>(s, Ql, K, S, rowmax, rowmin, status, st, chain);
 }
 cudaError_t tc_values(const Shape& s, const float* S, const uint32_t* rowmax, const void* V, float* part, float cs,
-                      int32_t* status, cudaStream_t st) {
-    return s.d == 64 ? tc_values_t<64>(s, S, rowmax, V, part, cs, status, st)
-                     : tc_values_t<128>(s, S, rowmax, V, part, cs, status, st);
+                      int32_t* status, cudaStream_t st, bool chain) {
+    return s.d == 64 ? tc_values_t<64>(s, S, rowmax, V, part, cs, status, st, chain)
+                     : tc_values_t<128>(s, S, rowmax, V, part, cs, status, st, chain);
 }
 cudaError_t tc_route(const Shape& s, const void* Q, const void* Ql, int32_t* route, int32_t* counts, int32_t* status,
-                     cudaStream_t st) {
-    return s.d == 64 ? tc_route_t<64>(s, Q, Ql, route, counts, status, st)
-                     : tc_route_t<128>(s, Q, Ql, route, counts, status, st);
+                     cudaStream_t st, bool chain) {
+    return s.d == 64 ? tc_route_t<64>(s, Q, Ql, route, counts, status, st, chain)
+                     : tc_route_t<128>(s, Q, Ql, route, counts, status, st, chain);
 }
 
 }  // namespace mita

@@ -30,6 +30,7 @@
 #include "tcgen.cuh"
 #include "tiled.cuh"
 #include "host_cache.cuh"
+#include "launch.cuh"
 
 namespace mita {
 namespace tl {
@@ -88,10 +89,12 @@ MITA_DEV int block_excl_scan(int x, int* wsum, int* total) {
 // more than kCandMax members (ties, flat rows) is resolved by bisecting the
 // order key of its need-th best member.
 constexpr int kBitsMaxN = 65536;
+constexpr int kChainMaxN = 16384;   // rows up to this length: overlapped (chained) launches
 
 __global__ void __launch_bounds__(kTB) tl_topk_bits(Shape s, const float* __restrict__ S,
                                                     const uint32_t* __restrict__ rowmax,
                                                     const uint32_t* __restrict__ rowmin, int32_t* __restrict__ idx) {
+    chain_wait_and_trigger();
     __shared__ int hist[kNB];
     __shared__ uint32_t bits[kBitsMaxN / 32];
     __shared__ float cval[kCandMax];
@@ -265,6 +268,7 @@ __global__ void __launch_bounds__(kTB) tl_topk_bits(Shape s, const float* __rest
 // V_l[i] = (sum over splits of the partial row) / (sum of the partial row sums).
 template <int D>
 __global__ void tl_values_fin(Shape s, const float* __restrict__ part, int ns, bf16* __restrict__ Vl) {
+    chain_wait_and_trigger();
     const int i = blockIdx.x, bh = blockIdx.y, f = threadIdx.x;
     const float* src = part + ((size_t)bh * ns * s.m + i) * (D + 1);
     float num = 0.0f, den = 0.0f;
@@ -281,6 +285,7 @@ __global__ void tl_values_fin(Shape s, const float* __restrict__ part, int ns, b
 __global__ void tl_bucket_off(Shape s, const int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                               int32_t* __restrict__ cursor, int32_t* __restrict__ tiles,
                               int32_t* __restrict__ ntiles, int maxt, int qt) {
+    chain_wait_and_trigger();
     const int bh = blockIdx.x, lane = threadIdx.x;
     const int32_t* cnt = counts + (size_t)bh * s.m;
     int carry = 0, tcarry = 0;
@@ -312,6 +317,7 @@ __global__ void tl_bucket_off(Shape s, const int32_t* __restrict__ counts, int32
 
 __global__ void tl_bucket_put(Shape s, const int32_t* __restrict__ route, int32_t* __restrict__ cursor,
                               int32_t* __restrict__ perm, int32_t* __restrict__ status) {
+    chain_wait_and_trigger();
     const int bh = blockIdx.y, q = blockIdx.x * blockDim.x + threadIdx.x;
     if (q >= s.N) return;
     const int r = route[(size_t)bh * s.N + q];
@@ -335,6 +341,7 @@ __global__ void __launch_bounds__(2 * QT, D == 64 ? 4 : 1)
               const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm,
               const int32_t* __restrict__ tiles, const int32_t* __restrict__ ntiles, int maxt,
               bf16* __restrict__ out, float cs, int32_t* __restrict__ status) {
+    chain_wait_and_trigger();
     constexpr int RB = 2 * D, CH = D / 8, KS = D / 16, NT = D / 8;
     extern __shared__ __align__(128) unsigned char sm[];
     constexpr int NTH = 2 * QT;   // threads
@@ -514,37 +521,53 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
     if ((err = cudaMemsetAsync(p->rowmax, 0, (size_t)BH * s.m * 4, st)) != cudaSuccess) return err;
     if ((err = cudaMemsetAsync(rowmin, 0xff, (size_t)BH * s.m * 4, st)) != cudaSuccess) return err;
     if ((err = cudaMemsetAsync(p->counts, 0, (size_t)BH * s.m * 4, st)) != cudaSuccess) return err;
-    if ((err = staged_pool(s, MITA_BF16, Q, Ql, st)) != cudaSuccess) return err;
+    // launches overlap their predecessor's tail on short rows, where launch
+    // latency is a visible share of the chain; on long rows (kernels of
+    // hundreds of microseconds) the overlap measured slower and is off
+    const bool chain = s.N <= kChainMaxN;
+    if ((err = staged_pool(s, MITA_BF16, Q, Ql, st, chain)) != cudaSuccess) return err;
     const int ns = nsplit(s), G = head_group(s);
     for (int h0 = 0; h0 < BH; h0 += G) {
         Shape sg = s;
         sg.B = 1;
         sg.H = min(G, BH - h0);
         const size_t mo = (size_t)h0 * s.m, no = (size_t)h0 * s.N;
-        if ((err = tc_scores(sg, Ql + mo * D, K + no * D, p->S, p->rowmax + mo, rowmin + mo, p->status, st)) !=
+        if ((err = tc_scores(sg, Ql + mo * D, K + no * D, p->S, p->rowmax + mo, rowmin + mo, p->status, st, chain)) !=
             cudaSuccess)
             return err;
         if (s.N <= kBitsMaxN) {
-            tl_topk_bits<<<dim3(s.m, sg.H), kTB, 0, st>>>(sg, p->S, p->rowmax + mo, rowmin + mo, idx + mo * s.k);
+            if ((err = launch_chained(chain, tl_topk_bits, dim3(s.m, sg.H), dim3(kTB), 0, st, sg, (const float*)p->S,
+                                      (const uint32_t*)(p->rowmax + mo), (const uint32_t*)(rowmin + mo),
+                                      idx + mo * s.k)) != cudaSuccess)
+                return err;
         } else {   // rows past the bitmap: the staged path's radix select
-            if ((err = staged_topk(sg, p->S, idx + mo * s.k, st)) != cudaSuccess) return err;
+            if ((err = staged_topk(sg, p->S, idx + mo * s.k, st, chain)) != cudaSuccess) return err;
         }
-        if ((err = tc_values(sg, p->S, p->rowmax + mo, V + no * D, p->vpart, cs, p->status, st)) != cudaSuccess)
+        if ((err = tc_values(sg, p->S, p->rowmax + mo, V + no * D, p->vpart, cs, p->status, st, chain)) != cudaSuccess)
             return err;
-        tl_values_fin<D><<<dim3(s.m, sg.H), D, 0, st>>>(sg, p->vpart, ns, Vl + mo * D);
+        if ((err = launch_chained(chain, tl_values_fin<D>, dim3(s.m, sg.H), dim3(D), 0, st, sg, (const float*)p->vpart, ns,
+                                  Vl + mo * D)) != cudaSuccess)
+            return err;
         p->launches += 4;
     }
-    if ((err = tc_route(s, Q, Ql, route, p->counts, p->status, st)) != cudaSuccess) return err;
+    if ((err = tc_route(s, Q, Ql, route, p->counts, p->status, st, chain)) != cudaSuccess) return err;
     const int maxt = max_tiles(s);
     constexpr int QT = qt_of(D);
-    tl_bucket_off<<<BH, 32, 0, st>>>(s, p->counts, p->offsets, p->cursor, p->tiles, p->ntiles, maxt, QT);
-    tl_bucket_put<<<dim3((s.N + 255) / 256, BH), 256, 0, st>>>(s, route, p->cursor, p->perm, p->status);
+    if ((err = launch_chained(chain, tl_bucket_off, dim3(BH), dim3(32), 0, st, s, (const int32_t*)p->counts, p->offsets,
+                              p->cursor, p->tiles, p->ntiles, maxt, QT)) != cudaSuccess)
+        return err;
+    if ((err = launch_chained(chain, tl_bucket_put, dim3((s.N + 255) / 256, BH), dim3(256), 0, st, s, (const int32_t*)route,
+                              p->cursor, p->perm, p->status)) != cudaSuccess)
+        return err;
     {
         const int smem = (QT + 4 * 64) * RB;
         auto kern = tl_attend<D, QT>;
         ensure_smem_attr((const void*)kern, smem);
-        kern<<<dim3(maxt, BH), 2 * QT, smem, st>>>(s, Q, K, V, Ql, Vl, idx, p->offsets, p->perm, p->tiles, p->ntiles,
-                                                  maxt, out, cs, p->status);
+        if ((err = launch_chained(chain, kern, dim3(maxt, BH), dim3(2 * QT), smem, st, s, Q, K, V, (const bf16*)Ql,
+                                  (const bf16*)Vl, (const int32_t*)idx, (const int32_t*)p->offsets,
+                                  (const int32_t*)p->perm, (const int32_t*)p->tiles, (const int32_t*)p->ntiles, maxt,
+                                  out, cs, p->status)) != cudaSuccess)
+            return err;
     }
     p->launches += 5;
     return cudaGetLastError();
