@@ -27,6 +27,10 @@
  *   6. attend    out_q = softmax over the m shared logits A[q, .]/sqrt(d)
  *                and the k routed logits q . K[j]/sqrt(d), j in E_r(q),
  *                applied to [V_l ; V[E_r(q)]]
+ * Routing-only variant (shared = 0; the ablation in the same article, section
+ * "长序列建模：训练时间从10.6小时降至2.4小时", that drops the shared expert):
+ * step 6 takes one softmax over the k routed logits alone; steps 1-5 are
+ * unchanged.
  */
 #include <math.h>
 #include <stdint.h>
@@ -179,15 +183,17 @@ int oracle_route_one(int d, int m, const double* q, const double* Ql, double* A)
 
 /* Step 6 (one query): one softmax over the concatenation of the m shared
  * logits (q . Q_l[i] / sqrt(d)) and the k routed logits (q . K[j] / sqrt(d),
- * j in E_r), applied to [V_l ; V[E_r]].  W (if not NULL) receives the m + k
- * weights in that order; out is rounded to the I/O type. */
-void oracle_attend_one(int d, int m, int k, int io, const double* q, const double* A,
+ * j in E_r), applied to [V_l ; V[E_r]].  With shared = 0 (routing only) the
+ * shared entries are left out of the softmax: their weights are zero and the
+ * softmax runs over the k routed logits alone.  W (if not NULL) receives the
+ * m + k weights in that order; out is rounded to the I/O type. */
+void oracle_attend_one(int d, int m, int k, int io, int shared, const double* q, const double* A,
                        const int32_t* E, const double* K, const double* V,
                        const double* Vl, double* out, double* W) {
     double scale = 1.0 / sqrt((double)d);
     int L = m + k;
     double* logit = (double*)malloc(sizeof(double) * (size_t)L);
-    for (int i = 0; i < m; ++i) logit[i] = A[i] * scale;
+    for (int i = 0; i < m; ++i) logit[i] = shared ? A[i] * scale : -INFINITY;
     for (int t = 0; t < k; ++t) {
         const double* key = K + (size_t)E[t] * d;
         double s = 0.0;
@@ -213,7 +219,7 @@ void oracle_attend_one(int d, int m, int k, int io, const double* q, const doubl
  * landmarks, experts and landmark values always cover the whole head.
  * Optional outputs (NULL to skip): Ql [m,d], Vl [m,d], R [m,N], A [nq,m],
  * W [nq, m+k].  Returns 0, or -1 on invalid sizes. */
-int oracle_head(int N, int d, int gh, int gw, int ph, int pw, int m, int k, int io,
+int oracle_head(int N, int d, int gh, int gw, int ph, int pw, int m, int k, int io, int shared,
                 const double* Q, const double* K, const double* V,
                 int nq, const int32_t* qlist,
                 double* out, int32_t* idx, int32_t* route,
@@ -235,7 +241,7 @@ int oracle_head(int N, int d, int gh, int gw, int ph, int pw, int m, int k, int 
         int r = oracle_route_one(d, m, q, Ql, A);
         route[n] = r;
         if (A_out) memcpy(A_out + (size_t)n * m, A, sizeof(double) * (size_t)m);
-        oracle_attend_one(d, m, k, io, q, A, idx + (size_t)r * k, K, V, Vl,
+        oracle_attend_one(d, m, k, io, shared, q, A, idx + (size_t)r * k, K, V, Vl,
                           out + (size_t)n * d, W_out ? W_out + (size_t)n * (m + k) : NULL);
     }
     free(A);
@@ -246,12 +252,12 @@ int oracle_head(int N, int d, int gh, int gw, int ph, int pw, int m, int k, int 
 }
 
 /* All heads of a [B*H, N, d] batch, every query. */
-int oracle_forward(int BH, int N, int d, int gh, int gw, int ph, int pw, int m, int k, int io,
+int oracle_forward(int BH, int N, int d, int gh, int gw, int ph, int pw, int m, int k, int io, int shared,
                    const double* Q, const double* K, const double* V,
                    double* out, int32_t* idx, int32_t* route) {
     for (int h = 0; h < BH; ++h) {
         size_t o = (size_t)h * N * d;
-        int rc = oracle_head(N, d, gh, gw, ph, pw, m, k, io, Q + o, K + o, V + o, N, NULL,
+        int rc = oracle_head(N, d, gh, gw, ph, pw, m, k, io, shared, Q + o, K + o, V + o, N, NULL,
                              out + o, idx + (size_t)h * m * k, route + (size_t)h * N,
                              NULL, NULL, NULL, NULL, NULL);
         if (rc) return rc;

@@ -162,6 +162,35 @@ def test_full_attention_special_case():
     np.testing.assert_allclose(r["out"], ref, rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("grid,m,k,d", [((14, 14, 5, 5), 25, 25, 16), ((1, 96, 1, 6), 6, 40, 12)])
+def test_routing_only_matches_masked_sdpa(grid, m, k, d):
+    # Routing-only variant (the article's ablation without the shared expert):
+    # each query attends to its expert's k keys alone.
+    N = grid[0] * grid[1]
+    Q, K, V = _rand((N, d), 14), _rand((N, d), 15), _rand((N, d), 16)
+    r = oracle.head(Q, K, V, grid, m, k, io="f64", debug=True, shared=False)
+    mask = np.zeros((N, N), bool)
+    for q in range(N):
+        mask[q, r["idx"][r["route"][q]]] = True
+    t = torch.from_numpy
+    ref = F.scaled_dot_product_attention(t(Q)[None], t(K)[None], t(V)[None], attn_mask=t(mask)[None])[0].numpy()
+    np.testing.assert_allclose(r["out"], ref, rtol=0, atol=1e-12)
+    W = r["W"]
+    assert (W[:, :m] == 0).all() and (W[:, m:] > 0).all()
+    np.testing.assert_allclose(W.sum(1), 1.0, rtol=0, atol=1e-12)
+
+
+def test_routing_only_full_attention_special_case():
+    # k = N, m = 1, routing only: every key is routed and nothing else takes
+    # part, so the operator is textbook attention over the N keys.
+    N, d = 48, 8
+    Q, K, V = _rand((N, d), 17), _rand((N, d), 18), _rand((N, d), 19)
+    r = oracle.head(Q, K, V, (6, 8, 1, 1), 1, N, io="f64", shared=False)
+    t = torch.from_numpy
+    ref = F.scaled_dot_product_attention(t(Q)[None], t(K)[None], t(V)[None])[0].numpy()
+    np.testing.assert_allclose(r["out"], ref, rtol=0, atol=1e-12)
+
+
 def _golden_keys_per_query():
     rows = []
     with open(os.path.join(GOLDEN, "keys_per_query.txt")) as f:
@@ -253,6 +282,7 @@ _MUTANTS = {
     "pool_bins_floor_end": ("*hi = ((i + 1) * G + P - 1) / P;", "*hi = ((i + 1) * G) / P;"),
     "route_last_argmax": ("if (s > A[best]) best = i;", "if (s >= A[best]) best = i;"),
     "values_wrong_row": ("acc[f] += w * V[(size_t)j * d + f];", "acc[f] += w * V[(size_t)(N - 1 - j) * d + f];"),
+    "routing_only_keeps_shared": ("logit[i] = shared ? A[i] * scale : -INFINITY;", "logit[i] = A[i] * scale;"),
 }
 
 
@@ -272,7 +302,8 @@ def test_planted_mistake_fails_a_pin(name, tmp_path):
             lambda: test_landmark_values_match_sdpa(),
             lambda: test_topk_brute_force_with_ties(17),
             lambda: test_route_is_first_argmax(),
-            lambda: test_pool_matches_adaptive_avg_pool2d(14, 14, 5, 5)]
+            lambda: test_pool_matches_adaptive_avg_pool2d(14, 14, 5, 5),
+            lambda: test_routing_only_full_attention_special_case()]
     failures = 0
     with oracle.swapped_library(str(so)):
         for pin in pins:
