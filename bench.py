@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
+    ap.add_argument("--routing-only", action="store_true",
+                    help="the routing-only variant: the shared expert dropped from every query's softmax")
     ap.add_argument("--no-soak", action="store_true", help="skip the untimed repeats that extend clock sampling")
     return ap.parse_args()
 
@@ -160,9 +162,10 @@ class ClockSampler:
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(w, seconds, full=False):
+def cpu_baseline(w, seconds, full=False, shared=True):
     """Time the CPU oracle (single thread, fp64) on whole heads of the
-    workload until about ``seconds`` of work; returns query-heads/s."""
+    workload until about ``seconds`` of work; returns query-heads/s
+    (``shared=False``: the routing-only variant)."""
     import oracle
     Q, K, V = synth.make_inputs(w.scaled(B=1, H=min(w.H, 4)) if not full else w)
     Qf, Kf, Vf = Q.double().numpy(), K.double().numpy(), V.double().numpy()
@@ -173,7 +176,7 @@ def cpu_baseline(w, seconds, full=False):
     nq = w.N if queries is None else len(queries)
     while True:
         h = heads % Q.shape[1]
-        oracle.head(Qf[0, h], Kf[0, h], Vf[0, h], w.grid, w.m, w.k, io=w.dtype, queries=queries)
+        oracle.head(Qf[0, h], Kf[0, h], Vf[0, h], w.grid, w.m, w.k, io=w.dtype, queries=queries, shared=shared)
         heads += 1
         el = time.perf_counter() - t0
         if el >= seconds or (queries is not None and heads >= 1):
@@ -183,7 +186,7 @@ def cpu_baseline(w, seconds, full=False):
                   f"{nq} queries; time scaled to all {w.N} queries by the attend share")
         # scale: landmark stages are per head, attend per query; measure attend share separately
         t1 = time.perf_counter()
-        oracle.head(Qf[0, 0], Kf[0, 0], Vf[0, 0], w.grid, w.m, w.k, io=w.dtype, queries=queries[:1])
+        oracle.head(Qf[0, 0], Kf[0, 0], Vf[0, 0], w.grid, w.m, w.k, io=w.dtype, queries=queries[:1], shared=shared)
         base = time.perf_counter() - t1
         per_q = max(0.0, (el / heads - base) / max(1, nq - 1))
         per_head = base + per_q * w.N
@@ -233,7 +236,7 @@ def run_reference(args, w, ws, rank):
     times = []
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
     for s in range(args.warmup + args.steps):
-        cb = cpu_baseline(w, per_step)
+        cb = cpu_baseline(w, per_step, shared=not args.routing_only)
         if s >= args.warmup:
             times.append(cb)
     v = sorted(c["value"] for c in times)[len(times) // 2]
@@ -242,7 +245,8 @@ def run_reference(args, w, ws, rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded generator, no dataset)",
             "config": {"workload": workload_desc(w), "global_batch": w.B * ws, "seq_len": w.N,
-                       "parallelism": f"heads sharded, {ws} replica(s)"},
+                       "parallelism": f"heads sharded, {ws} replica(s)",
+                       "variant": "routing_only" if args.routing_only else "mita"},
             "cpu_baseline": {"value": v, "unit": "query-heads/s", "cores": 1, "kind": "oracle",
                              "sample": times[0]["sample"] + " per step; median over steps"},
             "e2e": {"value": v, "unit": "query-heads/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -264,6 +268,8 @@ def main():
     dev = torch.device("cuda", local)
     plan = mita.Plan.for_workload(w)
     plan.set_path(args.path)
+    if args.routing_only:
+        plan.set_option(mita.OPT_ROUTING_ONLY, 1)
     path = plan.path
     stream = torch.cuda.current_stream()
 
@@ -332,7 +338,7 @@ def main():
     hbm_frac = bw / pk["hbm_gbs"]
     roof_t = max(nbytes / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12))
     bound = "hbm" if nbytes / (pk["hbm_gbs"] * 1e9) >= flops / (pk["bf16_tflops"] * 1e12) else "tensor"
-    traffic = traffic_from_profiles(kernel_tag, w.name)
+    traffic = traffic_from_profiles(kernel_tag, w.name + ("+routing_only" if args.routing_only else ""))
     roofline = {"bound": bound, "achieved": round(bw if bound == "hbm" else tf, 2),
                 "peak": pk["hbm_gbs"] if bound == "hbm" else pk["bf16_tflops"],
                 "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
@@ -415,7 +421,7 @@ def main():
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, args.cpu_seconds)
+        cpu = cpu_baseline(w, args.cpu_seconds, shared=not args.routing_only)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "query-heads/s", "n_gpus": ws, "steps": args.steps,
@@ -423,7 +429,8 @@ def main():
                 "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded generator, no dataset)",
                 "config": {"workload": workload_desc(w), "global_batch": w.B * ws, "seq_len": w.N,
                            "parallelism": f"heads sharded over {ws} GPU(s), no collective",
-                           "path": path, "l2": f"inputs rotate over {nsets} buffer sets "
+                           "path": path, "variant": "routing_only" if args.routing_only else "mita",
+                           "l2": f"inputs rotate over {nsets} buffer sets "
                                                f"({nsets * set_bytes / 1e6:.0f} MB > 126 MB L2)"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "graph": graph, "gpu_launches": launches,
                 "clocks": clocks, "achieved_tflops": round(tf, 2), "achieved_hbm_gbs": round(bw, 1),

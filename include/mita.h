@@ -112,8 +112,16 @@ const char* mita_strerror(int code);
  *                            (MITA_ERR_UNSUPPORTED at forward time if the
  *                            shape does not fit the forced path).
  *   MITA_OPT_KEEP_LANDMARKS  1: mita_forward also stores Q_l and V_l in the
- *                            workspace for mita_get_landmarks(). */
-typedef enum { MITA_OPT_PATH = 0, MITA_OPT_KEEP_LANDMARKS = 1 } mita_option_t;
+ *                            workspace for mita_get_landmarks().
+ *   MITA_OPT_ROUTING_ONLY    1: the routing-only variant (the ablation of
+ *                            36Kr / 新智元 "注意力也是FFN？", section
+ *                            "长序列建模：训练时间从10.6小时降至2.4小时"): the
+ *                            shared expert is dropped and each query takes
+ *                            one softmax over its routed expert's k keys
+ *                            alone; landmarks, experts and routes are
+ *                            unchanged.  0 (default): the m shared pairs
+ *                            join every query's softmax. */
+typedef enum { MITA_OPT_PATH = 0, MITA_OPT_KEEP_LANDMARKS = 1, MITA_OPT_ROUTING_ONLY = 2 } mita_option_t;
 typedef enum { MITA_PATH_AUTO = 0, MITA_PATH_STAGED = 1, MITA_PATH_FUSED = 2, MITA_PATH_TILED = 3 } mita_path_t;
 int mita_set_option(mita_plan_t plan, int option, int value);
 

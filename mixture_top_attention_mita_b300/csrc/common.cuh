@@ -106,6 +106,7 @@ struct mita_plan_s {
     int device;
     int path_opt;          // mita_path_t requested
     int keep_landmarks;
+    int routing_only;      // 1: softmax over the routed keys alone (no shared expert)
     int landmarks_valid;
     // workspace (one cudaMalloc)
     void* ws;

@@ -95,6 +95,7 @@ struct Params {
     __nv_bfloat16* Vl_keep;
     int32_t* status;
     float scale_log2;         // log2(e) / sqrt(d)
+    int shared;               // 1: the m shared slots join the softmax; 0: routing only
     float rcnt[kSlots];       // 1 / (tokens in the bin of landmark i)
     float cnt[kSlots];        // tokens in the bin of landmark i
     int win[kSlots];          // 16 - ceil(log2(tokens in the bin)): exact-sum exponent window
@@ -701,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             // mask the padding slots, then one softmax per query row
 #pragma unroll
             for (int n = 0; n < 8; ++n) {
-                const int lim = n < 4 ? m : k;
+                const int lim = n < 4 ? (P.shared ? m : 0) : k;
                 const int s0 = 8 * (n & 3);
                 if (s0 + 8 > lim) {
 #pragma unroll
@@ -836,6 +837,7 @@ cudaError_t run_fused(mita_plan_s* p, const void* Q, const void* K, const void* 
     prm.Vl_keep = keep_landmarks ? (__nv_bfloat16*)p->Vl : nullptr;
     prm.status = p->status;
     prm.scale_log2 = kLog2e / sqrtf((float)s.d);
+    prm.shared = p->routing_only ? 0 : 1;
     int ntok = 0;
     for (int i = 0; i < s.m; ++i) {
         // adaptive average pooling bins [floor(r*G/P), ceil((r+1)*G/P)) per axis

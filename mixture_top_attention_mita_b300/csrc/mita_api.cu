@@ -123,6 +123,11 @@ int mita_set_option(mita_plan_t p, int option, int value) {
         p->keep_landmarks = value;
         return MITA_OK;
     }
+    if (option == MITA_OPT_ROUTING_ONLY) {
+        if (value != 0 && value != 1) return MITA_ERR_INVALID_ARG;
+        p->routing_only = value;
+        return MITA_OK;
+    }
     return MITA_ERR_INVALID_ARG;
 }
 

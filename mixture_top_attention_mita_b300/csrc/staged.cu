@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(32 * kAttendWarps)
     attend_kernel(Shape s, const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
                   const T* __restrict__ Ql, const T* __restrict__ Vl, const int32_t* __restrict__ idx,
                   const int32_t* __restrict__ route, const int32_t* __restrict__ perm, T* __restrict__ out,
-                  int32_t* __restrict__ status) {
+                  int shared, int32_t* __restrict__ status) {
     extern __shared__ float smem[];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int L = s.m + s.k;
@@ -364,6 +364,10 @@ __global__ void __launch_bounds__(32 * kAttendWarps)
     const float scale = rsqrtf((float)D);
     float mx = -INFINITY;
     for (int t = lane; t < L; t += 32) {
+        if (t < s.m && !shared) {   // routing only: the shared slots take no weight
+            l_s[t] = -INFINITY;
+            continue;
+        }
         const T* key;
         if (t < s.m) key = lq + (size_t)t * D;
         else {
@@ -394,7 +398,7 @@ __global__ void __launch_bounds__(32 * kAttendWarps)
     float acc[D / 32];
 #pragma unroll
     for (int u = 0; u < D / 32; ++u) acc[u] = 0.0f;
-    for (int t = 0; t < s.m; ++t) {
+    for (int t = 0; t < (shared ? s.m : 0); ++t) {
         float p = l_s[t];
 #pragma unroll
         for (int u = 0; u < D / 32; ++u) acc[u] = fmaf(p, to_f32(lv[(size_t)t * D + lane + 32 * u]), acc[u]);
@@ -432,7 +436,7 @@ static cudaError_t run_staged_t(mita_plan_s* p, const T* Q, const T* K, const T*
     const size_t smem = staged_attend_smem(s);
     ensure_smem_attr((const void*)attend_kernel<T, D>, (int)smem);
     attend_kernel<T, D><<<dim3((s.N + kAttendWarps - 1) / kAttendWarps, BH), 32 * kAttendWarps, smem, st>>>(
-        s, Q, K, V, Ql, Vl, idx, route, p->perm, out, p->status);
+        s, Q, K, V, Ql, Vl, idx, route, p->perm, out, p->routing_only ? 0 : 1, p->status);
     p->launches += 7;
     return cudaGetLastError();
 }

@@ -318,15 +318,21 @@ __global__ void tl_bucket_off(Shape s, const int32_t* __restrict__ counts, int32
 __global__ void tl_bucket_put(Shape s, const int32_t* __restrict__ route, int32_t* __restrict__ cursor,
                               int32_t* __restrict__ perm, int32_t* __restrict__ status) {
     chain_wait_and_trigger();
-    const int bh = blockIdx.y, q = blockIdx.x * blockDim.x + threadIdx.x;
-    if (q >= s.N) return;
-    const int r = route[(size_t)bh * s.N + q];
-    if (r < 0 || r >= s.m) {
+    const int bh = blockIdx.y, q = blockIdx.x * blockDim.x + threadIdx.x, lane = threadIdx.x & 31;
+    int r = q < s.N ? route[(size_t)bh * s.N + q] : -1;
+    if (q < s.N && (r < 0 || r >= s.m)) {
         atomicExch(status, (int)MITA_ERR_DEVICE);
-        return;
+        r = -1;
     }
-    const int pos = atomicAdd(&cursor[(size_t)bh * s.m + r], 1);
-    perm[(size_t)bh * s.N + pos] = q;
+    // lanes of the warp with the same route take their places with one atomic:
+    // the group's lowest lane adds the group size, the others add their rank
+    const unsigned grp = __match_any_sync(0xffffffffu, r);
+    if (r < 0) return;
+    const int leader = __ffs(grp) - 1;
+    int base = 0;
+    if (lane == leader) base = atomicAdd(&cursor[(size_t)bh * s.m + r], __popc(grp));
+    base = __shfl_sync(grp, base, leader);
+    perm[(size_t)bh * s.N + base + __popc(grp & ((1u << lane) - 1u))] = q;
 }
 
 // ---------------------------------------------------------------- attention
@@ -340,7 +346,7 @@ __global__ void __launch_bounds__(2 * QT, D == 64 ? 4 : 1)
               const bf16* __restrict__ Ql, const bf16* __restrict__ Vl, const int32_t* __restrict__ idx,
               const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm,
               const int32_t* __restrict__ tiles, const int32_t* __restrict__ ntiles, int maxt,
-              bf16* __restrict__ out, float cs, int32_t* __restrict__ status) {
+              bf16* __restrict__ out, float cs, int shared, int32_t* __restrict__ status) {
     chain_wait_and_trigger();
     constexpr int RB = 2 * D, CH = D / 8, KS = D / 16, NT = D / 8;
     extern __shared__ __align__(128) unsigned char sm[];
@@ -436,6 +442,13 @@ __global__ void __launch_bounds__(2 * QT, D == 64 ? 4 : 1)
 #pragma unroll
                 for (int x = 0; x < 4; ++x)
                     if (b * 64 + 8 * n + 2 * t + (x & 1) >= L) sc[n][x] = -INFINITY;
+        }
+        if (!shared && b * 64 < s.m) {   // routing only: the shared slots take no weight
+#pragma unroll
+            for (int n = 0; n < 8; ++n)
+#pragma unroll
+                for (int x = 0; x < 4; ++x)
+                    if (b * 64 + 8 * n + 2 * t + (x & 1) < s.m) sc[n][x] = -INFINITY;
         }
         float bm0 = -INFINITY, bm1 = -INFINITY;
 #pragma unroll
@@ -566,7 +579,7 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
         if ((err = launch_chained(chain, kern, dim3(maxt, BH), dim3(2 * QT), smem, st, s, Q, K, V, (const bf16*)Ql,
                                   (const bf16*)Vl, (const int32_t*)idx, (const int32_t*)p->offsets,
                                   (const int32_t*)p->perm, (const int32_t*)p->tiles, (const int32_t*)p->ntiles, maxt,
-                                  out, cs, p->status)) != cudaSuccess)
+                                  out, cs, p->routing_only ? 0 : 1, p->status)) != cudaSuccess)
             return err;
     }
     p->launches += 5;

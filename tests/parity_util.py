@@ -24,11 +24,12 @@ TIE_EPS = 1e-4
 TOL = {"f32": (1e-5, 1e-5), "bf16": (2e-2, 1e-2)}
 
 
-def compare_head(w, Qh, Kh, Vh, out_h, idx_h, route_h, exact: bool, queries=None, report=None):
+def compare_head(w, Qh, Kh, Vh, out_h, idx_h, route_h, exact: bool, queries=None, report=None, shared=True):
     """Check one head.  Qh/Kh/Vh are the CPU input tensors [N, d]; out_h
     [nq, d], idx_h [m, k], route_h [nq] are the GPU results (CPU tensors)
-    for the queries listed in ``queries`` (default all)."""
-    r = oracle.head(Qh, Kh, Vh, w.grid, w.m, w.k, io=w.dtype, queries=queries, debug=True)
+    for the queries listed in ``queries`` (default all); ``shared=False``
+    checks the routing-only variant."""
+    r = oracle.head(Qh, Kh, Vh, w.grid, w.m, w.k, io=w.dtype, queries=queries, debug=True, shared=shared)
     scale = 1.0 / math.sqrt(w.d)
     g_idx = idx_h.numpy()
     g_route = route_h.numpy()
@@ -67,7 +68,7 @@ def compare_head(w, Qh, Kh, Vh, out_h, idx_h, route_h, exact: bool, queries=None
     return r
 
 
-def compare_batch(w, Q, K, V, out, idx, route, exact: bool, heads=None, queries=None, report=None):
+def compare_batch(w, Q, K, V, out, idx, route, exact: bool, heads=None, queries=None, report=None, shared=True):
     """Check the listed (b, h) heads (default all) of a batch."""
     out, idx, route = out.cpu(), idx.cpu(), route.cpu()
     if heads is None:
@@ -78,4 +79,5 @@ def compare_batch(w, Q, K, V, out, idx, route, exact: bool, heads=None, queries=
         else:
             qs = torch.as_tensor(queries, dtype=torch.long)
             o, rt = out[b, h][qs], route[b, h][qs]
-        compare_head(w, Q[b, h], K[b, h], V[b, h], o, idx[b, h], rt, exact, queries=queries, report=report)
+        compare_head(w, Q[b, h], K[b, h], V[b, h], o, idx[b, h], rt, exact, queries=queries, report=report,
+                     shared=shared)

@@ -22,11 +22,13 @@ W = synth.WORKLOADS
 PATHS = ["staged", "fused", "tiled"]
 
 
-def _run(w, Q, K, V, path="auto", keep=False):
+def _run(w, Q, K, V, path="auto", keep=False, routing_only=False):
     plan = mita.Plan.for_workload(w)
     plan.set_path(path)
     if keep:
         plan.set_option(mita.OPT_KEEP_LANDMARKS, 1)
+    if routing_only:
+        plan.set_option(mita.OPT_ROUTING_ONLY, 1)
     dev = torch.device("cuda")
     Qd, Kd, Vd = Q.to(dev), K.to(dev), V.to(dev)
     out = torch.empty_like(Qd)
@@ -89,6 +91,27 @@ def test_small_integer_exact(name, path):
     Q, K, V = synth.make_integer_inputs(w)
     r = _run(w, Q, K, V, path)
     compare_batch(w, Q, K, V, r["out"], r["idx"], r["route"], exact=True)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("name", ["deit_s", "deit_t", "hires56", "long1d_8k"])
+def test_routing_only(name, path):
+    """Routing-only variant (the shared expert dropped): each query's softmax
+    runs over its routed expert's k keys alone."""
+    w = SMALL[name]
+    _skip_unbuilt(w, path)
+    Q, K, V = synth.make_inputs(w, seed=41)
+    r = _run(w, Q, K, V, path, routing_only=True)
+    compare_batch(w, Q, K, V, r["out"], r["idx"], r["route"], exact=False, shared=False)
+    Q, K, V = synth.make_integer_inputs(w, seed=43)
+    r = _run(w, Q, K, V, path, routing_only=True)
+    compare_batch(w, Q, K, V, r["out"], r["idx"], r["route"], exact=True, shared=False)
+
+
+def test_routing_only_option_rejects_bad_values():
+    plan = mita.Plan.for_workload(SMALL["deit_t"])
+    with pytest.raises(mita.MitaError):
+        plan.set_option(mita.OPT_ROUTING_ONLY, 2)
 
 
 @pytest.mark.parametrize("path", PATHS)
