@@ -5,7 +5,8 @@
 // "用少量地标查询，同时构造全局概括与细节专家") as a chain of kernels on one
 // stream; the landmark scores, landmark values and routes run on tcgen05
 // (tcgen.cu), the grouped attention on bf16 mma.sync:
-//   pool            Q_l, correctly rounded bin means (shared with the staged path)
+//   tl_pool         Q_l, correctly rounded bin means (16-byte loads, TwoSum
+//                   partials per token lane combined error-free)
 //   tc_scores       S = Q_l . K^T (fp32, workspace) and each landmark's row
 //                   max and min
 //   tl_topk_bits    per landmark the k best keys (ties to the lower index):
@@ -48,6 +49,65 @@ constexpr int kMaxK = 512;  // routed keys per expert
 int nsplit(const Shape& s) { return tc_value_splits(s); }
 int max_tiles(const Shape& s) { return (s.N + qt_of(s.d) - 1) / qt_of(s.d) + s.m; }
 
+
+// ---------------------------------------------------------------- pool
+// Q_l (bf16): block per (landmark i, head bh), 128 threads.  Thread t sums the
+// 8 features of 16-byte group t % G (G = D / 8) over the bin's tokens
+// t / G, t / G + 128 / G, ... (one 16-byte load per token, four in flight),
+// each feature with TwoSum compensation; the 128 / G partial (hi, lo) pairs of
+// a feature are then combined the same way and the correctly rounded mean is
+// decided exactly against c times the midpoints (mean_to_bf16).
+template <int D>
+__global__ void __launch_bounds__(128) tl_pool(Shape s, const bf16* __restrict__ Q, bf16* __restrict__ Ql) {
+    chain_wait_and_trigger();
+    constexpr int G = D / 8, TL = 128 / G;   // feature groups, token lanes
+    __shared__ float2 part[TL][D];
+    const int i = blockIdx.x, bh = blockIdx.y, t = threadIdx.x, fg = t % G, tln = t / G;
+    int r0, r1, c0, c1;
+    pool_bin(i / s.pw, s.gh, s.ph, r0, r1);
+    pool_bin(i % s.pw, s.gw, s.pw, c0, c1);
+    const int w = c1 - c0, cnt = (r1 - r0) * w;
+    const bf16* q = Q + (size_t)bh * s.N * D + fg * 8;
+    float hi[8], lo[8];
+#pragma unroll
+    for (int f = 0; f < 8; ++f) hi[f] = lo[f] = 0.0f;
+    for (int e0 = tln; e0 < cnt; e0 += 4 * TL) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = e0 + u * TL;
+            v[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (e < cnt) {
+                const int y = r0 + e / w, x = c0 + e % w;
+                v[u] = *(const uint4*)(q + (size_t)(y * s.gw + x) * D);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (e0 + u * TL < cnt) {
+                const uint32_t pv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    acc2(hi[2 * h], lo[2 * h], __uint_as_float(pv[h] << 16));
+                    acc2(hi[2 * h + 1], lo[2 * h + 1], __uint_as_float(pv[h] & 0xffff0000u));
+                }
+            }
+    }
+#pragma unroll
+    for (int f = 0; f < 8; ++f) part[tln][fg * 8 + f] = make_float2(hi[f], lo[f]);
+    __syncthreads();
+    for (int f = t; f < D; f += 128) {
+        float h = 0.0f, l = 0.0f;
+        for (int u = 0; u < TL; ++u) {
+            const float2 p = part[u][f];
+            float sh, se;
+            two_sum(h, p.x, sh, se);
+            h = sh;
+            l += se + p.y;
+        }
+        Ql[((size_t)bh * s.m + i) * D + f] = mean_to_bf16(h, l, (float)cnt);
+    }
+}
 
 // ---------------------------------------------------------------- top-k
 constexpr int kTB = 256;          // threads per top-k block
@@ -539,7 +599,8 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
     // latency is a visible share of the chain; on long rows (kernels of
     // hundreds of microseconds) the overlap measured slower and is off
     const bool chain = s.N <= kChainMaxN;
-    if ((err = staged_pool(s, MITA_BF16, Q, Ql, st, chain)) != cudaSuccess) return err;
+    if ((err = launch_chained(chain, tl_pool<D>, dim3(s.m, BH), dim3(128), 0, st, s, Q, Ql)) != cudaSuccess)
+        return err;
     const int ns = nsplit(s), G = head_group(s);
     for (int h0 = 0; h0 < BH; h0 += G) {
         Shape sg = s;
