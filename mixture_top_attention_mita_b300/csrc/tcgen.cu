@@ -7,7 +7,7 @@
 //   tc_values  split-K partials of V_l: numerators exp(S / sqrt d - max) are
 //              computed from S straight into a 128-byte swizzled K-major A
 //              tile, V comes by TMA as an M/N-major B tile, and the MMAs of a
-//              1024-key split accumulate in tensor memory (two stages: the
+//              split of 1024-4096 keys accumulate in tensor memory (two stages: the
 //              next tile's numerators and V copy overlap the current MMAs).
 //   tc_route   q . Q_l^T for 128 queries against all landmarks; each thread
 //              owns one query and takes the first argmax (the route).
@@ -26,7 +26,6 @@ using bf16 = __nv_bfloat16;
 using namespace tc;
 
 constexpr uint32_t kChunk = 128 * 128;   // one 128-row x 64-column bf16 tile, bytes
-constexpr int kKCV = 1024;               // keys per tc_values split
 
 // ---------------------------------------------------------------- scores
 template <int D, bool VEC>
@@ -124,7 +123,8 @@ __global__ void __launch_bounds__(128) tc_scores(const __grid_constant__ CUtenso
 template <int D, bool VEC>
 __global__ void __launch_bounds__(512) tc_values(const __grid_constant__ CUtensorMap mV, Shape s,
                                                  const float* __restrict__ S, const uint32_t* __restrict__ rowmax,
-                                                 float* __restrict__ part, float cs, int32_t* __restrict__ status) {
+                                                 float* __restrict__ part, float cs, int kcv,
+                                                 int32_t* __restrict__ status) {
     chain_wait_and_trigger();
     constexpr int KC = D / 64;                       // 64-wide feature chunks of a V tile
     constexpr uint32_t PBYTES = 2 * kChunk;          // numerators: 128 rows x 128 keys
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(512) tc_values(const __grid_constant__ CUtenso
         return;
     }
     const int split = blockIdx.x, i0 = blockIdx.y * 128, bh = blockIdx.z, ns = gridDim.x;
-    const int jb0 = split * kKCV, je = min(s.N, jb0 + kKCV), ntile = (je - jb0 + 127) / 128;
+    const int jb0 = split * kcv, je = min(s.N, jb0 + kcv), ntile = (je - jb0 + 127) / 128;
     const uint32_t base = smem_u32(smem);
     const uint32_t bar0 = smem_u32(&bars[0]);
     auto v_full = [&](int st) { return bar0 + 8u * st; };
@@ -371,20 +371,34 @@ static cudaError_t tc_scores_t(const Shape& s, const void* Ql, const void* K, fl
     return cudaGetLastError();
 }
 
+// Keys per landmark-values split: the longest of 1024, 2048, 4096 that still
+// gives at least two blocks per SM (measured: 64K-token rows 3366 / 3251 /
+// 3237 us per forward at 1024 / 2048 / 4096; the 56x56 layer needs 1024).
+int tc_value_keys(const Shape& s) {
+    int sms = 148;
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long rows = (long long)((s.m + 127) / 128) * s.BH();
+    int kcv = 1024;
+    while (kcv < 4096 && rows * ((s.N + 2 * kcv - 1) / (2 * kcv)) >= 2LL * sms) kcv *= 2;
+    return kcv;
+}
+
 template <int D>
 static cudaError_t tc_values_t(const Shape& s, const float* S, const uint32_t* rowmax, const void* V, float* part,
                                float cs, int32_t* status, cudaStream_t st, bool chain) {
     CUtensorMap mv;
     if (!map_rows(&mv, V, D, (size_t)s.BH() * s.N, 128)) return cudaErrorInvalidValue;
     const int smem = 2 * (2 * (int)tcg::kChunk + (D / 64) * (int)tcg::kChunk) + 1024;
-    const dim3 grid((s.N + tcg::kKCV - 1) / tcg::kKCV, (s.m + 127) / 128, s.BH());
+    const int kcv = tc_value_keys(s);
+    const dim3 grid((s.N + kcv - 1) / kcv, (s.m + 127) / 128, s.BH());
     if (s.N % 4 == 0) {
         ensure_smem_attr((const void*)tcg::tc_values<D, true>, smem);
-        cudaError_t le = launch_chained(chain, tcg::tc_values<D, true>, grid, dim3(512), smem, st, mv, s, S, rowmax, part, cs, status);
+        cudaError_t le = launch_chained(chain, tcg::tc_values<D, true>, grid, dim3(512), smem, st, mv, s, S, rowmax, part, cs, kcv, status);
         if (le != cudaSuccess) return le;
     } else {
         ensure_smem_attr((const void*)tcg::tc_values<D, false>, smem);
-        cudaError_t le = launch_chained(chain, tcg::tc_values<D, false>, grid, dim3(512), smem, st, mv, s, S, rowmax, part, cs, status);
+        cudaError_t le = launch_chained(chain, tcg::tc_values<D, false>, grid, dim3(512), smem, st, mv, s, S, rowmax, part, cs, kcv, status);
         if (le != cudaSuccess) return le;
     }
     return cudaGetLastError();
@@ -407,7 +421,7 @@ static cudaError_t tc_route_t(const Shape& s, const void* Q, const void* Ql, int
     return cudaGetLastError();
 }
 
-int tc_value_splits(const Shape& s) { return (s.N + tcg::kKCV - 1) / tcg::kKCV; }
+int tc_value_splits(const Shape& s) { return (s.N + tc_value_keys(s) - 1) / tc_value_keys(s); }
 
 cudaError_t tc_scores(const Shape& s, const void* Ql, const void* K, float* S, uint32_t* rowmax, uint32_t* rowmin,
                       int32_t* status, cudaStream_t st, bool chain) {

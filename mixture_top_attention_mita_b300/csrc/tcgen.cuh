@@ -12,6 +12,7 @@ cudaError_t tc_scores(const Shape& s, const void* Ql, const void* K, float* S, u
 cudaError_t tc_values(const Shape& s, const float* S, const uint32_t* rowmax, const void* V, float* part,
                       float cs, int32_t* status, cudaStream_t st, bool chain);
 int tc_value_splits(const Shape& s);
+int tc_value_keys(const Shape& s);   // keys per split
 // Route of every query (first argmax of q . Q_l) and per-landmark query counts (added).
 cudaError_t tc_route(const Shape& s, const void* Q, const void* Ql, int32_t* route, int32_t* counts,
                      int32_t* status, cudaStream_t st, bool chain);

@@ -15,7 +15,7 @@
 //                   row read out in key order (rows up to 64K keys; longer
 //                   rows use the staged path's radix select)
 //   tc_values       split-K partial sums of exp(S / sqrt d - max) . V and of
-//                   the row sums, per 1024-key split
+//                   the row sums, per split of 1024-4096 keys
 //   tl_values_fin   V_l = sum of partials / sum of row sums, bf16
 //   tc_route        q . Q_l^T per query tile, first argmax (the route), and
 //                   per-landmark query counts
