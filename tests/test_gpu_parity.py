@@ -178,6 +178,58 @@ def test_flat_and_tied_rows(name, kind, path):
     compare_batch(w, Q, K, V, r["out"], r["idx"], r["route"], exact=True)
 
 
+EDGE_MORE = [
+    # the largest one-kernel shape: N = 256 on a 16x16 grid, m = k = 32
+    W["deit_t"].scaled(B=2, H=2, N=256, gh=16, gw=16, ph=4, pw=8, m=32, k=32),
+    # a 1-D sequence with m = 256 landmarks of 16 tokens and k = 100
+    W["long1d"].scaled(B=1, H=2, N=4096, gw=4096, pw=256, m=256, k=100),
+    # d = 64 on the tiled path with k at its limit
+    W["hires56"].scaled(B=1, H=1, N=1024, gh=32, gw=32, ph=4, pw=4, m=16, k=512),
+]
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("i", range(len(EDGE_MORE)))
+def test_edge_shapes_more(i, path):
+    w = EDGE_MORE[i]
+    _skip_unbuilt(w, path)
+    Q, K, V = synth.make_inputs(w, seed=300 + i)
+    r = _run(w, Q, K, V, path)
+    compare_batch(w, Q, K, V, r["out"], r["idx"], r["route"], exact=False)
+    Q, K, V = synth.make_integer_inputs(w, seed=400 + i)
+    r = _run(w, Q, K, V, path)
+    compare_batch(w, Q, K, V, r["out"], r["idx"], r["route"], exact=_means_exact(w, Q))
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("name", ["deit_s", "hires56"])
+def test_graph_capture_matches_stream(name, path):
+    """A forward captured in a CUDA graph (the tiled chain's overlapped
+    launches become programmatic graph edges) gives the stream forward's
+    results bit for bit."""
+    w = SMALL[name]
+    _skip_unbuilt(w, path)
+    Q, K, V = synth.make_inputs(w, seed=51)
+    ref = _run(w, Q, K, V, path)
+    plan = ref["plan"]
+    dev = torch.device("cuda")
+    Qd, Kd, Vd = Q.to(dev), K.to(dev), V.to(dev)
+    out = torch.empty_like(Qd)
+    idx = torch.full((w.B, w.H, w.m, w.k), -1, dtype=torch.int32, device=dev)
+    route = torch.full((w.B, w.H, w.N), -1, dtype=torch.int32, device=dev)
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
+        plan.forward(Qd, Kd, Vd, out, idx, route, torch.cuda.current_stream())
+    for _ in range(2):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert plan.status() == mita.MITA_OK
+        assert torch.equal(out, ref["out"]) and torch.equal(idx, ref["idx"]) and torch.equal(route, ref["route"])
+
+
 def _means_exact(w, Q):
     """True when every pooled mean of these integer inputs is exactly
     representable in the I/O type, so that all fp32 sums are exact."""
