@@ -81,13 +81,22 @@ def workload_desc(w):
             f"s=1 {w.dtype} {w.gen}")
 
 
-def source_hash():
+# Sources each recorded kernel is compiled from (its DRAM traffic changes only
+# with these); any other tag hashes every CUDA source.
+KERNEL_SOURCES = {"mita_fused": ["csrc/fused.cu", "csrc/fused.cuh", "csrc/common.cuh", "../include/mita.h"]}
+
+
+def source_hash(kernel_tag=None):
     import hashlib
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "mixture_top_attention_mita_b300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, fn), "rb").read())
+    pkg = os.path.join(ROOT, "mixture_top_attention_mita_b300")
+    csrc = os.path.join(pkg, "csrc")
+    if kernel_tag in KERNEL_SOURCES:
+        files = [os.path.normpath(os.path.join(pkg, f)) for f in KERNEL_SOURCES[kernel_tag]]
+    else:
+        files = [os.path.join(csrc, fn) for fn in sorted(os.listdir(csrc)) if fn.endswith((".cu", ".cuh"))]
+    for fn in files:
+        h.update(open(fn, "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -98,7 +107,7 @@ def traffic_from_profiles(kernel_tag, workload):
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    want = source_hash()
+    want = source_hash(kernel_tag)
     for line in open(path):
         if line.startswith("#") or not line.strip():
             continue

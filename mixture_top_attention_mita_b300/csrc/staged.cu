@@ -23,7 +23,6 @@ namespace mita {
 // tokens (coalesced row reads) and writes the correctly rounded mean.
 template <typename T>
 __global__ void pool_kernel(Shape s, const T* __restrict__ Q, T* __restrict__ Ql) {
-    chain_wait_and_trigger();
     const int i = blockIdx.x, bh = blockIdx.y, f = threadIdx.x;
     const int r = i / s.pw, c = i % s.pw;
     int r0, r1, c0, c1;
@@ -439,14 +438,6 @@ static cudaError_t run_staged_t(mita_plan_s* p, const T* Q, const T* K, const T*
         s, Q, K, V, Ql, Vl, idx, route, p->perm, out, p->routing_only ? 0 : 1, p->status);
     p->launches += 7;
     return cudaGetLastError();
-}
-
-cudaError_t staged_pool(const Shape& s, mita_dtype_t dtype, const void* Q, void* Ql, cudaStream_t st, bool chained) {
-    const dim3 grid(s.m, s.BH());
-    if (dtype == MITA_BF16)
-        return launch_chained(chained, pool_kernel<__nv_bfloat16>, grid, dim3(s.d), 0, st, s, (const __nv_bfloat16*)Q,
-                              (__nv_bfloat16*)Ql);
-    return launch_chained(chained, pool_kernel<float>, grid, dim3(s.d), 0, st, s, (const float*)Q, (float*)Ql);
 }
 
 cudaError_t staged_topk(const Shape& s, const float* S, int32_t* idx, cudaStream_t st, bool chained) {

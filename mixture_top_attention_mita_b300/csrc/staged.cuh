@@ -4,10 +4,9 @@
 
 namespace mita {
 size_t staged_attend_smem(const Shape& s);
-// Step 1 (landmark queries) and step 3 (exact top-k over raw scores S
-// [BH, m, N] fp32) of the staged path, for reuse by the tiled path.
-cudaError_t staged_pool(const Shape& s, mita_dtype_t dtype, const void* Q, void* Ql, cudaStream_t st,
-                        bool chained = false);
+// Step 3 of the staged path (exact top-k over raw scores S [BH, m, N] fp32),
+// reused by the tiled path for rows longer than its bitmap select takes;
+// `chained`: the launch may overlap the previous kernel (see launch.cuh).
 cudaError_t staged_topk(const Shape& s, const float* S, int32_t* idx, cudaStream_t st, bool chained = false);
 cudaError_t run_staged(mita_plan_s* p, const void* Q, const void* K, const void* V, void* out,
                        int32_t* idx, int32_t* route, cudaStream_t st);
