@@ -51,10 +51,10 @@ def _open(path):
     lib.oracle_round_bf16.argtypes = [ctypes.c_double]
     lib.oracle_round_bf16.restype = ctypes.c_double
     lib.oracle_bin.argtypes = [i, i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
-    lib.oracle_head.argtypes = [i, i, i, i, i, i, i, i, i, i, dp, dp, dp, i, ip,
+    lib.oracle_head.argtypes = [i, i, i, i, i, i, i, i, i, i, i, dp, dp, dp, i, ip,
                                 dp, ip, ip, dp, dp, dp, dp, dp]
     lib.oracle_head.restype = i
-    lib.oracle_forward.argtypes = [i, i, i, i, i, i, i, i, i, i, i, dp, dp, dp, dp, ip, ip]
+    lib.oracle_forward.argtypes = [i, i, i, i, i, i, i, i, i, i, i, i, dp, dp, dp, dp, ip, ip]
     lib.oracle_forward.restype = i
     return lib
 
@@ -106,7 +106,7 @@ def _f64(x) -> np.ndarray:
 
 
 def head(Q, K, V, grid, m: int, k: int, io: str = "f64", queries=None, debug: bool = False,
-         shared: bool = True):
+         shared: bool = True, s: int = 1):
     """Run the oracle on one head.
 
     Q, K, V: [N, d] arrays (values are taken exactly; bf16/fp32 torch tensors
@@ -116,7 +116,10 @@ def head(Q, K, V, grid, m: int, k: int, io: str = "f64", queries=None, debug: bo
     route [nq] and, with ``debug``, Ql, Vl, R [m,N] (raw scores),
     A [nq,m] (raw query-landmark scores) and W [nq, m+k] (attention weights).
     ``shared=False`` is the routing-only variant: one softmax over the k
-    routed logits alone (the shared weights are zero).
+    routed logits alone (the shared weights are zero).  ``s > 1`` routes each
+    query to its s best landmarks and takes one softmax over the shared
+    logits and the union of their experts' keys (W is then not returned;
+    route holds the best landmark).
     """
     lib = _load()
     Q, K, V = _f64(Q), _f64(K), _f64(V)
@@ -131,19 +134,21 @@ def head(Q, K, V, grid, m: int, k: int, io: str = "f64", queries=None, debug: bo
     Vl = np.zeros((m, d)) if debug else None
     R = np.zeros((m, N)) if debug else None
     A = np.zeros((nq, m)) if debug else None
-    W = np.zeros((nq, m + k)) if debug else None
-    rc = lib.oracle_head(N, d, gh, gw, ph, pw, m, k, _IO_NAMES[io], int(shared), _dp(Q), _dp(K), _dp(V),
+    W = np.zeros((nq, m + k)) if debug and s == 1 else None
+    rc = lib.oracle_head(N, d, gh, gw, ph, pw, m, k, _IO_NAMES[io], int(shared), int(s), _dp(Q), _dp(K), _dp(V),
                          nq, _ip(qlist), _dp(out), _ip(idx), _ip(route),
                          _dp(Ql), _dp(Vl), _dp(R), _dp(A), _dp(W))
     if rc != 0:
         raise ValueError("oracle: invalid sizes")
     res = {"out": out, "idx": idx, "route": route}
     if debug:
-        res.update(Ql=Ql, Vl=Vl, R=R, A=A, W=W)
+        res.update(Ql=Ql, Vl=Vl, R=R, A=A)
+        if W is not None:
+            res["W"] = W
     return res
 
 
-def forward(Q, K, V, grid, m: int, k: int, io: str = "f64", shared: bool = True):
+def forward(Q, K, V, grid, m: int, k: int, io: str = "f64", shared: bool = True, s: int = 1):
     """Run the oracle on a [B, H, N, d] batch; returns out [B,H,N,d] (fp64,
     holding values of the I/O type), idx [B,H,m,k] and route [B,H,N]."""
     lib = _load()
@@ -153,7 +158,7 @@ def forward(Q, K, V, grid, m: int, k: int, io: str = "f64", shared: bool = True)
     out = np.zeros((B, H, N, d))
     idx = np.zeros((B, H, m, k), dtype=np.int32)
     route = np.zeros((B, H, N), dtype=np.int32)
-    rc = lib.oracle_forward(B * H, N, d, gh, gw, ph, pw, m, k, _IO_NAMES[io], int(shared),
+    rc = lib.oracle_forward(B * H, N, d, gh, gw, ph, pw, m, k, _IO_NAMES[io], int(shared), int(s),
                             _dp(Q), _dp(K), _dp(V), _dp(out), _ip(idx), _ip(route))
     if rc != 0:
         raise ValueError("oracle: invalid sizes")

@@ -31,6 +31,10 @@
  * "长序列建模：训练时间从10.6小时降至2.4小时", that drops the shared expert):
  * step 6 takes one softmax over the k routed logits alone; steps 1-5 are
  * unchanged.
+ * Routing to s > 1 experts (the article's routing keeps s as a parameter and
+ * uses s = 1): a query is routed to its s best landmarks (A descending, ties
+ * to the lower landmark index) and takes one softmax over the m shared logits
+ * and the union of those s experts' keys, each key once.
  */
 #include <math.h>
 #include <stdint.h>
@@ -214,18 +218,71 @@ void oracle_attend_one(int d, int m, int k, int io, int shared, const double* q,
     free(logit);
 }
 
+/* Step 5 for s > 1 (one query): the s landmarks with the largest A[i], ties
+ * to the lower index, best first, in top[0 .. s-1]. */
+void oracle_route_top(int m, int s, const double* A, int32_t* top) {
+    for (int r = 0; r < s; ++r) {
+        int best = -1;
+        for (int i = 0; i < m; ++i) {
+            int taken = 0;
+            for (int u = 0; u < r; ++u) taken |= top[u] == i;
+            if (!taken && (best < 0 || A[i] > A[best])) best = i;
+        }
+        top[r] = best;
+    }
+}
+
+/* Step 6 for s > 1 (one query): one softmax over the m shared logits (none
+ * with shared = 0) and the logits of every key in the union of the experts
+ * E_top[0], ..., E_top[s-1], each key once; out is rounded to the I/O type. */
+void oracle_attend_multi(int N, int d, int m, int k, int s, int io, int shared, const double* q,
+                         const double* A, const int32_t* idx, const int32_t* top, const double* K,
+                         const double* V, const double* Vl, double* out) {
+    double scale = 1.0 / sqrt((double)d);
+    char* in_union = (char*)calloc((size_t)N, 1);
+    for (int r = 0; r < s; ++r)
+        for (int t = 0; t < k; ++t) in_union[idx[(size_t)top[r] * k + t]] = 1;
+    double* w = (double*)malloc(sizeof(double) * (size_t)(m + N));
+    double mx = -INFINITY;
+    for (int i = 0; i < m; ++i) {
+        w[i] = shared ? A[i] * scale : -INFINITY;
+        if (w[i] > mx) mx = w[i];
+    }
+    for (int j = 0; j < N; ++j) {
+        w[m + j] = -INFINITY;
+        if (!in_union[j]) continue;
+        double s2 = 0.0;
+        for (int f = 0; f < d; ++f) s2 += q[f] * K[(size_t)j * d + f];
+        w[m + j] = s2 * scale;
+        if (w[m + j] > mx) mx = w[m + j];
+    }
+    double den = 0.0;
+    for (int l = 0; l < m + N; ++l) { w[l] = exp(w[l] - mx); den += w[l]; }
+    for (int f = 0; f < d; ++f) {
+        double acc = 0.0;
+        for (int i = 0; i < m; ++i) acc += w[i] * Vl[(size_t)i * d + f];
+        for (int j = 0; j < N; ++j) if (in_union[j]) acc += w[m + j] * V[(size_t)j * d + f];
+        out[f] = round_io(acc / den, io);
+    }
+    free(w);
+    free(in_union);
+}
+
 /* The whole operator for one head.  qlist (nq entries, NULL = all N queries
  * in order) selects the queries whose route and output are produced; the
  * landmarks, experts and landmark values always cover the whole head.
  * Optional outputs (NULL to skip): Ql [m,d], Vl [m,d], R [m,N], A [nq,m],
- * W [nq, m+k].  Returns 0, or -1 on invalid sizes. */
-int oracle_head(int N, int d, int gh, int gw, int ph, int pw, int m, int k, int io, int shared,
+ * W [nq, m+k] (s = 1 only).  s: experts per query (1 <= s <= m); route[]
+ * holds each query's best landmark.  Returns 0, or -1 on invalid sizes. */
+int oracle_head(int N, int d, int gh, int gw, int ph, int pw, int m, int k, int io, int shared, int s,
                 const double* Q, const double* K, const double* V,
                 int nq, const int32_t* qlist,
                 double* out, int32_t* idx, int32_t* route,
                 double* Ql_out, double* Vl_out, double* R_out, double* A_out, double* W_out) {
     if (N < 1 || d < 1 || gh * gw != N || ph * pw != m || ph > gh || pw > gw || k < 1 || k > N)
         return -1;
+    if (s < 1 || s > m || (s > 1 && W_out)) return -1;
+    int32_t* top = (int32_t*)malloc(sizeof(int32_t) * (size_t)s);
     double* Ql = Ql_out ? Ql_out : (double*)malloc(sizeof(double) * (size_t)m * d);
     double* Vl = Vl_out ? Vl_out : (double*)malloc(sizeof(double) * (size_t)m * d);
     double* R = R_out ? R_out : (double*)malloc(sizeof(double) * (size_t)m * N);
@@ -241,9 +298,15 @@ int oracle_head(int N, int d, int gh, int gw, int ph, int pw, int m, int k, int 
         int r = oracle_route_one(d, m, q, Ql, A);
         route[n] = r;
         if (A_out) memcpy(A_out + (size_t)n * m, A, sizeof(double) * (size_t)m);
-        oracle_attend_one(d, m, k, io, shared, q, A, idx + (size_t)r * k, K, V, Vl,
-                          out + (size_t)n * d, W_out ? W_out + (size_t)n * (m + k) : NULL);
+        if (s == 1) {
+            oracle_attend_one(d, m, k, io, shared, q, A, idx + (size_t)r * k, K, V, Vl,
+                              out + (size_t)n * d, W_out ? W_out + (size_t)n * (m + k) : NULL);
+        } else {
+            oracle_route_top(m, s, A, top);
+            oracle_attend_multi(N, d, m, k, s, io, shared, q, A, idx, top, K, V, Vl, out + (size_t)n * d);
+        }
     }
+    free(top);
     free(A);
     if (!Ql_out) free(Ql);
     if (!Vl_out) free(Vl);
@@ -252,12 +315,12 @@ int oracle_head(int N, int d, int gh, int gw, int ph, int pw, int m, int k, int 
 }
 
 /* All heads of a [B*H, N, d] batch, every query. */
-int oracle_forward(int BH, int N, int d, int gh, int gw, int ph, int pw, int m, int k, int io, int shared,
+int oracle_forward(int BH, int N, int d, int gh, int gw, int ph, int pw, int m, int k, int io, int shared, int s,
                    const double* Q, const double* K, const double* V,
                    double* out, int32_t* idx, int32_t* route) {
     for (int h = 0; h < BH; ++h) {
         size_t o = (size_t)h * N * d;
-        int rc = oracle_head(N, d, gh, gw, ph, pw, m, k, io, shared, Q + o, K + o, V + o, N, NULL,
+        int rc = oracle_head(N, d, gh, gw, ph, pw, m, k, io, shared, s, Q + o, K + o, V + o, N, NULL,
                              out + o, idx + (size_t)h * m * k, route + (size_t)h * N,
                              NULL, NULL, NULL, NULL, NULL);
         if (rc) return rc;

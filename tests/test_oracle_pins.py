@@ -191,6 +191,43 @@ def test_routing_only_full_attention_special_case():
     np.testing.assert_allclose(r["out"], ref, rtol=0, atol=1e-12)
 
 
+def _top_s_reference(Q, K, V, r, m, s):
+    """Masked SDPA over [Q_l ; K]: every shared pair, and the keys of the s best
+    experts of each query (stable order on -A: ties to the lower landmark)."""
+    N = Q.shape[0]
+    top = np.argsort(-r["A"], axis=1, kind="stable")[:, :s]
+    mask = np.zeros((N, m + N), bool)
+    mask[:, :m] = True
+    for q in range(N):
+        for e in top[q]:
+            mask[q, m + r["idx"][e]] = True
+    t = torch.from_numpy
+    keys, vals = np.concatenate([r["Ql"], K]), np.concatenate([r["Vl"], V])
+    return F.scaled_dot_product_attention(t(Q)[None], t(keys)[None], t(vals)[None], attn_mask=t(mask)[None])[0].numpy()
+
+
+@pytest.mark.parametrize("s", [2, 3, 25])
+def test_top_s_routing_matches_masked_sdpa(s):
+    # s > 1: the union of the s best experts' keys, each key once, next to the
+    # m shared pairs in one softmax.
+    Q, K, V = _rand((196, 16), 21), _rand((196, 16), 22), _rand((196, 16), 23)
+    r = oracle.head(Q, K, V, (14, 14, 5, 5), 25, 25, io="f64", debug=True, s=s)
+    np.testing.assert_allclose(r["out"], _top_s_reference(Q, K, V, r, 25, s), rtol=0, atol=1e-12)
+
+
+def test_top_s_routing_ties_on_integer_inputs():
+    # small-integer inputs: many exactly tied query-landmark scores, so the
+    # tie rule (lower landmark first) decides which experts join
+    g = torch.Generator("cpu").manual_seed(24)
+    Q = torch.randint(-1, 2, (64, 8), generator=g).double().numpy()
+    K = torch.randint(-2, 3, (64, 8), generator=g).double().numpy()
+    V = torch.randint(-3, 4, (64, 8), generator=g).double().numpy()
+    r = oracle.head(Q, K, V, (8, 8, 2, 4), 8, 6, io="f64", debug=True, s=3)
+    A = r["A"]
+    assert any(len(np.unique(row)) < len(row) for row in A)   # ties present
+    np.testing.assert_allclose(r["out"], _top_s_reference(Q, K, V, r, 8, 3), rtol=0, atol=1e-12)
+
+
 def _golden_keys_per_query():
     rows = []
     with open(os.path.join(GOLDEN, "keys_per_query.txt")) as f:
@@ -283,6 +320,10 @@ _MUTANTS = {
     "route_last_argmax": ("if (s > A[best]) best = i;", "if (s >= A[best]) best = i;"),
     "values_wrong_row": ("acc[f] += w * V[(size_t)j * d + f];", "acc[f] += w * V[(size_t)(N - 1 - j) * d + f];"),
     "routing_only_keeps_shared": ("logit[i] = shared ? A[i] * scale : -INFINITY;", "logit[i] = A[i] * scale;"),
+    "top_s_first_expert_only": ("for (int r = 0; r < s; ++r)\n        for (int t = 0; t < k; ++t) in_union",
+                                "for (int r = 0; r < 1; ++r)\n        for (int t = 0; t < k; ++t) in_union"),
+    "top_s_ties_to_higher": ("if (!taken && (best < 0 || A[i] > A[best])) best = i;",
+                             "if (!taken && (best < 0 || A[i] >= A[best])) best = i;"),
 }
 
 
@@ -303,7 +344,9 @@ def test_planted_mistake_fails_a_pin(name, tmp_path):
             lambda: test_topk_brute_force_with_ties(17),
             lambda: test_route_is_first_argmax(),
             lambda: test_pool_matches_adaptive_avg_pool2d(14, 14, 5, 5),
-            lambda: test_routing_only_full_attention_special_case()]
+            lambda: test_routing_only_full_attention_special_case(),
+            lambda: test_top_s_routing_matches_masked_sdpa(3),
+            lambda: test_top_s_routing_ties_on_integer_inputs()]
     failures = 0
     with oracle.swapped_library(str(so)):
         for pin in pins:
