@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--routing-only", action="store_true",
                     help="the routing-only variant: the shared expert dropped from every query's softmax")
+    ap.add_argument("--routes", type=int, default=1,
+                    help="experts per query (s > 1 runs on the staged path)")
     ap.add_argument("--no-soak", action="store_true", help="skip the untimed repeats that extend clock sampling")
     return ap.parse_args()
 
@@ -75,10 +77,10 @@ def peaks():
         return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
 
 
-def workload_desc(w):
+def workload_desc(w, routes=1):
     grid = f"{w.gh}x{w.gw}" if w.gh > 1 else f"1-D {w.N}"
     return (f"{w.name}: B={w.B} H={w.H} N={w.N} ({grid}) d={w.d} m={w.m} ({w.ph}x{w.pw}) k={w.k} "
-            f"s=1 {w.dtype} {w.gen}")
+            f"s={routes} {w.dtype} {w.gen}")
 
 
 # Sources each recorded kernel is compiled from (its DRAM traffic changes only
@@ -171,7 +173,13 @@ class ClockSampler:
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(w, seconds, full=False, shared=True):
+def variant_name(args):
+    """The operator variant a run measures: mita, routing_only, routes_s<S>."""
+    parts = (["routing_only"] if args.routing_only else []) + ([f"routes_s{args.routes}"] if args.routes > 1 else [])
+    return "+".join(parts) if parts else "mita"
+
+
+def cpu_baseline(w, seconds, full=False, shared=True, routes=1):
     """Time the CPU oracle (single thread, fp64) on whole heads of the
     workload until about ``seconds`` of work; returns query-heads/s
     (``shared=False``: the routing-only variant)."""
@@ -185,7 +193,8 @@ def cpu_baseline(w, seconds, full=False, shared=True):
     nq = w.N if queries is None else len(queries)
     while True:
         h = heads % Q.shape[1]
-        oracle.head(Qf[0, h], Kf[0, h], Vf[0, h], w.grid, w.m, w.k, io=w.dtype, queries=queries, shared=shared)
+        oracle.head(Qf[0, h], Kf[0, h], Vf[0, h], w.grid, w.m, w.k, io=w.dtype, queries=queries, shared=shared,
+                    s=routes)
         heads += 1
         el = time.perf_counter() - t0
         if el >= seconds or (queries is not None and heads >= 1):
@@ -195,7 +204,8 @@ def cpu_baseline(w, seconds, full=False, shared=True):
                   f"{nq} queries; time scaled to all {w.N} queries by the attend share")
         # scale: landmark stages are per head, attend per query; measure attend share separately
         t1 = time.perf_counter()
-        oracle.head(Qf[0, 0], Kf[0, 0], Vf[0, 0], w.grid, w.m, w.k, io=w.dtype, queries=queries[:1], shared=shared)
+        oracle.head(Qf[0, 0], Kf[0, 0], Vf[0, 0], w.grid, w.m, w.k, io=w.dtype, queries=queries[:1], shared=shared,
+                    s=routes)
         base = time.perf_counter() - t1
         per_q = max(0.0, (el / heads - base) / max(1, nq - 1))
         per_head = base + per_q * w.N
@@ -245,7 +255,7 @@ def run_reference(args, w, ws, rank):
     times = []
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
     for s in range(args.warmup + args.steps):
-        cb = cpu_baseline(w, per_step, shared=not args.routing_only)
+        cb = cpu_baseline(w, per_step, shared=not args.routing_only, routes=args.routes)
         if s >= args.warmup:
             times.append(cb)
     v = sorted(c["value"] for c in times)[len(times) // 2]
@@ -253,9 +263,9 @@ def run_reference(args, w, ws, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * w.heads * w.N / v,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded generator, no dataset)",
-            "config": {"workload": workload_desc(w), "global_batch": w.B * ws, "seq_len": w.N,
+            "config": {"workload": workload_desc(w, args.routes), "global_batch": w.B * ws, "seq_len": w.N,
                        "parallelism": f"heads sharded, {ws} replica(s)",
-                       "variant": "routing_only" if args.routing_only else "mita"},
+                       "variant": variant_name(args)},
             "cpu_baseline": {"value": v, "unit": "query-heads/s", "cores": 1, "kind": "oracle",
                              "sample": times[0]["sample"] + " per step; median over steps"},
             "e2e": {"value": v, "unit": "query-heads/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -279,6 +289,8 @@ def main():
     plan.set_path(args.path)
     if args.routing_only:
         plan.set_option(mita.OPT_ROUTING_ONLY, 1)
+    if args.routes > 1:
+        plan.set_option(mita.OPT_ROUTES, args.routes)
     path = plan.path
     stream = torch.cuda.current_stream()
 
@@ -347,7 +359,8 @@ def main():
     hbm_frac = bw / pk["hbm_gbs"]
     roof_t = max(nbytes / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12))
     bound = "hbm" if nbytes / (pk["hbm_gbs"] * 1e9) >= flops / (pk["bf16_tflops"] * 1e12) else "tensor"
-    traffic = traffic_from_profiles(kernel_tag, w.name + ("+routing_only" if args.routing_only else ""))
+    traffic = traffic_from_profiles(kernel_tag, w.name if variant_name(args) == "mita" else
+                                    w.name + "+" + variant_name(args))
     roofline = {"bound": bound, "achieved": round(bw if bound == "hbm" else tf, 2),
                 "peak": pk["hbm_gbs"] if bound == "hbm" else pk["bf16_tflops"],
                 "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
@@ -430,15 +443,15 @@ def main():
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, args.cpu_seconds, shared=not args.routing_only)
+        cpu = cpu_baseline(w, args.cpu_seconds, shared=not args.routing_only, routes=args.routes)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "query-heads/s", "n_gpus": ws, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded generator, no dataset)",
-                "config": {"workload": workload_desc(w), "global_batch": w.B * ws, "seq_len": w.N,
+                "config": {"workload": workload_desc(w, args.routes), "global_batch": w.B * ws, "seq_len": w.N,
                            "parallelism": f"heads sharded over {ws} GPU(s), no collective",
-                           "path": path, "variant": "routing_only" if args.routing_only else "mita",
+                           "path": path, "variant": variant_name(args),
                            "l2": f"inputs rotate over {nsets} buffer sets "
                                                f"({nsets * set_bytes / 1e6:.0f} MB > 126 MB L2)"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "graph": graph, "gpu_launches": launches,

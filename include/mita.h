@@ -120,8 +120,21 @@ const char* mita_strerror(int code);
  *                            one softmax over its routed expert's k keys
  *                            alone; landmarks, experts and routes are
  *                            unchanged.  0 (default): the m shared pairs
- *                            join every query's softmax. */
-typedef enum { MITA_OPT_PATH = 0, MITA_OPT_KEEP_LANDMARKS = 1, MITA_OPT_ROUTING_ONLY = 2 } mita_option_t;
+ *                            join every query's softmax.
+ *   MITA_OPT_ROUTES          s, the experts per query (1 <= s <= min(m, 8);
+ *                            default 1): each query is routed to its s best
+ *                            landmarks (ties to the lower index) and takes
+ *                            one softmax over the shared pairs and the union
+ *                            of those experts' keys, each key once; route[]
+ *                            holds the best landmark.  s > 1 runs on the
+ *                            staged path (AUTO picks it; a forced fused or
+ *                            tiled path gives MITA_ERR_UNSUPPORTED). */
+typedef enum {
+    MITA_OPT_PATH = 0,
+    MITA_OPT_KEEP_LANDMARKS = 1,
+    MITA_OPT_ROUTING_ONLY = 2,
+    MITA_OPT_ROUTES = 3
+} mita_option_t;
 typedef enum { MITA_PATH_AUTO = 0, MITA_PATH_STAGED = 1, MITA_PATH_FUSED = 2, MITA_PATH_TILED = 3 } mita_path_t;
 int mita_set_option(mita_plan_t plan, int option, int value);
 

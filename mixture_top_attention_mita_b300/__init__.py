@@ -17,7 +17,7 @@ MITA_F32, MITA_BF16 = 0, 1
 MITA_OK = 0
 STATUS = {0: "MITA_OK", 1: "MITA_ERR_INVALID_ARG", 2: "MITA_ERR_UNSUPPORTED", 3: "MITA_ERR_CUDA",
           4: "MITA_ERR_TIMEOUT", 5: "MITA_ERR_OOM", 6: "MITA_ERR_DEVICE"}
-OPT_PATH, OPT_KEEP_LANDMARKS, OPT_ROUTING_ONLY = 0, 1, 2
+OPT_PATH, OPT_KEEP_LANDMARKS, OPT_ROUTING_ONLY, OPT_ROUTES = 0, 1, 2, 3
 PATH_AUTO, PATH_STAGED, PATH_FUSED, PATH_TILED = 0, 1, 2, 3
 PATH_NAMES = {PATH_STAGED: "staged", PATH_FUSED: "fused", PATH_TILED: "tiled"}
 

@@ -90,6 +90,7 @@ MITA_DEV float key_to_float(uint32_t k) {
 }
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxRoutes = 8;   // experts per query, at most
 
 // ---------------------------------------------------------------- plan
 struct Shape {
@@ -107,6 +108,7 @@ struct mita_plan_s {
     int path_opt;          // mita_path_t requested
     int keep_landmarks;
     int routing_only;      // 1: softmax over the routed keys alone (no shared expert)
+    int routes_s;          // experts per query (0 or 1: one; up to kMaxRoutes)
     int landmarks_valid;
     // workspace (one cudaMalloc)
     void* ws;

@@ -19,6 +19,7 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 int resolve_path(const mita_plan_s* p) {
     if (p->path_opt != MITA_PATH_AUTO) return p->path_opt;
+    if (p->routes_s > 1) return MITA_PATH_STAGED;   // s > 1: the staged kernels only
     if (mita::fused_supported(p->s, p->dtype)) return MITA_PATH_FUSED;
     if (mita::tiled_supported(p->s, p->dtype)) return MITA_PATH_TILED;
     return MITA_PATH_STAGED;
@@ -128,12 +129,18 @@ int mita_set_option(mita_plan_t p, int option, int value) {
         p->routing_only = value;
         return MITA_OK;
     }
+    if (option == MITA_OPT_ROUTES) {
+        if (value < 1 || value > mita::kMaxRoutes || value > p->s.m) return MITA_ERR_INVALID_ARG;
+        p->routes_s = value;
+        return MITA_OK;
+    }
     return MITA_ERR_INVALID_ARG;
 }
 
 int mita_get_path(mita_plan_t p) {
     if (!p) return -MITA_ERR_INVALID_ARG;
     const int path = resolve_path(p);
+    if (path != MITA_PATH_STAGED && p->routes_s > 1) return -MITA_ERR_UNSUPPORTED;
     if (path == MITA_PATH_FUSED && !mita::fused_supported(p->s, p->dtype)) return -MITA_ERR_UNSUPPORTED;
     if (path == MITA_PATH_TILED && !p->rowmax) return -MITA_ERR_UNSUPPORTED;
     return path;
@@ -149,6 +156,7 @@ int mita_forward(mita_plan_t p, const void* Q, const void* K, const void* V, voi
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t err;
     const int path = resolve_path(p);
+    if (path != MITA_PATH_STAGED && p->routes_s > 1) return MITA_ERR_UNSUPPORTED;
     if (path == MITA_PATH_FUSED) {
         if (!mita::fused_supported(p->s, p->dtype)) return MITA_ERR_UNSUPPORTED;
         err = mita::run_fused(p, Q, K, V, out, idx, rt, p->keep_landmarks, st);

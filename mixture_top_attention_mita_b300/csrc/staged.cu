@@ -248,7 +248,8 @@ __global__ void __launch_bounds__(256) values_kernel(Shape s, const float* __res
 // argmax.  Landmarks are staged through shared memory 32 at a time.
 template <typename T, int D>
 __global__ void __launch_bounds__(128) route_kernel(Shape s, const T* __restrict__ Q,
-                                                   const T* __restrict__ Ql, int32_t* __restrict__ route) {
+                                                   const T* __restrict__ Ql, int32_t* __restrict__ route, int ns,
+                                                   int32_t* __restrict__ tops) {
     __shared__ float l_s[32][D];
     const int bh = blockIdx.y;
     const int qi = blockIdx.x * 128 + threadIdx.x;
@@ -259,6 +260,15 @@ __global__ void __launch_bounds__(128) route_kernel(Shape s, const T* __restrict
     for (int f = 0; f < D; ++f) q[f] = to_f32(qp[f]);
     float best = -INFINITY;
     int arg = 0;
+    // s > 1: the ns best landmarks, best first (a later landmark displaces an
+    // earlier one only with a strictly larger score: ties go to the lower index)
+    float tv[kMaxRoutes];
+    int ti[kMaxRoutes];
+#pragma unroll
+    for (int r = 0; r < kMaxRoutes; ++r) {
+        tv[r] = -INFINITY;
+        ti[r] = -1;
+    }
     const T* lp = Ql + (size_t)bh * s.m * D;
     for (int i0 = 0; i0 < s.m; i0 += 32) {
         const int n = min(32, s.m - i0);
@@ -270,9 +280,35 @@ __global__ void __launch_bounds__(128) route_kernel(Shape s, const T* __restrict
 #pragma unroll
             for (int f = 0; f < D; ++f) a = fmaf(q[f], l_s[u][f], a);
             if (i0 + u == 0 || a > best) { best = a; arg = i0 + u; }
+            if (ns > 1) {
+                int pos = ns;   // first place whose entry this score beats
+#pragma unroll
+                for (int r = kMaxRoutes - 1; r >= 0; --r)
+                    if (r < ns && (ti[r] < 0 || a > tv[r])) pos = r;
+                if (pos < ns) {
+#pragma unroll
+                    for (int r = kMaxRoutes - 1; r > 0; --r)
+                        if (r < ns && r > pos) {
+                            tv[r] = tv[r - 1];
+                            ti[r] = ti[r - 1];
+                        }
+#pragma unroll
+                    for (int r = 0; r < kMaxRoutes; ++r)
+                        if (r == pos) {
+                            tv[r] = a;
+                            ti[r] = i0 + u;
+                        }
+                }
+            }
         }
     }
-    if (live) route[(size_t)bh * s.N + qi] = arg;
+    if (live) {
+        route[(size_t)bh * s.N + qi] = arg;
+        if (ns > 1)
+#pragma unroll
+            for (int r = 0; r < kMaxRoutes; ++r)
+                if (r < ns) tops[((size_t)bh * s.N + qi) * ns + r] = ti[r];
+    }
 }
 
 // One warp per head: per-landmark counts, exclusive offsets, and the
@@ -342,10 +378,10 @@ __global__ void __launch_bounds__(32 * kAttendWarps)
     attend_kernel(Shape s, const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
                   const T* __restrict__ Ql, const T* __restrict__ Vl, const int32_t* __restrict__ idx,
                   const int32_t* __restrict__ route, const int32_t* __restrict__ perm, T* __restrict__ out,
-                  int shared, int32_t* __restrict__ status) {
+                  int shared, int ns, const int32_t* __restrict__ tops, int32_t* __restrict__ status) {
     extern __shared__ float smem[];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int L = s.m + s.k;
+    const int L = s.m + ns * s.k;   // shared slots, then the k keys of each of the ns experts
     float* q_s = smem + w * (D + L);
     float* l_s = q_s + D;
     const int bh = blockIdx.y;
@@ -355,11 +391,20 @@ __global__ void __launch_bounds__(32 * kAttendWarps)
     if (qi < 0 || qi >= s.N) { if (lane == 0) atomicExch(status, (int)MITA_ERR_DEVICE); return; }
     const int r = route[(size_t)bh * s.N + qi];
     if (r < 0 || r >= s.m) { if (lane == 0) atomicExch(status, (int)MITA_ERR_DEVICE); return; }
+    const int32_t* tq = ns > 1 ? tops + ((size_t)bh * s.N + qi) * ns : nullptr;
+    // expert e of this query (e = 0: the route); an invalid landmark falls back to the route
+    auto expert = [&](int e) -> const int32_t* {
+        int re = e == 0 ? r : tq[e];
+        if (re < 0 || re >= s.m) {
+            atomicExch(status, (int)MITA_ERR_DEVICE);
+            re = r;
+        }
+        return idx + ((size_t)bh * s.m + re) * s.k;
+    };
     const size_t hoff = (size_t)bh * s.N * D;
     for (int f = lane; f < D; f += 32) q_s[f] = to_f32(Q[hoff + (size_t)qi * D + f]);
     __syncwarp();
     const T* lq = Ql + (size_t)bh * s.m * D;
-    const int32_t* E = idx + ((size_t)bh * s.m + r) * s.k;
     const float scale = rsqrtf((float)D);
     float mx = -INFINITY;
     for (int t = lane; t < L; t += 32) {
@@ -370,8 +415,24 @@ __global__ void __launch_bounds__(32 * kAttendWarps)
         const T* key;
         if (t < s.m) key = lq + (size_t)t * D;
         else {
-            int j = E[t - s.m];
+            const int u = t - s.m, e = u / s.k;
+            int j = expert(e)[u - e * s.k];
             if (j < 0 || j >= s.N) { atomicExch(status, (int)MITA_ERR_DEVICE); j = 0; }
+            // a key already held by an earlier expert of this query takes part once
+            bool dup = false;
+            for (int e2 = 0; e2 < e && !dup; ++e2) {
+                const int32_t* E2 = expert(e2);   // ascending key order
+                int lo = 0, hi = s.k - 1;
+                while (lo <= hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (E2[mid] == j) { dup = true; break; }
+                    if (E2[mid] < j) lo = mid + 1; else hi = mid - 1;
+                }
+            }
+            if (dup) {
+                l_s[t] = -INFINITY;
+                continue;
+            }
             key = K + hoff + (size_t)j * D;
         }
         float a = 0.0f;
@@ -402,20 +463,24 @@ __global__ void __launch_bounds__(32 * kAttendWarps)
 #pragma unroll
         for (int u = 0; u < D / 32; ++u) acc[u] = fmaf(p, to_f32(lv[(size_t)t * D + lane + 32 * u]), acc[u]);
     }
-    for (int t = 0; t < s.k; ++t) {
-        float p = l_s[s.m + t];
-        int j = E[t];
-        j = (j < 0 || j >= s.N) ? 0 : j;
+    for (int e = 0; e < ns; ++e) {
+        const int32_t* Ee = expert(e);
+        for (int t = 0; t < s.k; ++t) {
+            const float p = l_s[s.m + e * s.k + t];
+            if (p == 0.0f) continue;   // a repeated key (or an underflow: no weight either way)
+            int j = Ee[t];
+            j = (j < 0 || j >= s.N) ? 0 : j;
 #pragma unroll
-        for (int u = 0; u < D / 32; ++u) acc[u] = fmaf(p, to_f32(V[hoff + (size_t)j * D + lane + 32 * u]), acc[u]);
+            for (int u = 0; u < D / 32; ++u) acc[u] = fmaf(p, to_f32(V[hoff + (size_t)j * D + lane + 32 * u]), acc[u]);
+        }
     }
     const float inv = 1.0f / den;
 #pragma unroll
     for (int u = 0; u < D / 32; ++u) out[hoff + (size_t)qi * D + lane + 32 * u] = from_f32<T>(acc[u] * inv);
 }
 
-size_t staged_attend_smem(const Shape& s) {
-    return (size_t)kAttendWarps * (s.d + s.m + s.k) * sizeof(float);
+size_t staged_attend_smem(const Shape& s, int ns) {
+    return (size_t)kAttendWarps * (s.d + s.m + (size_t)ns * s.k) * sizeof(float);
 }
 
 // ---------------------------------------------------------------- launcher
@@ -430,12 +495,17 @@ static cudaError_t run_staged_t(mita_plan_s* p, const T* Q, const T* K, const T*
     scores_kernel<T><<<dim3((s.N + 127) / 128, (s.m + 31) / 32, BH), 256, 0, st>>>(s, Ql, K, p->S);
     topk_kernel<<<dim3(s.m, BH), kTopkThreads, 0, st>>>(s, p->S, idx);
     values_kernel<T><<<dim3(s.m, BH), 256, 0, st>>>(s, p->S, V, Vl);
-    route_kernel<T, D><<<dim3((s.N + 127) / 128, BH), 128, 0, st>>>(s, Q, Ql, route);
+    // s > 1: each query's landmark list goes into the score buffer, free once
+    // the landmark values are done (BH x N x s <= BH x m x N entries)
+    const int ns = p->routes_s > 1 ? p->routes_s : 1;
+    int32_t* tops = (int32_t*)p->S;
+    route_kernel<T, D><<<dim3((s.N + 127) / 128, BH), 128, 0, st>>>(s, Q, Ql, route, ns, tops);
     bucket_kernel<<<BH, 32, 0, st>>>(s, route, p->counts, p->offsets, p->perm, p->status);
-    const size_t smem = staged_attend_smem(s);
+    const size_t smem = staged_attend_smem(s, ns);
+    if (smem > 227 * 1024) return cudaErrorInvalidValue;
     ensure_smem_attr((const void*)attend_kernel<T, D>, (int)smem);
     attend_kernel<T, D><<<dim3((s.N + kAttendWarps - 1) / kAttendWarps, BH), 32 * kAttendWarps, smem, st>>>(
-        s, Q, K, V, Ql, Vl, idx, route, p->perm, out, p->routing_only ? 0 : 1, p->status);
+        s, Q, K, V, Ql, Vl, idx, route, p->perm, out, p->routing_only ? 0 : 1, ns, tops, p->status);
     p->launches += 7;
     return cudaGetLastError();
 }

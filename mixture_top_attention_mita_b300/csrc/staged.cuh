@@ -3,7 +3,7 @@
 #include "common.cuh"
 
 namespace mita {
-size_t staged_attend_smem(const Shape& s);
+size_t staged_attend_smem(const Shape& s, int ns);   // dynamic shared bytes, ns experts per query
 // Step 3 of the staged path (exact top-k over raw scores S [BH, m, N] fp32),
 // reused by the tiled path for rows longer than its bitmap select takes;
 // `chained`: the launch may overlap the previous kernel (see launch.cuh).

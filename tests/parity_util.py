@@ -24,12 +24,13 @@ TIE_EPS = 1e-4
 TOL = {"f32": (1e-5, 1e-5), "bf16": (2e-2, 1e-2)}
 
 
-def compare_head(w, Qh, Kh, Vh, out_h, idx_h, route_h, exact: bool, queries=None, report=None, shared=True):
+def compare_head(w, Qh, Kh, Vh, out_h, idx_h, route_h, exact: bool, queries=None, report=None, shared=True,
+                 s=1):
     """Check one head.  Qh/Kh/Vh are the CPU input tensors [N, d]; out_h
     [nq, d], idx_h [m, k], route_h [nq] are the GPU results (CPU tensors)
     for the queries listed in ``queries`` (default all); ``shared=False``
-    checks the routing-only variant."""
-    r = oracle.head(Qh, Kh, Vh, w.grid, w.m, w.k, io=w.dtype, queries=queries, debug=True, shared=shared)
+    checks the routing-only variant, ``s > 1`` routing to s experts."""
+    r = oracle.head(Qh, Kh, Vh, w.grid, w.m, w.k, io=w.dtype, queries=queries, debug=True, shared=shared, s=s)
     scale = 1.0 / math.sqrt(w.d)
     g_idx = idx_h.numpy()
     g_route = route_h.numpy()
@@ -53,6 +54,15 @@ def compare_head(w, Qh, Kh, Vh, out_h, idx_h, route_h, exact: bool, queries=None
         for q in np.flatnonzero(g_route != o_route):
             assert abs(A[q, g_route[q]] - A[q, o_route[q]]) < TIE_EPS, (q, g_route[q], o_route[q])
     ok = (g_route == o_route) & ~np.isin(o_route, list(bad_experts))
+    if s > 1:
+        # every one of the s experts must be the oracle's, and unflipped
+        A = r["A"] * scale
+        order = np.argsort(-A, axis=1, kind="stable")
+        tops = order[:, :s]
+        if s < w.m:
+            gap = np.take_along_axis(A, order[:, s - 1:s], 1)[:, 0] - np.take_along_axis(A, order[:, s:s + 1], 1)[:, 0]
+            ok &= exact | (gap >= TIE_EPS)
+        ok &= ~np.isin(tops, list(bad_experts)).any(1)
     g_out = out_h.double().numpy()
     d = np.abs(g_out[ok] - r["out"][ok])
     max_tol, mean_tol = TOL[w.dtype]
@@ -68,7 +78,8 @@ def compare_head(w, Qh, Kh, Vh, out_h, idx_h, route_h, exact: bool, queries=None
     return r
 
 
-def compare_batch(w, Q, K, V, out, idx, route, exact: bool, heads=None, queries=None, report=None, shared=True):
+def compare_batch(w, Q, K, V, out, idx, route, exact: bool, heads=None, queries=None, report=None, shared=True,
+                  s=1):
     """Check the listed (b, h) heads (default all) of a batch."""
     out, idx, route = out.cpu(), idx.cpu(), route.cpu()
     if heads is None:
@@ -80,4 +91,4 @@ def compare_batch(w, Q, K, V, out, idx, route, exact: bool, heads=None, queries=
             qs = torch.as_tensor(queries, dtype=torch.long)
             o, rt = out[b, h][qs], route[b, h][qs]
         compare_head(w, Q[b, h], K[b, h], V[b, h], o, idx[b, h], rt, exact, queries=queries, report=report,
-                     shared=shared)
+                     shared=shared, s=s)

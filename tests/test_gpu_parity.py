@@ -22,13 +22,15 @@ W = synth.WORKLOADS
 PATHS = ["staged", "fused", "tiled"]
 
 
-def _run(w, Q, K, V, path="auto", keep=False, routing_only=False):
+def _run(w, Q, K, V, path="auto", keep=False, routing_only=False, s=1):
     plan = mita.Plan.for_workload(w)
     plan.set_path(path)
     if keep:
         plan.set_option(mita.OPT_KEEP_LANDMARKS, 1)
     if routing_only:
         plan.set_option(mita.OPT_ROUTING_ONLY, 1)
+    if s > 1:
+        plan.set_option(mita.OPT_ROUTES, s)
     dev = torch.device("cuda")
     Qd, Kd, Vd = Q.to(dev), K.to(dev), V.to(dev)
     out = torch.empty_like(Qd)
@@ -106,6 +108,30 @@ def test_routing_only(name, path):
     Q, K, V = synth.make_integer_inputs(w, seed=43)
     r = _run(w, Q, K, V, path, routing_only=True)
     compare_batch(w, Q, K, V, r["out"], r["idx"], r["route"], exact=True, shared=False)
+
+
+@pytest.mark.parametrize("s", [2, 3])
+@pytest.mark.parametrize("name", ["deit_t", "deit_s", "hires56"])
+def test_top_s_routing(name, s):
+    """Each query routed to its s best landmarks: one softmax over the shared
+    pairs and the union of the s experts' keys (the staged path)."""
+    w = SMALL[name]
+    Q, K, V = synth.make_inputs(w, seed=61)
+    r = _run(w, Q, K, V, "auto", s=s)
+    assert r["plan"].path == "staged"
+    compare_batch(w, Q, K, V, r["out"], r["idx"], r["route"], exact=False, s=s)
+    Q, K, V = synth.make_integer_inputs(w, seed=63)
+    r = _run(w, Q, K, V, "auto", s=s, routing_only=(s == 3))
+    compare_batch(w, Q, K, V, r["out"], r["idx"], r["route"], exact=True, s=s, shared=(s != 3))
+
+
+def test_top_s_routing_rejected_off_the_staged_path():
+    plan = mita.Plan.for_workload(SMALL["deit_s"])
+    plan.set_option(mita.OPT_ROUTES, 2)
+    plan.set_path("fused")
+    assert plan.lib.mita_get_path(plan.handle) < 0
+    with pytest.raises(mita.MitaError):
+        plan.set_option(mita.OPT_ROUTES, 9)
 
 
 def test_routing_only_option_rejects_bad_values():
