@@ -56,6 +56,8 @@ def _open(path):
     lib.oracle_head.restype = i
     lib.oracle_forward.argtypes = [i, i, i, i, i, i, i, i, i, i, i, i, dp, dp, dp, dp, ip, ip]
     lib.oracle_forward.restype = i
+    lib.oracle_backward_head.argtypes = [i, i, i, i, i, i, i, i, i, i, dp, dp, dp, dp, dp, dp, dp]
+    lib.oracle_backward_head.restype = i
     return lib
 
 
@@ -163,3 +165,19 @@ def forward(Q, K, V, grid, m: int, k: int, io: str = "f64", shared: bool = True,
     if rc != 0:
         raise ValueError("oracle: invalid sizes")
     return {"out": out, "idx": idx, "route": route}
+
+
+def backward(Q, K, V, dOut, grid, m: int, k: int, io: str = "f64", shared: bool = True):
+    """Gradients dQ, dK, dV [N, d] of one head (s = 1) for the output gradient
+    dOut [N, d]; experts and routes are constants, the roundings to the I/O
+    type pass gradients through.  fp64."""
+    lib = _load()
+    Q, K, V, dOut = _f64(Q), _f64(K), _f64(V), _f64(dOut)
+    N, d = Q.shape
+    gh, gw, ph, pw = grid
+    dQ, dK, dV = np.zeros((N, d)), np.zeros((N, d)), np.zeros((N, d))
+    rc = lib.oracle_backward_head(N, d, gh, gw, ph, pw, m, k, _IO_NAMES[io], int(shared), _dp(Q), _dp(K), _dp(V),
+                                  _dp(dOut), _dp(dQ), _dp(dK), _dp(dV))
+    if rc != 0:
+        raise ValueError("oracle: invalid sizes")
+    return dQ, dK, dV

@@ -314,6 +314,135 @@ int oracle_head(int N, int d, int gh, int gw, int ph, int pw, int m, int k, int 
     return 0;
 }
 
+/* Backward of one head (s = 1; `shared` as in step 6), fp64.  The experts
+ * and routes are constants of the forward (their selection has no gradient);
+ * the roundings of Q_l, V_l and out to the I/O type pass gradients through
+ * unchanged.  Given dOut [N, d], writes dQ, dK, dV [N, d].  The chain rule
+ * taken step by step, in reverse order:
+ *   6  per query: w = softmax(logits); dw_l = dOut . v_l; dlogit = w (dw - w.dw);
+ *      value gradients to V_l (shared) and V (routed); logit gradients to the
+ *      query, to Q_l (shared keys) and to K (routed keys), all over sqrt(d)
+ *   4  V_l = P V with P = softmax(R / sqrt(d)): dP = dV_l V^T, dV += P^T dV_l,
+ *      dR = P (dP - rowsum(P dP)) / sqrt(d)
+ *   2  R = Q_l K^T: dQ_l += dR K, dK += dR^T Q_l
+ *   1  Q_l = bin means of Q: each token of bin i gets dQ_l[i] / |bin i|
+ * Returns 0, or -1 on invalid sizes. */
+int oracle_backward_head(int N, int d, int gh, int gw, int ph, int pw, int m, int k, int io, int shared,
+                         const double* Q, const double* K, const double* V, const double* dOut,
+                         double* dQ, double* dK, double* dV) {
+    if (N < 1 || d < 1 || gh * gw != N || ph * pw != m || ph > gh || pw > gw || k < 1 || k > N)
+        return -1;
+    const double scale = 1.0 / sqrt((double)d);
+    double* Ql = (double*)malloc(sizeof(double) * (size_t)m * d);
+    double* Vl = (double*)malloc(sizeof(double) * (size_t)m * d);
+    double* R = (double*)malloc(sizeof(double) * (size_t)m * N);
+    double* P = (double*)malloc(sizeof(double) * (size_t)m * N);
+    int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)m * k);
+    double* dQl = (double*)calloc((size_t)m * d, sizeof(double));
+    double* dVl = (double*)calloc((size_t)m * d, sizeof(double));
+    double* A = (double*)malloc(sizeof(double) * (size_t)m);
+    double* w = (double*)malloc(sizeof(double) * (size_t)(m + k));
+    double* dl = (double*)malloc(sizeof(double) * (size_t)(m + k));
+    memset(dQ, 0, sizeof(double) * (size_t)N * d);
+    memset(dK, 0, sizeof(double) * (size_t)N * d);
+    memset(dV, 0, sizeof(double) * (size_t)N * d);
+
+    oracle_pool(gh, gw, ph, pw, d, io, Q, Ql);
+    oracle_scores(N, d, m, Ql, K, R);
+    oracle_topk(N, m, k, R, idx);
+    oracle_landmark_values(N, d, m, io, R, V, Vl);
+    for (int i = 0; i < m; ++i) {   /* P = softmax(R / sqrt(d)) per landmark */
+        double mx = -INFINITY, den = 0.0;
+        for (int j = 0; j < N; ++j) if (R[(size_t)i * N + j] * scale > mx) mx = R[(size_t)i * N + j] * scale;
+        for (int j = 0; j < N; ++j) {
+            P[(size_t)i * N + j] = exp(R[(size_t)i * N + j] * scale - mx);
+            den += P[(size_t)i * N + j];
+        }
+        for (int j = 0; j < N; ++j) P[(size_t)i * N + j] /= den;
+    }
+    /* step 6 */
+    for (int qi = 0; qi < N; ++qi) {
+        const double* q = Q + (size_t)qi * d;
+        const double* g = dOut + (size_t)qi * d;
+        const int r = oracle_route_one(d, m, q, Ql, A);
+        const int32_t* E = idx + (size_t)r * k;
+        double mx = -INFINITY;
+        for (int i = 0; i < m; ++i) {
+            w[i] = shared ? A[i] * scale : -INFINITY;
+            if (w[i] > mx) mx = w[i];
+        }
+        for (int t = 0; t < k; ++t) {
+            double s2 = 0.0;
+            for (int f = 0; f < d; ++f) s2 += q[f] * K[(size_t)E[t] * d + f];
+            w[m + t] = s2 * scale;
+            if (w[m + t] > mx) mx = w[m + t];
+        }
+        double den = 0.0;
+        for (int l = 0; l < m + k; ++l) { w[l] = exp(w[l] - mx); den += w[l]; }
+        for (int l = 0; l < m + k; ++l) w[l] /= den;
+        double wdw = 0.0;
+        for (int l = 0; l < m + k; ++l) {
+            const double* v = l < m ? Vl + (size_t)l * d : V + (size_t)E[l - m] * d;
+            double dw = 0.0;
+            for (int f = 0; f < d; ++f) dw += g[f] * v[f];
+            dl[l] = dw;
+            wdw += w[l] * dw;
+        }
+        for (int l = 0; l < m + k; ++l) dl[l] = w[l] * (dl[l] - wdw);
+        for (int i = 0; i < m; ++i)
+            for (int f = 0; f < d; ++f) {
+                dVl[(size_t)i * d + f] += w[i] * g[f];
+                dQ[(size_t)qi * d + f] += dl[i] * Ql[(size_t)i * d + f] * scale;
+                dQl[(size_t)i * d + f] += dl[i] * q[f] * scale;
+            }
+        for (int t = 0; t < k; ++t) {
+            const size_t j = (size_t)E[t];
+            for (int f = 0; f < d; ++f) {
+                dV[j * d + f] += w[m + t] * g[f];
+                dQ[(size_t)qi * d + f] += dl[m + t] * K[j * d + f] * scale;
+                dK[j * d + f] += dl[m + t] * q[f] * scale;
+            }
+        }
+    }
+    /* step 4, then step 2 */
+    for (int i = 0; i < m; ++i) {
+        double* dP = (double*)malloc(sizeof(double) * (size_t)N);
+        double pdp = 0.0;
+        for (int j = 0; j < N; ++j) {
+            double s2 = 0.0;
+            for (int f = 0; f < d; ++f) s2 += dVl[(size_t)i * d + f] * V[(size_t)j * d + f];
+            dP[j] = s2;
+            pdp += P[(size_t)i * N + j] * s2;
+        }
+        for (int j = 0; j < N; ++j) {
+            const double pij = P[(size_t)i * N + j];
+            const double dR = pij * (dP[j] - pdp) * scale;
+            for (int f = 0; f < d; ++f) {
+                dV[(size_t)j * d + f] += pij * dVl[(size_t)i * d + f];
+                dQl[(size_t)i * d + f] += dR * K[(size_t)j * d + f];
+                dK[(size_t)j * d + f] += dR * Ql[(size_t)i * d + f];
+            }
+        }
+        free(dP);
+    }
+    /* step 1 */
+    for (int r = 0; r < ph; ++r) {
+        int r0, r1;
+        oracle_bin(r, gh, ph, &r0, &r1);
+        for (int c = 0; c < pw; ++c) {
+            int c0, c1;
+            oracle_bin(c, gw, pw, &c0, &c1);
+            const double count = (double)((r1 - r0) * (c1 - c0));
+            const double* src = dQl + (size_t)(r * pw + c) * d;
+            for (int y = r0; y < r1; ++y)
+                for (int x = c0; x < c1; ++x)
+                    for (int f = 0; f < d; ++f) dQ[(size_t)(y * gw + x) * d + f] += src[f] / count;
+        }
+    }
+    free(Ql); free(Vl); free(R); free(P); free(idx); free(dQl); free(dVl); free(A); free(w); free(dl);
+    return 0;
+}
+
 /* All heads of a [B*H, N, d] batch, every query. */
 int oracle_forward(int BH, int N, int d, int gh, int gw, int ph, int pw, int m, int k, int io, int shared, int s,
                    const double* Q, const double* K, const double* V,

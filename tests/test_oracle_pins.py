@@ -228,6 +228,40 @@ def test_top_s_routing_ties_on_integer_inputs():
     np.testing.assert_allclose(r["out"], _top_s_reference(Q, K, V, r, 8, 3), rtol=0, atol=1e-12)
 
 
+def _fd_check(grid, m, k, d, shared, seed):
+    """Central finite differences of L = sum(out * G) against the oracle's
+    backward (fp64, no rounding), with the experts and routes checked to be
+    the same at every perturbed point."""
+    N = grid[0] * grid[1]
+    Q, K, V = _rand((N, d), seed), _rand((N, d), seed + 1), _rand((N, d), seed + 2)
+    G = _rand((N, d), seed + 3)
+    base = oracle.head(Q, K, V, grid, m, k, io="f64", shared=shared)
+    dQ, dK, dV = oracle.backward(Q, K, V, G, grid, m, k, io="f64", shared=shared)
+    eps = 1e-6
+    for X, dX in ((Q, dQ), (K, dK), (V, dV)):
+        num = np.zeros_like(X)
+        for a in range(N):
+            for b in range(d):
+                old = X[a, b]
+                X[a, b] = old + eps
+                rp = oracle.head(Q, K, V, grid, m, k, io="f64", shared=shared)
+                X[a, b] = old - eps
+                rm = oracle.head(Q, K, V, grid, m, k, io="f64", shared=shared)
+                X[a, b] = old
+                for rr in (rp, rm):
+                    assert (rr["idx"] == base["idx"]).all() and (rr["route"] == base["route"]).all()
+                num[a, b] = ((rp["out"] * G).sum() - (rm["out"] * G).sum()) / (2 * eps)
+        np.testing.assert_allclose(dX, num, rtol=1e-6, atol=1e-8)
+
+
+@pytest.mark.parametrize("grid,m,k,d,shared", [((6, 6, 2, 3), 6, 5, 4, True), ((1, 20, 1, 4), 4, 7, 3, True),
+                                               ((6, 6, 2, 3), 6, 5, 4, False)])
+def test_backward_matches_finite_differences(grid, m, k, d, shared):
+    # NEXT-1 backward pass: the experts and routes are constants; gradients
+    # flow through both softmaxes, the landmark values and the pooling.
+    _fd_check(grid, m, k, d, shared, seed=31)
+
+
 def _golden_keys_per_query():
     rows = []
     with open(os.path.join(GOLDEN, "keys_per_query.txt")) as f:
@@ -324,6 +358,12 @@ _MUTANTS = {
                                 "for (int r = 0; r < 1; ++r)\n        for (int t = 0; t < k; ++t) in_union"),
     "top_s_ties_to_higher": ("if (!taken && (best < 0 || A[i] > A[best])) best = i;",
                              "if (!taken && (best < 0 || A[i] >= A[best])) best = i;"),
+    "backward_softmax_sign": ("for (int l = 0; l < m + k; ++l) dl[l] = w[l] * (dl[l] - wdw);",
+                              "for (int l = 0; l < m + k; ++l) dl[l] = w[l] * (dl[l] + wdw);"),
+    "backward_pool_count": ("dQ[(size_t)(y * gw + x) * d + f] += src[f] / count;",
+                            "dQ[(size_t)(y * gw + x) * d + f] += src[f];"),
+    "backward_values_transpose": ("dV[(size_t)j * d + f] += pij * dVl[(size_t)i * d + f];",
+                                  "dV[(size_t)j * d + f] += pij * dVl[(size_t)((i + 1) % m) * d + f];"),
 }
 
 
@@ -346,7 +386,8 @@ def test_planted_mistake_fails_a_pin(name, tmp_path):
             lambda: test_pool_matches_adaptive_avg_pool2d(14, 14, 5, 5),
             lambda: test_routing_only_full_attention_special_case(),
             lambda: test_top_s_routing_matches_masked_sdpa(3),
-            lambda: test_top_s_routing_ties_on_integer_inputs()]
+            lambda: test_top_s_routing_ties_on_integer_inputs(),
+            lambda: _fd_check((6, 6, 2, 3), 6, 5, 4, True, seed=31)]
     failures = 0
     with oracle.swapped_library(str(so)):
         for pin in pins:
