@@ -98,6 +98,22 @@ int mita_get_status(mita_plan_t plan);
  * plan's device first. */
 void mita_destroy(mita_plan_t plan);
 
+/* Backward pass (routes s = 1; the routing-only option is honoured): given
+ * the output gradient dOut ([B, H, N, d], plan dtype, device), writes the
+ * input gradients dQ, dK, dV ([B, H, N, d], fp32, device, overwritten) on
+ * `stream`.  The forward's discrete choices (experts and routes) are
+ * recomputed from Q and K exactly as mita_forward makes them and held
+ * constant; gradients flow through the output softmax, the landmark values
+ * V_l = softmax(Q_l K^T / sqrt d) V and the bin means into Q; the roundings of
+ * Q_l, V_l and out to the I/O type pass gradients unchanged (the reading of
+ * 36Kr / 新智元 "注意力也是FFN？", which trains the operator end to end without
+ * stating its gradients).  Runs the stage-by-stage kernels with fp32
+ * atomics (sums in a nondeterministic order).  MITA_ERR_UNSUPPORTED when the
+ * plan routes to s > 1 experts; MITA_ERR_INVALID_ARG for a null or
+ * misaligned pointer. */
+int mita_backward(mita_plan_t plan, const void* Q, const void* K, const void* V, const void* dOut, float* dQ,
+                  float* dK, float* dV, struct CUstream_st* stream);
+
 /* Static string for a status code (never NULL). */
 const char* mita_strerror(int code);
 

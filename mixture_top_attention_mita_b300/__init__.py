@@ -22,7 +22,7 @@ PATH_AUTO, PATH_STAGED, PATH_FUSED, PATH_TILED = 0, 1, 2, 3
 PATH_NAMES = {PATH_STAGED: "staged", PATH_FUSED: "fused", PATH_TILED: "tiled"}
 
 # Every entry point declared in include/mita.h.
-EXPORTS = ("mita_plan", "mita_forward", "mita_get_status", "mita_destroy", "mita_strerror",
+EXPORTS = ("mita_plan", "mita_forward", "mita_backward", "mita_get_status", "mita_destroy", "mita_strerror",
            "mita_set_option", "mita_get_path", "mita_get_landmarks", "mita_workspace_bytes",
            "mita_launch_count", "mita_forward_noalloc", "mita_noalloc_scratch_bytes")
 
@@ -52,6 +52,7 @@ def load(path: str | None = None):
     vp, i, ip = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int32)
     lib.mita_plan.argtypes = [ctypes.POINTER(vp), i, i, i, i, Grid, i, i, i]
     lib.mita_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.mita_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.mita_get_status.argtypes = [vp]
     lib.mita_destroy.argtypes = [vp]
     lib.mita_destroy.restype = None
@@ -134,6 +135,13 @@ class Plan:
         rc = self.lib.mita_forward(self.handle, _ptr(Q), _ptr(K), _ptr(V), _ptr(out), _ptr(expert_idx),
                                    _ptr(route), _stream_ptr(stream))
         _check(rc, "mita_forward")
+
+    def backward(self, Q, K, V, dOut, dQ, dK, dV, stream=None):
+        """Enqueue ``mita_backward``: input gradients dQ, dK, dV (fp32 CUDA
+        tensors [B, H, N, d], overwritten) for the output gradient dOut."""
+        rc = self.lib.mita_backward(self.handle, _ptr(Q), _ptr(K), _ptr(V), _ptr(dOut), _ptr(dQ), _ptr(dK),
+                                    _ptr(dV), _stream_ptr(stream))
+        _check(rc, "mita_backward")
 
     def status(self) -> int:
         return self.lib.mita_get_status(self.handle)

@@ -109,6 +109,8 @@ struct mita_plan_s {
     int keep_landmarks;
     int routing_only;      // 1: softmax over the routed keys alone (no shared expert)
     int routes_s;          // experts per query (0 or 1: one; up to kMaxRoutes)
+    float* dQl;            // backward: gradients of Q_l and V_l [BH, m, d] fp32
+    float* dVl;
     int landmarks_valid;
     // workspace (one cudaMalloc)
     void* ws;

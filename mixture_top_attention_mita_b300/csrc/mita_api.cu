@@ -71,6 +71,7 @@ int mita_plan(mita_plan_t* plan, int B, int H, int N, int d, mita_grid_t grid, i
     const size_t oIdx = take(BH * m * (size_t)k * 4), oRoute = take(BH * (size_t)N * 4);
     const size_t oCnt = take(BH * m * 4), oOff = take(BH * (m + 1) * 4), oPerm = take(BH * (size_t)N * 4);
     const size_t oStatus = take(256);
+    const size_t oGradL = take(2 * BH * m * d * 4);   // backward: dQ_l, dV_l (fp32)
     const bool tiled = mita::tiled_supported(p->s, dtype);
     const size_t oRowmax = take(tiled ? 2 * BH * m * 4 : 0);   // row max, then row min
     const size_t oVpart = take(tiled ? mita::tiled_part_bytes(p->s) : 0);
@@ -94,6 +95,8 @@ int mita_plan(mita_plan_t* plan, int B, int H, int N, int d, mita_grid_t grid, i
     p->offsets = (int32_t*)(b + oOff);
     p->perm = (int32_t*)(b + oPerm);
     p->status = (int32_t*)(b + oStatus);
+    p->dQl = (float*)(b + oGradL);
+    p->dVl = p->dQl + BH * m * d;
     if (tiled) {
         p->rowmax = (uint32_t*)(b + oRowmax);
         p->vpart = (float*)(b + oVpart);
@@ -168,6 +171,17 @@ int mita_forward(mita_plan_t p, const void* Q, const void* K, const void* V, voi
     }
     if (err != cudaSuccess) return MITA_ERR_CUDA;
     p->landmarks_valid = p->keep_landmarks || path != MITA_PATH_FUSED;
+    return MITA_OK;
+}
+
+int mita_backward(mita_plan_t p, const void* Q, const void* K, const void* V, const void* dOut, float* dQ,
+                  float* dK, float* dV, struct CUstream_st* stream) {
+    if (!p || !Q || !K || !V || !dOut || !dQ || !dK || !dV) return MITA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(dOut) || !aligned16(dQ) || !aligned16(dK) ||
+        !aligned16(dV))
+        return MITA_ERR_INVALID_ARG;
+    if (p->routes_s > 1) return MITA_ERR_UNSUPPORTED;
+    if (mita::run_backward(p, Q, K, V, dOut, dQ, dK, dV, (cudaStream_t)stream) != cudaSuccess) return MITA_ERR_CUDA;
     return MITA_OK;
 }
 

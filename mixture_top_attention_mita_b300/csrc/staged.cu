@@ -510,6 +510,255 @@ static cudaError_t run_staged_t(mita_plan_s* p, const T* Q, const T* K, const T*
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- backward
+// The backward pass of the operator with the experts and routes held as
+// constants (see mita.h): attend_bwd_kernel takes the output softmax (warp per
+// query), values_bwd_kernel the landmark values (block per landmark row),
+// pool_bwd_kernel the bin means.  Gradients accumulate in fp32 with atomics.
+
+// Warp per query: the forward's logits and weights again, dw = dOut . v,
+// dlogit = w (dw - w . dw); the query's own gradient is stored, the shared
+// keys' and values' (dQ_l, dV_l) and the routed rows' (dK, dV) are added.
+template <typename T, int D>
+__global__ void __launch_bounds__(32 * kAttendWarps)
+    attend_bwd_kernel(Shape s, const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
+                      const T* __restrict__ Ql, const T* __restrict__ Vl, const int32_t* __restrict__ idx,
+                      const int32_t* __restrict__ route, const T* __restrict__ dOut, float* __restrict__ dQ,
+                      float* __restrict__ dK, float* __restrict__ dV, float* __restrict__ dQl,
+                      float* __restrict__ dVl, int shared, int32_t* __restrict__ status) {
+    extern __shared__ float smem[];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int L = s.m + s.k;
+    float* q_s = smem + w * (2 * D + 2 * L);
+    float* g_s = q_s + D;     // dOut row
+    float* l_s = g_s + D;     // weights
+    float* d_s = l_s + L;     // logit gradients
+    const int bh = blockIdx.y, qi = blockIdx.x * kAttendWarps + w;
+    if (qi >= s.N) return;
+    const int r = route[(size_t)bh * s.N + qi];
+    if (r < 0 || r >= s.m) { if (lane == 0) atomicExch(status, (int)MITA_ERR_DEVICE); return; }
+    const size_t hoff = (size_t)bh * s.N * D;
+    for (int f = lane; f < D; f += 32) {
+        q_s[f] = to_f32(Q[hoff + (size_t)qi * D + f]);
+        g_s[f] = to_f32(dOut[hoff + (size_t)qi * D + f]);
+    }
+    __syncwarp();
+    const T* lq = Ql + (size_t)bh * s.m * D;
+    const T* lv = Vl + (size_t)bh * s.m * D;
+    const int32_t* E = idx + ((size_t)bh * s.m + r) * s.k;
+    auto key_row = [&](int t) -> int {   // routed slot t: its key, checked
+        int j = E[t - s.m];
+        if (j < 0 || j >= s.N) { atomicExch(status, (int)MITA_ERR_DEVICE); j = 0; }
+        return j;
+    };
+    const float scale = rsqrtf((float)D);
+    float mx = -INFINITY;
+    for (int t = lane; t < L; t += 32) {
+        float a = -INFINITY;
+        if (t >= s.m || shared) {
+            const T* key = t < s.m ? lq + (size_t)t * D : K + hoff + (size_t)key_row(t) * D;
+            a = 0.0f;
+#pragma unroll 8
+            for (int f = 0; f < D; ++f) a = fmaf(q_s[f], to_f32(key[f]), a);
+            a *= scale;
+        }
+        l_s[t] = a;
+        mx = fmaxf(mx, a);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    __syncwarp();
+    float den = 0.0f;
+    for (int t = lane; t < L; t += 32) {
+        const float p = exp2f((l_s[t] - mx) * kLog2e);
+        l_s[t] = p;
+        den += p;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    const float inv = 1.0f / den;
+    float wdw = 0.0f;
+    for (int t = lane; t < L; t += 32) {
+        const float wt = l_s[t] * inv;
+        l_s[t] = wt;
+        float dw = 0.0f;
+        if (wt != 0.0f) {
+            const T* v = t < s.m ? lv + (size_t)t * D : V + hoff + (size_t)key_row(t) * D;
+#pragma unroll 8
+            for (int f = 0; f < D; ++f) dw = fmaf(g_s[f], to_f32(v[f]), dw);
+        }
+        d_s[t] = dw;
+        wdw = fmaf(wt, dw, wdw);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wdw += __shfl_xor_sync(0xffffffffu, wdw, o);
+    for (int t = lane; t < L; t += 32) d_s[t] = l_s[t] * (d_s[t] - wdw);
+    __syncwarp();
+    float dq[D / 32];
+#pragma unroll
+    for (int u = 0; u < D / 32; ++u) dq[u] = 0.0f;
+    for (int t = 0; t < L; ++t) {
+        const float c = d_s[t], wt = l_s[t];
+        if (c == 0.0f && wt == 0.0f) continue;
+        const bool sh = t < s.m;
+        const int j = sh ? t : key_row(t);
+        const T* key = sh ? lq + (size_t)j * D : K + hoff + (size_t)j * D;
+        float* gk = sh ? dQl + ((size_t)bh * s.m + j) * D : dK + hoff + (size_t)j * D;
+        float* gv = sh ? dVl + ((size_t)bh * s.m + j) * D : dV + hoff + (size_t)j * D;
+#pragma unroll
+        for (int u = 0; u < D / 32; ++u) {
+            const int f = lane + 32 * u;
+            dq[u] = fmaf(c, to_f32(key[f]), dq[u]);
+            if (c != 0.0f) atomicAdd(gk + f, c * q_s[f] * scale);
+            if (wt != 0.0f) atomicAdd(gv + f, wt * g_s[f]);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < D / 32; ++u) dQ[hoff + (size_t)qi * D + lane + 32 * u] = dq[u] * scale;
+}
+
+// Block per (landmark i, head), 8 warps: P = softmax(S[i] / sqrt d) again,
+// dP_j = dV_l[i] . V[j] (warp per key), dR_j = P_j (dP_j - P . dP) / sqrt d;
+// dV[j] += P_j dV_l[i] and dK[j] += dR_j Q_l[i] are added, dQ_l[i] += dR . K.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) values_bwd_kernel(Shape s, const float* __restrict__ S,
+                                                         const T* __restrict__ K, const T* __restrict__ V,
+                                                         const T* __restrict__ Ql, float* __restrict__ dK,
+                                                         float* __restrict__ dV, float* __restrict__ dQl,
+                                                         const float* __restrict__ dVl) {
+    __shared__ float dvl_s[D], ql_s[D], red[8];
+    __shared__ float part[8][D];
+    const int i = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const float* row = S + ((size_t)bh * s.m + i) * s.N;
+    const float scale = rsqrtf((float)D);
+    for (int f = tid; f < D; f += 256) {
+        dvl_s[f] = dVl[((size_t)bh * s.m + i) * D + f];
+        ql_s[f] = to_f32(Ql[((size_t)bh * s.m + i) * D + f]);
+    }
+    auto block_sum = [&](float x, bool is_max) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float y = __shfl_xor_sync(0xffffffffu, x, o);
+            x = is_max ? fmaxf(x, y) : x + y;
+        }
+        __syncthreads();
+        if (lane == 0) red[warp] = x;
+        __syncthreads();
+        float t = red[0];
+        for (int u = 1; u < 8; ++u) t = is_max ? fmaxf(t, red[u]) : t + red[u];
+        return t;
+    };
+    float mx = -INFINITY;
+    for (int j = tid; j < s.N; j += 256) mx = fmaxf(mx, row[j] * scale);
+    mx = block_sum(mx, true);
+    float den = 0.0f;
+    for (int j = tid; j < s.N; j += 256) den += exp2f((row[j] * scale - mx) * kLog2e);
+    const float inv = 1.0f / block_sum(den, false);
+    const size_t hoff = (size_t)bh * s.N * D;
+    auto dP = [&](int j) {   // warp-wide dV_l[i] . V[j]
+        float a = 0.0f;
+#pragma unroll
+        for (int u = 0; u < D / 32; ++u) a = fmaf(dvl_s[lane + 32 * u], to_f32(V[hoff + (size_t)j * D + lane + 32 * u]), a);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        return a;
+    };
+    float pdp = 0.0f;
+    for (int j = warp; j < s.N; j += 8) {
+        const float p = exp2f((row[j] * scale - mx) * kLog2e) * inv;
+        pdp = fmaf(p, dP(j), pdp);   // the same value in every lane
+    }
+    pdp = block_sum(lane == 0 ? pdp : 0.0f, false);
+    float acc[D / 32];
+#pragma unroll
+    for (int u = 0; u < D / 32; ++u) acc[u] = 0.0f;
+    for (int j = warp; j < s.N; j += 8) {
+        const float p = exp2f((row[j] * scale - mx) * kLog2e) * inv;
+        const float dr = p * (dP(j) - pdp) * scale;
+#pragma unroll
+        for (int u = 0; u < D / 32; ++u) {
+            const int f = lane + 32 * u;
+            atomicAdd(dV + hoff + (size_t)j * D + f, p * dvl_s[f]);
+            atomicAdd(dK + hoff + (size_t)j * D + f, dr * ql_s[f]);
+            acc[u] = fmaf(dr, to_f32(K[hoff + (size_t)j * D + f]), acc[u]);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < D / 32; ++u) part[warp][lane + 32 * u] = acc[u];
+    __syncthreads();
+    for (int f = tid; f < D; f += 256) {
+        float t = 0.0f;
+        for (int u = 0; u < 8; ++u) t += part[u][f];
+        dQl[((size_t)bh * s.m + i) * D + f] += t;   // this block is the row's only writer here
+    }
+}
+
+// Thread per (token, feature): dQ[t] += dQ_l[i] / |bin i| over the (at most
+// two per axis) bins that hold token t.
+__global__ void pool_bwd_kernel(Shape s, const float* __restrict__ dQl, float* __restrict__ dQ) {
+    const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int bh = blockIdx.y;
+    if (e >= (size_t)s.N * s.d) return;
+    const int t = (int)(e / s.d), f = (int)(e % s.d), y = t / s.gw, x = t % s.gw;
+    float acc = 0.0f;
+    const int rc = y * s.ph / s.gh, cc = x * s.pw / s.gw;
+    for (int r = max(0, rc - 1); r <= min(s.ph - 1, rc + 1); ++r) {
+        int r0, r1;
+        pool_bin(r, s.gh, s.ph, r0, r1);
+        if (y < r0 || y >= r1) continue;
+        for (int c = max(0, cc - 1); c <= min(s.pw - 1, cc + 1); ++c) {
+            int c0, c1;
+            pool_bin(c, s.gw, s.pw, c0, c1);
+            if (x < c0 || x >= c1) continue;
+            acc += dQl[((size_t)bh * s.m + r * s.pw + c) * s.d + f] / (float)((r1 - r0) * (c1 - c0));
+        }
+    }
+    dQ[(size_t)bh * s.N * s.d + e] += acc;
+}
+
+template <typename T, int D>
+static cudaError_t run_backward_t(mita_plan_s* p, const T* Q, const T* K, const T* V, const T* dOut, float* dQ,
+                                  float* dK, float* dV, cudaStream_t st) {
+    const Shape& s = p->s;
+    const int BH = s.BH();
+    T* Ql = (T*)p->Ql;
+    T* Vl = (T*)p->Vl;
+    const size_t nbytes = (size_t)BH * s.N * D * sizeof(float);
+    cudaError_t e;
+    if ((e = cudaMemsetAsync(dK, 0, nbytes, st)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(dV, 0, nbytes, st)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(p->dQl, 0, (size_t)2 * BH * s.m * D * sizeof(float), st)) != cudaSuccess) return e;
+    // the forward's landmarks, scores, experts, landmark values and routes
+    pool_kernel<T><<<dim3(s.m, BH), D, 0, st>>>(s, Q, Ql);
+    scores_kernel<T><<<dim3((s.N + 127) / 128, (s.m + 31) / 32, BH), 256, 0, st>>>(s, Ql, K, p->S);
+    topk_kernel<<<dim3(s.m, BH), kTopkThreads, 0, st>>>(s, p->S, p->idx);
+    values_kernel<T><<<dim3(s.m, BH), 256, 0, st>>>(s, p->S, V, Vl);
+    route_kernel<T, D><<<dim3((s.N + 127) / 128, BH), 128, 0, st>>>(s, Q, Ql, p->route, 1, nullptr);
+    const size_t smem = (size_t)kAttendWarps * (2 * D + 2 * (s.m + s.k)) * sizeof(float);
+    if (smem > 227 * 1024) return cudaErrorInvalidValue;
+    ensure_smem_attr((const void*)attend_bwd_kernel<T, D>, (int)smem);
+    attend_bwd_kernel<T, D><<<dim3((s.N + kAttendWarps - 1) / kAttendWarps, BH), 32 * kAttendWarps, smem, st>>>(
+        s, Q, K, V, Ql, Vl, p->idx, p->route, dOut, dQ, dK, dV, p->dQl, p->dVl, p->routing_only ? 0 : 1, p->status);
+    values_bwd_kernel<T, D><<<dim3(s.m, BH), 256, 0, st>>>(s, p->S, K, V, Ql, dK, dV, p->dQl, p->dVl);
+    pool_bwd_kernel<<<dim3((unsigned)(((size_t)s.N * D + 255) / 256), BH), 256, 0, st>>>(s, p->dQl, dQ);
+    p->launches += 8;
+    return cudaGetLastError();
+}
+
+cudaError_t run_backward(mita_plan_s* p, const void* Q, const void* K, const void* V, const void* dOut, float* dQ,
+                         float* dK, float* dV, cudaStream_t st) {
+    if (p->dtype == MITA_BF16) {
+        using T = __nv_bfloat16;
+        if (p->s.d == 64)
+            return run_backward_t<T, 64>(p, (const T*)Q, (const T*)K, (const T*)V, (const T*)dOut, dQ, dK, dV, st);
+        return run_backward_t<T, 128>(p, (const T*)Q, (const T*)K, (const T*)V, (const T*)dOut, dQ, dK, dV, st);
+    }
+    using T = float;
+    if (p->s.d == 64)
+        return run_backward_t<T, 64>(p, (const T*)Q, (const T*)K, (const T*)V, (const T*)dOut, dQ, dK, dV, st);
+    return run_backward_t<T, 128>(p, (const T*)Q, (const T*)K, (const T*)V, (const T*)dOut, dQ, dK, dV, st);
+}
+
 cudaError_t staged_topk(const Shape& s, const float* S, int32_t* idx, cudaStream_t st, bool chained) {
     return launch_chained(chained, topk_kernel, dim3(s.m, s.BH()), dim3(kTopkThreads), 0, st, s, S, idx);
 }

@@ -134,6 +134,59 @@ def test_top_s_routing_rejected_off_the_staged_path():
         plan.set_option(mita.OPT_ROUTES, 9)
 
 
+BWD = {
+    "deit_t": W["deit_t"].scaled(B=1, H=2),
+    "tiny_f32": W["tiny_f32"],
+    "hires_small": W["hires56"].scaled(B=1, H=1, N=1024, gh=32, gw=32, ph=4, pw=4, m=16, k=48),
+    "long_small": W["long1d"].scaled(B=1, H=1, N=2048, gw=2048, pw=16, m=16, k=64),
+}
+
+
+@pytest.mark.parametrize("routing_only", [False, True])
+@pytest.mark.parametrize("name", sorted(BWD))
+def test_backward_matches_oracle(name, routing_only):
+    """mita_backward against the oracle's backward (experts and routes held
+    constant) on every head whose discrete choices agree with the oracle's."""
+    import oracle
+    w = BWD[name]
+    Q, K, V = synth.make_inputs(w, seed=71)
+    g = torch.Generator("cpu").manual_seed(72)
+    dOut = torch.randn(w.B, w.H, w.N, w.d, generator=g).to(synth.torch_dtype(w))
+    fwd = _run(w, Q, K, V, "staged", routing_only=routing_only)
+    plan = fwd["plan"]
+    dev = torch.device("cuda")
+    Qd, Kd, Vd, Gd = Q.to(dev), K.to(dev), V.to(dev), dOut.to(dev)
+    dQ, dK, dV = (torch.empty(w.B, w.H, w.N, w.d, dtype=torch.float32, device=dev) for _ in range(3))
+    plan.backward(Qd, Kd, Vd, Gd, dQ, dK, dV)
+    assert plan.status() == mita.MITA_OK
+    dQ, dK, dV = dQ.cpu().double().numpy(), dK.cpu().double().numpy(), dV.cpu().double().numpy()
+    checked = 0
+    for b in range(w.B):
+        for h in range(w.H):
+            o = oracle.head(Q[b, h], K[b, h], V[b, h], w.grid, w.m, w.k, io=w.dtype)
+            if not (np.array_equal(fwd["idx"][b, h].cpu().numpy(), o["idx"])
+                    and np.array_equal(fwd["route"][b, h].cpu().numpy(), o["route"])):
+                continue   # a near-tie flip: another operator's gradient
+            ref = oracle.backward(Q[b, h], K[b, h], V[b, h], dOut[b, h], w.grid, w.m, w.k, io=w.dtype,
+                                  shared=not routing_only)
+            for got, want in zip((dQ[b, h], dK[b, h], dV[b, h]), ref):
+                scale = np.abs(want).max()
+                np.testing.assert_allclose(got, want, rtol=1e-3, atol=1e-3 * scale + 1e-6)
+            checked += 1
+    assert checked >= 1
+
+
+def test_backward_rejects_top_s():
+    w = BWD["deit_t"]
+    plan = mita.Plan.for_workload(w)
+    plan.set_option(mita.OPT_ROUTES, 2)
+    dev = torch.device("cuda")
+    x = torch.zeros(w.B, w.H, w.N, w.d, dtype=torch.bfloat16, device=dev)
+    gq = torch.zeros(w.B, w.H, w.N, w.d, dtype=torch.float32, device=dev)
+    with pytest.raises(mita.MitaError):
+        plan.backward(x, x, x, x, gq, gq, gq)
+
+
 def test_routing_only_option_rejects_bad_values():
     plan = mita.Plan.for_workload(SMALL["deit_t"])
     with pytest.raises(mita.MitaError):
