@@ -19,6 +19,8 @@ from __future__ import annotations
 import argparse
 import json
 import math
+
+import numpy as np
 import os
 import subprocess
 import sys
@@ -52,18 +54,24 @@ def parse():
                     help="the routing-only variant: the shared expert dropped from every query's softmax")
     ap.add_argument("--routes", type=int, default=1,
                     help="experts per query (s > 1 runs on the staged path)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time mita_backward (input gradients for an output gradient) instead of the forward")
     ap.add_argument("--no-soak", action="store_true", help="skip the untimed repeats that extend clock sampling")
     return ap.parse_args()
 
 
-def algorithmic(w):
+def algorithmic(w, backward=False):
     """Compulsory HBM bytes and algorithmic FLOPs per step: read Q, K, V once,
     write out, expert indices and routes; FLOPs of the six contractions
     (landmark scores, landmark values, query-landmark scores reused for the
-    route, shared and routed QK and PV)."""
+    route, shared and routed QK and PV).  Backward: read Q, K, V and dOut,
+    write fp32 dQ, dK, dV; the forward's contractions once (recomputed) and
+    twice more for the gradients."""
     e = 2 if w.dtype == "bf16" else 4
-    per_head_bytes = 4 * w.N * w.d * e + 4 * w.m * w.k + 4 * w.N
     per_head_flops = 4 * w.N * w.d * (2 * w.m + w.k)
+    if backward:
+        return (4 * w.N * w.d * e + 3 * w.N * w.d * 4) * w.heads, 3 * per_head_flops * w.heads
+    per_head_bytes = 4 * w.N * w.d * e + 4 * w.m * w.k + 4 * w.N
     return per_head_bytes * w.heads, per_head_flops * w.heads
 
 
@@ -174,12 +182,13 @@ class ClockSampler:
 
 
 def variant_name(args):
-    """The operator variant a run measures: mita, routing_only, routes_s<S>."""
+    """The operator variant a run measures: mita, routing_only, routes_s<S>, backward."""
     parts = (["routing_only"] if args.routing_only else []) + ([f"routes_s{args.routes}"] if args.routes > 1 else [])
+    parts += ["backward"] if getattr(args, "backward", False) else []
     return "+".join(parts) if parts else "mita"
 
 
-def cpu_baseline(w, seconds, full=False, shared=True, routes=1):
+def cpu_baseline(w, seconds, full=False, shared=True, routes=1, backward=False):
     """Time the CPU oracle (single thread, fp64) on whole heads of the
     workload until about ``seconds`` of work; returns query-heads/s
     (``shared=False``: the routing-only variant)."""
@@ -191,10 +200,17 @@ def cpu_baseline(w, seconds, full=False, shared=True, routes=1):
     if w.N > 16384:   # a long sequence: all landmark work, a slice of queries
         queries = list(range(0, w.N, max(1, w.N // 512)))
     nq = w.N if queries is None else len(queries)
+    if backward:   # whole heads only: the backward has no per-query slice
+        queries = None
+        nq = w.N
+        G = np.random.default_rng(0).standard_normal(Qf.shape[2:])
     while True:
         h = heads % Q.shape[1]
-        oracle.head(Qf[0, h], Kf[0, h], Vf[0, h], w.grid, w.m, w.k, io=w.dtype, queries=queries, shared=shared,
-                    s=routes)
+        if backward:
+            oracle.backward(Qf[0, h], Kf[0, h], Vf[0, h], G, w.grid, w.m, w.k, io=w.dtype, shared=shared)
+        else:
+            oracle.head(Qf[0, h], Kf[0, h], Vf[0, h], w.grid, w.m, w.k, io=w.dtype, queries=queries, shared=shared,
+                        s=routes)
         heads += 1
         el = time.perf_counter() - t0
         if el >= seconds or (queries is not None and heads >= 1):
@@ -255,7 +271,7 @@ def run_reference(args, w, ws, rank):
     times = []
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
     for s in range(args.warmup + args.steps):
-        cb = cpu_baseline(w, per_step, shared=not args.routing_only, routes=args.routes)
+        cb = cpu_baseline(w, per_step, shared=not args.routing_only, routes=args.routes, backward=args.backward)
         if s >= args.warmup:
             times.append(cb)
     v = sorted(c["value"] for c in times)[len(times) // 2]
@@ -291,7 +307,7 @@ def main():
         plan.set_option(mita.OPT_ROUTING_ONLY, 1)
     if args.routes > 1:
         plan.set_option(mita.OPT_ROUTES, args.routes)
-    path = plan.path
+    path = "staged" if args.backward else plan.path   # the backward runs the stage-by-stage kernels
     stream = torch.cuda.current_stream()
 
     # inputs: enough rotating sets that consecutive steps never hit in L2
@@ -307,9 +323,18 @@ def main():
         route = torch.empty(w.B, w.H, w.N, dtype=torch.int32, device=dev)
         sets.append((Q, K, V, out, idx, route))
 
+    grads = None
+    if args.backward:
+        gen = torch.Generator("cpu").manual_seed(w.seed + 17)
+        dOuts = [torch.randn(Qc.shape, generator=gen).to(Qc.dtype).to(dev) for _ in range(nsets)]
+        grads = [torch.empty(Qc.shape, dtype=torch.float32, device=dev) for _ in range(3)]
+
     def step(i):
         Q, K, V, out, idx, route = sets[i % nsets]
-        plan.forward(Q, K, V, out, idx, route, stream)
+        if args.backward:
+            plan.backward(Q, K, V, dOuts[i % nsets], *grads, stream)
+        else:
+            plan.forward(Q, K, V, out, idx, route, stream)
 
     for i in range(args.warmup):
         step(i)
@@ -347,12 +372,13 @@ def main():
         raise SystemExit(f"device status {mita.STATUS.get(st, st)}")
     qh = w.heads * w.N
     value, ms = whole_job_rate(qh, ms, ws, dev)
-    nbytes, flops = algorithmic(w)
+    nbytes, flops = algorithmic(w, args.backward)
     pk = peaks()
     # dominant kernel: on the fused path the step is one launch; on the
     # staged path the whole step is reported (kernel-level shares live in
     # the ncu launch list under profiles/).
-    kernel_tag = "mita_fused" if path == "fused" else f"mita_{path}_step"
+    kernel_tag = "mita_fused" if path == "fused" and not args.backward else \
+        f"mita_{'backward' if args.backward else path}_step"
     t_s = ms / 1000.0
     bw = nbytes / t_s / 1e9
     tf = flops / t_s / 1e12
@@ -372,7 +398,7 @@ def main():
     # end to end through the public API: pinned host inputs -> device ->
     # forward -> host results, every step
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.backward:
         hQ, hK, hV = Qc.pin_memory(), Kc.pin_memory(), Vc.pin_memory()
         Q, K, V, out, idx, route = sets[0]
         hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -418,7 +444,10 @@ def main():
                 cs = torch.cuda.current_stream()
                 for i in range(nsets):
                     Q, K, V, out, idx, route = sets[i]
-                    plan.forward(Q, K, V, out, idx, route, cs)
+                    if args.backward:
+                        plan.backward(Q, K, V, dOuts[i], *grads, cs)
+                    else:
+                        plan.forward(Q, K, V, out, idx, route, cs)
             reps = max(3, args.steps // nsets)
             for _ in range(3):
                 g.replay()
@@ -443,7 +472,8 @@ def main():
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, args.cpu_seconds, shared=not args.routing_only, routes=args.routes)
+        cpu = cpu_baseline(w, args.cpu_seconds, shared=not args.routing_only, routes=args.routes,
+                           backward=args.backward)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "query-heads/s", "n_gpus": ws, "steps": args.steps,
