@@ -54,6 +54,8 @@ def parse():
                     help="the routing-only variant: the shared expert dropped from every query's softmax")
     ap.add_argument("--routes", type=int, default=1,
                     help="experts per query (s > 1 runs on the staged path)")
+    ap.add_argument("--long-sweep", action="store_true",
+                    help="long-sequence throughput against full attention (one JSON line per length)")
     ap.add_argument("--backward", action="store_true",
                     help="time mita_backward (input gradients for an output gradient) instead of the forward")
     ap.add_argument("--no-soak", action="store_true", help="skip the untimed repeats that extend clock sampling")
@@ -289,12 +291,57 @@ def run_reference(args, w, ws, rank):
     return 0
 
 
+def long_sweep(args):
+    """MiTA forward against full attention (torch scaled_dot_product_attention,
+    the fused flash kernel) on single-head 1-D sequences with m * k = N / 4
+    (N / 8 at 1M tokens, where the tiled path's k <= 512 sets the limit),
+    d = 128, bf16 (the shape of the method's long-sequence throughput figure).
+    One JSON line per length: both times from CUDA events, median of a few
+    runs after a warm-up."""
+    import mixture_top_attention_mita_b300 as mita
+    dev = torch.device("cuda")
+    for N, m, k in ((16384, 64, 64), (65536, 128, 128), (262144, 256, 256), (1048576, 256, 512)):
+        w = synth.WORKLOADS["long1d"].scaled(name=f"long_{N}", B=1, H=1, N=N, gw=N, pw=m, m=m, k=k,
+                                             span=1024, seed=2000 + N % 997)
+        Qc, Kc, Vc = synth.make_inputs(w)
+        Q, K, V = Qc.to(dev), Kc.to(dev), Vc.to(dev)
+        out = torch.empty_like(Q)
+        plan = mita.Plan.for_workload(w)
+
+        def timed(fn, reps):
+            for _ in range(2):
+                fn()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(reps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b))
+            return sorted(ts)[len(ts) // 2]
+
+        t_mita = timed(lambda: plan.forward(Q, K, V, out), 5)
+        st = plan.status()
+        t_sdpa = timed(lambda: torch.nn.functional.scaled_dot_product_attention(Q, K, V), 3 if N > 300000 else 5)
+        print(json.dumps({"sweep": "long_sequence", "N": N, "m": m, "k": k, "d": w.d, "dtype": w.dtype,
+                          "path": plan.path, "status": st, "mita_ms": round(t_mita, 4),
+                          "full_attention_ms": round(t_sdpa, 4), "speedup": round(t_sdpa / t_mita, 2)}))
+        plan.close()
+        del Q, K, V, out
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     args = parse()
     ws, rank, local = dist_setup()
     w = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w, ws, rank)
+    if args.long_sweep:
+        return long_sweep(args) if rank == 0 else 0
 
     import mixture_top_attention_mita_b300 as mita
     if not torch.cuda.is_available():
