@@ -111,7 +111,8 @@ __global__ void __launch_bounds__(128) tl_pool(Shape s, const bf16* __restrict__
 
 // ---------------------------------------------------------------- top-k
 constexpr int kTB = 256;          // threads per top-k block
-constexpr int kNB = 2048;         // histogram bins
+constexpr int kNB = 2048;         // histogram bins (rows past kShortRow keys)
+constexpr int kShortRow = 4096;   // rows up to this many keys: 256 bins
 constexpr int kCandMax = 1024;    // boundary members ranked exactly
 
 // Block-wide exclusive prefix sum of one int per thread (kTB threads);
@@ -140,7 +141,8 @@ MITA_DEV int block_excl_scan(int x, int* wsum, int* total) {
 
 // Block per (landmark i, head bh), rows up to kBitsMaxN keys: the k keys
 // with the largest raw scores S[bh, i, :], ties to the lower key index, in
-// ascending order.  Bins of equal width over [row min, row max] find the bin
+// ascending order.  NB bins of equal width over [row min, row max] (256 on
+// rows up to kShortRow keys, 2048 beyond) find the bin
 // bin* holding the k-th largest score; every pass over the row is coalesced.
 // Pass 1 builds the histogram; pass 2 marks the keys of the bins above bin* in a bitmap
 // over the row (one ballot word per 32 keys) and lists bin*'s members with
@@ -152,11 +154,13 @@ MITA_DEV int block_excl_scan(int x, int* wsum, int* total) {
 constexpr int kBitsMaxN = 65536;
 constexpr int kChainMaxN = 16384;   // rows up to this length: overlapped (chained) launches
 
+template <int NB>
 __global__ void __launch_bounds__(kTB) tl_topk_bits(Shape s, const float* __restrict__ S,
                                                     const uint32_t* __restrict__ rowmax,
                                                     const uint32_t* __restrict__ rowmin, int32_t* __restrict__ idx) {
     chain_wait_and_trigger();
-    __shared__ int hist[kNB];
+    constexpr int BPT = NB / kTB;   // bins per thread in the boundary search
+    __shared__ int hist[NB];
     __shared__ uint32_t bits[kBitsMaxN / 32];
     __shared__ float cval[kCandMax];
     __shared__ int cidx[kCandMax];
@@ -168,9 +172,9 @@ __global__ void __launch_bounds__(kTB) tl_topk_bits(Shape s, const float* __rest
     const float mx = key_to_float(rowmax[(size_t)bh * s.m + i]);
     const float mn = key_to_float(rowmin[(size_t)bh * s.m + i]);
     const float range = mx - mn;
-    const float sc = range > 0.0f ? (float)kNB / range : 0.0f;
-    auto bin_of = [&](float v) { return min(kNB - 1, (int)((v - mn) * sc)); };
-    for (int b = tid; b < kNB; b += kTB) hist[b] = 0;
+    const float sc = range > 0.0f ? (float)NB / range : 0.0f;
+    auto bin_of = [&](float v) { return min(NB - 1, (int)((v - mn) * sc)); };
+    for (int b = tid; b < NB; b += kTB) hist[b] = 0;
     for (int w = tid; w < nw; w += kTB) bits[w] = 0u;
     if (tid == 0) sh[3] = 0;
     __syncthreads();
@@ -200,20 +204,20 @@ __global__ void __launch_bounds__(kTB) tl_topk_bits(Shape s, const float* __rest
         for (int j = tid; j < N; j += kTB) atomicAdd(&hist[bin_of(row[j])], 1);
     }
     __syncthreads();
-    // thread t holds bins [8t, 8t + 8); counts of bins above, from the top down
+    // thread t holds bins [BPT t, BPT t + BPT); counts of bins above, from the top down
     {
-        int c[8], tot = 0;
+        int c[BPT], tot = 0;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) { c[u] = hist[8 * tid + u]; tot += c[u]; }
+        for (int u = 0; u < BPT; ++u) { c[u] = hist[BPT * tid + u]; tot += c[u]; }
         int all;
         const int below = block_excl_scan(tot, wsum, &all);
         const int above = all - below - tot;
         if (above < k && above + tot >= k) {
             int run = above;
 #pragma unroll
-            for (int u = 7; u >= 0; --u) {
+            for (int u = BPT - 1; u >= 0; --u) {
                 if (run < k && run + c[u] >= k) {
-                    sh[0] = 8 * tid + u;
+                    sh[0] = BPT * tid + u;
                     sh[1] = k - run;
                     sh[2] = c[u];
                 }
@@ -611,7 +615,8 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
             cudaSuccess)
             return err;
         if (s.N <= kBitsMaxN) {
-            if ((err = launch_chained(chain, tl_topk_bits, dim3(s.m, sg.H), dim3(kTB), 0, st, sg, (const float*)p->S,
+            auto kern = s.N <= kShortRow ? tl_topk_bits<256> : tl_topk_bits<kNB>;
+            if ((err = launch_chained(chain, kern, dim3(s.m, sg.H), dim3(kTB), 0, st, sg, (const float*)p->S,
                                       (const uint32_t*)(p->rowmax + mo), (const uint32_t*)(rowmin + mo),
                                       idx + mo * s.k)) != cudaSuccess)
                 return err;
