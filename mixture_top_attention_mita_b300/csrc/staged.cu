@@ -617,6 +617,264 @@ __global__ void __launch_bounds__(32 * kAttendWarps)
     for (int u = 0; u < D / 32; ++u) dQ[hoff + (size_t)qi * D + lane + 32 * u] = dq[u] * scale;
 }
 
+// Block of NW warps per (expert e, head): the queries routed to e, in bucket
+// order and in chunks of 4 NW, against the expert's m + k keys and values, which stay in
+// shared memory as fp32 for the whole block.  Per chunk: logits and dw =
+// dOut . v (lane per key, 4 queries per warp), the softmax and dlogit =
+// w (dw - w . dw) in registers, the chunk's dQ rows (stored: a query has one
+// expert), and the key and value gradients of the chunk added to per-thread
+// 4 x 4 tiles.  Those are summed over all of e's queries on chip and leave
+// with one float4 atomic add per (slot, 4 features): to dQ_l / dV_l for the
+// shared slots, to dK / dV for the routed keys.  Slots are padded to LP =
+// 32 JT; a padded slot reads the last real row and is masked out.
+
+MITA_DEV float dot4(float4 a, float4 b, float acc) {
+    return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, fmaf(a.x, b.x, acc))));
+}
+
+template <typename T>
+MITA_DEV float4 load4(const T* p) {
+    if constexpr (sizeof(T) == 4) {
+        return *reinterpret_cast<const float4*>(p);
+    } else {
+        const uint2 u = *reinterpret_cast<const uint2*>(p);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    }
+}
+
+template <int D, int NW>
+constexpr size_t expert_bwd_floats(int L, int LP) {
+    return 2 * (size_t)L * (D + 4) + 2 * (size_t)(4 * NW) * D + 2 * (size_t)(4 * NW) * LP;
+}
+
+template <typename T, int D, int JT, int NW>
+__global__ void __launch_bounds__(32 * NW)
+    expert_bwd_kernel(Shape s, const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
+                      const T* __restrict__ Ql, const T* __restrict__ Vl, const int32_t* __restrict__ idx,
+                      const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm,
+                      const T* __restrict__ dOut, float* __restrict__ dQ, float* __restrict__ dK,
+                      float* __restrict__ dV, float* __restrict__ dQl, float* __restrict__ dVl, int shared,
+                      int32_t* __restrict__ status) {
+    constexpr int kEbThreads = 32 * NW, kEbQ = 4 * NW;
+    constexpr int KS = D + 4;                  // key / value row stride (floats)
+    constexpr int LP = 32 * JT;                // padded slots
+    constexpr int NC = D / 4;                  // float4 columns
+    constexpr int RG = kEbThreads / NC;        // row groups of the tiles
+    constexpr int QPT = kEbQ / RG;             // dQ rows per thread
+    constexpr int TR = (LP / 4 + RG - 1) / RG; // 4-slot gradient tiles per thread
+    static_assert(kEbQ % RG == 0 && kEbQ == 4 * (kEbThreads / 32), "tile split");
+    extern __shared__ float4 eb_smem[];
+    __shared__ int32_t qid[kEbQ];
+    __shared__ int32_t kid[LP];
+    const int e = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int L = s.m + s.k;
+    const int32_t* off = offsets + (size_t)bh * (s.m + 1);
+    const int beg = off[e], cnt = off[e + 1] - beg;
+    if (cnt <= 0) return;
+    float* Ks = reinterpret_cast<float*>(eb_smem);
+    float* Vs = Ks + (size_t)L * KS;
+    float* Qs = Vs + (size_t)L * KS;   // [kEbQ][D]
+    float* Gs = Qs + kEbQ * D;         // dOut rows
+    float* Ws = Gs + kEbQ * D;         // [kEbQ][LP] weights
+    float* Cs = Ws + kEbQ * LP;        // [kEbQ][LP] logit gradients
+    const size_t hoff = (size_t)bh * s.N * D;
+    const int32_t* E = idx + ((size_t)bh * s.m + e) * s.k;
+    for (int t = tid; t < LP; t += kEbThreads) {
+        int j = -1;
+        if (t >= s.m && t < L) {
+            j = E[t - s.m];
+            if (j < 0 || j >= s.N) { atomicExch(status, (int)MITA_ERR_DEVICE); j = -1; }
+        }
+        kid[t] = j;
+    }
+    __syncthreads();
+    for (int u = tid; u < L * NC; u += kEbThreads) {
+        const int t = u / NC, c = 4 * (u % NC);
+        float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
+        if (t < s.m) {
+            kv = load4(Ql + ((size_t)bh * s.m + t) * D + c);
+            vv = load4(Vl + ((size_t)bh * s.m + t) * D + c);
+        } else if (kid[t] >= 0) {
+            kv = load4(K + hoff + (size_t)kid[t] * D + c);
+            vv = load4(V + hoff + (size_t)kid[t] * D + c);
+        }
+        *reinterpret_cast<float4*>(Ks + t * KS + c) = kv;
+        *reinterpret_cast<float4*>(Vs + t * KS + c) = vv;
+    }
+    const float scale = rsqrtf((float)D);
+    const int tc = tid % NC, rg = tid / NC;
+    float gk[TR][4][4], gv[TR][4][4];
+#pragma unroll
+    for (int r = 0; r < TR; ++r)
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) gk[r][a][b] = gv[r][a][b] = 0.0f;
+    const int32_t* P = perm + (size_t)bh * s.N + beg;
+    for (int c0 = 0; c0 < cnt; c0 += kEbQ) {
+        const int nq = min(kEbQ, cnt - c0);
+        __syncthreads();   // the previous chunk's tiles are consumed
+        if (tid < kEbQ) {
+            int q = tid < nq ? P[c0 + tid] : -1;
+            if (tid < nq && (q < 0 || q >= s.N)) { atomicExch(status, (int)MITA_ERR_DEVICE); q = -1; }
+            qid[tid] = q;
+        }
+        __syncthreads();
+        for (int u = tid; u < kEbQ * NC; u += kEbThreads) {
+            const int r = u / NC, c = 4 * (u % NC);
+            float4 qv = make_float4(0.f, 0.f, 0.f, 0.f), g = qv;
+            if (qid[r] >= 0) {
+                qv = load4(Q + hoff + (size_t)qid[r] * D + c);
+                g = load4(dOut + hoff + (size_t)qid[r] * D + c);
+            }
+            *reinterpret_cast<float4*>(Qs + r * D + c) = qv;
+            *reinterpret_cast<float4*>(Gs + r * D + c) = g;
+        }
+        __syncthreads();
+        // logits and dw: warp w takes chunk rows 4w..4w+3, lane the slots lane + 32j
+        const int r0 = 4 * w;
+        if (r0 < nq) {
+            float a[4][JT], dw[4][JT];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < JT; ++j) a[i][j] = dw[i][j] = 0.0f;
+#pragma unroll 1
+            for (int f = 0; f < D; f += 4) {
+                float4 qv[4], g[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    qv[i] = *reinterpret_cast<const float4*>(Qs + (r0 + i) * D + f);
+                    g[i] = *reinterpret_cast<const float4*>(Gs + (r0 + i) * D + f);
+                }
+#pragma unroll
+                for (int j = 0; j < JT; ++j) {
+                    const int t = min(lane + 32 * j, L - 1);
+                    const float4 kv = *reinterpret_cast<const float4*>(Ks + t * KS + f);
+                    const float4 vv = *reinterpret_cast<const float4*>(Vs + t * KS + f);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        a[i][j] = dot4(qv[i], kv, a[i][j]);
+                        dw[i][j] = dot4(g[i], vv, dw[i][j]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float mx = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < JT; ++j) {
+                    const int t = lane + 32 * j;
+                    const bool live = t < L && (t >= s.m ? kid[t] >= 0 : shared != 0);
+                    a[i][j] = live ? a[i][j] * scale : -INFINITY;
+                    mx = fmaxf(mx, a[i][j]);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                float den = 0.0f;
+#pragma unroll
+                for (int j = 0; j < JT; ++j) {
+                    a[i][j] = exp2f((a[i][j] - mx) * kLog2e);
+                    den += a[i][j];
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+                const float inv = 1.0f / den;
+                float wdw = 0.0f;
+#pragma unroll
+                for (int j = 0; j < JT; ++j) {
+                    a[i][j] *= inv;
+                    wdw = fmaf(a[i][j], dw[i][j], wdw);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) wdw += __shfl_xor_sync(0xffffffffu, wdw, o);
+#pragma unroll
+                for (int j = 0; j < JT; ++j) {
+                    Ws[(r0 + i) * LP + lane + 32 * j] = a[i][j];
+                    Cs[(r0 + i) * LP + lane + 32 * j] = a[i][j] * (dw[i][j] - wdw);
+                }
+            }
+        }
+        __syncthreads();
+        // dQ rows rg + RG u: sum over slots of dlogit . key, 4 features per thread
+        {
+            float acc[QPT][4];
+#pragma unroll
+            for (int u = 0; u < QPT; ++u)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) acc[u][b] = 0.0f;
+            if (rg < nq) {
+                for (int t = 0; t < L; ++t) {
+                    const float4 kv = *reinterpret_cast<const float4*>(Ks + t * KS + 4 * tc);
+#pragma unroll
+                    for (int u = 0; u < QPT; ++u) {
+                        const float c = Cs[(rg + RG * u) * LP + t];
+                        acc[u][0] = fmaf(c, kv.x, acc[u][0]);
+                        acc[u][1] = fmaf(c, kv.y, acc[u][1]);
+                        acc[u][2] = fmaf(c, kv.z, acc[u][2]);
+                        acc[u][3] = fmaf(c, kv.w, acc[u][3]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < QPT; ++u) {
+                const int r = rg + RG * u;
+                if (r < nq && qid[r] >= 0)
+                    *reinterpret_cast<float4*>(dQ + hoff + (size_t)qid[r] * D + 4 * tc) =
+                        make_float4(acc[u][0] * scale, acc[u][1] * scale, acc[u][2] * scale, acc[u][3] * scale);
+            }
+        }
+        // key and value gradients of the slot tiles (rg + RG r), features 4 tc..
+        for (int q = 0; q < nq; ++q) {
+            const float4 qv = *reinterpret_cast<const float4*>(Qs + q * D + 4 * tc);
+            const float4 g = *reinterpret_cast<const float4*>(Gs + q * D + 4 * tc);
+#pragma unroll
+            for (int r = 0; r < TR; ++r) {
+                const int t0 = 4 * (rg + RG * r);
+                if (t0 < LP) {
+                    const float4 c = *reinterpret_cast<const float4*>(Cs + q * LP + t0);
+                    const float4 wt = *reinterpret_cast<const float4*>(Ws + q * LP + t0);
+                    const float cc[4] = {c.x, c.y, c.z, c.w}, ww[4] = {wt.x, wt.y, wt.z, wt.w};
+                    const float qq[4] = {qv.x, qv.y, qv.z, qv.w}, gg[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+                    for (int a = 0; a < 4; ++a)
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            gk[r][a][b] = fmaf(cc[a], qq[b], gk[r][a][b]);
+                            gv[r][a][b] = fmaf(ww[a], gg[b], gv[r][a][b]);
+                        }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < TR; ++r) {
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const int t = 4 * (rg + RG * r) + a;
+            if (t >= L) continue;
+            float* rk;
+            float* rv;
+            if (t < s.m) {
+                if (!shared) continue;
+                rk = dQl + ((size_t)bh * s.m + t) * D;
+                rv = dVl + ((size_t)bh * s.m + t) * D;
+            } else {
+                if (kid[t] < 0) continue;
+                rk = dK + hoff + (size_t)kid[t] * D;
+                rv = dV + hoff + (size_t)kid[t] * D;
+            }
+            atomicAdd(reinterpret_cast<float4*>(rk + 4 * tc),
+                      make_float4(gk[r][a][0] * scale, gk[r][a][1] * scale, gk[r][a][2] * scale,
+                                  gk[r][a][3] * scale));
+            atomicAdd(reinterpret_cast<float4*>(rv + 4 * tc),
+                      make_float4(gv[r][a][0], gv[r][a][1], gv[r][a][2], gv[r][a][3]));
+        }
+    }
+}
+
 // Block per (landmark i, head), 8 warps: P = softmax(S[i] / sqrt d) again,
 // dP_j = dV_l[i] . V[j] (warp per key), dR_j = P_j (dP_j - P . dP) / sqrt d;
 // dV[j] += P_j dV_l[i] and dK[j] += dR_j Q_l[i] are added, dQ_l[i] += dR . K.
@@ -734,14 +992,40 @@ static cudaError_t run_backward_t(mita_plan_s* p, const T* Q, const T* K, const 
     topk_kernel<<<dim3(s.m, BH), kTopkThreads, 0, st>>>(s, p->S, p->idx);
     values_kernel<T><<<dim3(s.m, BH), 256, 0, st>>>(s, p->S, V, Vl);
     route_kernel<T, D><<<dim3((s.N + 127) / 128, BH), 128, 0, st>>>(s, Q, Ql, p->route, 1, nullptr);
-    const size_t smem = (size_t)kAttendWarps * (2 * D + 2 * (s.m + s.k)) * sizeof(float);
-    if (smem > 227 * 1024) return cudaErrorInvalidValue;
-    ensure_smem_attr((const void*)attend_bwd_kernel<T, D>, (int)smem);
-    attend_bwd_kernel<T, D><<<dim3((s.N + kAttendWarps - 1) / kAttendWarps, BH), 32 * kAttendWarps, smem, st>>>(
-        s, Q, K, V, Ql, Vl, p->idx, p->route, dOut, dQ, dK, dV, p->dQl, p->dVl, p->routing_only ? 0 : 1, p->status);
+    const int L = s.m + s.k;
+    const int shared = p->routing_only ? 0 : 1;
+    // expert-major output softmax where the expert's slots fit (L <= 128 at
+    // d = 64, L <= 64 at d = 128; 16 warps where a thread would otherwise hold
+    // more than 32 gradient accumulators); the warp-per-query kernel otherwise
+    auto expert_launch = [&](auto kern, int LP, int NW) -> bool {
+        const size_t bytes = (NW == 8 ? expert_bwd_floats<D, 8>(L, LP) : expert_bwd_floats<D, 16>(L, LP)) *
+                             sizeof(float);
+        if (bytes > 200 * 1024) return false;
+        ensure_smem_attr((const void*)kern, (int)bytes);
+        bucket_kernel<<<BH, 32, 0, st>>>(s, p->route, p->counts, p->offsets, p->perm, p->status);
+        kern<<<dim3(s.m, BH), 32 * NW, bytes, st>>>(s, Q, K, V, Ql, Vl, p->idx, p->offsets, p->perm, dOut, dQ,
+                                                       dK, dV, p->dQl, p->dVl, shared, p->status);
+        p->launches += 2;
+        return true;
+    };
+    bool done = false;
+    if constexpr (D == 64) {
+        if (L <= 64) done = expert_launch(expert_bwd_kernel<T, D, 2, 8>, 64, 8);
+        else if (L <= 128) done = expert_launch(expert_bwd_kernel<T, D, 4, 16>, 128, 16);
+    } else {
+        if (L <= 64) done = expert_launch(expert_bwd_kernel<T, D, 2, 16>, 64, 16);
+    }
+    if (!done) {
+        const size_t smem = (size_t)kAttendWarps * (2 * D + 2 * L) * sizeof(float);
+        if (smem > 227 * 1024) return cudaErrorInvalidValue;
+        ensure_smem_attr((const void*)attend_bwd_kernel<T, D>, (int)smem);
+        attend_bwd_kernel<T, D><<<dim3((s.N + kAttendWarps - 1) / kAttendWarps, BH), 32 * kAttendWarps, smem, st>>>(
+            s, Q, K, V, Ql, Vl, p->idx, p->route, dOut, dQ, dK, dV, p->dQl, p->dVl, shared, p->status);
+        p->launches += 1;
+    }
     values_bwd_kernel<T, D><<<dim3(s.m, BH), 256, 0, st>>>(s, p->S, K, V, Ql, dK, dV, p->dQl, p->dVl);
     pool_bwd_kernel<<<dim3((unsigned)(((size_t)s.N * D + 255) / 256), BH), 256, 0, st>>>(s, p->dQl, dQ);
-    p->launches += 8;
+    p->launches += 7;
     return cudaGetLastError();
 }
 
