@@ -71,7 +71,8 @@ int mita_plan(mita_plan_t* plan, int B, int H, int N, int d, mita_grid_t grid, i
     const size_t oIdx = take(BH * m * (size_t)k * 4), oRoute = take(BH * (size_t)N * 4);
     const size_t oCnt = take(BH * m * 4), oOff = take(BH * (m + 1) * 4), oPerm = take(BH * (size_t)N * 4);
     const size_t oStatus = take(256);
-    const size_t oGradL = take(2 * BH * m * d * 4);   // backward: dQ_l, dV_l (fp32)
+    // backward (fp32): dQ_l, dV_l, V_l, then per landmark row {max S, sum of weights}
+    const size_t oGradL = take((3 * BH * m * d + 2 * BH * m) * 4);
     const bool tiled = mita::tiled_supported(p->s, dtype);
     const size_t oRowmax = take(tiled ? 2 * BH * m * 4 : 0);   // row max, then row min
     const size_t oVpart = take(tiled ? mita::tiled_part_bytes(p->s) : 0);

@@ -875,90 +875,255 @@ __global__ void __launch_bounds__(32 * NW)
     }
 }
 
-// Block per (landmark i, head), 8 warps: P = softmax(S[i] / sqrt d) again,
-// dP_j = dV_l[i] . V[j] (warp per key), dR_j = P_j (dP_j - P . dP) / sqrt d;
-// dV[j] += P_j dV_l[i] and dK[j] += dR_j Q_l[i] are added, dQ_l[i] += dR . K.
+// Landmark values again for the backward, a block per (32 landmarks, head):
+// row maxima of S, then 64-key chunks of V staged once in shared memory for
+// all 32 rows, weights w = exp((S - max) / sqrt d) and their sums.  Writes
+// V_l in the I/O type (as the forward uses it), V_l in fp32 and per row
+// {max S, sum w} for values_bwd_tile_kernel.
+constexpr int kVrRows = 32, kVrKeys = 64;
+
 template <typename T, int D>
-__global__ void __launch_bounds__(256) values_bwd_kernel(Shape s, const float* __restrict__ S,
-                                                         const T* __restrict__ K, const T* __restrict__ V,
-                                                         const T* __restrict__ Ql, float* __restrict__ dK,
-                                                         float* __restrict__ dV, float* __restrict__ dQl,
-                                                         const float* __restrict__ dVl) {
-    __shared__ float dvl_s[D], ql_s[D], red[8];
-    __shared__ float part[8][D];
-    const int i = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const float* row = S + ((size_t)bh * s.m + i) * s.N;
-    const float scale = rsqrtf((float)D);
-    for (int f = tid; f < D; f += 256) {
-        dvl_s[f] = dVl[((size_t)bh * s.m + i) * D + f];
-        ql_s[f] = to_f32(Ql[((size_t)bh * s.m + i) * D + f]);
-    }
-    auto block_sum = [&](float x, bool is_max) {
+__global__ void __launch_bounds__(256) values_rows_kernel(Shape s, const float* __restrict__ S,
+                                                          const T* __restrict__ V, T* __restrict__ Vl,
+                                                          float* __restrict__ Vl32, float* __restrict__ stats) {
+    constexpr int NC = D / 4, KS = D + 4, WS = kVrKeys + 1;
+    constexpr int RG = 256 / NC, RPT = kVrRows / RG;
+    __shared__ __align__(16) float Vt[kVrKeys * KS];
+    __shared__ float Wt[kVrRows * WS];
+    __shared__ float mx_s[kVrRows], den_s[kVrRows];
+    const int i0 = blockIdx.x * kVrRows, bh = blockIdx.y, tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int nr = min(kVrRows, s.m - i0);
+    const float* Sh = S + ((size_t)bh * s.m + i0) * s.N;
+    for (int r = w; r < kVrRows; r += 8) {
+        float mx = -INFINITY;
+        if (r < nr)
+            for (int j = lane; j < s.N; j += 32) mx = fmaxf(mx, Sh[(size_t)r * s.N + j]);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float y = __shfl_xor_sync(0xffffffffu, x, o);
-            x = is_max ? fmaxf(x, y) : x + y;
-        }
-        __syncthreads();
-        if (lane == 0) red[warp] = x;
-        __syncthreads();
-        float t = red[0];
-        for (int u = 1; u < 8; ++u) t = is_max ? fmaxf(t, red[u]) : t + red[u];
-        return t;
-    };
-    float mx = -INFINITY;
-    for (int j = tid; j < s.N; j += 256) mx = fmaxf(mx, row[j] * scale);
-    mx = block_sum(mx, true);
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) mx_s[r] = mx;
+    }
+    const float c = rsqrtf((float)D) * kLog2e;
+    const int tc = tid % NC, rg = tid / NC, wr = tid >> 3, wk = tid & 7;
+    float acc[RPT][4] = {};
     float den = 0.0f;
-    for (int j = tid; j < s.N; j += 256) den += exp2f((row[j] * scale - mx) * kLog2e);
-    const float inv = 1.0f / block_sum(den, false);
-    const size_t hoff = (size_t)bh * s.N * D;
-    auto dP = [&](int j) {   // warp-wide dV_l[i] . V[j]
-        float a = 0.0f;
+    const T* Vh = V + (size_t)bh * s.N * D;
+    for (int j0 = 0; j0 < s.N; j0 += kVrKeys) {
+        const int nk = min(kVrKeys, s.N - j0);
+        __syncthreads();   // row maxima ready; the previous chunk consumed
+        for (int u = tid; u < kVrKeys * NC; u += 256) {
+            const int r = u / NC, c4 = 4 * (u % NC);
+            *reinterpret_cast<float4*>(Vt + r * KS + c4) =
+                r < nk ? load4(Vh + (size_t)(j0 + r) * D + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
-        for (int u = 0; u < D / 32; ++u) a = fmaf(dvl_s[lane + 32 * u], to_f32(V[hoff + (size_t)j * D + lane + 32 * u]), a);
+        for (int v = 0; v < 8; ++v) {
+            const int key = wk + 8 * v;
+            float x = 0.0f;
+            if (wr < nr && key < nk) x = exp2f((Sh[(size_t)wr * s.N + j0 + key] - mx_s[wr]) * c);
+            Wt[wr * WS + key] = x;
+            den += x;
+        }
+        __syncthreads();
+        for (int key = 0; key < nk; ++key) {
+            const float4 vv = *reinterpret_cast<const float4*>(Vt + key * KS + 4 * tc);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-        return a;
-    };
-    float pdp = 0.0f;
-    for (int j = warp; j < s.N; j += 8) {
-        const float p = exp2f((row[j] * scale - mx) * kLog2e) * inv;
-        pdp = fmaf(p, dP(j), pdp);   // the same value in every lane
-    }
-    pdp = block_sum(lane == 0 ? pdp : 0.0f, false);
-    float acc[D / 32];
-#pragma unroll
-    for (int u = 0; u < D / 32; ++u) acc[u] = 0.0f;
-    for (int j = warp; j < s.N; j += 8) {
-        const float p = exp2f((row[j] * scale - mx) * kLog2e) * inv;
-        const float dr = p * (dP(j) - pdp) * scale;
-#pragma unroll
-        for (int u = 0; u < D / 32; ++u) {
-            const int f = lane + 32 * u;
-            atomicAdd(dV + hoff + (size_t)j * D + f, p * dvl_s[f]);
-            atomicAdd(dK + hoff + (size_t)j * D + f, dr * ql_s[f]);
-            acc[u] = fmaf(dr, to_f32(K[hoff + (size_t)j * D + f]), acc[u]);
+            for (int u = 0; u < RPT; ++u) {
+                const float x = Wt[(rg + RG * u) * WS + key];
+                acc[u][0] = fmaf(x, vv.x, acc[u][0]);
+                acc[u][1] = fmaf(x, vv.y, acc[u][1]);
+                acc[u][2] = fmaf(x, vv.z, acc[u][2]);
+                acc[u][3] = fmaf(x, vv.w, acc[u][3]);
+            }
         }
     }
 #pragma unroll
-    for (int u = 0; u < D / 32; ++u) part[warp][lane + 32 * u] = acc[u];
+    for (int o = 1; o < 8; o <<= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    if (wk == 0) den_s[wr] = den;
     __syncthreads();
-    for (int f = tid; f < D; f += 256) {
-        float t = 0.0f;
-        for (int u = 0; u < 8; ++u) t += part[u][f];
-        dQl[((size_t)bh * s.m + i) * D + f] += t;   // this block is the row's only writer here
+#pragma unroll
+    for (int u = 0; u < RPT; ++u) {
+        const int r = rg + RG * u;
+        if (r >= nr) continue;
+        const size_t o = ((size_t)bh * s.m + i0 + r) * D + 4 * tc;
+        const float rsum = den_s[r];
+        float y[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            y[b] = acc[u][b] / rsum;
+            Vl[o + b] = from_f32<T>(y[b]);
+        }
+        *reinterpret_cast<float4*>(Vl32 + o) = make_float4(y[0], y[1], y[2], y[3]);
+        if (tc == 0) {
+            stats[2 * ((size_t)bh * s.m + i0 + r)] = mx_s[r];
+            stats[2 * ((size_t)bh * s.m + i0 + r) + 1] = rsum;
+        }
     }
 }
 
-// Thread per (token, feature): dQ[t] += dQ_l[i] / |bin i| over the (at most
-// two per axis) bins that hold token t.
-__global__ void pool_bwd_kernel(Shape s, const float* __restrict__ dQl, float* __restrict__ dQ) {
-    const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+// Landmark-value backward, a block per (64-key tile, head); the block owns its
+// keys' rows of dK and dV.  With P = softmax(S / sqrt d) per landmark row
+// (max and sum from values_rows_kernel), per chunk of 32 landmarks:
+// dP = dV_l . V_tile^T, dR = P (dP - dV_l . V_l) / sqrt d (the row's
+// P . dP is dV_l . V_l), then dV_tile += P^T dV_l and dK_tile += dR^T Q_l in
+// 4 x 4 register tiles, and dQ_l += dR . K_tile by float4 atomics.  The tile's
+// dK, dV rows are added once at the end.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) values_bwd_tile_kernel(Shape s, const float* __restrict__ S,
+                                                              const float* __restrict__ stats,
+                                                              const float* __restrict__ Vl32,
+                                                              const T* __restrict__ K, const T* __restrict__ V,
+                                                              const T* __restrict__ Ql,
+                                                              const float* __restrict__ dVl, float* __restrict__ dK,
+                                                              float* __restrict__ dV, float* __restrict__ dQl) {
+    constexpr int KT = kVrKeys, RT = kVrRows, NC = D / 4, KS = D + 4, PS = KT + 8;
+    constexpr int TT = (KT / 4) * NC / 256;   // 4 x 4 gradient tiles per thread
+    constexpr int RG = 256 / NC, RPT = RT / RG;
+    extern __shared__ float4 vb_smem[];
+    float* Kt = reinterpret_cast<float*>(vb_smem);   // [KT][KS]
+    float* Vt = Kt + KT * KS;
+    float* Gl = Vt + KT * KS;   // [RT][KS] dV_l rows
+    float* Qc = Gl + RT * KS;   // [RT][KS] Q_l rows
+    float* Pt = Qc + RT * KS;   // [RT][PS]
+    float* Rt = Pt + RT * PS;   // [RT][PS]
+    float* Dr = Rt + RT * PS;   // [RT] dV_l . V_l
+    const int j0 = blockIdx.x * KT, bh = blockIdx.y, tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int nk = min(KT, s.N - j0);
+    const size_t hoff = (size_t)bh * s.N * D;
+    for (int u = tid; u < KT * NC; u += 256) {
+        const int r = u / NC, c4 = 4 * (u % NC);
+        const bool in = r < nk;
+        *reinterpret_cast<float4*>(Kt + r * KS + c4) =
+            in ? load4(K + hoff + (size_t)(j0 + r) * D + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(Vt + r * KS + c4) =
+            in ? load4(V + hoff + (size_t)(j0 + r) * D + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const float scale = rsqrtf((float)D), c = scale * kLog2e;
+    float gk[TT][4][4], gv[TT][4][4];
+#pragma unroll
+    for (int t = 0; t < TT; ++t)
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) gk[t][a][b] = gv[t][a][b] = 0.0f;
+    const int pr = tid >> 3, pk = tid & 7;     // P / dR entries: row pr, keys pk + 8 v
+    const int tc = tid % NC, rg = tid / NC;    // dQ_l rows rg + RG u, features 4 tc
+    for (int i0 = 0; i0 < s.m; i0 += RT) {
+        const int nr = min(RT, s.m - i0);
+        __syncthreads();   // tiles staged; the previous chunk consumed
+        for (int u = tid; u < RT * NC; u += 256) {
+            const int r = u / NC, c4 = 4 * (u % NC);
+            const size_t o = ((size_t)bh * s.m + i0 + r) * D + c4;
+            const bool in = r < nr;
+            *reinterpret_cast<float4*>(Gl + r * KS + c4) =
+                in ? *reinterpret_cast<const float4*>(dVl + o) : make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(Qc + r * KS + c4) = in ? load4(Ql + o) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        for (int r = w; r < RT; r += 8) {
+            float x = 0.0f;
+            if (r < nr) {
+                const size_t o = ((size_t)bh * s.m + i0 + r) * D;
+                for (int f = lane; f < D; f += 32) x = fmaf(dVl[o + f], Vl32[o + f], x);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+            if (lane == 0) Dr[r] = x;
+        }
+        __syncthreads();
+        {
+            float dp[8] = {};
+#pragma unroll 2
+            for (int f = 0; f < D; f += 4) {
+                const float4 g = *reinterpret_cast<const float4*>(Gl + pr * KS + f);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) dp[v] = dot4(g, *reinterpret_cast<const float4*>(Vt + (pk + 8 * v) * KS + f), dp[v]);
+            }
+            const bool row = pr < nr;
+            const size_t so = ((size_t)bh * s.m + i0 + pr);
+            const float mx = row ? stats[2 * so] : 0.0f, den = row ? stats[2 * so + 1] : 1.0f;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const int key = pk + 8 * v;
+                float p = 0.0f;
+                if (row && key < nk) p = exp2f((S[so * s.N + j0 + key] - mx) * c) / den;
+                Pt[pr * PS + key] = p;
+                Rt[pr * PS + key] = p * (dp[v] - Dr[pr]) * scale;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+            const int tile = tid + 256 * t, kg = tile / NC, fc = tile % NC;
+            for (int r = 0; r < nr; ++r) {
+                const float4 p4 = *reinterpret_cast<const float4*>(Pt + r * PS + 4 * kg);
+                const float4 d4 = *reinterpret_cast<const float4*>(Rt + r * PS + 4 * kg);
+                const float4 g4 = *reinterpret_cast<const float4*>(Gl + r * KS + 4 * fc);
+                const float4 q4 = *reinterpret_cast<const float4*>(Qc + r * KS + 4 * fc);
+                const float pp[4] = {p4.x, p4.y, p4.z, p4.w}, dd[4] = {d4.x, d4.y, d4.z, d4.w};
+                const float gg[4] = {g4.x, g4.y, g4.z, g4.w}, qq[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        gv[t][a][b] = fmaf(pp[a], gg[b], gv[t][a][b]);
+                        gk[t][a][b] = fmaf(dd[a], qq[b], gk[t][a][b]);
+                    }
+            }
+        }
+        {
+            float acc[RPT][4] = {};
+            for (int key = 0; key < nk; ++key) {
+                const float4 kv = *reinterpret_cast<const float4*>(Kt + key * KS + 4 * tc);
+#pragma unroll
+                for (int u = 0; u < RPT; ++u) {
+                    const float x = Rt[(rg + RG * u) * PS + key];
+                    acc[u][0] = fmaf(x, kv.x, acc[u][0]);
+                    acc[u][1] = fmaf(x, kv.y, acc[u][1]);
+                    acc[u][2] = fmaf(x, kv.z, acc[u][2]);
+                    acc[u][3] = fmaf(x, kv.w, acc[u][3]);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < RPT; ++u) {
+                const int r = rg + RG * u;
+                if (r < nr)
+                    atomicAdd(reinterpret_cast<float4*>(dQl + ((size_t)bh * s.m + i0 + r) * D + 4 * tc),
+                              make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]));
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+        const int tile = tid + 256 * t, kg = tile / NC, fc = tile % NC;
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const int key = 4 * kg + a;
+            if (key >= nk) continue;
+            const size_t o = hoff + (size_t)(j0 + key) * D + 4 * fc;
+            float4 k4 = *reinterpret_cast<float4*>(dK + o), v4 = *reinterpret_cast<float4*>(dV + o);
+            k4.x += gk[t][a][0]; k4.y += gk[t][a][1]; k4.z += gk[t][a][2]; k4.w += gk[t][a][3];
+            v4.x += gv[t][a][0]; v4.y += gv[t][a][1]; v4.z += gv[t][a][2]; v4.w += gv[t][a][3];
+            *reinterpret_cast<float4*>(dK + o) = k4;
+            *reinterpret_cast<float4*>(dV + o) = v4;
+        }
+    }
+}
+
+template <int D>
+constexpr size_t values_bwd_tile_bytes() {
+    return ((size_t)2 * kVrKeys * (D + 4) + 2 * kVrRows * (D + 4) + 2 * kVrRows * (kVrKeys + 8) + kVrRows) *
+           sizeof(float);
+}
+
+// Thread per (token, 4 features): dQ[t] += dQ_l[i] / |bin i| over the (at
+// most two per axis) bins that hold token t.
+template <int D>
+__global__ void __launch_bounds__(256) pool_bwd_kernel(Shape s, const float* __restrict__ dQl, float* __restrict__ dQ) {
+    constexpr int NC = D / 4;
+    const int e = blockIdx.x * 256 + threadIdx.x;
     const int bh = blockIdx.y;
-    if (e >= (size_t)s.N * s.d) return;
-    const int t = (int)(e / s.d), f = (int)(e % s.d), y = t / s.gw, x = t % s.gw;
-    float acc = 0.0f;
+    if (e >= s.N * NC) return;
+    const int t = e / NC, c4 = 4 * (e % NC), y = t / s.gw, x = t % s.gw;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     const int rc = y * s.ph / s.gh, cc = x * s.pw / s.gw;
     for (int r = max(0, rc - 1); r <= min(s.ph - 1, rc + 1); ++r) {
         int r0, r1;
@@ -968,10 +1133,15 @@ __global__ void pool_bwd_kernel(Shape s, const float* __restrict__ dQl, float* _
             int c0, c1;
             pool_bin(c, s.gw, s.pw, c0, c1);
             if (x < c0 || x >= c1) continue;
-            acc += dQl[((size_t)bh * s.m + r * s.pw + c) * s.d + f] / (float)((r1 - r0) * (c1 - c0));
+            const float n = (float)((r1 - r0) * (c1 - c0));
+            const float4 g = *reinterpret_cast<const float4*>(dQl + ((size_t)bh * s.m + r * s.pw + c) * D + c4);
+            acc.x += g.x / n; acc.y += g.y / n; acc.z += g.z / n; acc.w += g.w / n;
         }
     }
-    dQ[(size_t)bh * s.N * s.d + e] += acc;
+    float4* o = reinterpret_cast<float4*>(dQ + ((size_t)bh * s.N + t) * D + c4);
+    float4 q = *o;
+    q.x += acc.x; q.y += acc.y; q.z += acc.z; q.w += acc.w;
+    *o = q;
 }
 
 template <typename T, int D>
@@ -990,7 +1160,9 @@ static cudaError_t run_backward_t(mita_plan_s* p, const T* Q, const T* K, const 
     pool_kernel<T><<<dim3(s.m, BH), D, 0, st>>>(s, Q, Ql);
     scores_kernel<T><<<dim3((s.N + 127) / 128, (s.m + 31) / 32, BH), 256, 0, st>>>(s, Ql, K, p->S);
     topk_kernel<<<dim3(s.m, BH), kTopkThreads, 0, st>>>(s, p->S, p->idx);
-    values_kernel<T><<<dim3(s.m, BH), 256, 0, st>>>(s, p->S, V, Vl);
+    float* Vl32 = p->dVl + (size_t)BH * s.m * D;   // fp32 landmark values, then per-row {max S, sum w}
+    float* stats = Vl32 + (size_t)BH * s.m * D;
+    values_rows_kernel<T, D><<<dim3((s.m + kVrRows - 1) / kVrRows, BH), 256, 0, st>>>(s, p->S, V, Vl, Vl32, stats);
     route_kernel<T, D><<<dim3((s.N + 127) / 128, BH), 128, 0, st>>>(s, Q, Ql, p->route, 1, nullptr);
     const int L = s.m + s.k;
     const int shared = p->routing_only ? 0 : 1;
@@ -1023,8 +1195,11 @@ static cudaError_t run_backward_t(mita_plan_s* p, const T* Q, const T* K, const 
             s, Q, K, V, Ql, Vl, p->idx, p->route, dOut, dQ, dK, dV, p->dQl, p->dVl, shared, p->status);
         p->launches += 1;
     }
-    values_bwd_kernel<T, D><<<dim3(s.m, BH), 256, 0, st>>>(s, p->S, K, V, Ql, dK, dV, p->dQl, p->dVl);
-    pool_bwd_kernel<<<dim3((unsigned)(((size_t)s.N * D + 255) / 256), BH), 256, 0, st>>>(s, p->dQl, dQ);
+    const size_t vb_bytes = values_bwd_tile_bytes<D>();
+    ensure_smem_attr((const void*)values_bwd_tile_kernel<T, D>, (int)vb_bytes);
+    values_bwd_tile_kernel<T, D><<<dim3((s.N + kVrKeys - 1) / kVrKeys, BH), 256, vb_bytes, st>>>(
+        s, p->S, stats, Vl32, K, V, Ql, p->dVl, dK, dV, p->dQl);
+    pool_bwd_kernel<D><<<dim3((unsigned)((s.N * (D / 4) + 255) / 256), BH), 256, 0, st>>>(s, p->dQl, dQ);
     p->launches += 7;
     return cudaGetLastError();
 }
