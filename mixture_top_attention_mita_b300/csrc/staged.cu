@@ -5,12 +5,15 @@
 //   pool_kernel      step 1, landmark queries by adaptive average pooling
 //   scores_kernel    step 2, raw landmark scores S = Q_l . K^T (fp32, [m, N])
 //   topk_kernel      step 3, per-landmark radix select of the k best keys
+//                    (topk_warp_kernel: rows of up to 256 keys)
 //   values_kernel    step 4, landmark values V_l = softmax(S / sqrt d) . V
 //   route_kernel     step 5, first argmax of q . Q_l per query
 //   bucket_kernel    step 5, stable counting sort of the queries by route
 //   attend_kernel    step 6, one softmax over m shared + k routed keys
 // These kernels favour plain structure over speed; the fused and tensor-core
 // kernels handle the shapes they cover faster.
+#include <type_traits>
+
 #include "common.cuh"
 #include "staged.cuh"
 #include "host_cache.cuh"
@@ -191,6 +194,62 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(Shape s, const float
         taken += sel_tot;
         eq_seen += eq_tot;
     }
+}
+
+// Rows of up to kWarpTopkN keys: a warp per (landmark, head) with the row's
+// order keys in registers (key lane + 32 u).  The k-th largest order key T is
+// built bit by bit from the top (a warp-wide count of keys >= each
+// candidate); the expert is every key above T plus the lowest-index keys
+// equal to T, emitted in index order through ballots: the selection of
+// topk_kernel, without its block-wide passes.
+constexpr int kWarpTopkN = 256;
+
+__global__ void __launch_bounds__(256) topk_warp_kernel(Shape s, const float* __restrict__ S,
+                                                        int32_t* __restrict__ idx) {
+    constexpr int U = kWarpTopkN / 32;
+    const int lane = threadIdx.x & 31;
+    const int i = blockIdx.x * 8 + (threadIdx.x >> 5), bh = blockIdx.y;
+    if (i >= s.m) return;
+    const float* row = S + ((size_t)bh * s.m + i) * s.N;
+    uint32_t key[U];   // 0 marks a slot past the row (no finite score maps to 0)
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int j = lane + 32 * u;
+        key[u] = j < s.N ? order_key(row[j]) : 0u;
+    }
+    uint32_t T = 0;
+    for (int b = 31; b >= 0; --b) {
+        const uint32_t cand = T | (1u << b);
+        int c = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u) c += key[u] >= cand ? 1 : 0;
+        if (__reduce_add_sync(0xffffffffu, c) >= s.k) T = cand;
+    }
+    int gt = 0;
+#pragma unroll
+    for (int u = 0; u < U; ++u) gt += key[u] > T ? 1 : 0;
+    const int need = s.k - __reduce_add_sync(0xffffffffu, gt);
+    int32_t* out = idx + ((size_t)bh * s.m + i) * s.k;
+    const unsigned lt = (1u << lane) - 1u;
+    int taken = 0, eq_seen = 0;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const bool eq = key[u] == T;
+        const unsigned be = __ballot_sync(0xffffffffu, eq);
+        const bool sel = key[u] > T || (eq && eq_seen + __popc(be & lt) < need);
+        const unsigned bs = __ballot_sync(0xffffffffu, sel);
+        if (sel) out[taken + __popc(bs & lt)] = lane + 32 * u;
+        taken += __popc(bs);
+        eq_seen += __popc(be);
+    }
+}
+
+// The expert lists of all landmarks from S (topk_warp_kernel on short rows).
+static void launch_topk(const Shape& s, const float* S, int32_t* idx, cudaStream_t st) {
+    if (s.N <= kWarpTopkN)
+        topk_warp_kernel<<<dim3((s.m + 7) / 8, s.BH()), 256, 0, st>>>(s, S, idx);
+    else
+        topk_kernel<<<dim3(s.m, s.BH()), kTopkThreads, 0, st>>>(s, S, idx);
 }
 
 // ---------------------------------------------------------------- step 4
@@ -493,7 +552,7 @@ static cudaError_t run_staged_t(mita_plan_s* p, const T* Q, const T* K, const T*
     T* Vl = (T*)p->Vl;
     pool_kernel<T><<<dim3(s.m, BH), D, 0, st>>>(s, Q, Ql);
     scores_kernel<T><<<dim3((s.N + 127) / 128, (s.m + 31) / 32, BH), 256, 0, st>>>(s, Ql, K, p->S);
-    topk_kernel<<<dim3(s.m, BH), kTopkThreads, 0, st>>>(s, p->S, idx);
+    launch_topk(s, p->S, idx, st);
     values_kernel<T><<<dim3(s.m, BH), 256, 0, st>>>(s, p->S, V, Vl);
     // s > 1: each query's landmark list goes into the score buffer, free once
     // the landmark values are done (BH x N x s <= BH x m x N entries)
@@ -618,9 +677,10 @@ __global__ void __launch_bounds__(32 * kAttendWarps)
 }
 
 // Block of NW warps per (expert e, head): the queries routed to e, in bucket
-// order and in chunks of 4 NW, against the expert's m + k keys and values, which stay in
+// order and in chunks of QW NW, against the expert's m + k keys and values, which stay in
 // shared memory as fp32 for the whole block.  Per chunk: logits and dw =
-// dOut . v (lane per key, 4 queries per warp), the softmax and dlogit =
+// dOut . v (lane per key; warp w takes rows w, w + NW, ... so that a short
+// chunk still gives every warp a row), the softmax and dlogit =
 // w (dw - w . dw) in registers, the chunk's dQ rows (stored: a query has one
 // expert), and the key and value gradients of the chunk added to per-thread
 // 4 x 4 tiles.  Those are summed over all of e's queries on chip and leave
@@ -644,27 +704,26 @@ MITA_DEV float4 load4(const T* p) {
     }
 }
 
-template <int D, int NW>
-constexpr size_t expert_bwd_floats(int L, int LP) {
-    return 2 * (size_t)L * (D + 4) + 2 * (size_t)(4 * NW) * D + 2 * (size_t)(4 * NW) * LP;
+inline size_t expert_bwd_bytes(int D, int L, int LP, int QC) {
+    return (2 * (size_t)L * (D + 4) + 2 * (size_t)QC * D + 2 * (size_t)QC * LP) * sizeof(float);
 }
 
-template <typename T, int D, int JT, int NW>
-__global__ void __launch_bounds__(32 * NW)
+template <typename T, int D, int JT, int NW, int QW>
+__global__ void __launch_bounds__(32 * NW, NW == 8 ? 3 : 1)
     expert_bwd_kernel(Shape s, const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
                       const T* __restrict__ Ql, const T* __restrict__ Vl, const int32_t* __restrict__ idx,
                       const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm,
                       const T* __restrict__ dOut, float* __restrict__ dQ, float* __restrict__ dK,
                       float* __restrict__ dV, float* __restrict__ dQl, float* __restrict__ dVl, int shared,
                       int32_t* __restrict__ status) {
-    constexpr int kEbThreads = 32 * NW, kEbQ = 4 * NW;
+    constexpr int kEbThreads = 32 * NW, kEbQ = QW * NW;
     constexpr int KS = D + 4;                  // key / value row stride (floats)
     constexpr int LP = 32 * JT;                // padded slots
     constexpr int NC = D / 4;                  // float4 columns
     constexpr int RG = kEbThreads / NC;        // row groups of the tiles
     constexpr int QPT = kEbQ / RG;             // dQ rows per thread
     constexpr int TR = (LP / 4 + RG - 1) / RG; // 4-slot gradient tiles per thread
-    static_assert(kEbQ % RG == 0 && kEbQ == 4 * (kEbThreads / 32), "tile split");
+    static_assert(kEbQ % RG == 0 && kEbQ >= RG, "tile split");
     extern __shared__ float4 eb_smem[];
     __shared__ int32_t qid[kEbQ];
     __shared__ int32_t kid[LP];
@@ -733,21 +792,21 @@ __global__ void __launch_bounds__(32 * NW)
             *reinterpret_cast<float4*>(Gs + r * D + c) = g;
         }
         __syncthreads();
-        // logits and dw: warp w takes chunk rows 4w..4w+3, lane the slots lane + 32j
-        const int r0 = 4 * w;
-        if (r0 < nq) {
-            float a[4][JT], dw[4][JT];
+        // logits and dw: warp w takes chunk rows w + NW i (i < n), lane the slots lane + 32j
+        auto rows = [&](auto nc) {
+            constexpr int n = decltype(nc)::value;
+            float a[n][JT], dw[n][JT];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < n; ++i)
 #pragma unroll
                 for (int j = 0; j < JT; ++j) a[i][j] = dw[i][j] = 0.0f;
 #pragma unroll 1
             for (int f = 0; f < D; f += 4) {
-                float4 qv[4], g[4];
+                float4 qv[n], g[n];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    qv[i] = *reinterpret_cast<const float4*>(Qs + (r0 + i) * D + f);
-                    g[i] = *reinterpret_cast<const float4*>(Gs + (r0 + i) * D + f);
+                for (int i = 0; i < n; ++i) {
+                    qv[i] = *reinterpret_cast<const float4*>(Qs + (w + NW * i) * D + f);
+                    g[i] = *reinterpret_cast<const float4*>(Gs + (w + NW * i) * D + f);
                 }
 #pragma unroll
                 for (int j = 0; j < JT; ++j) {
@@ -755,14 +814,15 @@ __global__ void __launch_bounds__(32 * NW)
                     const float4 kv = *reinterpret_cast<const float4*>(Ks + t * KS + f);
                     const float4 vv = *reinterpret_cast<const float4*>(Vs + t * KS + f);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
+                    for (int i = 0; i < n; ++i) {
                         a[i][j] = dot4(qv[i], kv, a[i][j]);
                         dw[i][j] = dot4(g[i], vv, dw[i][j]);
                     }
                 }
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < n; ++i) {
+                const int r = w + NW * i;
                 float mx = -INFINITY;
 #pragma unroll
                 for (int j = 0; j < JT; ++j) {
@@ -792,10 +852,16 @@ __global__ void __launch_bounds__(32 * NW)
                 for (int o = 16; o > 0; o >>= 1) wdw += __shfl_xor_sync(0xffffffffu, wdw, o);
 #pragma unroll
                 for (int j = 0; j < JT; ++j) {
-                    Ws[(r0 + i) * LP + lane + 32 * j] = a[i][j];
-                    Cs[(r0 + i) * LP + lane + 32 * j] = a[i][j] * (dw[i][j] - wdw);
+                    Ws[r * LP + lane + 32 * j] = a[i][j];
+                    Cs[r * LP + lane + 32 * j] = a[i][j] * (dw[i][j] - wdw);
                 }
             }
+        };
+        {
+            const int nrow = w < nq ? min(QW, (nq - w + NW - 1) / NW) : 0;   // rows of this warp
+            if (nrow == 1) rows(std::integral_constant<int, 1>{});
+            else if (nrow == 2 || (QW == 2 && nrow > 0)) rows(std::integral_constant<int, 2>{});
+            else if (nrow > 2) rows(std::integral_constant<int, QW>{});
         }
         __syncthreads();
         // dQ rows rg + RG u: sum over slots of dlogit . key, 4 features per thread
@@ -1159,7 +1225,7 @@ static cudaError_t run_backward_t(mita_plan_s* p, const T* Q, const T* K, const 
     // the forward's landmarks, scores, experts, landmark values and routes
     pool_kernel<T><<<dim3(s.m, BH), D, 0, st>>>(s, Q, Ql);
     scores_kernel<T><<<dim3((s.N + 127) / 128, (s.m + 31) / 32, BH), 256, 0, st>>>(s, Ql, K, p->S);
-    topk_kernel<<<dim3(s.m, BH), kTopkThreads, 0, st>>>(s, p->S, p->idx);
+    launch_topk(s, p->S, p->idx, st);
     float* Vl32 = p->dVl + (size_t)BH * s.m * D;   // fp32 landmark values, then per-row {max S, sum w}
     float* stats = Vl32 + (size_t)BH * s.m * D;
     values_rows_kernel<T, D><<<dim3((s.m + kVrRows - 1) / kVrRows, BH), 256, 0, st>>>(s, p->S, V, Vl, Vl32, stats);
@@ -1168,10 +1234,10 @@ static cudaError_t run_backward_t(mita_plan_s* p, const T* Q, const T* K, const 
     const int shared = p->routing_only ? 0 : 1;
     // expert-major output softmax where the expert's slots fit (L <= 128 at
     // d = 64, L <= 64 at d = 128; 16 warps where a thread would otherwise hold
-    // more than 32 gradient accumulators); the warp-per-query kernel otherwise
-    auto expert_launch = [&](auto kern, int LP, int NW) -> bool {
-        const size_t bytes = (NW == 8 ? expert_bwd_floats<D, 8>(L, LP) : expert_bwd_floats<D, 16>(L, LP)) *
-                             sizeof(float);
+    // more than 32 gradient accumulators, 16-query chunks on 8 warps for the
+    // short experts of small images); the warp-per-query kernel otherwise
+    auto expert_launch = [&](auto kern, int LP, int NW, int QC) -> bool {
+        const size_t bytes = expert_bwd_bytes(D, L, LP, QC);
         if (bytes > 200 * 1024) return false;
         ensure_smem_attr((const void*)kern, (int)bytes);
         bucket_kernel<<<BH, 32, 0, st>>>(s, p->route, p->counts, p->offsets, p->perm, p->status);
@@ -1182,10 +1248,10 @@ static cudaError_t run_backward_t(mita_plan_s* p, const T* Q, const T* K, const 
     };
     bool done = false;
     if constexpr (D == 64) {
-        if (L <= 64) done = expert_launch(expert_bwd_kernel<T, D, 2, 8>, 64, 8);
-        else if (L <= 128) done = expert_launch(expert_bwd_kernel<T, D, 4, 16>, 128, 16);
+        if (L <= 64) done = expert_launch(expert_bwd_kernel<T, D, 2, 8, 2>, 64, 8, 16);
+        else if (L <= 128) done = expert_launch(expert_bwd_kernel<T, D, 4, 16, 4>, 128, 16, 64);
     } else {
-        if (L <= 64) done = expert_launch(expert_bwd_kernel<T, D, 2, 16>, 64, 16);
+        if (L <= 64) done = expert_launch(expert_bwd_kernel<T, D, 2, 16, 4>, 64, 16, 64);
     }
     if (!done) {
         const size_t smem = (size_t)kAttendWarps * (2 * D + 2 * L) * sizeof(float);
