@@ -18,6 +18,7 @@
 #include "staged.cuh"
 #include "host_cache.cuh"
 #include "launch.cuh"
+#include "mma_util.cuh"
 
 namespace mita {
 
@@ -740,6 +741,30 @@ __global__ void __launch_bounds__(32 * NW, NW == 8 ? 3 : 1)
     float* Cs = Ws + kEbQ * LP;        // [kEbQ][LP] logit gradients
     const size_t hoff = (size_t)bh * s.N * D;
     const int32_t* E = idx + ((size_t)bh * s.m + e) * s.k;
+    const int32_t* P = perm + (size_t)bh * s.N + beg;
+    // query ids of the chunk at c0, then its Q and dOut rows (after a barrier)
+    auto load_ids = [&](int c0) {
+        const int nq = min(kEbQ, cnt - c0);
+        if (tid < kEbQ) {
+            int q = tid < nq ? P[c0 + tid] : -1;
+            if (tid < nq && (q < 0 || q >= s.N)) { atomicExch(status, (int)MITA_ERR_DEVICE); q = -1; }
+            qid[tid] = q;
+        }
+    };
+    auto stage_rows = [&]() {
+        for (int u = tid; u < kEbQ * NC; u += kEbThreads) {
+            const int r = u / NC, c = 4 * (u % NC);
+            float4 qv = make_float4(0.f, 0.f, 0.f, 0.f), g = qv;
+            if (qid[r] >= 0) {
+                qv = load4(Q + hoff + (size_t)qid[r] * D + c);
+                g = load4(dOut + hoff + (size_t)qid[r] * D + c);
+            }
+            *reinterpret_cast<float4*>(Qs + r * D + c) = qv;
+            *reinterpret_cast<float4*>(Gs + r * D + c) = g;
+        }
+    };
+    // slot keys and the first chunk's ids in one round trip, then the slot
+    // rows and the first chunk's rows in another
     for (int t = tid; t < LP; t += kEbThreads) {
         int j = -1;
         if (t >= s.m && t < L) {
@@ -748,7 +773,8 @@ __global__ void __launch_bounds__(32 * NW, NW == 8 ? 3 : 1)
         }
         kid[t] = j;
     }
-    __syncthreads();
+    load_ids(0);
+    __syncthreads();   // ids ready
     for (int u = tid; u < L * NC; u += kEbThreads) {
         const int t = u / NC, c = 4 * (u % NC);
         float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
@@ -771,26 +797,9 @@ __global__ void __launch_bounds__(32 * NW, NW == 8 ? 3 : 1)
         for (int a = 0; a < 4; ++a)
 #pragma unroll
             for (int b = 0; b < 4; ++b) gk[r][a][b] = gv[r][a][b] = 0.0f;
-    const int32_t* P = perm + (size_t)bh * s.N + beg;
-    for (int c0 = 0; c0 < cnt; c0 += kEbQ) {
+    for (int c0 = 0;;) {
         const int nq = min(kEbQ, cnt - c0);
-        __syncthreads();   // the previous chunk's tiles are consumed
-        if (tid < kEbQ) {
-            int q = tid < nq ? P[c0 + tid] : -1;
-            if (tid < nq && (q < 0 || q >= s.N)) { atomicExch(status, (int)MITA_ERR_DEVICE); q = -1; }
-            qid[tid] = q;
-        }
-        __syncthreads();
-        for (int u = tid; u < kEbQ * NC; u += kEbThreads) {
-            const int r = u / NC, c = 4 * (u % NC);
-            float4 qv = make_float4(0.f, 0.f, 0.f, 0.f), g = qv;
-            if (qid[r] >= 0) {
-                qv = load4(Q + hoff + (size_t)qid[r] * D + c);
-                g = load4(dOut + hoff + (size_t)qid[r] * D + c);
-            }
-            *reinterpret_cast<float4*>(Qs + r * D + c) = qv;
-            *reinterpret_cast<float4*>(Gs + r * D + c) = g;
-        }
+        stage_rows();      // the first chunk's rows load with the slot rows
         __syncthreads();
         // logits and dw: warp w takes chunk rows w + NW i (i < n), lane the slots lane + 32j
         auto rows = [&](auto nc) {
@@ -914,6 +923,11 @@ __global__ void __launch_bounds__(32 * NW, NW == 8 ? 3 : 1)
                 }
             }
         }
+        c0 += kEbQ;
+        if (c0 >= cnt) break;
+        __syncthreads();   // the chunk's tiles are consumed
+        load_ids(c0);
+        __syncthreads();
     }
 #pragma unroll
     for (int r = 0; r < TR; ++r) {
@@ -939,6 +953,299 @@ __global__ void __launch_bounds__(32 * NW, NW == 8 ? 3 : 1)
                       make_float4(gv[r][a][0], gv[r][a][1], gv[r][a][2], gv[r][a][3]));
         }
     }
+}
+
+// expert_bwd_kernel for bf16 I/O at d = 64 with the five products on
+// mma.sync (m16n8k16, fp32 accumulation): logits = Q . K_slots^T and
+// dw = dOut . V_slots^T take the bf16 rows as they are (exact products);
+// dQ = C . K_slots, dK_slots = C^T . Q and dV_slots = W^T . dOut take the
+// fp32 weights W and logit gradients C as a bf16 pair hi + lo (about 16
+// mantissa bits).  The softmax between them runs per row on the fp32 logits
+// (lane per slot).  Tiles are bf16 rows with XOR-swizzled 16-byte chunks;
+// rows past the chunk's queries and slots past the expert are zero.  Chunks
+// hold QC queries; the slot gradients stay in registers (warp w: slot tile
+// w % (LP/16)) until one float2 atomic add per (slot, 2 features).
+template <int LP, int QC, int NW>
+__global__ void __launch_bounds__(32 * NW, NW == 8 ? 3 : 1)
+    expert_bwd_mma_kernel(Shape s, const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
+                          const __nv_bfloat16* __restrict__ V, const __nv_bfloat16* __restrict__ Ql,
+                          const __nv_bfloat16* __restrict__ Vl, const int32_t* __restrict__ idx,
+                          const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm,
+                          const __nv_bfloat16* __restrict__ dOut, float* __restrict__ dQ, float* __restrict__ dK,
+                          float* __restrict__ dV, float* __restrict__ dQl, float* __restrict__ dVl, int shared,
+                          int32_t* __restrict__ status) {
+    using namespace mx;
+    constexpr int D = 64, NT = 32 * NW;
+    constexpr int RBk = D * 2;    // bytes per row of the K, V, Q, dOut tiles
+    constexpr int RBc = LP * 2;   // bytes per row of the C and W tiles
+    constexpr int FS = LP + 8;    // fp32 row stride of the logit tiles
+    constexpr int MT1 = QC / 16, N1 = (LP / 8) / (NW / MT1);
+    constexpr int MTq = QC / 16, Nq = (D / 8) / (NW / MTq);
+    constexpr int MTk = LP / 16, Nk = (D / 8) / (NW / MTk);
+    static_assert(NW % MT1 == 0 && NW % MTk == 0 && N1 % 2 == 0 && Nq % 2 == 0 && Nk % 2 == 0, "warp split");
+    extern __shared__ __align__(128) uint8_t ebm_raw[];
+    uint8_t* Kb = ebm_raw;           // [LP][D]
+    uint8_t* Vb = Kb + LP * RBk;
+    uint8_t* Qb = Vb + LP * RBk;     // [QC][D]
+    uint8_t* Gb = Qb + QC * RBk;
+    uint8_t* Ch = Gb + QC * RBk;     // [QC][LP] C hi, C lo, W hi, W lo
+    uint8_t* Cl = Ch + QC * RBc;
+    uint8_t* Wh = Cl + QC * RBc;
+    uint8_t* Wl = Wh + QC * RBc;
+    float* Af = reinterpret_cast<float*>(Wl + QC * RBc);   // [QC][FS] logits
+    float* Df = Af + QC * FS;                              // [QC][FS] dw
+    __shared__ int32_t qid[QC];
+    __shared__ int32_t kid[LP];
+    const int e = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int L = s.m + s.k;
+    const int32_t* off = offsets + (size_t)bh * (s.m + 1);
+    const int beg = off[e], cnt = off[e + 1] - beg;
+    if (cnt <= 0) return;
+    const size_t hoff = (size_t)bh * s.N * D;
+    const int32_t* E = idx + ((size_t)bh * s.m + e) * s.k;
+    const int32_t* P = perm + (size_t)bh * s.N + beg;
+    auto load_ids = [&](int c0) {
+        const int nq = min(QC, cnt - c0);
+        if (tid < QC) {
+            int q = tid < nq ? P[c0 + tid] : -1;
+            if (tid < nq && (q < 0 || q >= s.N)) { atomicExch(status, (int)MITA_ERR_DEVICE); q = -1; }
+            qid[tid] = q;
+        }
+    };
+    auto stage_rows = [&]() {
+        for (int u = tid; u < QC * (D / 8); u += NT) {
+            const int r = u >> 3, c = u & 7, q = qid[r];
+            const size_t o = hoff + (size_t)(q >= 0 ? q : 0) * D + 8 * c;
+            cp_async16(smem_u32(Qb + swz<RBk>(r, c)), Q + o, q >= 0 ? 16u : 0u);
+            cp_async16(smem_u32(Gb + swz<RBk>(r, c)), dOut + o, q >= 0 ? 16u : 0u);
+        }
+        cp_async_commit();
+    };
+    for (int t = tid; t < LP; t += NT) {
+        int j = -1;
+        if (t >= s.m && t < L) {
+            j = E[t - s.m];
+            if (j < 0 || j >= s.N) { atomicExch(status, (int)MITA_ERR_DEVICE); j = -1; }
+        }
+        kid[t] = j;
+    }
+    load_ids(0);
+    __syncthreads();
+    for (int u = tid; u < LP * (D / 8); u += NT) {
+        const int t = u >> 3, c = u & 7;
+        const __nv_bfloat16 *sk = K + hoff, *sv = V + hoff;
+        uint32_t bytes = 0;
+        if (t < s.m) {
+            sk = Ql + ((size_t)bh * s.m + t) * D + 8 * c;
+            sv = Vl + ((size_t)bh * s.m + t) * D + 8 * c;
+            bytes = 16;
+        } else if (t < L && kid[t] >= 0) {
+            sk = K + hoff + (size_t)kid[t] * D + 8 * c;
+            sv = V + hoff + (size_t)kid[t] * D + 8 * c;
+            bytes = 16;
+        }
+        cp_async16(smem_u32(Kb + swz<RBk>(t, c)), sk, bytes);
+        cp_async16(smem_u32(Vb + swz<RBk>(t, c)), sv, bytes);
+    }
+    const float scale = rsqrtf((float)D);
+    const int g8 = lane >> 2, q2 = 2 * (lane & 3);
+    float kacc[Nk][4], vacc[Nk][4];
+#pragma unroll
+    for (int n = 0; n < Nk; ++n)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) kacc[n][v] = vacc[n][v] = 0.0f;
+    for (int c0 = 0;;) {
+        const int nq = min(QC, cnt - c0), nm = (nq + 15) >> 4;
+        stage_rows();   // the first chunk's rows load with the slot rows
+        cp_async_wait<0>();
+        __syncthreads();
+        // logits and dw: warp w takes row tile w % MT1 and N1 slot tiles
+        {
+            const int mt = w % MT1, n0 = (w / MT1) * N1;
+            if (mt < nm) {
+                float a[N1][4], g[N1][4];
+#pragma unroll
+                for (int n = 0; n < N1; ++n)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) a[n][v] = g[n][v] = 0.0f;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    uint32_t qa[4], ga[4];
+                    ldsm_x4(smem_u32(Qb + swz<RBk>(mt * 16 + (lane & 15), 2 * kk + (lane >> 4))), qa[0], qa[1], qa[2], qa[3]);
+                    ldsm_x4(smem_u32(Gb + swz<RBk>(mt * 16 + (lane & 15), 2 * kk + (lane >> 4))), ga[0], ga[1], ga[2], ga[3]);
+#pragma unroll
+                    for (int np = 0; np < N1; np += 2) {
+                        const int row = (n0 + np) * 8 + (lane & 7) + ((lane >> 4) << 3);
+                        const int ch = 2 * kk + ((lane >> 3) & 1);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(smem_u32(Kb + swz<RBk>(row, ch)), b0, b1, b2, b3);
+                        mma16816(a[np], qa[0], qa[1], qa[2], qa[3], b0, b1);
+                        mma16816(a[np + 1], qa[0], qa[1], qa[2], qa[3], b2, b3);
+                        ldsm_x4(smem_u32(Vb + swz<RBk>(row, ch)), b0, b1, b2, b3);
+                        mma16816(g[np], ga[0], ga[1], ga[2], ga[3], b0, b1);
+                        mma16816(g[np + 1], ga[0], ga[1], ga[2], ga[3], b2, b3);
+                    }
+                }
+#pragma unroll
+                for (int n = 0; n < N1; ++n) {
+                    const int col = (n0 + n) * 8 + q2, r0 = mt * 16 + g8;
+                    *reinterpret_cast<float2*>(Af + r0 * FS + col) = make_float2(a[n][0], a[n][1]);
+                    *reinterpret_cast<float2*>(Af + (r0 + 8) * FS + col) = make_float2(a[n][2], a[n][3]);
+                    *reinterpret_cast<float2*>(Df + r0 * FS + col) = make_float2(g[n][0], g[n][1]);
+                    *reinterpret_cast<float2*>(Df + (r0 + 8) * FS + col) = make_float2(g[n][2], g[n][3]);
+                }
+            }
+        }
+        __syncthreads();
+        // softmax per row (lane per slot); W and C leave as bf16 hi / lo pairs
+        for (int r = w; r < nm * 16; r += NW) {
+            constexpr int JT = LP / 32;
+            float x[JT], dw[JT];
+            const bool row = r < nq;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < JT; ++j) {
+                const int t = lane + 32 * j;
+                const bool live = row && t < L && (t >= s.m ? kid[t] >= 0 : shared != 0);
+                x[j] = live ? Af[r * FS + t] * scale : -INFINITY;
+                dw[j] = Df[r * FS + t];
+                mx = fmaxf(mx, x[j]);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            float den = 0.0f;
+#pragma unroll
+            for (int j = 0; j < JT; ++j) {
+                x[j] = row ? exp2f((x[j] - mx) * kLog2e) : 0.0f;
+                den += x[j];
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+            const float inv = row ? 1.0f / den : 0.0f;
+            float wdw = 0.0f;
+#pragma unroll
+            for (int j = 0; j < JT; ++j) {
+                x[j] *= inv;
+                wdw = fmaf(x[j], dw[j], wdw);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) wdw += __shfl_xor_sync(0xffffffffu, wdw, o);
+#pragma unroll
+            for (int j = 0; j < JT; ++j) {
+                const int t = lane + 32 * j;
+                const float c = x[j] * (dw[j] - wdw);
+                const uint32_t o = swz<RBc>(r, t >> 3) + 2 * (t & 7);
+                const __nv_bfloat16 wh = __float2bfloat16_rn(x[j]), chi = __float2bfloat16_rn(c);
+                *reinterpret_cast<__nv_bfloat16*>(Wh + o) = wh;
+                *reinterpret_cast<__nv_bfloat16*>(Wl + o) = __float2bfloat16_rn(x[j] - __bfloat162float(wh));
+                *reinterpret_cast<__nv_bfloat16*>(Ch + o) = chi;
+                *reinterpret_cast<__nv_bfloat16*>(Cl + o) = __float2bfloat16_rn(c - __bfloat162float(chi));
+            }
+        }
+        __syncthreads();
+        // dQ = C . K_slots: warp w takes row tile w % MTq and Nq feature tiles
+        {
+            const int mt = w % MTq, n0 = (w / MTq) * Nq;
+            if (mt < nm) {
+                float acc[Nq][4];
+#pragma unroll
+                for (int n = 0; n < Nq; ++n)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) acc[n][v] = 0.0f;
+#pragma unroll
+                for (int kk = 0; kk < LP / 16; ++kk) {
+                    uint32_t h[4], l[4];
+                    ldsm_x4(smem_u32(Ch + swz<RBc>(mt * 16 + (lane & 15), 2 * kk + (lane >> 4))), h[0], h[1], h[2], h[3]);
+                    ldsm_x4(smem_u32(Cl + swz<RBc>(mt * 16 + (lane & 15), 2 * kk + (lane >> 4))), l[0], l[1], l[2], l[3]);
+#pragma unroll
+                    for (int np = 0; np < Nq; np += 2) {
+                        const int krow = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(smem_u32(Kb + swz<RBk>(krow, n0 + np + (lane >> 4))), b0, b1, b2, b3);
+                        mma16816(acc[np], h[0], h[1], h[2], h[3], b0, b1);
+                        mma16816(acc[np], l[0], l[1], l[2], l[3], b0, b1);
+                        mma16816(acc[np + 1], h[0], h[1], h[2], h[3], b2, b3);
+                        mma16816(acc[np + 1], l[0], l[1], l[2], l[3], b2, b3);
+                    }
+                }
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int r = mt * 16 + g8 + 8 * hh;
+                    if (r < nq && qid[r] >= 0) {
+                        float* dst = dQ + hoff + (size_t)qid[r] * D;
+#pragma unroll
+                        for (int n = 0; n < Nq; ++n)
+                            *reinterpret_cast<float2*>(dst + (n0 + n) * 8 + q2) =
+                                make_float2(acc[n][2 * hh] * scale, acc[n][2 * hh + 1] * scale);
+                    }
+                }
+            }
+        }
+        // dK_slots += C^T . Q, dV_slots += W^T . dOut: warp w takes slot tile w % MTk
+        {
+            const int mt = w % MTk, n0 = (w / MTk) * Nk;
+            for (int kk = 0; kk < nm; ++kk) {
+                uint32_t ch4[4], cl4[4], wh4[4], wl4[4];
+                const int arow = kk * 16 + (lane & 7) + ((lane >> 4) << 3);
+                const int ach = 2 * mt + ((lane >> 3) & 1);
+                ldsm_x4_t(smem_u32(Ch + swz<RBc>(arow, ach)), ch4[0], ch4[1], ch4[2], ch4[3]);
+                ldsm_x4_t(smem_u32(Cl + swz<RBc>(arow, ach)), cl4[0], cl4[1], cl4[2], cl4[3]);
+                ldsm_x4_t(smem_u32(Wh + swz<RBc>(arow, ach)), wh4[0], wh4[1], wh4[2], wh4[3]);
+                ldsm_x4_t(smem_u32(Wl + swz<RBc>(arow, ach)), wl4[0], wl4[1], wl4[2], wl4[3]);
+#pragma unroll
+                for (int np = 0; np < Nk; np += 2) {
+                    const int brow = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                    const int bch = n0 + np + (lane >> 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(smem_u32(Qb + swz<RBk>(brow, bch)), b0, b1, b2, b3);
+                    mma16816(kacc[np], ch4[0], ch4[1], ch4[2], ch4[3], b0, b1);
+                    mma16816(kacc[np], cl4[0], cl4[1], cl4[2], cl4[3], b0, b1);
+                    mma16816(kacc[np + 1], ch4[0], ch4[1], ch4[2], ch4[3], b2, b3);
+                    mma16816(kacc[np + 1], cl4[0], cl4[1], cl4[2], cl4[3], b2, b3);
+                    ldsm_x4_t(smem_u32(Gb + swz<RBk>(brow, bch)), b0, b1, b2, b3);
+                    mma16816(vacc[np], wh4[0], wh4[1], wh4[2], wh4[3], b0, b1);
+                    mma16816(vacc[np], wl4[0], wl4[1], wl4[2], wl4[3], b0, b1);
+                    mma16816(vacc[np + 1], wh4[0], wh4[1], wh4[2], wh4[3], b2, b3);
+                    mma16816(vacc[np + 1], wl4[0], wl4[1], wl4[2], wl4[3], b2, b3);
+                }
+            }
+        }
+        c0 += QC;
+        if (c0 >= cnt) break;
+        __syncthreads();   // the chunk's tiles are consumed
+        load_ids(c0);
+        __syncthreads();
+    }
+    {
+        const int mt = w % MTk, n0 = (w / MTk) * Nk;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int t = mt * 16 + g8 + 8 * hh;
+            if (t >= L) continue;
+            float* rk;
+            float* rv;
+            if (t < s.m) {
+                if (!shared) continue;
+                rk = dQl + ((size_t)bh * s.m + t) * D;
+                rv = dVl + ((size_t)bh * s.m + t) * D;
+            } else {
+                if (kid[t] < 0) continue;
+                rk = dK + hoff + (size_t)kid[t] * D;
+                rv = dV + hoff + (size_t)kid[t] * D;
+            }
+#pragma unroll
+            for (int n = 0; n < Nk; ++n) {
+                const int col = (n0 + n) * 8 + q2;
+                atomicAdd(reinterpret_cast<float2*>(rk + col),
+                          make_float2(kacc[n][2 * hh] * scale, kacc[n][2 * hh + 1] * scale));
+                atomicAdd(reinterpret_cast<float2*>(rv + col), make_float2(vacc[n][2 * hh], vacc[n][2 * hh + 1]));
+            }
+        }
+    }
+}
+
+inline size_t expert_bwd_mma_bytes(int LP, int QC) {
+    return (size_t)2 * LP * 128 + (size_t)2 * QC * 128 + (size_t)4 * QC * LP * 2 + (size_t)2 * QC * (LP + 8) * 4;
 }
 
 // Landmark values again for the backward, a block per (32 landmarks, head):
@@ -1034,7 +1341,7 @@ __global__ void __launch_bounds__(256) values_rows_kernel(Shape s, const float* 
 // 4 x 4 register tiles, and dQ_l += dR . K_tile by float4 atomics.  The tile's
 // dK, dV rows are added once at the end.
 template <typename T, int D>
-__global__ void __launch_bounds__(256) values_bwd_tile_kernel(Shape s, const float* __restrict__ S,
+__global__ void __launch_bounds__(256, D == 64 ? 3 : 1) values_bwd_tile_kernel(Shape s, const float* __restrict__ S,
                                                               const float* __restrict__ stats,
                                                               const float* __restrict__ Vl32,
                                                               const T* __restrict__ K, const T* __restrict__ V,
@@ -1075,7 +1382,15 @@ __global__ void __launch_bounds__(256) values_bwd_tile_kernel(Shape s, const flo
     const int tc = tid % NC, rg = tid / NC;    // dQ_l rows rg + RG u, features 4 tc
     for (int i0 = 0; i0 < s.m; i0 += RT) {
         const int nr = min(RT, s.m - i0);
-        __syncthreads();   // tiles staged; the previous chunk consumed
+        if (i0 > 0) __syncthreads();   // the previous chunk consumed
+        // the chunk's scores go to Pt (turned into P in place below)
+        for (int u = tid; u < RT * KT; u += 256) {
+            const int r = u / KT, key = u % KT;
+            Pt[r * PS + key] = r < nr && key < nk ? S[((size_t)bh * s.m + i0 + r) * s.N + j0 + key] : 0.0f;
+        }
+        const bool row = pr < nr;
+        const size_t so = ((size_t)bh * s.m + i0 + pr);
+        const float mx = row ? stats[2 * so] : 0.0f, den = row ? stats[2 * so + 1] : 1.0f;
         for (int u = tid; u < RT * NC; u += 256) {
             const int r = u / NC, c4 = 4 * (u % NC);
             const size_t o = ((size_t)bh * s.m + i0 + r) * D + c4;
@@ -1103,14 +1418,11 @@ __global__ void __launch_bounds__(256) values_bwd_tile_kernel(Shape s, const flo
 #pragma unroll
                 for (int v = 0; v < 8; ++v) dp[v] = dot4(g, *reinterpret_cast<const float4*>(Vt + (pk + 8 * v) * KS + f), dp[v]);
             }
-            const bool row = pr < nr;
-            const size_t so = ((size_t)bh * s.m + i0 + pr);
-            const float mx = row ? stats[2 * so] : 0.0f, den = row ? stats[2 * so + 1] : 1.0f;
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
                 const int key = pk + 8 * v;
                 float p = 0.0f;
-                if (row && key < nk) p = exp2f((S[so * s.N + j0 + key] - mx) * c) / den;
+                if (row && key < nk) p = exp2f((Pt[pr * PS + key] - mx) * c) / den;
                 Pt[pr * PS + key] = p;
                 Rt[pr * PS + key] = p * (dp[v] - Dr[pr]) * scale;
             }
@@ -1181,25 +1493,34 @@ constexpr size_t values_bwd_tile_bytes() {
 }
 
 // Thread per (token, 4 features): dQ[t] += dQ_l[i] / |bin i| over the (at
-// most two per axis) bins that hold token t.
+// most two per axis) bins that hold token t.  Each block first tabulates the
+// bins' row and column ranges in shared memory (ph + pw <= 2048 entries).
+constexpr int kPoolBwdTab = 2048;
+
 template <int D>
 __global__ void __launch_bounds__(256) pool_bwd_kernel(Shape s, const float* __restrict__ dQl, float* __restrict__ dQ) {
     constexpr int NC = D / 4;
+    __shared__ int2 rng[kPoolBwdTab];   // rows [0, ph), then columns [ph, ph + pw)
+    for (int u = threadIdx.x; u < s.ph + s.pw; u += 256) {
+        int lo, hi;
+        if (u < s.ph) pool_bin(u, s.gh, s.ph, lo, hi);
+        else pool_bin(u - s.ph, s.gw, s.pw, lo, hi);
+        rng[u] = make_int2(lo, hi);
+    }
+    __syncthreads();
     const int e = blockIdx.x * 256 + threadIdx.x;
     const int bh = blockIdx.y;
     if (e >= s.N * NC) return;
-    const int t = e / NC, c4 = 4 * (e % NC), y = t / s.gw, x = t % s.gw;
+    const int t = e / NC, c4 = 4 * (e % NC), y = t / s.gw, x = t - y * s.gw;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     const int rc = y * s.ph / s.gh, cc = x * s.pw / s.gw;
     for (int r = max(0, rc - 1); r <= min(s.ph - 1, rc + 1); ++r) {
-        int r0, r1;
-        pool_bin(r, s.gh, s.ph, r0, r1);
-        if (y < r0 || y >= r1) continue;
+        const int2 rr = rng[r];
+        if (y < rr.x || y >= rr.y) continue;
         for (int c = max(0, cc - 1); c <= min(s.pw - 1, cc + 1); ++c) {
-            int c0, c1;
-            pool_bin(c, s.gw, s.pw, c0, c1);
-            if (x < c0 || x >= c1) continue;
-            const float n = (float)((r1 - r0) * (c1 - c0));
+            const int2 cr = rng[s.ph + c];
+            if (x < cr.x || x >= cr.y) continue;
+            const float n = (float)((rr.y - rr.x) * (cr.y - cr.x));
             const float4 g = *reinterpret_cast<const float4*>(dQl + ((size_t)bh * s.m + r * s.pw + c) * D + c4);
             acc.x += g.x / n; acc.y += g.y / n; acc.z += g.z / n; acc.w += g.w / n;
         }
@@ -1247,7 +1568,19 @@ static cudaError_t run_backward_t(mita_plan_s* p, const T* Q, const T* K, const 
         return true;
     };
     bool done = false;
-    if constexpr (D == 64) {
+    if constexpr (D == 64 && std::is_same<T, __nv_bfloat16>::value) {
+        auto mma_launch = [&](auto kern, int LP, int QC, int NW) {
+            const size_t bytes = expert_bwd_mma_bytes(LP, QC);
+            ensure_smem_attr((const void*)kern, (int)bytes);
+            bucket_kernel<<<BH, 32, 0, st>>>(s, p->route, p->counts, p->offsets, p->perm, p->status);
+            kern<<<dim3(s.m, BH), 32 * NW, bytes, st>>>(s, Q, K, V, Ql, Vl, p->idx, p->offsets, p->perm, dOut, dQ,
+                                                         dK, dV, p->dQl, p->dVl, shared, p->status);
+            p->launches += 2;
+            return true;
+        };
+        if (L <= 64) done = mma_launch(expert_bwd_mma_kernel<64, 32, 8>, 64, 32, 8);
+        else if (L <= 128) done = mma_launch(expert_bwd_mma_kernel<128, 64, 16>, 128, 64, 16);
+    } else if constexpr (D == 64) {
         if (L <= 64) done = expert_launch(expert_bwd_kernel<T, D, 2, 8, 2>, 64, 8, 16);
         else if (L <= 128) done = expert_launch(expert_bwd_kernel<T, D, 4, 16, 4>, 128, 16, 64);
     } else {

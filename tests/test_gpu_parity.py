@@ -139,8 +139,10 @@ BWD = {
     "tiny_f32": W["tiny_f32"],
     "hires_small": W["hires56"].scaled(B=1, H=1, N=1024, gh=32, gw=32, ph=4, pw=4, m=16, k=48),
     "long_small": W["long1d"].scaled(B=1, H=1, N=2048, gw=2048, pw=16, m=16, k=64),
-    # expert-major kernel instances: 113 slots at d = 64, 48 slots at d = 128
+    # expert-major kernel instances: 113 slots at d = 64 (tensor-core bf16
+    # and SIMT fp32), 48 slots at d = 128
     "hires56_heads": W["hires56"].scaled(B=1, H=2),
+    "hires56_f32": W["hires56"].scaled(B=1, H=2, dtype="f32"),
     "long_k32": W["long1d"].scaled(B=1, H=1, N=2048, gw=2048, pw=16, m=16, k=32),
 }
 
