@@ -12,6 +12,7 @@
 //   attend_kernel    step 6, one softmax over m shared + k routed keys
 // These kernels favour plain structure over speed; the fused and tensor-core
 // kernels handle the shapes they cover faster.
+#include <algorithm>
 #include <type_traits>
 
 #include "common.cuh"
@@ -426,6 +427,88 @@ __global__ void bucket_kernel(Shape s, const int32_t* __restrict__ route, int32_
     for (int i = lane; i < s.m; i += 32) cnt[i] = off[i + 1] - off[i];
 }
 
+// Longer rows, m <= kBucketMaxM: a block of 32 warps per head, warp w taking
+// the queries of its contiguous segment.  Per-(bucket, warp) counts, one
+// block-wide exclusive scan over them in (bucket, warp) order, then each warp
+// places its segment again: the same stable listing as bucket_kernel.
+constexpr int kBucketMaxM = 256;
+
+__global__ void __launch_bounds__(1024) bucket_block_kernel(Shape s, const int32_t* __restrict__ route,
+                                                            int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                            int32_t* __restrict__ perm, int32_t* __restrict__ status) {
+    __shared__ int wc[kBucketMaxM * 32];   // [bucket][warp]: counts, then cursors
+    __shared__ int warp_sums[32];
+    const int bh = blockIdx.x, tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int32_t* r = route + (size_t)bh * s.N;
+    int32_t* cnt = counts + (size_t)bh * s.m;
+    int32_t* off = offsets + (size_t)bh * (s.m + 1);
+    int32_t* p = perm + (size_t)bh * s.N;
+    const int seg = (s.N + 1023) / 1024 * 32;   // queries per warp, whole 32-query steps
+    const int q_beg = w * seg, q_end = min(s.N, q_beg + seg);
+    for (int u = tid; u < s.m * 32; u += 1024) wc[u] = 0;
+    __syncthreads();
+    for (int q0 = q_beg; q0 < q_end; q0 += 32) {
+        const int q = q0 + lane;
+        const int b = q < q_end ? r[q] : -1;
+        const bool ok = b >= 0 && b < s.m;
+        if (q < q_end && !ok) atomicExch(status, (int)MITA_ERR_DEVICE);
+        const unsigned peers = __match_any_sync(0xffffffffu, ok ? b : -1);
+        if (ok && lane == __ffs(peers) - 1) wc[b * 32 + w] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int b = tid; b < s.m; b += 1024) {
+        int c = 0;
+        for (int x = 0; x < 32; ++x) c += wc[b * 32 + x];
+        cnt[b] = c;
+    }
+    const int E = (s.m * 32 + 1023) / 1024;   // entries per thread, <= 8
+    int loc[8], sum = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int u = tid * E + j;
+        loc[j] = j < E && u < s.m * 32 ? wc[u] : 0;
+        sum += loc[j];
+    }
+    int total;
+    int run = block_exclusive_scan<1024>(sum, warp_sums, &total);   // its barriers order the reads above
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int u = tid * E + j;
+        if (j < E && u < s.m * 32) {
+            wc[u] = run;
+            run += loc[j];
+        }
+    }
+    __syncthreads();
+    for (int b = tid; b < s.m; b += 1024) off[b] = wc[b * 32];
+    if (tid == 0) off[s.m] = total;
+    for (int q0 = q_beg; q0 < q_end; q0 += 32) {
+        const int q = q0 + lane;
+        const int b = q < q_end ? r[q] : -1;
+        const bool ok = b >= 0 && b < s.m;
+        const unsigned peers = __match_any_sync(0xffffffffu, ok ? b : -1);
+        const unsigned lower = peers & ((1u << lane) - 1u);
+        const int leader = __ffs(peers) - 1;
+        int base = 0;
+        if (ok && lane == leader) {
+            base = wc[b * 32 + w];
+            wc[b * 32 + w] = base + __popc(peers);
+        }
+        base = __shfl_sync(peers, base, leader);
+        if (ok) p[base + __popc(lower)] = q;
+        __syncwarp();
+    }
+}
+
+static void launch_bucket(const Shape& s, const int32_t* route, int32_t* counts, int32_t* offsets, int32_t* perm,
+                          int32_t* status, cudaStream_t st) {
+    if (s.N >= 2048 && s.m <= kBucketMaxM)
+        bucket_block_kernel<<<s.BH(), 1024, 0, st>>>(s, route, counts, offsets, perm, status);
+    else
+        bucket_kernel<<<s.BH(), 32, 0, st>>>(s, route, counts, offsets, perm, status);
+}
+
 // ---------------------------------------------------------------- step 6
 // One warp per query, queries taken in bucket order so that neighbouring
 // warps share an expert.  Lane t computes logits t, t+32, ... of the m + k
@@ -560,7 +643,7 @@ static cudaError_t run_staged_t(mita_plan_s* p, const T* Q, const T* K, const T*
     const int ns = p->routes_s > 1 ? p->routes_s : 1;
     int32_t* tops = (int32_t*)p->S;
     route_kernel<T, D><<<dim3((s.N + 127) / 128, BH), 128, 0, st>>>(s, Q, Ql, route, ns, tops);
-    bucket_kernel<<<BH, 32, 0, st>>>(s, route, p->counts, p->offsets, p->perm, p->status);
+    launch_bucket(s, route, p->counts, p->offsets, p->perm, p->status, st);
     const size_t smem = staged_attend_smem(s, ns);
     if (smem > 227 * 1024) return cudaErrorInvalidValue;
     ensure_smem_attr((const void*)attend_kernel<T, D>, (int)smem);
@@ -1248,17 +1331,20 @@ inline size_t expert_bwd_mma_bytes(int LP, int QC) {
     return (size_t)2 * LP * 128 + (size_t)2 * QC * 128 + (size_t)4 * QC * LP * 2 + (size_t)2 * QC * (LP + 8) * 4;
 }
 
-// Landmark values again for the backward, a block per (32 landmarks, head):
-// row maxima of S, then 64-key chunks of V staged once in shared memory for
-// all 32 rows, weights w = exp((S - max) / sqrt d) and their sums.  Writes
-// V_l in the I/O type (as the forward uses it), V_l in fp32 and per row
-// {max S, sum w} for values_bwd_tile_kernel.
+// Landmark values again for the backward, a block per (32 landmarks, head,
+// key split): row maxima of S over the split's keys, then 64-key chunks of V
+// staged once in shared memory for all 32 rows, weights
+// w = exp((S - max) / sqrt d) and their sums.  One split writes V_l in the
+// I/O type (as the forward uses it), V_l in fp32 and per row {max S, sum w}
+// for values_bwd_tile_kernel; several write {sums, sum w, max} per split to
+// `part` for values_rows_fin_kernel.
 constexpr int kVrRows = 32, kVrKeys = 64;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(256) values_rows_kernel(Shape s, const float* __restrict__ S,
                                                           const T* __restrict__ V, T* __restrict__ Vl,
-                                                          float* __restrict__ Vl32, float* __restrict__ stats) {
+                                                          float* __restrict__ Vl32, float* __restrict__ stats,
+                                                          int ksplit, float* __restrict__ part) {
     constexpr int NC = D / 4, KS = D + 4, WS = kVrKeys + 1;
     constexpr int RG = 256 / NC, RPT = kVrRows / RG;
     __shared__ __align__(16) float Vt[kVrKeys * KS];
@@ -1266,11 +1352,13 @@ __global__ void __launch_bounds__(256) values_rows_kernel(Shape s, const float* 
     __shared__ float mx_s[kVrRows], den_s[kVrRows];
     const int i0 = blockIdx.x * kVrRows, bh = blockIdx.y, tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int nr = min(kVrRows, s.m - i0);
+    const int cps = ((s.N + kVrKeys - 1) / kVrKeys + ksplit - 1) / ksplit;   // chunks per split
+    const int k_lo = blockIdx.z * cps * kVrKeys, k_hi = min(s.N, k_lo + cps * kVrKeys);
     const float* Sh = S + ((size_t)bh * s.m + i0) * s.N;
     for (int r = w; r < kVrRows; r += 8) {
         float mx = -INFINITY;
         if (r < nr)
-            for (int j = lane; j < s.N; j += 32) mx = fmaxf(mx, Sh[(size_t)r * s.N + j]);
+            for (int j = k_lo + lane; j < k_hi; j += 32) mx = fmaxf(mx, Sh[(size_t)r * s.N + j]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         if (lane == 0) mx_s[r] = mx;
@@ -1280,8 +1368,8 @@ __global__ void __launch_bounds__(256) values_rows_kernel(Shape s, const float* 
     float acc[RPT][4] = {};
     float den = 0.0f;
     const T* Vh = V + (size_t)bh * s.N * D;
-    for (int j0 = 0; j0 < s.N; j0 += kVrKeys) {
-        const int nk = min(kVrKeys, s.N - j0);
+    for (int j0 = k_lo; j0 < k_hi; j0 += kVrKeys) {
+        const int nk = min(kVrKeys, k_hi - j0);
         __syncthreads();   // row maxima ready; the previous chunk consumed
         for (int u = tid; u < kVrKeys * NC; u += 256) {
             const int r = u / NC, c4 = 4 * (u % NC);
@@ -1313,6 +1401,21 @@ __global__ void __launch_bounds__(256) values_rows_kernel(Shape s, const float* 
     for (int o = 1; o < 8; o <<= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     if (wk == 0) den_s[wr] = den;
     __syncthreads();
+    if (ksplit > 1) {
+#pragma unroll
+        for (int u = 0; u < RPT; ++u) {
+            const int r = rg + RG * u;
+            if (r >= nr) continue;
+            float* pr = part + (((size_t)bh * s.m + i0 + r) * ksplit + blockIdx.z) * (D + 2);
+            *reinterpret_cast<float2*>(pr + 4 * tc) = make_float2(acc[u][0], acc[u][1]);
+            *reinterpret_cast<float2*>(pr + 4 * tc + 2) = make_float2(acc[u][2], acc[u][3]);
+            if (tc == 0) {
+                pr[D] = den_s[r];
+                pr[D + 1] = mx_s[r];
+            }
+        }
+        return;
+    }
 #pragma unroll
     for (int u = 0; u < RPT; ++u) {
         const int r = rg + RG * u;
@@ -1330,6 +1433,43 @@ __global__ void __launch_bounds__(256) values_rows_kernel(Shape s, const float* 
             stats[2 * ((size_t)bh * s.m + i0 + r)] = mx_s[r];
             stats[2 * ((size_t)bh * s.m + i0 + r) + 1] = rsum;
         }
+    }
+}
+
+// Combines values_rows_kernel's key splits: thread per (landmark row, 4
+// features); the splits' sums are rescaled to the row's largest max.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) values_rows_fin_kernel(Shape s, int ksplit, const float* __restrict__ part,
+                                                              T* __restrict__ Vl, float* __restrict__ Vl32,
+                                                              float* __restrict__ stats) {
+    constexpr int NC = D / 4;
+    const size_t e = (size_t)blockIdx.x * 256 + threadIdx.x;
+    if (e >= (size_t)s.BH() * s.m * NC) return;
+    const size_t row = e / NC;
+    const int tc = (int)(e % NC);
+    const float* pr = part + row * ksplit * (D + 2);
+    const float c = rsqrtf((float)D) * kLog2e;
+    float M = -INFINITY;
+    for (int z = 0; z < ksplit; ++z) M = fmaxf(M, pr[z * (D + 2) + D + 1]);
+    float den = 0.0f, a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int z = 0; z < ksplit; ++z) {
+        const float* q = pr + z * (D + 2);
+        const float f = exp2f((q[D + 1] - M) * c);
+        den = fmaf(q[D], f, den);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) a[b] = fmaf(q[4 * tc + b], f, a[b]);
+    }
+    const size_t o = row * D + 4 * tc;
+    float y[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        y[b] = a[b] / den;
+        Vl[o + b] = from_f32<T>(y[b]);
+    }
+    *reinterpret_cast<float4*>(Vl32 + o) = make_float4(y[0], y[1], y[2], y[3]);
+    if (tc == 0) {
+        stats[2 * row] = M;
+        stats[2 * row + 1] = den;
     }
 }
 
@@ -1540,8 +1680,6 @@ static cudaError_t run_backward_t(mita_plan_s* p, const T* Q, const T* K, const 
     T* Vl = (T*)p->Vl;
     const size_t nbytes = (size_t)BH * s.N * D * sizeof(float);
     cudaError_t e;
-    if ((e = cudaMemsetAsync(dK, 0, nbytes, st)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(dV, 0, nbytes, st)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(p->dQl, 0, (size_t)2 * BH * s.m * D * sizeof(float), st)) != cudaSuccess) return e;
     // the forward's landmarks, scores, experts, landmark values and routes
     pool_kernel<T><<<dim3(s.m, BH), D, 0, st>>>(s, Q, Ql);
@@ -1549,8 +1687,23 @@ static cudaError_t run_backward_t(mita_plan_s* p, const T* Q, const T* K, const 
     launch_topk(s, p->S, p->idx, st);
     float* Vl32 = p->dVl + (size_t)BH * s.m * D;   // fp32 landmark values, then per-row {max S, sum w}
     float* stats = Vl32 + (size_t)BH * s.m * D;
-    values_rows_kernel<T, D><<<dim3((s.m + kVrRows - 1) / kVrRows, BH), 256, 0, st>>>(s, p->S, V, Vl, Vl32, stats);
+    // key splits when the row tiles alone fill fewer than two blocks per SM; their
+    // partial sums use dK as scratch before it is cleared
+    const int row_tiles = (s.m + kVrRows - 1) / kVrRows;
+    int ksplit = 1;
+    if ((size_t)row_tiles * BH < 296) {
+        ksplit = std::min(8, (s.N + 511) / 512);
+        while (ksplit > 1 && (size_t)s.m * ksplit * (D + 2) > (size_t)s.N * D) --ksplit;
+    }
+    values_rows_kernel<T, D><<<dim3(row_tiles, BH, ksplit), 256, 0, st>>>(s, p->S, V, Vl, Vl32, stats, ksplit, dK);
+    if (ksplit > 1) {
+        values_rows_fin_kernel<T, D><<<(unsigned)(((size_t)BH * s.m * (D / 4) + 255) / 256), 256, 0, st>>>(
+            s, ksplit, dK, Vl, Vl32, stats);
+        p->launches += 1;
+    }
     route_kernel<T, D><<<dim3((s.N + 127) / 128, BH), 128, 0, st>>>(s, Q, Ql, p->route, 1, nullptr);
+    if ((e = cudaMemsetAsync(dK, 0, nbytes, st)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(dV, 0, nbytes, st)) != cudaSuccess) return e;
     const int L = s.m + s.k;
     const int shared = p->routing_only ? 0 : 1;
     // expert-major output softmax where the expert's slots fit (L <= 128 at
@@ -1561,7 +1714,7 @@ static cudaError_t run_backward_t(mita_plan_s* p, const T* Q, const T* K, const 
         const size_t bytes = expert_bwd_bytes(D, L, LP, QC);
         if (bytes > 200 * 1024) return false;
         ensure_smem_attr((const void*)kern, (int)bytes);
-        bucket_kernel<<<BH, 32, 0, st>>>(s, p->route, p->counts, p->offsets, p->perm, p->status);
+        launch_bucket(s, p->route, p->counts, p->offsets, p->perm, p->status, st);
         kern<<<dim3(s.m, BH), 32 * NW, bytes, st>>>(s, Q, K, V, Ql, Vl, p->idx, p->offsets, p->perm, dOut, dQ,
                                                        dK, dV, p->dQl, p->dVl, shared, p->status);
         p->launches += 2;
@@ -1572,7 +1725,7 @@ static cudaError_t run_backward_t(mita_plan_s* p, const T* Q, const T* K, const 
         auto mma_launch = [&](auto kern, int LP, int QC, int NW) {
             const size_t bytes = expert_bwd_mma_bytes(LP, QC);
             ensure_smem_attr((const void*)kern, (int)bytes);
-            bucket_kernel<<<BH, 32, 0, st>>>(s, p->route, p->counts, p->offsets, p->perm, p->status);
+            launch_bucket(s, p->route, p->counts, p->offsets, p->perm, p->status, st);
             kern<<<dim3(s.m, BH), 32 * NW, bytes, st>>>(s, Q, K, V, Ql, Vl, p->idx, p->offsets, p->perm, dOut, dQ,
                                                          dK, dV, p->dQl, p->dVl, shared, p->status);
             p->launches += 2;
