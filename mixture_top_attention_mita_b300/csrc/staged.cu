@@ -509,12 +509,53 @@ static void launch_bucket(const Shape& s, const int32_t* route, int32_t* counts,
         bucket_kernel<<<s.BH(), 32, 0, st>>>(s, route, counts, offsets, perm, status);
 }
 
+// Small vector helpers: a 4-term fused dot product and 4 elements of a row as
+// fp32 (a bf16 is the upper half of the fp32 with the same value).
+MITA_DEV float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+MITA_DEV float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+MITA_DEV float dot4(float4 a, float4 b, float acc) {
+    return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, fmaf(a.x, b.x, acc))));
+}
+
+template <typename T>
+MITA_DEV float4 load4(const T* p) {
+    if constexpr (sizeof(T) == 4) {
+        return *reinterpret_cast<const float4*>(p);
+    } else {
+        const uint2 u = *reinterpret_cast<const uint2*>(p);
+        return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+    }
+}
+
 // ---------------------------------------------------------------- step 6
 // One warp per query, queries taken in bucket order so that neighbouring
-// warps share an expert.  Lane t computes logits t, t+32, ... of the m + k
-// concatenated keys; the softmax is exact (max, exp, sum) in fp32; lane f
-// accumulates output features f, f+32, ...
+// warps share an expert.  The query's slots (m shared, then the k keys of
+// each of its ns experts) are listed in shared memory first: the landmark or
+// key row of each, or -1 for a slot without weight (routing only, or a key
+// an earlier expert of the query already holds, found by binary search in
+// that expert's ascending list).  Logits and the output then take 4 slots per
+// step, 8 lanes per slot, each lane D/8 features of the row (16-byte loads);
+// the softmax is exact (max, exp, sum) in fp32.
 constexpr int kAttendWarps = 4;
+
+template <typename T, int F>
+MITA_DEV void load_feats(const T* p, float (&v)[F]) {   // F consecutive elements, 16-byte aligned
+    if constexpr (sizeof(T) == 2) {
+#pragma unroll
+        for (int i = 0; i < F; i += 8) {
+            const uint4 u = *reinterpret_cast<const uint4*>(p + i);
+            v[i] = bf16_lo(u.x); v[i + 1] = bf16_hi(u.x); v[i + 2] = bf16_lo(u.y); v[i + 3] = bf16_hi(u.y);
+            v[i + 4] = bf16_lo(u.z); v[i + 5] = bf16_hi(u.z); v[i + 6] = bf16_lo(u.w); v[i + 7] = bf16_hi(u.w);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < F; i += 4) {
+            const float4 x = load4(p + i);
+            v[i] = x.x; v[i + 1] = x.y; v[i + 2] = x.z; v[i + 3] = x.w;
+        }
+    }
+}
 
 template <typename T, int D>
 __global__ void __launch_bounds__(32 * kAttendWarps)
@@ -522,11 +563,13 @@ __global__ void __launch_bounds__(32 * kAttendWarps)
                   const T* __restrict__ Ql, const T* __restrict__ Vl, const int32_t* __restrict__ idx,
                   const int32_t* __restrict__ route, const int32_t* __restrict__ perm, T* __restrict__ out,
                   int shared, int ns, const int32_t* __restrict__ tops, int32_t* __restrict__ status) {
+    constexpr int FPL = D / 8;   // features per lane
     extern __shared__ float smem[];
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ int r_s[kAttendWarps][kMaxRoutes];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, grp = lane >> 3, sub = lane & 7;
     const int L = s.m + ns * s.k;   // shared slots, then the k keys of each of the ns experts
-    float* q_s = smem + w * (D + L);
-    float* l_s = q_s + D;
+    float* l_s = smem + (size_t)w * 2 * L;
+    int* c_s = reinterpret_cast<int*>(l_s + L);
     const int bh = blockIdx.y;
     const int slot = blockIdx.x * kAttendWarps + w;
     if (slot >= s.N) return;
@@ -534,37 +577,31 @@ __global__ void __launch_bounds__(32 * kAttendWarps)
     if (qi < 0 || qi >= s.N) { if (lane == 0) atomicExch(status, (int)MITA_ERR_DEVICE); return; }
     const int r = route[(size_t)bh * s.N + qi];
     if (r < 0 || r >= s.m) { if (lane == 0) atomicExch(status, (int)MITA_ERR_DEVICE); return; }
-    const int32_t* tq = ns > 1 ? tops + ((size_t)bh * s.N + qi) * ns : nullptr;
     // expert e of this query (e = 0: the route); an invalid landmark falls back to the route
-    auto expert = [&](int e) -> const int32_t* {
-        int re = e == 0 ? r : tq[e];
-        if (re < 0 || re >= s.m) {
-            atomicExch(status, (int)MITA_ERR_DEVICE);
-            re = r;
-        }
-        return idx + ((size_t)bh * s.m + re) * s.k;
-    };
-    const size_t hoff = (size_t)bh * s.N * D;
-    for (int f = lane; f < D; f += 32) q_s[f] = to_f32(Q[hoff + (size_t)qi * D + f]);
+    if (lane < ns) {
+        int re = lane == 0 ? r : tops[((size_t)bh * s.N + qi) * ns + lane];
+        if (re < 0 || re >= s.m) { atomicExch(status, (int)MITA_ERR_DEVICE); re = r; }
+        r_s[w][lane] = re;
+    }
     __syncwarp();
-    const T* lq = Ql + (size_t)bh * s.m * D;
-    const float scale = rsqrtf((float)D);
-    float mx = -INFINITY;
     for (int t = lane; t < L; t += 32) {
-        if (t < s.m && !shared) {   // routing only: the shared slots take no weight
-            l_s[t] = -INFINITY;
-            continue;
-        }
-        const T* key;
-        if (t < s.m) key = lq + (size_t)t * D;
-        else {
+        int c;
+        if (t < s.m) {
+            c = shared ? t : -1;   // routing only: the shared slots take no weight
+        } else {
             const int u = t - s.m, e = u / s.k;
-            int j = expert(e)[u - e * s.k];
-            if (j < 0 || j >= s.N) { atomicExch(status, (int)MITA_ERR_DEVICE); j = 0; }
-            // a key already held by an earlier expert of this query takes part once
+            c = idx[((size_t)bh * s.m + r_s[w][e]) * s.k + (u - e * s.k)];
+            if (c < 0 || c >= s.N) { atomicExch(status, (int)MITA_ERR_DEVICE); c = 0; }
+        }
+        c_s[t] = c;
+    }
+    __syncwarp();
+    if (ns > 1) {   // a key already held by an earlier expert of this query takes part once
+        for (int t = s.m + s.k + lane; t < L; t += 32) {
+            const int u = t - s.m, e = u / s.k, j = c_s[t];
             bool dup = false;
             for (int e2 = 0; e2 < e && !dup; ++e2) {
-                const int32_t* E2 = expert(e2);   // ascending key order
+                const int* E2 = c_s + s.m + e2 * s.k;
                 int lo = 0, hi = s.k - 1;
                 while (lo <= hi) {
                     const int mid = (lo + hi) >> 1;
@@ -572,58 +609,78 @@ __global__ void __launch_bounds__(32 * kAttendWarps)
                     if (E2[mid] < j) lo = mid + 1; else hi = mid - 1;
                 }
             }
-            if (dup) {
-                l_s[t] = -INFINITY;
-                continue;
-            }
-            key = K + hoff + (size_t)j * D;
+            l_s[t] = dup ? 1.0f : 0.0f;
         }
+        __syncwarp();
+        for (int t = s.m + s.k + lane; t < L; t += 32)
+            if (l_s[t] != 0.0f) c_s[t] = -1;
+        __syncwarp();
+    }
+    const size_t hoff = (size_t)bh * s.N * D;
+    const T* lq = Ql + (size_t)bh * s.m * D;
+    const T* lv = Vl + (size_t)bh * s.m * D;
+    float qf[FPL];
+    load_feats<T, FPL>(Q + hoff + (size_t)qi * D + sub * FPL, qf);
+    const float scale = rsqrtf((float)D);
+    float mx = -INFINITY;
+    for (int t0 = 0; t0 < L; t0 += 4) {
+        const int t = t0 + grp;
+        const int c = t < L ? c_s[t] : -1;
         float a = 0.0f;
-#pragma unroll 8
-        for (int f = 0; f < D; ++f) a = fmaf(q_s[f], to_f32(key[f]), a);
-        a *= scale;
-        l_s[t] = a;
-        mx = fmaxf(mx, a);
+        if (c >= 0) {
+            float kf[FPL];
+            load_feats<T, FPL>((t < s.m ? lq : K + hoff) + (size_t)c * D + sub * FPL, kf);
+#pragma unroll
+            for (int i = 0; i < FPL; ++i) a = fmaf(qf[i], kf[i], a);
+        }
+        a += __shfl_xor_sync(0xffffffffu, a, 1);
+        a += __shfl_xor_sync(0xffffffffu, a, 2);
+        a += __shfl_xor_sync(0xffffffffu, a, 4);
+        const float lg = c >= 0 ? a * scale : -INFINITY;
+        if (sub == 0 && t < L) l_s[t] = lg;
+        mx = fmaxf(mx, lg);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     __syncwarp();
     float den = 0.0f;
     for (int t = lane; t < L; t += 32) {
-        float p = exp2f((l_s[t] - mx) * kLog2e);
+        const float p = exp2f((l_s[t] - mx) * kLog2e);
         l_s[t] = p;
         den += p;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     __syncwarp();
-    const T* lv = Vl + (size_t)bh * s.m * D;
-    float acc[D / 32];
+    float acc[FPL];
 #pragma unroll
-    for (int u = 0; u < D / 32; ++u) acc[u] = 0.0f;
-    for (int t = 0; t < (shared ? s.m : 0); ++t) {
-        float p = l_s[t];
+    for (int i = 0; i < FPL; ++i) acc[i] = 0.0f;
+    for (int t0 = 0; t0 < L; t0 += 4) {
+        const int t = t0 + grp;
+        if (t >= L) continue;
+        const float p = l_s[t];
+        const int c = c_s[t];
+        if (p == 0.0f || c < 0) continue;   // no weight (or an underflow: none either way)
+        float vf[FPL];
+        load_feats<T, FPL>((t < s.m ? lv : V + hoff) + (size_t)c * D + sub * FPL, vf);
 #pragma unroll
-        for (int u = 0; u < D / 32; ++u) acc[u] = fmaf(p, to_f32(lv[(size_t)t * D + lane + 32 * u]), acc[u]);
+        for (int i = 0; i < FPL; ++i) acc[i] = fmaf(p, vf[i], acc[i]);
     }
-    for (int e = 0; e < ns; ++e) {
-        const int32_t* Ee = expert(e);
-        for (int t = 0; t < s.k; ++t) {
-            const float p = l_s[s.m + e * s.k + t];
-            if (p == 0.0f) continue;   // a repeated key (or an underflow: no weight either way)
-            int j = Ee[t];
-            j = (j < 0 || j >= s.N) ? 0 : j;
 #pragma unroll
-            for (int u = 0; u < D / 32; ++u) acc[u] = fmaf(p, to_f32(V[hoff + (size_t)j * D + lane + 32 * u]), acc[u]);
-        }
+    for (int i = 0; i < FPL; ++i) {
+        acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 8);
+        acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 16);
     }
-    const float inv = 1.0f / den;
+    if (grp == 0) {
+        const float inv = 1.0f / den;
+        T* o = out + hoff + (size_t)qi * D + sub * FPL;
 #pragma unroll
-    for (int u = 0; u < D / 32; ++u) out[hoff + (size_t)qi * D + lane + 32 * u] = from_f32<T>(acc[u] * inv);
+        for (int i = 0; i < FPL; ++i) o[i] = from_f32<T>(acc[i] * inv);
+    }
 }
 
 size_t staged_attend_smem(const Shape& s, int ns) {
-    return (size_t)kAttendWarps * (s.d + s.m + (size_t)ns * s.k) * sizeof(float);
+    return (size_t)kAttendWarps * 2 * (s.m + (size_t)ns * s.k) * sizeof(float);
 }
 
 // ---------------------------------------------------------------- launcher
@@ -772,21 +829,6 @@ __global__ void __launch_bounds__(32 * kAttendWarps)
 // shared slots, to dK / dV for the routed keys.  Slots are padded to LP =
 // 32 JT; a padded slot reads the last real row and is masked out.
 
-MITA_DEV float dot4(float4 a, float4 b, float acc) {
-    return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, fmaf(a.x, b.x, acc))));
-}
-
-template <typename T>
-MITA_DEV float4 load4(const T* p) {
-    if constexpr (sizeof(T) == 4) {
-        return *reinterpret_cast<const float4*>(p);
-    } else {
-        const uint2 u = *reinterpret_cast<const uint2*>(p);
-        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-        return make_float4(a.x, a.y, b.x, b.y);
-    }
-}
 
 inline size_t expert_bwd_bytes(int D, int L, int LP, int QC) {
     return (2 * (size_t)L * (D + 4) + 2 * (size_t)QC * D + 2 * (size_t)QC * LP) * sizeof(float);
