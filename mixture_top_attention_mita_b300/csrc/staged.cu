@@ -6,7 +6,7 @@
 //   scores_kernel    step 2, raw landmark scores S = Q_l . K^T (fp32, [m, N])
 //   topk_kernel      step 3, per-landmark radix select of the k best keys
 //                    (topk_warp_kernel: rows of up to 256 keys)
-//   values_kernel    step 4, landmark values V_l = softmax(S / sqrt d) . V
+//   values_rows_kernel  step 4, landmark values V_l = softmax(S / sqrt d) . V
 //   route_kernel     step 5, first argmax of q . Q_l per query
 //   bucket_kernel    step 5, stable counting sort of the queries by route
 //   attend_kernel    step 6, one softmax over m shared + k routed keys
@@ -255,54 +255,7 @@ static void launch_topk(const Shape& s, const float* S, int32_t* idx, cudaStream
 }
 
 // ---------------------------------------------------------------- step 4
-// One block per (landmark, head).  V_l[i] = sum_j w_j V[j] / sum_j w_j with
-// w_j = exp((S_j - max S) / sqrt d); 256 / d groups of d threads each take
-// every (256/d)-th key of a 256-key chunk.
-template <typename T>
-__global__ void __launch_bounds__(256) values_kernel(Shape s, const float* __restrict__ S,
-                                                    const T* __restrict__ V, T* __restrict__ Vl) {
-    __shared__ float w_s[256];
-    __shared__ float red[256];
-    __shared__ float acc_s[256];
-    const int i = blockIdx.x, bh = blockIdx.y, t = threadIdx.x;
-    const float* row = S + ((size_t)bh * s.m + i) * s.N;
-    const T* v = V + (size_t)bh * s.N * s.d;
-    float mx = -INFINITY;
-    for (int j = t; j < s.N; j += 256) mx = fmaxf(mx, row[j]);
-    red[t] = mx;
-    __syncthreads();
-    for (int o = 128; o > 0; o >>= 1) {
-        if (t < o) red[t] = fmaxf(red[t], red[t + o]);
-        __syncthreads();
-    }
-    mx = red[0];
-    __syncthreads();
-    const float c = rsqrtf((float)s.d) * kLog2e;
-    const int groups = 256 / s.d, g = t / s.d, f = t % s.d;
-    float acc = 0.0f, den = 0.0f;
-    for (int j0 = 0; j0 < s.N; j0 += 256) {
-        int j = j0 + t;
-        float w = j < s.N ? exp2f((row[j] - mx) * c) : 0.0f;
-        w_s[t] = w;
-        den += w;
-        __syncthreads();
-        int jn = min(256, s.N - j0);
-        for (int u = g; u < jn; u += groups) acc = fmaf(w_s[u], to_f32(v[(size_t)(j0 + u) * s.d + f]), acc);
-        __syncthreads();
-    }
-    red[t] = den;
-    acc_s[t] = acc;
-    __syncthreads();
-    for (int o = 128; o > 0; o >>= 1) {
-        if (t < o) red[t] += red[t + o];
-        __syncthreads();
-    }
-    if (t < s.d) {
-        float a = 0.0f;
-        for (int u = 0; u < groups; ++u) a += acc_s[u * s.d + t];
-        Vl[((size_t)bh * s.m + i) * s.d + t] = from_f32<T>(a / red[0]);
-    }
-}
+// Landmark values: values_rows_kernel (below, with the backward's kernels).
 
 // ---------------------------------------------------------------- step 5
 // One thread per query: raw scores q . Q_l[i] over all landmarks, first
@@ -685,6 +638,10 @@ size_t staged_attend_smem(const Shape& s, int ns) {
 
 // ---------------------------------------------------------------- launcher
 template <typename T, int D>
+static int launch_values_rows(const Shape& s, const float* S, const T* V, T* Vl, float* Vl32, float* stats,
+                              float* scratch, size_t scratch_bytes, cudaStream_t st);
+
+template <typename T, int D>
 static cudaError_t run_staged_t(mita_plan_s* p, const T* Q, const T* K, const T* V, T* out, int32_t* idx,
                                 int32_t* route, cudaStream_t st) {
     const Shape& s = p->s;
@@ -694,7 +651,9 @@ static cudaError_t run_staged_t(mita_plan_s* p, const T* Q, const T* K, const T*
     pool_kernel<T><<<dim3(s.m, BH), D, 0, st>>>(s, Q, Ql);
     scores_kernel<T><<<dim3((s.N + 127) / 128, (s.m + 31) / 32, BH), 256, 0, st>>>(s, Ql, K, p->S);
     launch_topk(s, p->S, idx, st);
-    values_kernel<T><<<dim3(s.m, BH), 256, 0, st>>>(s, p->S, V, Vl);
+    // key-split partial sums (if any) use the output as scratch before the attention writes it
+    const int nv = launch_values_rows<T, D>(s, p->S, V, Vl, nullptr, nullptr, reinterpret_cast<float*>(out),
+                                            (size_t)BH * s.N * D * sizeof(T), st);
     // s > 1: each query's landmark list goes into the score buffer, free once
     // the landmark values are done (BH x N x s <= BH x m x N entries)
     const int ns = p->routes_s > 1 ? p->routes_s : 1;
@@ -706,7 +665,7 @@ static cudaError_t run_staged_t(mita_plan_s* p, const T* Q, const T* K, const T*
     ensure_smem_attr((const void*)attend_kernel<T, D>, (int)smem);
     attend_kernel<T, D><<<dim3((s.N + kAttendWarps - 1) / kAttendWarps, BH), 32 * kAttendWarps, smem, st>>>(
         s, Q, K, V, Ql, Vl, idx, route, p->perm, out, p->routing_only ? 0 : 1, ns, tops, p->status);
-    p->launches += 7;
+    p->launches += 6 + nv;
     return cudaGetLastError();
 }
 
@@ -1377,9 +1336,9 @@ inline size_t expert_bwd_mma_bytes(int LP, int QC) {
 // key split): row maxima of S over the split's keys, then 64-key chunks of V
 // staged once in shared memory for all 32 rows, weights
 // w = exp((S - max) / sqrt d) and their sums.  One split writes V_l in the
-// I/O type (as the forward uses it), V_l in fp32 and per row {max S, sum w}
-// for values_bwd_tile_kernel; several write {sums, sum w, max} per split to
-// `part` for values_rows_fin_kernel.
+// I/O type (as the forward uses it) and, where Vl32 is not null, V_l in fp32
+// and per row {max S, sum w} for values_bwd_tile_kernel; several write
+// {sums, sum w, max} per split to `part` for values_rows_fin_kernel.
 constexpr int kVrRows = 32, kVrKeys = 64;
 
 template <typename T, int D>
@@ -1470,6 +1429,7 @@ __global__ void __launch_bounds__(256) values_rows_kernel(Shape s, const float* 
             y[b] = acc[u][b] / rsum;
             Vl[o + b] = from_f32<T>(y[b]);
         }
+        if (Vl32 == nullptr) continue;
         *reinterpret_cast<float4*>(Vl32 + o) = make_float4(y[0], y[1], y[2], y[3]);
         if (tc == 0) {
             stats[2 * ((size_t)bh * s.m + i0 + r)] = mx_s[r];
@@ -1479,7 +1439,8 @@ __global__ void __launch_bounds__(256) values_rows_kernel(Shape s, const float* 
 }
 
 // Combines values_rows_kernel's key splits: thread per (landmark row, 4
-// features); the splits' sums are rescaled to the row's largest max.
+// features); the splits' sums are rescaled to the row's largest max.  The
+// fp32 copy and row stats are written where Vl32 is not null.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) values_rows_fin_kernel(Shape s, int ksplit, const float* __restrict__ part,
                                                               T* __restrict__ Vl, float* __restrict__ Vl32,
@@ -1508,6 +1469,7 @@ __global__ void __launch_bounds__(256) values_rows_fin_kernel(Shape s, int kspli
         y[b] = a[b] / den;
         Vl[o + b] = from_f32<T>(y[b]);
     }
+    if (Vl32 == nullptr) return;
     *reinterpret_cast<float4*>(Vl32 + o) = make_float4(y[0], y[1], y[2], y[3]);
     if (tc == 0) {
         stats[2 * row] = M;
@@ -1713,6 +1675,28 @@ __global__ void __launch_bounds__(256) pool_bwd_kernel(Shape s, const float* __r
     *o = q;
 }
 
+// Landmark values V_l (with their fp32 copy and row stats where Vl32 is not
+// null) by values_rows_kernel, with key splits when the row tiles alone give
+// fewer than two blocks per SM; the splits' partial sums go to `scratch`
+// (bytes available: scratch_bytes).  Returns the number of launches.
+template <typename T, int D>
+static int launch_values_rows(const Shape& s, const float* S, const T* V, T* Vl, float* Vl32, float* stats,
+                              float* scratch, size_t scratch_bytes, cudaStream_t st) {
+    const int BH = s.BH();
+    const int row_tiles = (s.m + kVrRows - 1) / kVrRows;
+    int ksplit = 1;
+    if ((size_t)row_tiles * BH < 296) {
+        ksplit = std::min(8, (s.N + 511) / 512);
+        while (ksplit > 1 && (size_t)BH * s.m * ksplit * (D + 2) * sizeof(float) > scratch_bytes) --ksplit;
+    }
+    values_rows_kernel<T, D><<<dim3(row_tiles, BH, ksplit), 256, 0, st>>>(s, S, V, Vl, Vl32, stats, ksplit,
+                                                                          scratch);
+    if (ksplit == 1) return 1;
+    values_rows_fin_kernel<T, D><<<(unsigned)(((size_t)BH * s.m * (D / 4) + 255) / 256), 256, 0, st>>>(
+        s, ksplit, scratch, Vl, Vl32, stats);
+    return 2;
+}
+
 template <typename T, int D>
 static cudaError_t run_backward_t(mita_plan_s* p, const T* Q, const T* K, const T* V, const T* dOut, float* dQ,
                                   float* dK, float* dV, cudaStream_t st) {
@@ -1729,20 +1713,8 @@ static cudaError_t run_backward_t(mita_plan_s* p, const T* Q, const T* K, const 
     launch_topk(s, p->S, p->idx, st);
     float* Vl32 = p->dVl + (size_t)BH * s.m * D;   // fp32 landmark values, then per-row {max S, sum w}
     float* stats = Vl32 + (size_t)BH * s.m * D;
-    // key splits when the row tiles alone fill fewer than two blocks per SM; their
-    // partial sums use dK as scratch before it is cleared
-    const int row_tiles = (s.m + kVrRows - 1) / kVrRows;
-    int ksplit = 1;
-    if ((size_t)row_tiles * BH < 296) {
-        ksplit = std::min(8, (s.N + 511) / 512);
-        while (ksplit > 1 && (size_t)s.m * ksplit * (D + 2) > (size_t)s.N * D) --ksplit;
-    }
-    values_rows_kernel<T, D><<<dim3(row_tiles, BH, ksplit), 256, 0, st>>>(s, p->S, V, Vl, Vl32, stats, ksplit, dK);
-    if (ksplit > 1) {
-        values_rows_fin_kernel<T, D><<<(unsigned)(((size_t)BH * s.m * (D / 4) + 255) / 256), 256, 0, st>>>(
-            s, ksplit, dK, Vl, Vl32, stats);
-        p->launches += 1;
-    }
+    // key-split partial sums use dK as scratch before it is cleared
+    p->launches += launch_values_rows<T, D>(s, p->S, V, Vl, Vl32, stats, dK, nbytes, st) - 1;
     route_kernel<T, D><<<dim3((s.N + 127) / 128, BH), 128, 0, st>>>(s, Q, Ql, p->route, 1, nullptr);
     if ((e = cudaMemsetAsync(dK, 0, nbytes, st)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(dV, 0, nbytes, st)) != cudaSuccess) return e;
