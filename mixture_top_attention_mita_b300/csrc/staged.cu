@@ -671,9 +671,12 @@ static cudaError_t run_staged_t(mita_plan_s* p, const T* Q, const T* K, const T*
 
 // ---------------------------------------------------------------- backward
 // The backward pass of the operator with the experts and routes held as
-// constants (see mita.h): attend_bwd_kernel takes the output softmax (warp per
-// query), values_bwd_kernel the landmark values (block per landmark row),
-// pool_bwd_kernel the bin means.  Gradients accumulate in fp32 with atomics.
+// constants (see mita.h).  The output softmax: expert_bwd_mma_kernel (bf16,
+// d = 64) or expert_bwd_kernel (fp32 I/O, d = 128), a block per expert, where
+// the expert's m + k slots fit on chip; attend_bwd_kernel (warp per query)
+// otherwise.  The landmark values: values_bwd_tile_kernel (block per 64-key
+// tile).  The bin means: pool_bwd_kernel.  Gradients are fp32; the slot and
+// landmark gradients are added with atomics.
 
 // Warp per query: the forward's logits and weights again, dw = dOut . v,
 // dlogit = w (dw - w . dw); the query's own gradient is stored, the shared
