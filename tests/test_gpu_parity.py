@@ -144,6 +144,11 @@ BWD = {
     "hires56_heads": W["hires56"].scaled(B=1, H=2),
     "hires56_f32": W["hires56"].scaled(B=1, H=2, dtype="f32"),
     "long_k32": W["long1d"].scaled(B=1, H=1, N=2048, gw=2048, pw=16, m=16, k=32),
+    # edges: every expert holds all N keys; experts of ~49 queries (several
+    # chunks per block); exactly 128 slots (m = k = 64)
+    "k_equals_n": W["deit_t"].scaled(B=1, H=4, N=16, gh=4, gw=4, ph=2, pw=2, m=4, k=16),
+    "few_landmarks": W["deit_t"].scaled(B=1, H=4, ph=2, pw=2, m=4, k=25),
+    "slots_128": W["hires56"].scaled(B=1, H=4, N=1024, gh=32, gw=32, ph=8, pw=8, m=64, k=64),
 }
 
 
