@@ -255,10 +255,12 @@ def _fd_check(grid, m, k, d, shared, seed):
 
 
 @pytest.mark.parametrize("grid,m,k,d,shared", [((6, 6, 2, 3), 6, 5, 4, True), ((1, 20, 1, 4), 4, 7, 3, True),
-                                               ((6, 6, 2, 3), 6, 5, 4, False)])
+                                               ((6, 6, 2, 3), 6, 5, 4, False), ((5, 5, 2, 3), 6, 5, 3, True)])
 def test_backward_matches_finite_differences(grid, m, k, d, shared):
-    # NEXT-1 backward pass: the experts and routes are constants; gradients
-    # flow through both softmaxes, the landmark values and the pooling.
+    # The backward pass: the experts and routes are constants; gradients flow
+    # through both softmaxes, the landmark values and the pooling (the 5 x 5
+    # grid into 2 x 3 bins has overlapping bins, so some tokens feed two or
+    # four landmarks).
     _fd_check(grid, m, k, d, shared, seed=31)
 
 
