@@ -366,6 +366,14 @@ _MUTANTS = {
                             "dQ[(size_t)(y * gw + x) * d + f] += src[f];"),
     "backward_values_transpose": ("dV[(size_t)j * d + f] += pij * dVl[(size_t)i * d + f];",
                                   "dV[(size_t)j * d + f] += pij * dVl[(size_t)((i + 1) % m) * d + f];"),
+    # the bins taken as a partition (floor bounds) in the pool backward: the
+    # same as the adaptive bins unless bins overlap
+    "backward_pool_partition": ("            for (int y = r0; y < r1; ++y)\n"
+                                "                for (int x = c0; x < c1; ++x)\n"
+                                "                    for (int f = 0; f < d; ++f) dQ[",
+                                "            for (int y = r * gh / ph; y < (r + 1) * gh / ph; ++y)\n"
+                                "                for (int x = c * gw / pw; x < (c + 1) * gw / pw; ++x)\n"
+                                "                    for (int f = 0; f < d; ++f) dQ["),
 }
 
 
@@ -389,7 +397,8 @@ def test_planted_mistake_fails_a_pin(name, tmp_path):
             lambda: test_routing_only_full_attention_special_case(),
             lambda: test_top_s_routing_matches_masked_sdpa(3),
             lambda: test_top_s_routing_ties_on_integer_inputs(),
-            lambda: _fd_check((6, 6, 2, 3), 6, 5, 4, True, seed=31)]
+            lambda: _fd_check((6, 6, 2, 3), 6, 5, 4, True, seed=31),
+            lambda: _fd_check((5, 5, 2, 3), 6, 5, 3, True, seed=31)]
     failures = 0
     with oracle.swapped_library(str(so)):
         for pin in pins:
