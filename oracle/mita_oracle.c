@@ -91,18 +91,14 @@ void oracle_pool(int gh, int gw, int ph, int pw, int d, int io,
                 for (int y = r0; y < r1; ++y)
                     for (int x = c0; x < c1; ++x)
                         s += Q[(size_t)(y * gw + x) * d + f];
+                /* The fp64 sum s is exact while the bin's values, of p
+                 * significant bits each (8 for bf16, 24 for fp32), span at
+                 * most 53 - p - ceil(log2 count) binades; the checked inputs
+                 * stay far inside that.  The exact quotient is then rounded
+                 * twice, to fp64 and to the I/O type, and with 53 >= 2p + 2
+                 * that gives the rounding of the exact mean itself
+                 * (Figueroa, "When is double rounding innocuous?", 1995). */
                 double mean = s / count;
-                /* A quotient that lands exactly on a bf16 rounding midpoint
-                 * is only a midpoint if s == count * mean exactly; otherwise
-                 * nudge it to the side the exact quotient lies on, so that
-                 * the bf16 result is the rounding of s / count itself. */
-                if (io == ORACLE_IO_BF16 && oracle_round_bf16(mean) != mean) {
-                    double lo_b = oracle_round_bf16(nextafter(mean, -INFINITY));
-                    double hi_b = oracle_round_bf16(nextafter(mean, INFINITY));
-                    if (lo_b != hi_b && fma(count, mean, -s) != 0.0)
-                        mean = (fma(count, mean, -s) > 0.0) ? nextafter(mean, -INFINITY)
-                                                           : nextafter(mean, INFINITY);
-                }
                 dst[f] = round_io(mean, io);
             }
         }
@@ -121,7 +117,7 @@ void oracle_scores(int N, int d, int m, const double* Ql, const double* K, doubl
 
 /* Order used by the top-k: higher score first, then lower index first.
  * -0.0 and +0.0 compare equal in C, so they tie and the index decides. */
-static const double* g_sort_row;
+static _Thread_local const double* g_sort_row;   /* one per thread: heads and rows run in parallel */
 static int cmp_desc_then_index(const void* a, const void* b) {
     int ia = *(const int32_t*)a, ib = *(const int32_t*)b;
     double sa = g_sort_row[ia], sb = g_sort_row[ib];

@@ -76,6 +76,62 @@ def test_pool_bf16_rounds_the_exact_mean():
     np.testing.assert_array_equal(b, np.vectorize(oracle.round_bf16)(f))
 
 
+def _bf16_nearest(x):
+    """Nearest bf16 value to the rational x, ties to the even significand:
+    written here from the format's definition (8 significant bits), with
+    exact fractions, independently of the oracle's rounding routine."""
+    from fractions import Fraction
+    if x == 0:
+        return Fraction(0)
+    sign, a = (-1, -x) if x < 0 else (1, x)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    ulp = Fraction(2) ** (e - 7)               # spacing of bf16 values in [2^e, 2^(e+1))
+    lo = (a // ulp) * ulp
+    rem = a - lo
+    if rem * 2 > ulp or (rem * 2 == ulp and (lo / ulp) % 2 == 1):
+        lo += ulp
+    return sign * lo
+
+
+@pytest.mark.parametrize("count_grid", [(3, 4), (4, 4)])
+def test_pool_bf16_rounds_exact_rational_means_at_midpoints(count_grid):
+    # One bin of 12 or 16 tokens.  Each feature's values are integers below
+    # 256 (exact in bf16) whose sum puts the exact mean on a bf16 rounding
+    # midpoint (k + 1/2 for a mean in [128, 256)), or a 2^-20 value shifts
+    # the sum just above or just below that midpoint.  The landmark must be
+    # the bf16 value nearest to the exact rational mean: ties to even on the
+    # midpoint, away from it otherwise.
+    from fractions import Fraction
+    gh, gw = count_grid
+    n = gh * gw
+    rng = np.random.default_rng(n)
+    d = 48
+    Q = np.zeros((n, d))
+    for f in range(d):
+        kind = f % 3
+        k = int(rng.integers(128, 220))          # keeps every value below 256
+        target = n * k + n // 2                      # n * (k + 1/2)
+        free = n - 1 if kind else n                  # one token carries the 2^-20 shift
+        vals = np.full(free, target // free)
+        vals[: target - vals.sum()] += 1
+        rng.shuffle(vals)
+        Q[:free, f] = vals
+        if kind:
+            Q[n - 1, f] = 2.0 ** -20 if kind == 1 else -(2.0 ** -20)
+    assert (np.abs(Q) < 256).all()
+    Qb = torch.from_numpy(Q).to(torch.bfloat16)
+    assert np.array_equal(Qb.double().numpy(), Q)    # every value exact in bf16
+    r = oracle.head(Qb, Qb, Qb, (gh, gw, 1, 1), 1, 1, io="bf16", debug=True)
+    want = [float(_bf16_nearest(sum(Fraction(float(v)) for v in Q[:, f]) / n)) for f in range(d)]
+    np.testing.assert_array_equal(r["Ql"][0], want)
+    means = Q.sum(0) / n
+    assert (np.round(means[0::3] * 2) % 2 == 1).all()   # the tie features sit on midpoints
+
+
 # ---------------------------------------------------------------- top-k
 def _brute_topk(R, k):
     # j is selected iff fewer than k keys beat it, where l beats j when
@@ -352,6 +408,8 @@ _MUTANTS = {
     "drop_shared_values": ("for (int i = 0; i < m; ++i) s += logit[i] * Vl[(size_t)i * d + f];", ""),
     "unscaled_routed_logit": ("logit[m + t] = s * scale;", "logit[m + t] = s;"),
     "ties_to_higher_index": ("return (ia > ib) - (ia < ib);", "return (ia < ib) - (ia > ib);"),
+    # bf16 rounding with ties away from zero instead of to even
+    "bf16_ties_away": ("double r = nearbyint(y);", "double r = round(y);"),
     "pool_bins_floor_end": ("*hi = ((i + 1) * G + P - 1) / P;", "*hi = ((i + 1) * G) / P;"),
     "route_last_argmax": ("if (s > A[best]) best = i;", "if (s >= A[best]) best = i;"),
     "values_wrong_row": ("acc[f] += w * V[(size_t)j * d + f];", "acc[f] += w * V[(size_t)(N - 1 - j) * d + f];"),
@@ -394,6 +452,7 @@ def test_planted_mistake_fails_a_pin(name, tmp_path):
             lambda: test_topk_brute_force_with_ties(17),
             lambda: test_route_is_first_argmax(),
             lambda: test_pool_matches_adaptive_avg_pool2d(14, 14, 5, 5),
+            lambda: test_pool_bf16_rounds_exact_rational_means_at_midpoints((3, 4)),
             lambda: test_routing_only_full_attention_special_case(),
             lambda: test_top_s_routing_matches_masked_sdpa(3),
             lambda: test_top_s_routing_ties_on_integer_inputs(),
