@@ -293,14 +293,13 @@ def run_reference(args, w, ws, rank):
 
 def long_sweep(args):
     """MiTA forward against full attention (torch scaled_dot_product_attention,
-    the fused flash kernel) on single-head 1-D sequences with m * k = N / 4
-    (N / 8 at 1M tokens, where the tiled path's k <= 512 sets the limit),
+    the fused flash kernel) on single-head 1-D sequences with m * k = N / 4,
     d = 128, bf16 (the shape of the method's long-sequence throughput figure).
     One JSON line per length: both times from CUDA events, median of a few
     runs after a warm-up."""
     import mixture_top_attention_mita_b300 as mita
     dev = torch.device("cuda")
-    for N, m, k in ((16384, 64, 64), (65536, 128, 128), (262144, 256, 256), (1048576, 256, 512)):
+    for N, m, k in ((16384, 64, 64), (65536, 128, 128), (262144, 256, 256), (1048576, 256, 1024)):
         w = synth.WORKLOADS["long1d"].scaled(name=f"long_{N}", B=1, H=1, N=N, gw=N, pw=m, m=m, k=k,
                                              span=1024, seed=2000 + N % 997)
         Qc, Kc, Vc = synth.make_inputs(w)

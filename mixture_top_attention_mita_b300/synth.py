@@ -35,6 +35,7 @@ class Workload:
     gen: str         # "iid", "cluster_token", "cluster_patch", "cluster_span"
     centres: int = 0
     patch: int = 0   # cluster id fixed per patch x patch tile (cluster_patch)
+    patch_offset: int = 0   # tiles start this many tokens before the grid's origin (cluster_patch)
     span: int = 0    # cluster id fixed per span of tokens (cluster_span)
     noise: float = 0.5
     seed: int = 1000
@@ -57,8 +58,10 @@ WORKLOADS = {
     "deit_t": Workload("deit_t", 128, 3, 196, 64, 14, 14, 5, 5, 25, 25, "bf16", "iid", seed=1002),
     "deit_s": Workload("deit_s", 256, 6, 196, 64, 14, 14, 5, 5, 25, 25, "bf16", "cluster_token",
                        centres=16, seed=1003),
+    # 8 x 8 cluster tiles offset by 4 tokens from the 8 x 8 pooling bins, so
+    # that related tokens are contiguous but not aligned with the landmarks
     "hires56": Workload("hires56", 16, 6, 3136, 64, 56, 56, 7, 7, 49, 64, "bf16", "cluster_patch",
-                        centres=16, patch=8, seed=1004),
+                        centres=16, patch=8, patch_offset=4, seed=1004),
     "long1d": Workload("long1d", 2, 8, 65536, 128, 1, 65536, 1, 256, 256, 512, "bf16",
                        "cluster_span", centres=64, span=1024, seed=1005),
 }
@@ -68,10 +71,12 @@ def torch_dtype(w: Workload):
     return torch.float32 if w.dtype == "f32" else torch.bfloat16
 
 
-def make_inputs(w: Workload, seed: int | None = None):
-    """Q, K, V as contiguous CPU tensors [B, H, N, d] of the workload's type."""
+def make_inputs(w: Workload, seed: int | None = None, return_ids: bool = False):
+    """Q, K, V as contiguous CPU tensors [B, H, N, d] of the workload's type
+    (and, with ``return_ids``, the cluster id of every token, [B, H, N])."""
     g = torch.Generator("cpu").manual_seed(w.seed if seed is None else seed)
     B, H, N, d = w.B, w.H, w.N, w.d
+    ids = None
     if w.gen == "iid":
         Q = torch.randn(B, H, N, d, generator=g)
         K = torch.randn(B, H, N, d, generator=g)
@@ -81,10 +86,13 @@ def make_inputs(w: Workload, seed: int | None = None):
         if w.gen == "cluster_token":
             ids = torch.randint(0, C, (B, H, N), generator=g)
         elif w.gen == "cluster_patch":
-            ph_, pw_ = w.gh // w.patch, w.gw // w.patch
+            # token (y, x) lies in tile ((y + o) // patch, (x + o) // patch)
+            o = w.patch_offset
+            ph_, pw_ = -(-(w.gh + o) // w.patch), -(-(w.gw + o) // w.patch)
             pid = torch.randint(0, C, (B, H, ph_, pw_), generator=g)
-            ids = pid.repeat_interleave(w.patch, dim=2).repeat_interleave(w.patch, dim=3)
-            ids = ids.reshape(B, H, N)
+            ty = (torch.arange(w.gh) + o) // w.patch
+            tx = (torch.arange(w.gw) + o) // w.patch
+            ids = pid[:, :, ty][:, :, :, tx].reshape(B, H, N)
         elif w.gen == "cluster_span":
             sid = torch.randint(0, C, (B, H, N // w.span), generator=g)
             ids = sid.repeat_interleave(w.span, dim=2)
@@ -95,7 +103,8 @@ def make_inputs(w: Workload, seed: int | None = None):
         K = base + w.noise * torch.randn(B, H, N, d, generator=g)
     V = torch.randn(B, H, N, d, generator=g)
     dt = torch_dtype(w)
-    return Q.to(dt).contiguous(), K.to(dt).contiguous(), V.to(dt).contiguous()
+    out = Q.to(dt).contiguous(), K.to(dt).contiguous(), V.to(dt).contiguous()
+    return out + (ids,) if return_ids else out
 
 
 def make_integer_inputs(w: Workload, seed: int = 7):

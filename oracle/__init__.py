@@ -58,6 +58,18 @@ def _open(path):
     lib.oracle_forward.restype = i
     lib.oracle_backward_head.argtypes = [i, i, i, i, i, i, i, i, i, i, dp, dp, dp, dp, dp, dp, dp]
     lib.oracle_backward_head.restype = i
+    lib.oracle_pool.argtypes = [i, i, i, i, i, i, dp, dp]
+    lib.oracle_pool.restype = None
+    lib.oracle_scores.argtypes = [i, i, i, dp, dp, dp]
+    lib.oracle_scores.restype = None
+    lib.oracle_topk.argtypes = [i, i, i, dp, ip]
+    lib.oracle_topk.restype = None
+    lib.oracle_landmark_values.argtypes = [i, i, i, i, dp, dp, dp]
+    lib.oracle_landmark_values.restype = None
+    lib.oracle_route_one.argtypes = [i, i, dp, dp, dp]
+    lib.oracle_route_one.restype = i
+    lib.oracle_attend_one.argtypes = [i, i, i, i, i, dp, dp, ip, dp, dp, dp, dp, dp]
+    lib.oracle_attend_one.restype = None
     return lib
 
 
@@ -181,3 +193,102 @@ def backward(Q, K, V, dOut, grid, m: int, k: int, io: str = "f64", shared: bool 
     if rc != 0:
         raise ValueError("oracle: invalid sizes")
     return dQ, dK, dV
+
+
+def attend_one(q, A, expert, K, V, Vl, io: str = "f64", shared: bool = True):
+    """Step 6 for one query: one softmax over the m shared logits (raw
+    query-landmark scores ``A`` [m], scaled here) and the routed logits of the
+    keys listed in ``expert`` (any k key indices), applied to [V_l ; V[expert]].
+    The arguments are the oracle's own intermediates (``head(debug=True)``)
+    or alternatives the caller builds from them; returns out [d]."""
+    lib = _load()
+    q, A, K, V, Vl = _f64(q), _f64(A), _f64(K), _f64(V), _f64(Vl)
+    E = np.ascontiguousarray(expert, dtype=np.int32)
+    d, m, k = q.shape[0], A.shape[0], E.shape[0]
+    out = np.zeros(d)
+    lib.oracle_attend_one(d, m, k, _IO_NAMES[io], int(shared), _dp(q), _dp(A), _ip(E), _dp(K), _dp(V), _dp(Vl),
+                          _dp(out), None)
+    return out
+
+
+def scores_row(Ql_i, K):
+    """Raw landmark scores R[i, :] = Q_l[i] . K^T of one landmark (step 2)."""
+    lib = _load()
+    Ql_i, K = _f64(Ql_i).reshape(1, -1), _f64(K)
+    N, d = K.shape
+    R = np.zeros(N)
+    lib.oracle_scores(N, d, 1, _dp(Ql_i), _dp(K), _dp(R))
+    return R
+
+
+def threads_available() -> int:
+    return max(1, len(os.sched_getaffinity(0)))
+
+
+def head_threaded(Q, K, V, grid, m: int, k: int, io: str = "f64", queries=None, shared: bool = True,
+                  threads: int | None = None):
+    """The whole operator for one long head, its landmark rows spread over
+    host threads (the C routines release the interpreter lock), for the
+    queries listed in ``queries`` (default all).  Each landmark row is the
+    same sequence of oracle steps as in ``head`` -- scores (2), top-k (3),
+    landmark values (4) -- run on that row alone, and each listed query takes
+    route (5) and attend (6); no arithmetic differs from ``head``.  Only
+    O(N) memory per thread: the raw score rows are not kept (``scores_row``
+    recomputes one).  Returns out [nq,d], idx [m,k], route [nq], Ql, Vl,
+    A [nq,m] and kth [m], the k-th best raw score of every landmark."""
+    from concurrent.futures import ThreadPoolExecutor
+    lib = _load()
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    N, d = Q.shape
+    gh, gw, ph, pw = grid
+    if gh * gw != N or ph * pw != m or not (1 <= k <= N):
+        raise ValueError("oracle: invalid sizes")
+    Ql = np.zeros((m, d))
+    lib.oracle_pool(gh, gw, ph, pw, d, _IO_NAMES[io], _dp(Q), _dp(Ql))
+    idx = np.zeros((m, k), dtype=np.int32)
+    Vl = np.zeros((m, d))
+    kth = np.zeros(m)
+
+    def landmark(i):
+        R = np.zeros(N)
+        lib.oracle_scores(N, d, 1, _dp(Ql[i:i + 1]), _dp(K), _dp(R))
+        row = np.zeros(k, dtype=np.int32)
+        lib.oracle_topk(N, 1, k, _dp(R), _ip(row))
+        vl = np.zeros(d)
+        lib.oracle_landmark_values(N, d, 1, _IO_NAMES[io], _dp(R), _dp(V), _dp(vl))
+        idx[i], Vl[i] = row, vl
+        kth[i] = R[row].min()
+
+    with ThreadPoolExecutor(max_workers=threads or threads_available()) as ex:
+        list(ex.map(landmark, range(m)))
+    qs = np.arange(N) if queries is None else np.asarray(queries)
+    out = np.zeros((len(qs), d))
+    route = np.zeros(len(qs), dtype=np.int32)
+    A = np.zeros((len(qs), m))
+    for n, qi in enumerate(qs):
+        q = np.ascontiguousarray(Q[qi])
+        a = np.zeros(m)
+        r = lib.oracle_route_one(d, m, _dp(q), _dp(Ql), _dp(a))
+        E = np.ascontiguousarray(idx[r])
+        o = np.zeros(d)
+        lib.oracle_attend_one(d, m, k, _IO_NAMES[io], int(shared), _dp(q), _dp(a), _ip(E), _dp(K), _dp(V),
+                              _dp(Vl), _dp(o), None)
+        out[n], route[n], A[n] = o, r, a
+    return {"out": out, "idx": idx, "route": route, "Ql": Ql, "Vl": Vl, "A": A, "kth": kth}
+
+
+def forward_heads_threaded(Q, K, V, grid, m: int, k: int, heads, io: str = "f64", shared: bool = True,
+                           s: int = 1, threads: int | None = None):
+    """``head`` on each listed (b, h) head of [B, H, N, d] inputs, the heads
+    spread over host threads; returns the number of heads run.  Used to time
+    the oracle on all host cores."""
+    from concurrent.futures import ThreadPoolExecutor
+    Qf, Kf, Vf = _f64(Q), _f64(K), _f64(V)
+
+    def one(bh):
+        b, h = bh
+        head(Qf[b, h], Kf[b, h], Vf[b, h], grid, m, k, io=io, shared=shared, s=s)
+
+    with ThreadPoolExecutor(max_workers=threads or threads_available()) as ex:
+        list(ex.map(one, heads))
+    return len(heads)

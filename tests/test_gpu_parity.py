@@ -149,17 +149,28 @@ BWD = {
     "k_equals_n": W["deit_t"].scaled(B=1, H=4, N=16, gh=4, gw=4, ph=2, pw=2, m=4, k=16),
     "few_landmarks": W["deit_t"].scaled(B=1, H=4, ph=2, pw=2, m=4, k=25),
     "slots_128": W["hires56"].scaled(B=1, H=4, N=1024, gh=32, gw=32, ph=8, pw=8, m=64, k=64),
+    # overlapping pool bins at d = 128 (10 x 13 tokens into 3 x 4 bins), fp32
+    "overlap_d128_f32": W["tiny_f32"].scaled(B=1, H=2, d=128, gh=10, gw=13, N=130, ph=3, pw=4, m=12, k=40),
+    # overlapping bins with m + k = 145 slots at d = 64: the warp-per-query kernel
+    "overlap_wide_expert": W["deit_t"].scaled(B=1, H=2, k=120),
 }
 
 
+@pytest.mark.parametrize("inputs", ["random", "integer"])
 @pytest.mark.parametrize("routing_only", [False, True])
 @pytest.mark.parametrize("name", sorted(BWD))
-def test_backward_matches_oracle(name, routing_only):
+def test_backward_matches_oracle(name, routing_only, inputs):
     """mita_backward against the oracle's backward (experts and routes held
-    constant) on every head whose discrete choices agree with the oracle's."""
+    constant) on every head whose discrete choices agree with the oracle's:
+    at least three heads in four on random inputs (a near-tie flip makes a
+    head another operator), every head on small-integer inputs (nothing may
+    flip)."""
     import oracle
     w = BWD[name]
-    Q, K, V = synth.make_inputs(w, seed=71)
+    if inputs == "random":
+        Q, K, V = synth.make_inputs(w, seed=71)
+    else:
+        Q, K, V = synth.make_integer_inputs(w, seed=73)
     g = torch.Generator("cpu").manual_seed(72)
     dOut = torch.randn(w.B, w.H, w.N, w.d, generator=g).to(synth.torch_dtype(w))
     fwd = _run(w, Q, K, V, "staged", routing_only=routing_only)
@@ -183,7 +194,10 @@ def test_backward_matches_oracle(name, routing_only):
                 scale = np.abs(want).max()
                 np.testing.assert_allclose(got, want, rtol=1e-3, atol=1e-3 * scale + 1e-6)
             checked += 1
-    assert checked >= 1
+    heads = w.B * w.H
+    if inputs == "integer" and _means_exact(w, Q):
+        assert checked == heads
+    assert checked >= max(1, math.ceil(0.75 * heads)), f"{checked} of {heads} heads checked"
 
 
 def test_backward_rejects_top_s():
@@ -389,9 +403,40 @@ def test_full_size_sampled(name):
     report = []
     compare_batch(w, Q, K, V, r["out"], r["idx"], r["route"], exact=False, heads=FULL_HEADS[name],
                   queries=queries, report=report)
-    print(name, report)
+    print(name, report)   # compared / alternative-checked / unchecked queries (bounded in compare_batch)
     # every query of every head has a valid route; experts ascending
     route, idx = r["route"], r["idx"]
     assert int(route.min()) >= 0 and int(route.max()) < w.m
     assert bool((idx[..., 1:] > idx[..., :-1]).all())
+    assert bool(torch.isfinite(r["out"].float()).all())
+
+
+# ------------------------------------------------------------- long sequences
+# The long-sequence throughput shapes: one head of 1-D tokens, d = 128, bf16,
+# m * k = N / 4 at 1M tokens (the article's long-sequence figure uses
+# m * k of about N / 4), 64-centre cluster spans.  Every landmark's expert is
+# checked under the tie rule (the oracle runs every landmark row, spread over
+# the host cores) and 256 sampled queries' routes and outputs.
+LONG = {
+    "long_262k": W["long1d"].scaled(name="long_262144", B=1, H=1, N=262144, gw=262144, pw=256, m=256, k=256),
+    "long_1m": W["long1d"].scaled(name="long_1048576", B=1, H=1, N=1048576, gw=1048576, pw=256, m=256, k=1024),
+}
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", sorted(LONG))
+def test_long_sequence_sampled(name):
+    from parity_util import compare_long_head
+    w = LONG[name]
+    Q, K, V = synth.make_inputs(w)
+    r = _run(w, Q, K, V, "auto")
+    assert r["plan"].path == "tiled"
+    queries = np.sort(np.random.default_rng(1).choice(w.N, 256, replace=False))
+    qs = torch.as_tensor(queries, dtype=torch.long)
+    out, idx, route = r["out"].cpu(), r["idx"].cpu(), r["route"].cpu()
+    report = []
+    compare_long_head(w, Q[0, 0], K[0, 0], V[0, 0], out[0, 0][qs], idx[0, 0], route[0, 0][qs], queries,
+                      report=report)
+    print(name, report)
+    assert int(route.min()) >= 0 and int(route.max()) < w.m
     assert bool(torch.isfinite(r["out"].float()).all())

@@ -466,3 +466,24 @@ def test_planted_mistake_fails_a_pin(name, tmp_path):
             except AssertionError:
                 failures += 1
     assert failures >= 1, name
+
+
+def test_threaded_driver_matches_head():
+    # The long-sequence parity tests run the same oracle steps landmark row
+    # by landmark row over host threads; the results must be head()'s, bit
+    # for bit, and scores_row / attend_one must restate head()'s rows.
+    w = synth.WORKLOADS["long1d"].scaled(B=1, H=1, N=4096, gw=4096, pw=16, m=16, k=100)
+    Q, K, V = synth.make_inputs(w)
+    a = oracle.head(Q[0, 0], K[0, 0], V[0, 0], w.grid, w.m, w.k, io="bf16", debug=True)
+    qs = [0, 5, 2047, 4095]
+    b = oracle.head_threaded(Q[0, 0], K[0, 0], V[0, 0], w.grid, w.m, w.k, io="bf16", queries=qs, threads=4)
+    for key in ("idx", "Ql", "Vl"):
+        np.testing.assert_array_equal(a[key], b[key])
+    np.testing.assert_array_equal(a["out"][qs], b["out"])
+    np.testing.assert_array_equal(a["route"][qs], b["route"])
+    np.testing.assert_array_equal(a["A"][qs], b["A"])
+    np.testing.assert_array_equal(np.sort(a["R"], 1)[:, ::-1][:, w.k - 1], b["kth"])
+    np.testing.assert_array_equal(oracle.scores_row(a["Ql"][3], K[0, 0]), a["R"][3])
+    q = 5
+    o = oracle.attend_one(Q[0, 0][q], a["A"][q], a["idx"][a["route"][q]], K[0, 0], V[0, 0], a["Vl"], io="bf16")
+    np.testing.assert_array_equal(o, a["out"][q])
