@@ -67,9 +67,12 @@ typedef struct {
  * ph*pw == m; 1 <= ph <= gh; 1 <= pw <= gw; 1 <= k <= N; plan != NULL.
  * Supported (else MITA_ERR_UNSUPPORTED): d in {64, 128}; m <= 1024;
  * k <= 4096; m + k <= 4096; B*H*N*d < 2^40.
- * The plan owns a device workspace on the current device, allocated here
- * (MITA_ERR_OOM if that fails) and freed by mita_destroy().  *plan is set to
- * NULL on failure. */
+ * The plan owns a device workspace on the current device, freed by
+ * mita_destroy().  mita_plan() allocates the part every path needs and the
+ * part of the path the plan starts on (MITA_ERR_OOM if that fails); a path
+ * chosen later by mita_set_option(), and the first mita_backward(), may add
+ * one allocation each, so make those calls before any stream capture.
+ * mita_forward() never allocates.  *plan is set to NULL on failure. */
 int mita_plan(mita_plan_t* plan, int B, int H, int N, int d, mita_grid_t grid,
               int m, int k, mita_dtype_t dtype);
 
@@ -89,9 +92,12 @@ int mita_plan(mita_plan_t* plan, int B, int H, int N, int d, mita_grid_t grid,
 int mita_forward(mita_plan_t plan, const void* Q, const void* K, const void* V, void* out,
                  int32_t* expert_idx, int32_t* route, struct CUstream_st* stream);
 
-/* Synchronise the plan's device and return the device status word of the
- * plan's kernels since the last call (MITA_OK or MITA_ERR_DEVICE /
- * MITA_ERR_TIMEOUT), then clear it. */
+/* Wait for the plan's last mita_forward() / mita_backward() launch and
+ * return the device status word of the plan's kernels since the last call
+ * (MITA_OK or MITA_ERR_DEVICE / MITA_ERR_TIMEOUT), then clear it.  It waits
+ * on that launch's stream position only (an event), not on the whole
+ * device; after a launch captured into a CUDA graph it waits for the whole
+ * device, and after a graph replay the caller synchronises first. */
 int mita_get_status(mita_plan_t plan);
 
 /* Free the workspace and the plan (NULL is a no-op).  Synchronises the
@@ -110,7 +116,9 @@ void mita_destroy(mita_plan_t plan);
  * stating its gradients).  Runs the stage-by-stage kernels with fp32
  * atomics (sums in a nondeterministic order).  MITA_ERR_UNSUPPORTED when the
  * plan routes to s > 1 experts; MITA_ERR_INVALID_ARG for a null or
- * misaligned pointer. */
+ * misaligned pointer.  The first call on a plan allocates the backward's
+ * fp32 workspace (MITA_ERR_OOM if that fails): make it before capturing a
+ * backward in a graph. */
 int mita_backward(mita_plan_t plan, const void* Q, const void* K, const void* V, const void* dOut, float* dQ,
                   float* dK, float* dV, struct CUstream_st* stream);
 

@@ -24,7 +24,8 @@ PATH_NAMES = {PATH_STAGED: "staged", PATH_FUSED: "fused", PATH_TILED: "tiled"}
 # Every entry point declared in include/mita.h.
 EXPORTS = ("mita_plan", "mita_forward", "mita_backward", "mita_get_status", "mita_destroy", "mita_strerror",
            "mita_set_option", "mita_get_path", "mita_get_landmarks", "mita_workspace_bytes",
-           "mita_launch_count", "mita_forward_noalloc", "mita_noalloc_scratch_bytes")
+           "mita_launch_count", "mita_forward_noalloc", "mita_noalloc_scratch_bytes",
+           "mita_testing_bucket", "mita_testing_wait")
 
 
 class MitaError(RuntimeError):
@@ -65,6 +66,8 @@ def load(path: str | None = None):
     lib.mita_launch_count.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64)]
     lib.mita_forward_noalloc.argtypes = [i, i, i, i, Grid, i, i, i, vp, vp, vp, vp, vp, vp, vp]
     lib.mita_noalloc_scratch_bytes.argtypes = []
+    lib.mita_testing_bucket.argtypes = [vp, vp, vp]
+    lib.mita_testing_wait.argtypes = [vp, ctypes.c_longlong, vp]
     for name in EXPORTS:
         if name not in ("mita_destroy", "mita_strerror", "mita_noalloc_scratch_bytes"):
             getattr(lib, name).restype = i

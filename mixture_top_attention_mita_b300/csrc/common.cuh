@@ -112,9 +112,18 @@ struct mita_plan_s {
     float* dQl;            // backward: gradients of Q_l and V_l [BH, m, d] fp32
     float* dVl;
     int landmarks_valid;
-    // workspace (one cudaMalloc)
+    // workspace: the core region (landmarks, experts, routes, buckets,
+    // status) from mita_plan, and the regions only some paths need, each its
+    // own allocation made when a path that needs it is first chosen
     void* ws;
-    size_t ws_bytes;
+    size_t ws_bytes;       // all regions held
+    void* ws_S;            // raw scores (staged and tiled paths, backward)
+    void* ws_tiled;        // tiled path's row keys, value partials, tile lists
+    void* ws_grad;         // backward's fp32 region
+    // completion of the plan's last eager launch, for mita_get_status()
+    cudaEvent_t done;
+    cudaStream_t aux;      // non-blocking stream for the status word's copy
+    int done_valid;
     void* Ql;              // [BH, m, d] io type
     void* Vl;              // [BH, m, d] io type
     float* S;              // [BH, m, N] raw scores (staged path)

@@ -25,6 +25,112 @@ int resolve_path(const mita_plan_s* p) {
     return MITA_PATH_STAGED;
 }
 
+// One device allocation of `bytes` on the plan's device (MITA_ERR_OOM on failure).
+int alloc_region(mita_plan_s* p, void** out, size_t bytes) {
+    int prev = 0;
+    cudaGetDevice(&prev);
+    cudaSetDevice(p->device);
+    const cudaError_t e = cudaMalloc(out, bytes);
+    cudaSetDevice(prev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *out = nullptr;
+        return MITA_ERR_OOM;
+    }
+    p->ws_bytes += bytes;
+    return MITA_OK;
+}
+
+// The regions a path needs beyond the core: raw scores for the staged and
+// tiled paths (and the backward), the tiled path's own buffers, and the
+// backward's fp32 region.  Each is allocated once, the first time it is
+// needed: at plan time for the path the plan starts on, else when an option
+// or the first backward call selects a path that needs it.
+int ensure_scores(mita_plan_s* p) {
+    if (p->ws_S) return MITA_OK;
+    const mita::Shape& s = p->s;
+    int rc = alloc_region(p, &p->ws_S, (size_t)s.BH() * s.m * s.N * 4);
+    if (rc == MITA_OK) p->S = (float*)p->ws_S;
+    return rc;
+}
+
+int ensure_tiled(mita_plan_s* p) {
+    if (p->ws_tiled || !mita::tiled_supported(p->s, p->dtype)) return MITA_OK;
+    int rc = ensure_scores(p);
+    if (rc != MITA_OK) return rc;
+    const mita::Shape& s = p->s;
+    const size_t BH = (size_t)s.BH();
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+    const size_t oRowmax = take(2 * BH * s.m * 4);   // row max, then row min
+    const size_t oVpart = take(mita::tiled_part_bytes(s));
+    const size_t oCursor = take(BH * s.m * 4);
+    const size_t oTiles = take(BH * (size_t)mita::tiled_max_tiles(s) * 4);
+    const size_t oNtiles = take(BH * 4);
+    if ((rc = alloc_region(p, &p->ws_tiled, off)) != MITA_OK) return rc;
+    char* b = (char*)p->ws_tiled;
+    p->rowmax = (uint32_t*)(b + oRowmax);
+    p->vpart = (float*)(b + oVpart);
+    p->cursor = (int32_t*)(b + oCursor);
+    p->tiles = (int32_t*)(b + oTiles);
+    p->ntiles = (int32_t*)(b + oNtiles);
+    return MITA_OK;
+}
+
+int ensure_grad(mita_plan_s* p) {
+    if (p->ws_grad) return MITA_OK;
+    int rc = ensure_scores(p);
+    if (rc != MITA_OK) return rc;
+    const mita::Shape& s = p->s;
+    const size_t BH = (size_t)s.BH();
+    // dQ_l, dV_l, V_l in fp32 [BH, m, d] each, then per landmark row {max S, sum of weights}
+    if ((rc = alloc_region(p, &p->ws_grad, (3 * BH * s.m * s.d + 2 * BH * s.m) * 4)) != MITA_OK) return rc;
+    p->dQl = (float*)p->ws_grad;
+    p->dVl = p->dQl + BH * s.m * s.d;
+    return MITA_OK;
+}
+
+// Regions for the path the plan currently resolves to.
+int ensure_path(mita_plan_s* p) {
+    const int path = resolve_path(p);
+    if (path == MITA_PATH_STAGED) return ensure_scores(p);
+    if (path == MITA_PATH_TILED) return ensure_tiled(p);
+    return MITA_OK;
+}
+
+void free_plan(mita_plan_s* p) {
+    int prev = 0;
+    cudaGetDevice(&prev);
+    cudaSetDevice(p->device);
+    cudaDeviceSynchronize();
+    if (p->ws) cudaFree(p->ws);
+    if (p->ws_S) cudaFree(p->ws_S);
+    if (p->ws_tiled) cudaFree(p->ws_tiled);
+    if (p->ws_grad) cudaFree(p->ws_grad);
+    if (p->done) cudaEventDestroy(p->done);
+    if (p->aux) cudaStreamDestroy(p->aux);
+    cudaSetDevice(prev);
+    free(p);
+}
+
+// Remember the stream's last launch for mita_get_status(); a launch captured
+// into a graph completes only when the graph runs, so then the status waits
+// for the whole device instead.
+void note_launch(mita_plan_s* p, cudaStream_t st) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) {
+        cudaGetLastError();
+        p->done_valid = 0;
+        return;
+    }
+    if (cap != cudaStreamCaptureStatusNone) {
+        p->done_valid = 0;
+        return;
+    }
+    p->done_valid = cudaEventRecord(p->done, st) == cudaSuccess;
+    if (!p->done_valid) cudaGetLastError();
+}
+
 }  // namespace
 
 extern "C" {
@@ -67,48 +173,34 @@ int mita_plan(mita_plan_t* plan, int B, int H, int N, int d, mita_grid_t grid, i
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
     const size_t oQl = take(BH * m * d * e), oVl = take(BH * m * d * e);
-    const size_t oS = take(BH * m * (size_t)N * 4);
     const size_t oIdx = take(BH * m * (size_t)k * 4), oRoute = take(BH * (size_t)N * 4);
     const size_t oCnt = take(BH * m * 4), oOff = take(BH * (m + 1) * 4), oPerm = take(BH * (size_t)N * 4);
     const size_t oStatus = take(256);
-    // backward (fp32): dQ_l, dV_l, V_l, then per landmark row {max S, sum of weights}
-    const size_t oGradL = take((3 * BH * m * d + 2 * BH * m) * 4);
-    const bool tiled = mita::tiled_supported(p->s, dtype);
-    const size_t oRowmax = take(tiled ? 2 * BH * m * 4 : 0);   // row max, then row min
-    const size_t oVpart = take(tiled ? mita::tiled_part_bytes(p->s) : 0);
-    const size_t oCursor = take(tiled ? BH * m * 4 : 0);
-    const size_t oTiles = take(tiled ? BH * (size_t)mita::tiled_max_tiles(p->s) * 4 : 0);
-    const size_t oNtiles = take(tiled ? BH * 4 : 0);
 
-    p->ws_bytes = off;
-    if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
-        cudaGetLastError();
+    if (alloc_region(p, &p->ws, off) != MITA_OK) {
         free(p);
         return MITA_ERR_OOM;
     }
     char* b = (char*)p->ws;
     p->Ql = b + oQl;
     p->Vl = b + oVl;
-    p->S = (float*)(b + oS);
     p->idx = (int32_t*)(b + oIdx);
     p->route = (int32_t*)(b + oRoute);
     p->counts = (int32_t*)(b + oCnt);
     p->offsets = (int32_t*)(b + oOff);
     p->perm = (int32_t*)(b + oPerm);
     p->status = (int32_t*)(b + oStatus);
-    p->dQl = (float*)(b + oGradL);
-    p->dVl = p->dQl + BH * m * d;
-    if (tiled) {
-        p->rowmax = (uint32_t*)(b + oRowmax);
-        p->vpart = (float*)(b + oVpart);
-        p->cursor = (int32_t*)(b + oCursor);
-        p->tiles = (int32_t*)(b + oTiles);
-        p->ntiles = (int32_t*)(b + oNtiles);
-    }
-    if (cudaMemset(p->status, 0, 256) != cudaSuccess) {
-        cudaFree(p->ws);
-        free(p);
+    if (cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&p->aux, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaMemset(p->status, 0, 256) != cudaSuccess) {
+        cudaGetLastError();
+        free_plan(p);
         return MITA_ERR_CUDA;
+    }
+    const int rc = ensure_path(p);
+    if (rc != MITA_OK) {
+        free_plan(p);
+        return rc;
     }
     *plan = p;
     return MITA_OK;
@@ -121,7 +213,7 @@ int mita_set_option(mita_plan_t p, int option, int value) {
             value != MITA_PATH_TILED)
             return MITA_ERR_INVALID_ARG;
         p->path_opt = value;
-        return MITA_OK;
+        return ensure_path(p);
     }
     if (option == MITA_OPT_KEEP_LANDMARKS) {
         if (value != 0 && value != 1) return MITA_ERR_INVALID_ARG;
@@ -136,7 +228,7 @@ int mita_set_option(mita_plan_t p, int option, int value) {
     if (option == MITA_OPT_ROUTES) {
         if (value < 1 || value > mita::kMaxRoutes || value > p->s.m) return MITA_ERR_INVALID_ARG;
         p->routes_s = value;
-        return MITA_OK;
+        return ensure_path(p);
     }
     return MITA_ERR_INVALID_ARG;
 }
@@ -168,9 +260,11 @@ int mita_forward(mita_plan_t p, const void* Q, const void* K, const void* V, voi
         if (!p->rowmax) return MITA_ERR_UNSUPPORTED;
         err = mita::run_tiled(p, Q, K, V, out, idx, rt, st);
     } else {
+        if (!p->S) return MITA_ERR_UNSUPPORTED;
         err = mita::run_staged(p, Q, K, V, out, idx, rt, st);
     }
     if (err != cudaSuccess) return MITA_ERR_CUDA;
+    note_launch(p, st);
     p->landmarks_valid = p->keep_landmarks || path != MITA_PATH_FUSED;
     return MITA_OK;
 }
@@ -182,7 +276,10 @@ int mita_backward(mita_plan_t p, const void* Q, const void* K, const void* V, co
         !aligned16(dV))
         return MITA_ERR_INVALID_ARG;
     if (p->routes_s > 1) return MITA_ERR_UNSUPPORTED;
+    const int rc = ensure_grad(p);
+    if (rc != MITA_OK) return rc;
     if (mita::run_backward(p, Q, K, V, dOut, dQ, dK, dV, (cudaStream_t)stream) != cudaSuccess) return MITA_ERR_CUDA;
+    note_launch(p, (cudaStream_t)stream);
     return MITA_OK;
 }
 
@@ -193,12 +290,16 @@ int mita_get_status(mita_plan_t p) {
     cudaSetDevice(p->device);
     int32_t st = 0;
     int rc = MITA_OK;
-    if (cudaDeviceSynchronize() != cudaSuccess) rc = MITA_ERR_CUDA;
-    else if (cudaMemcpy(&st, p->status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) rc = MITA_ERR_CUDA;
-    else {
+    // wait for the plan's last launch only (the whole device after a
+    // captured one), then read and clear the status word on the plan's own
+    // non-blocking stream, which waits for no other stream
+    const cudaError_t w = p->done_valid ? cudaEventSynchronize(p->done) : cudaDeviceSynchronize();
+    if (w != cudaSuccess) rc = MITA_ERR_CUDA;
+    else if (cudaMemcpyAsync(&st, p->status, 4, cudaMemcpyDeviceToHost, p->aux) != cudaSuccess ||
+             cudaMemsetAsync(p->status, 0, 4, p->aux) != cudaSuccess || cudaStreamSynchronize(p->aux) != cudaSuccess)
+        rc = MITA_ERR_CUDA;
+    else
         rc = st;
-        cudaMemset(p->status, 0, 4);
-    }
     cudaSetDevice(prev);
     return rc;
 }
@@ -226,13 +327,7 @@ int mita_workspace_bytes(mita_plan_t p, uint64_t* bytes) {
 
 void mita_destroy(mita_plan_t p) {
     if (!p) return;
-    int prev = 0;
-    cudaGetDevice(&prev);
-    cudaSetDevice(p->device);
-    cudaDeviceSynchronize();
-    cudaFree(p->ws);
-    cudaSetDevice(prev);
-    free(p);
+    free_plan(p);
 }
 
 }  // extern "C"

@@ -52,7 +52,7 @@ extern "C" int mita_forward_noalloc(int B, int H, int N, int d, mita_grid_t grid
                                     mita_dtype_t dtype, const void* Q, const void* K, const void* V,
                                     void* out, int32_t* expert_idx, int32_t* route,
                                     struct CUstream_st* stream) {
-    if (B < 1 || H < 1 || N < 1 || m < 1 || k < 1 || k > N) return MITA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || d < 1 || m < 1 || k < 1 || k > N) return MITA_ERR_INVALID_ARG;
     if (grid.gh < 1 || grid.gw < 1 || grid.ph < 1 || grid.pw < 1) return MITA_ERR_INVALID_ARG;
     if ((long long)grid.gh * grid.gw != N || (long long)grid.ph * grid.pw != m) return MITA_ERR_INVALID_ARG;
     if (grid.ph > grid.gh || grid.pw > grid.gw) return MITA_ERR_INVALID_ARG;

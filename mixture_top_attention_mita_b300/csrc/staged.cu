@@ -462,6 +462,12 @@ static void launch_bucket(const Shape& s, const int32_t* route, int32_t* counts,
         bucket_kernel<<<s.BH(), 32, 0, st>>>(s, route, counts, offsets, perm, status);
 }
 
+// The bucketing step alone, on a caller-made route array (test entry point).
+cudaError_t testing_bucket(mita_plan_s* p, const int32_t* route, cudaStream_t st) {
+    launch_bucket(p->s, route, p->counts, p->offsets, p->perm, p->status, st);
+    return cudaGetLastError();
+}
+
 // Small vector helpers: a 4-term fused dot product and 4 elements of a row as
 // fp32 (a bf16 is the upper half of the fp32 with the same value).
 MITA_DEV float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

@@ -99,12 +99,13 @@ MITA_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Wait for the phase with the given parity, giving up after about a second
-// (returns false; the caller reports MITA_ERR_TIMEOUT).
-MITA_DEV bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Wait for the phase with the given parity, giving up after `budget` SM
+// cycles (about a second by default; returns false and the caller reports
+// MITA_ERR_TIMEOUT).
+MITA_DEV bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long budget = 2000000000LL) {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity))
-        if (clock64() - t0 > 2000000000LL) return false;
+        if (clock64() - t0 > budget) return false;
     return true;
 }
 MITA_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {

@@ -71,3 +71,18 @@ def test_null_handles(lib):
     assert lib.mita_set_option(None, 0, 0) == 1
     assert lib.mita_get_status(None) == 1
     lib.mita_destroy(None)
+
+
+@pytest.mark.parametrize("d", [0, -64])
+def test_noalloc_rejects_bad_head_dim_as_invalid(lib, d):
+    # the argument checks of mita_plan(): d < 1 is an invalid argument, not
+    # an unsupported size; no device is touched
+    rc = lib.mita_forward_noalloc(1, 1, 196, d, mita.Grid(14, 14, 5, 5), 25, 25, mita.MITA_BF16,
+                                  None, None, None, None, None, None, None)
+    assert rc == 1
+
+
+def test_plan_rejects_bad_head_dim_as_invalid(lib):
+    h = ctypes.c_void_p(1)
+    assert lib.mita_plan(ctypes.byref(h), 1, 1, 196, 0, mita.Grid(14, 14, 5, 5), 25, 25, mita.MITA_BF16) == 1
+    assert h.value is None
