@@ -190,47 +190,79 @@ def variant_name(args):
     return "+".join(parts) if parts else "mita"
 
 
-def cpu_baseline(w, seconds, full=False, shared=True, routes=1, backward=False):
-    """Time the CPU oracle (single thread, fp64) on whole heads of the
-    workload until about ``seconds`` of work; returns query-heads/s
+def _oracle_sample(w, seconds, threads, shared=True, routes=1, backward=False):
+    """Time the CPU oracle (fp64) on ``threads`` host threads, whole heads of
+    the workload spread over the threads, until about ``seconds`` of work.
+    Returns (query-heads/s, description of the sample).  A long sequence
+    (N > 16384) takes all landmark work of one head over the threads and the
+    route and attend steps of a slice of its queries; the per-query time is
+    scaled to all N queries run on the same threads, which the description
+    says."""
+    import oracle
+    if w.N > 16384 and not backward:
+        Q, K, V = synth.make_inputs(w.scaled(B=1, H=1))
+        nq = 256
+        qs = list(range(0, w.N, w.N // nq))[:nq]
+        t0 = time.perf_counter()
+        oracle.head_threaded(Q[0, 0], K[0, 0], V[0, 0], w.grid, w.m, w.k, io=w.dtype, queries=qs[:1],
+                             shared=shared, threads=threads)
+        t_land = time.perf_counter() - t0
+        t1 = time.perf_counter()
+        oracle.head_threaded(Q[0, 0], K[0, 0], V[0, 0], w.grid, w.m, w.k, io=w.dtype, queries=qs, shared=shared,
+                             threads=threads)
+        per_q = max(0.0, (time.perf_counter() - t1 - t_land) / (nq - 1))
+        per_head = t_land + per_q * w.N / threads
+        return w.N / per_head, (f"1 head of {w.name}: every landmark row on {threads} thread(s), route+attend of "
+                                f"{nq} queries; per-query time scaled to {w.N} queries over {threads} thread(s)")
+    n_heads = 16 * threads   # enough heads per batch that every thread stays busy
+    H = min(w.H, n_heads)
+    B = -(-n_heads // H)
+    sample = w.scaled(B=B, H=H)
+    Q, K, V = synth.make_inputs(sample)
+    heads = [(b, h) for b in range(B) for h in range(H)]
+    G = None
+    if backward:
+        G = np.random.default_rng(0).standard_normal((w.N, w.d))
+    done, t0 = 0, time.perf_counter()
+    while True:
+        if backward:
+            from concurrent.futures import ThreadPoolExecutor
+            Qf, Kf, Vf = Q.double().numpy(), K.double().numpy(), V.double().numpy()
+            with ThreadPoolExecutor(max_workers=threads) as ex:
+                list(ex.map(lambda bh: oracle.backward(Qf[bh], Kf[bh], Vf[bh], G, w.grid, w.m, w.k, io=w.dtype,
+                                                       shared=shared), heads))
+            done += len(heads)
+        else:
+            done += oracle.forward_heads_threaded(Q, K, V, w.grid, w.m, w.k, heads, io=w.dtype, shared=shared,
+                                                  s=routes, threads=threads)
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return done * w.N / el, f"{done} whole heads of {w.name} ({done * w.N} query-heads) on {threads} thread(s), {el:.1f} s"
+
+
+def cpu_baseline(w, seconds, shared=True, routes=1, backward=False):
+    """The CPU oracle timed on the host cores: on every core the process may
+    run on (``cores``, one thread each, heads spread over them) and on one
+    core (``value_1core``), about ``seconds`` of work in all; query-heads/s
     (``shared=False``: the routing-only variant)."""
     import oracle
-    Q, K, V = synth.make_inputs(w.scaled(B=1, H=min(w.H, 4)) if not full else w)
-    Qf, Kf, Vf = Q.double().numpy(), K.double().numpy(), V.double().numpy()
-    heads, t0 = 0, time.perf_counter()
-    queries = None
-    if w.N > 16384:   # a long sequence: all landmark work, a slice of queries
-        queries = list(range(0, w.N, max(1, w.N // 512)))
-    nq = w.N if queries is None else len(queries)
-    if backward:   # whole heads only: the backward has no per-query slice
-        queries = None
-        nq = w.N
-        G = np.random.default_rng(0).standard_normal(Qf.shape[2:])
-    while True:
-        h = heads % Q.shape[1]
-        if backward:
-            oracle.backward(Qf[0, h], Kf[0, h], Vf[0, h], G, w.grid, w.m, w.k, io=w.dtype, shared=shared)
-        else:
-            oracle.head(Qf[0, h], Kf[0, h], Vf[0, h], w.grid, w.m, w.k, io=w.dtype, queries=queries, shared=shared,
-                        s=routes)
-        heads += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or (queries is not None and heads >= 1):
-            break
-    if queries is not None:
-        sample = (f"{heads} head(s) of {w.name}: landmark stages on all {w.N} tokens, route+attend on "
-                  f"{nq} queries; time scaled to all {w.N} queries by the attend share")
-        # scale: landmark stages are per head, attend per query; measure attend share separately
-        t1 = time.perf_counter()
-        oracle.head(Qf[0, 0], Kf[0, 0], Vf[0, 0], w.grid, w.m, w.k, io=w.dtype, queries=queries[:1], shared=shared,
-                    s=routes)
-        base = time.perf_counter() - t1
-        per_q = max(0.0, (el / heads - base) / max(1, nq - 1))
-        per_head = base + per_q * w.N
-        return {"value": w.N / per_head, "unit": "query-heads/s", "cores": 1, "kind": "oracle",
-                "sample": sample}
-    return {"value": heads * w.N / el, "unit": "query-heads/s", "cores": 1, "kind": "oracle",
-            "sample": f"{heads} whole heads of {w.name} ({heads * w.N} query-heads), {el:.1f} s, 1 thread"}
+    cores = oracle.threads_available()
+    v1, s1 = _oracle_sample(w, seconds / 2, 1, shared, routes, backward)
+    vn, sn = _oracle_sample(w, seconds / 2, cores, shared, routes, backward)
+    return {"value": vn, "unit": "query-heads/s", "cores": cores, "kind": "oracle", "value_1core": v1,
+            "sample": f"{sn}; one core: {s1}"}
+
+
+def bench_config(w, ws, routes, variant):
+    """The ``config`` object both arms print: the workload, its batch and
+    sequence length, the sharding and the L2 rule of the timed loop."""
+    e = 2 if w.dtype == "bf16" else 4
+    set_bytes = 4 * w.heads * w.N * w.d * e
+    nsets = min(8, max(2, math.ceil(3 * L2_BYTES / set_bytes) + 1))
+    return {"workload": workload_desc(w, routes), "global_batch": w.B * ws, "seq_len": w.N,
+            "parallelism": f"heads sharded over {ws} GPU(s), no collective", "variant": variant,
+            "l2": f"inputs rotate over {nsets} buffer sets ({nsets * set_bytes / 1e6:.0f} MB > 126 MB L2)"}
 
 
 def dist_setup():
@@ -267,25 +299,37 @@ def whole_job_rate(units_per_rank, ms_per_rank, ws, device):
 
 
 def run_reference(args, w, ws, rank):
+    """The reference arm: the CPU oracle on every host core.  Each step runs
+    a bounded sample of the workload's heads (sized so that all steps take
+    about --cpu-seconds) and is timed as it runs; ms_per_step is that time,
+    value the sample's query-heads over it (median step).  The time the
+    whole workload would take at that rate is reported apart, labelled as an
+    extrapolation."""
     if rank != 0:
         return 0
-    import oracle  # noqa: F401  (build happens in cpu_baseline)
-    times = []
-    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
-    for s in range(args.warmup + args.steps):
-        cb = cpu_baseline(w, per_step, shared=not args.routing_only, routes=args.routes, backward=args.backward)
-        if s >= args.warmup:
-            times.append(cb)
-    v = sorted(c["value"] for c in times)[len(times) // 2]
+    import oracle
+    cores = oracle.threads_available()
+    per_step = max(0.05, args.cpu_seconds / max(1, args.steps + args.warmup))
+    rates, times, sample = [], [], ""
+    for st in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        v, sample = _oracle_sample(w, per_step, cores, shared=not args.routing_only, routes=args.routes,
+                                   backward=args.backward)
+        el = time.perf_counter() - t0
+        if st >= args.warmup:
+            rates.append(v)
+            times.append(el)
+    order = sorted(range(len(rates)), key=lambda i: rates[i])
+    mid = order[len(order) // 2]
+    v, ms = rates[mid], 1000.0 * times[mid]
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "query-heads/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * w.heads * w.N / v,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded generator, no dataset)",
-            "config": {"workload": workload_desc(w, args.routes), "global_batch": w.B * ws, "seq_len": w.N,
-                       "parallelism": f"heads sharded, {ws} replica(s)",
-                       "variant": variant_name(args)},
-            "cpu_baseline": {"value": v, "unit": "query-heads/s", "cores": 1, "kind": "oracle",
-                             "sample": times[0]["sample"] + " per step; median over steps"},
+            "config": bench_config(w, ws, args.routes, variant_name(args)),
+            "extrapolated_ms_per_full_workload": round(1000.0 * w.heads * w.N / v, 1),
+            "cpu_baseline": {"value": v, "unit": "query-heads/s", "cores": cores, "kind": "oracle",
+                             "sample": sample + " per step; median step"},
             "e2e": {"value": v, "unit": "query-heads/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -359,8 +403,7 @@ def main():
     # inputs: enough rotating sets that consecutive steps never hit in L2
     Qc, Kc, Vc = synth.make_inputs(w, seed=w.seed + 7919 * rank)
     set_bytes = 4 * Qc.numel() * Qc.element_size()
-    nsets = max(2, math.ceil(3 * L2_BYTES / set_bytes) + 1)
-    nsets = min(nsets, 8)
+    nsets = min(8, max(2, math.ceil(3 * L2_BYTES / set_bytes) + 1))   # as bench_config states
     sets = []
     for s in range(nsets):
         Q, K, V = Qc.to(dev), Kc.to(dev), Vc.to(dev)
@@ -525,11 +568,7 @@ def main():
         line = {"metric": METRIC, "value": value, "unit": "query-heads/s", "n_gpus": ws, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded generator, no dataset)",
-                "config": {"workload": workload_desc(w, args.routes), "global_batch": w.B * ws, "seq_len": w.N,
-                           "parallelism": f"heads sharded over {ws} GPU(s), no collective",
-                           "path": path, "variant": variant_name(args),
-                           "l2": f"inputs rotate over {nsets} buffer sets "
-                                               f"({nsets * set_bytes / 1e6:.0f} MB > 126 MB L2)"},
+                "config": bench_config(w, ws, args.routes, variant_name(args)), "path": path,
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "graph": graph, "gpu_launches": launches,
                 "clocks": clocks, "achieved_tflops": round(tf, 2), "achieved_hbm_gbs": round(bw, 1),
                 "hbm_frac": round(hbm_frac, 4)}

@@ -7,6 +7,7 @@ import json
 import os
 import subprocess
 import sys
+import time
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -15,9 +16,11 @@ REQUIRED = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step
 
 
 def test_reference_arm_prints_one_contract_line():
+    t0 = time.monotonic()
     r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny_f32",
                         "--steps", "2", "--warmup", "1", "--cpu-seconds", "1"],
                        cwd=ROOT, capture_output=True, text=True, timeout=600)
+    wall = time.monotonic() - t0
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
     assert len(lines) == 1, r.stdout[-2000:]
@@ -31,6 +34,8 @@ def test_reference_arm_prints_one_contract_line():
     assert isinstance(d["config"], dict) and d["config"]["workload"].startswith("tiny_f32")
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["steps"] * d["ms_per_step"] / 1000.0 <= wall     # the steps' own time, not a projection
+    assert d["extrapolated_ms_per_full_workload"] > 0
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
