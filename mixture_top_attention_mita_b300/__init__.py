@@ -14,7 +14,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmita.so")
 
 MITA_F32, MITA_BF16 = 0, 1
-MITA_OK = 0
+MITA_OK, MITA_ERR_INVALID_ARG, MITA_ERR_UNSUPPORTED, MITA_ERR_CUDA = 0, 1, 2, 3
+MITA_ERR_TIMEOUT, MITA_ERR_OOM, MITA_ERR_DEVICE = 4, 5, 6
 STATUS = {0: "MITA_OK", 1: "MITA_ERR_INVALID_ARG", 2: "MITA_ERR_UNSUPPORTED", 3: "MITA_ERR_CUDA",
           4: "MITA_ERR_TIMEOUT", 5: "MITA_ERR_OOM", 6: "MITA_ERR_DEVICE"}
 OPT_PATH, OPT_KEEP_LANDMARKS, OPT_ROUTING_ONLY, OPT_ROUTES = 0, 1, 2, 3
