@@ -10,11 +10,12 @@
 //   phase B   contraction [K ; Q] . Q_l^T with mma.sync: raw landmark scores
 //                         (fp32, shared memory) and each query's first argmax
 //                         landmark (the route)
-//   phase C   select      per landmark (warp per landmark) the k best keys,
-//                         ties to the lower index, by a monotone 64-bin
-//                         histogram and an exact rank of the boundary bin;
-//                         the bf16 softmax numerators overwrite the scores;
-//                         one warp bucket-sorts the queries by route
+//   phase C   select      per landmark (an 8-lane group per landmark, four
+//                         per warp) the k best keys, ties to the lower index,
+//                         by a monotone 64-bin histogram and an exact rank of
+//                         the boundary bin's members; the bf16 softmax
+//                         numerators overwrite the scores; one warp
+//                         bucket-sorts the queries by route
 //   phase D   values      V_l = P . V with mma.sync, normalised, bf16
 //   phase E   attention   per (expert, 16 queries) tile: logits against the
 //                         32 shared slots (Q_l) and 32 routed slots (the
@@ -41,25 +42,45 @@ constexpr int kD = 64;
 constexpr int kSlots = 32;      // shared slots (m <= 32) and routed slots (k <= 32)
 constexpr int kMaxN = 256;
 constexpr int kBins = 64;       // histogram bins of the select
-constexpr int kCand = 32;       // boundary-bin members resolved by exact rank
+constexpr int kCandG = 16;      // boundary-bin members ranked exactly per landmark
 constexpr int kTile = 16;       // queries per attention tile
 constexpr int kMaxSmem = 232448;
 constexpr int kTokMax = 1024;   // bin memberships of all landmarks (the pool's token table)
 
+// Select layout: one landmark per 8-lane group, lane g of the group holding
+// the NV = 4 * NV4 consecutive keys [g * NV, g * NV + NV) of the landmark's
+// score row, stored from column g * nvp (nvp = NV, or NV + 4 when NV is a
+// multiple of 8, so that the 16-byte loads of the 8 lanes hit distinct banks).
+constexpr int nv4_of(int N) { return ((N + 7) / 8 + 3) / 4; }
+constexpr int nvp_of(int nv4) { return (4 * nv4) % 8 == 0 ? 4 * nv4 + 4 : 4 * nv4; }
+// Per-landmark scratch inside the landmark's own score row (fp32 words), used
+// after its scores are in registers and before its numerators overwrite it:
+constexpr int kRowHist = 0;                 // 64 bin counts
+constexpr int kRowCand = kBins;             // kCandG (score, key) pairs
+constexpr int kRowTJ = kBins + 2 * kCandG;  // the threshold (score, key)
+constexpr int kRowCnt = kRowTJ + 2;         // members of b* listed so far
+constexpr int kRowScratch = kRowCnt + 1;
+
 struct Layout {
-    int N, np16, nk16, sstr, qkv;
-    int oQ, oK, oV, oQl, oVl, oS, oIdx, oRoute, oPerm, oCnt, oOff, oTiles, oCtl, oBar, oHist,
-        oCand, total;
+    int N, np16, nk16, sstr, nvp, qkv;
+    int oQ, oK, oV, oQl, oVl, oS, oIdx, oRoute, oPerm, oCnt, oOff, oTiles, oCtl, oBar, oTok, total;
 };
 
 static int align_to(int x, int a) { return (x + a - 1) / a * a; }
 
-static Layout make_layout(int N, int m) {
+static Layout make_layout(int N, int m, int ntok) {
     Layout L{};
     L.N = N;
     L.np16 = align_to(N, 16);
     L.nk16 = L.np16 / 16;
-    L.sstr = L.np16 + 4;                 // fp32 words per score row: conflict-free ldmatrix rows
+    L.nvp = nvp_of(nv4_of(N));
+    // fp32 words per score row: the 8 lanes' segments and the row scratch, a
+    // multiple of 4 (16-byte rows) that is 4 mod 8, so that the 8 rows of a
+    // phase-D ldmatrix fall in distinct banks
+    int sstr = std::max(8 * L.nvp, kRowScratch);
+    sstr = align_to(sstr, 4);
+    if (sstr % 8 == 0) sstr += 4;
+    L.sstr = sstr;
     L.qkv = align_to(N * 128, 1024);
     int o = 0;
     auto take = [&](int bytes, int al) { o = align_to(o, al); int r = o; o += bytes; return r; };
@@ -77,8 +98,7 @@ static Layout make_layout(int N, int m) {
     L.oTiles = take((kMaxN / kTile + kSlots) * 4, 16);
     L.oCtl = take(16, 16);
     L.oBar = take(16, 16);
-    L.oHist = take(kWarps * kBins * 4, 16);
-    L.oCand = take(kWarps * kCand * 8, 16);
+    L.oTok = take((ntok + kSlots + 1) * 2, 16);   // the pool's token table, then its landmark starts
     L.total = o + 1024;                  // slack to align the dynamic base to 1024
     return L;
 }
@@ -98,7 +118,10 @@ struct Params {
     int shared;               // 1: the m shared slots join the softmax; 0: routing only
     float rcnt[kSlots];       // 1 / (tokens in the bin of landmark i)
     float cnt[kSlots];        // tokens in the bin of landmark i
-    int win[kSlots];          // 16 - ceil(log2(tokens in the bin)): exact-sum exponent window
+    uint32_t wpair[kSlots];   // 128 win in both 16-bit halves: the exact-sum exponent span test
+    int ntok;                 // entries of the token table
+    int ptasks;               // pool tasks: four landmarks each, the largest bins first
+    uint8_t ptask[kWarps][4]; // landmarks of pool task t (0xff: none)
     uint16_t tstart[kSlots + 1];   // landmark i pools tokens toff[tstart[i] .. tstart[i + 1])
     uint16_t toff[kTokMax];        // byte offset of a token's row in the swizzled Q tile, r*128 + (r%8)*16
 };
@@ -230,8 +253,215 @@ MITA_DEV uint32_t umin16x2(uint32_t a, uint32_t b) {
     return y;
 }
 
+// ---------------------------------------------------------------- the select
+// Expert of one landmark (step 3) and its softmax numerators (for step 4), by
+// the 8-lane group that owns the landmark's score row `srow`.  Lane g holds
+// the raw scores of keys [g NV, g NV + NV) (NaN past key N).  A 64-bin
+// histogram of equal-width bins over [row min, row max] (the bin is a
+// monotone function of the score) finds the bin b* holding the k-th best
+// score; the members of b* are ranked exactly (score descending, key
+// ascending) and the need-th of them is the threshold (T, J).  The expert is
+// every key with (score, key) at or above (T, J) in that order, written in
+// ascending key order to `irow` and `grow`.  The histogram, the members of
+// b* and (T, J) live in the row itself once its scores are in registers; the
+// bf16 numerators exp(s/sqrt d - max) (0 past key N) overwrite its start.
+template <int NV4>
+MITA_DEV void select_landmark(float* srow, int nvp, int N, int k, float cs, uint8_t* irow, int32_t* grow) {
+    constexpr int NV = 4 * NV4;
+    const int lane = threadIdx.x & 31, gl = lane & 7;
+    const unsigned gmask = 0xffu << (lane & 24);
+    const int jbase = gl * NV;
+    float v[NV];
+#pragma unroll
+    for (int u = 0; u < NV4; ++u) {
+        const float4 x = *(const float4*)(srow + gl * nvp + 4 * u);
+        v[4 * u] = x.x;
+        v[4 * u + 1] = x.y;
+        v[4 * u + 2] = x.z;
+        v[4 * u + 3] = x.w;
+    }
+    // row max and min (max and min ignore the NaN padding)
+    float mx = v[0], mn = v[0];
+#pragma unroll
+    for (int e = 1; e < NV; e += 2) {
+        const float b = e + 1 < NV ? v[e + 1] : v[e];
+        mx = max3(mx, v[e], b);
+        mn = min3(mn, v[e], b);
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(gmask, mx, o));
+        mn = fminf(mn, __shfl_xor_sync(gmask, mn, o));
+    }
+    float sc = mx > mn ? (float)kBins / (mx - mn) : 0.0f;
+    float off = -mn * sc;
+    if (!(fabsf(off) <= 3.0e38f)) sc = off = 0.0f;   // overflow: one bin, ranked exactly below
+    // bins: the unsigned conversion takes negatives and NaN to 0
+    int bin[NV];
+#pragma unroll
+    for (int e = 0; e < NV; ++e) bin[e] = (int)min((unsigned)(kBins - 1), __float2uint_rz(fmaf(v[e], sc, off)));
+    int* hist = (int*)srow + kRowHist;
+    __syncwarp(gmask);   // every lane has loaded its scores: the row is scratch now
+    ((int4*)hist)[2 * gl] = make_int4(0, 0, 0, 0);
+    ((int4*)hist)[2 * gl + 1] = make_int4(0, 0, 0, 0);
+    __syncwarp(gmask);
+#pragma unroll
+    for (int e = 0; e < NV; ++e) atomicAdd(&hist[bin[e]], 1);
+    __syncwarp(gmask);
+    // lane g holds bins [8g, 8g + 8); the padding past key N fell into bin 0
+    const int4 h0 = ((const int4*)hist)[2 * gl], h1 = ((const int4*)hist)[2 * gl + 1];
+    int c[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    if (gl == 0) c[0] -= 8 * NV - N;
+    int tot = 0;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) tot += c[b];
+    int suf = tot;   // members of this lane's bins and of every higher lane's
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+        const int y = __shfl_down_sync(gmask, suf, o, 8);
+        if (gl + o < 8) suf += y;
+    }
+    const int above = suf - tot;
+    const bool mine = above < k && suf >= k;   // exactly one lane: the suffix counts fall from N
+    int bstar = 0, need = 0, cstar = 0;
+    if (mine) {
+        int run = above;
+#pragma unroll
+        for (int b = 7; b >= 0; --b) {
+            if (run < k && run + c[b] >= k) {
+                bstar = 8 * gl + b;
+                need = k - run;
+                cstar = c[b];
+            }
+            run += c[b];
+        }
+    }
+    const int src = __ffs(__ballot_sync(gmask, mine)) - 1;
+    bstar = __shfl_sync(gmask, bstar, src);
+    need = __shfl_sync(gmask, need, src);
+    cstar = __shfl_sync(gmask, cstar, src);
+    // (T, J): the need-th best member of bin b*
+    float T;
+    int J;
+    float* tj = srow + kRowTJ;
+    if (cstar <= kCandG) {
+        float2* cand = (float2*)(srow + kRowCand);
+        int* ccnt = (int*)srow + kRowCnt;
+        if (gl == 0) *ccnt = 0;
+        __syncwarp(gmask);
+#pragma unroll
+        for (int e = 0; e < NV; ++e)
+            if (bin[e] == bstar && jbase + e < N) cand[atomicAdd(ccnt, 1)] = make_float2(v[e], __int_as_float(jbase + e));
+        __syncwarp(gmask);
+        for (int ci = gl; ci < cstar; ci += 8) {
+            const float2 me = cand[ci];
+            const int jm = __float_as_int(me.y);
+            int rank = 0;
+            for (int e = 0; e < cstar; ++e) {
+                const float2 o = cand[e];
+                rank += (o.x > me.x || (o.x == me.x && __float_as_int(o.y) < jm)) ? 1 : 0;
+            }
+            if (rank == need - 1) {
+                tj[0] = me.x;
+                tj[1] = me.y;
+            }
+        }
+        __syncwarp(gmask);
+        T = tj[0];
+        J = __float_as_int(tj[1]);
+    } else {
+        // many members (flat or tied rows): the need-th best member's order key
+        // by bisection, then the key of the last one taken among its equals
+        uint32_t key[NV];
+#pragma unroll
+        for (int e = 0; e < NV; ++e) key[e] = (bin[e] == bstar && jbase + e < N) ? order_key(v[e]) : 0u;
+        uint32_t TK = 0u;
+        for (int bb = 31; bb >= 0; --bb) {
+            const uint32_t ct = TK | (1u << bb);
+            int n = 0;
+#pragma unroll
+            for (int e = 0; e < NV; ++e) n += key[e] >= ct ? 1 : 0;
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) n += __shfl_xor_sync(gmask, n, o);
+            if (n >= need) TK = ct;
+        }
+        int gt = 0, eq = 0;
+#pragma unroll
+        for (int e = 0; e < NV; ++e) {
+            gt += key[e] > TK ? 1 : 0;
+            eq += key[e] == TK ? 1 : 0;
+        }
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) gt += __shfl_xor_sync(gmask, gt, o);
+        const int eq_left = need - gt;   // >= 1 members equal to TK are taken, the lowest keys first
+        int x = eq;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            const int y = __shfl_up_sync(gmask, x, o, 8);
+            if (gl >= o) x += y;
+        }
+        const int before = x - eq;
+        int jl = 0;
+        const bool has = before < eq_left && x >= eq_left;
+        if (has) {
+            int r = eq_left - before;
+#pragma unroll
+            for (int e = 0; e < NV; ++e)
+                if (key[e] == TK && r > 0 && --r == 0) jl = jbase + e;
+        }
+        J = __shfl_sync(gmask, jl, __ffs(__ballot_sync(gmask, has)) - 1);
+        T = key_to_float(TK);
+    }
+    // the expert: every key at or above (T, J), in ascending key order; keys
+    // tied with T past J are dropped only when the row has such ties
+    uint32_t sel = 0u;
+#pragma unroll
+    for (int e = 0; e < NV; ++e)
+        if (v[e] >= T) sel |= 1u << e;
+    int ns = __popc(sel);
+    int pos = ns;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+        const int y = __shfl_up_sync(gmask, pos, o, 8);
+        if (gl >= o) pos += y;
+    }
+    if (__shfl_sync(gmask, pos, (lane & 24) | 7) != k) {   // ties at T past J
+        const int Jr = J - jbase;
+        sel = 0u;
+#pragma unroll
+        for (int e = 0; e < NV; ++e)
+            if (v[e] > T || (v[e] == T && e <= Jr)) sel |= 1u << e;
+        ns = __popc(sel);
+        pos = ns;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            const int y = __shfl_up_sync(gmask, pos, o, 8);
+            if (gl >= o) pos += y;
+        }
+    }
+    pos -= ns;
+    while (sel) {
+        const int e = __ffs(sel) - 1;
+        sel &= sel - 1u;
+        irow[pos] = (uint8_t)(jbase + e);
+        grow[pos] = jbase + e;
+        ++pos;
+    }
+    // softmax numerators over the row's own start, bf16 as the MMA reads them
+    const float mb = mx * cs;
+    __syncwarp(gmask);   // every lane has read (T, J) from the row
+    uint2* prow = (uint2*)((__nv_bfloat16*)srow + jbase);
+#pragma unroll
+    for (int u = 0; u < NV4; ++u) {
+        float p[4];
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) p[c4] = ex2(fmaxf(fmaf(v[4 * u + c4], cs, -mb), -INFINITY));   // NaN -> 0
+        prow[u] = make_uint2(pack2(p[0], p[1]), pack2(p[2], p[3]));
+    }
+}
+
 // ---------------------------------------------------------------- the kernel
-template <int NV>   // score values per lane in the select: ceil(N / 32)
+template <int NV4>   // the select's score float4s per lane: nv4_of(N)
 __global__ void __launch_bounds__(kThreads, 2)
     fused_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                  const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapO,
@@ -252,8 +482,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t sstrB = (uint32_t)L.sstr * 4u;
     const unsigned char* Qb = sm + L.oQ;
     float* S_s = (float*)(sm + L.oS);
-    int* hist = (int*)(sm + L.oHist) + warp * kBins;
-    float2* cand = (float2*)(sm + L.oCand) + warp * kCand;
     uint8_t* idx_s = sm + L.oIdx;
     uint8_t* route_s = sm + L.oRoute;
     uint8_t* perm_s = sm + L.oPerm;
@@ -268,7 +496,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         ((uint32_t*)(sm + L.oQl))[e] = 0u;
         ((uint32_t*)(sm + L.oVl))[e] = 0u;
     }
-    for (int e = tid; e < kWarps * kBins; e += kThreads) ((int*)(sm + L.oHist))[e] = 0;
+    uint16_t* toff_s = (uint16_t*)(sm + L.oTok);
+    uint16_t* tstart_s = toff_s + P.ntok;
+    for (int e = tid; e < P.ntok; e += kThreads) toff_s[e] = P.toff[e];
+    for (int e = tid; e <= m; e += kThreads) tstart_s[e] = P.tstart[e];
     if (tid == 0) {
         mbar_init(uBar, 1);
         ctl[1] = 0;
@@ -315,53 +546,100 @@ __global__ void __launch_bounds__(kThreads, 2)
             prefetch_l2(P.Vg + off, (uint32_t)N * 128u);
         }
 
-        // ---------------- phase A: landmark queries (warp per landmark)
-        // Lane L sums features 2L, 2L+1 over the bin's tokens (a flat list of
-        // row offsets; a lane's 4 bytes of a swizzled row sit at offset ^ lx).
-        // The fp32 sums are exact when no value is zero and the exponents span
-        // at most P.win[i] binades (then every partial sum is a multiple of the
-        // smallest value's last bit below 2^24 of them); features without that
-        // certificate are listed and summed again error-free after the loop.
+        // ---------------- phase A: landmark queries (8-lane group per landmark)
+        // Lane g of a group sums features 8g .. 8g + 7 over the bin's tokens
+        // (one 16-byte load of the swizzled row per token) in fp32, and keeps
+        // the largest and smallest magnitude of each feature.  A bin of c
+        // bf16 values whose exponents span at most win = 16 - ceil(log2 c)
+        // binades sums exactly in fp32 (every partial sum is a multiple of the
+        // smallest value's last bit and below 2^24 of them), tested on the
+        // packed exponent fields of the largest and smallest magnitude.
+        // The mean of an exact sum s: q1 = s * (1/c), then one correction step
+        // q = q1 + (s - q1 c) (1/c) with both steps fused multiply-adds gives
+        // the correctly rounded fp32 quotient s / c (checked exhaustively over
+        // every fp32 significand of s for every count c up to 256; s normal),
+        // and its bf16 rounding is the bf16 rounding of s / c (24 >= 2 * 8 + 2
+        // bits: double rounding is innocuous).  A feature without the exactness
+        // certificate is summed again error-free (TwoSum) by its group, each
+        // lane taking every eighth token, and decided exactly (mean_to_bf16).
         {
-            uint16_t* fb_list = (uint16_t*)S_s;   // the scores' region is idle until phase B
-            const uint32_t lx = ((uint32_t)(lane >> 2) << 4) | ((uint32_t)(lane & 3) * 4u);
-            for (int i = warp; i < m; i += kWarps) {
-                const int e0 = P.tstart[i], e1 = P.tstart[i + 1];
-                float s0 = 0.0f, s1 = 0.0f;
-                uint32_t mag_hi = 0u, mag_lo = 0x7fff7fffu;
-#pragma unroll 4
+            const int grp = lane >> 3, gl = lane & 7;
+            const unsigned gmask = 0xffu << (lane & 24);
+            const uint32_t lx = (uint32_t)gl << 4;   // the lane's 16-byte chunk of a row
+            for (int task = warp; task < P.ptasks; task += kWarps) {
+                const int i = P.ptask[task][grp];
+                if (i >= m) continue;
+                const int e0 = tstart_s[i], e1 = tstart_s[i + 1];
+                float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                uint32_t mhi[4] = {0u, 0u, 0u, 0u};
+                uint32_t mlo[4] = {0x7fff7fffu, 0x7fff7fffu, 0x7fff7fffu, 0x7fff7fffu};
+#pragma unroll 2
                 for (int e = e0; e < e1; ++e) {
-                    const uint32_t v = *(const uint32_t*)(Qb + ((uint32_t)P.toff[e] ^ lx));
-                    s0 += __uint_as_float(v << 16);
-                    s1 += __uint_as_float(v & 0xffff0000u);
-                    const uint32_t mag = v & 0x7fff7fffu;
-                    mag_hi = umax16x2(mag_hi, mag);
-                    mag_lo = umin16x2(mag_lo, mag);
+                    const uint4 q = *(const uint4*)(Qb + ((uint32_t)toff_s[e] ^ lx));
+                    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        sum[2 * h] += __uint_as_float(w[h] << 16);
+                        sum[2 * h + 1] += __uint_as_float(w[h] & 0xffff0000u);
+                        const uint32_t a = w[h] & 0x7fff7fffu;
+                        mhi[h] = umax16x2(mhi[h], a);
+                        mlo[h] = umin16x2(mlo[h], a);
+                    }
                 }
-                const int win = P.win[i];
-                const bool exact0 = (mag_lo & 0xffffu) != 0u &&
-                                    (int)((mag_hi >> 7) & 0xffu) - (int)((mag_lo >> 7) & 0xffu) <= win;
-                const bool exact1 = (mag_lo >> 16) != 0u &&
-                                    (int)((mag_hi >> 23) & 0xffu) - (int)((mag_lo >> 23) & 0xffu) <= win;
-                const float cnt = P.cnt[i], rc = P.rcnt[i];
-                unsigned char* dst = sm + L.oQl + ((uint32_t)(i * 128 + (i & 7) * 16) ^ lx);
-                if (exact0) *(__nv_bfloat16*)dst = round_mean(s0, 0.0f, cnt, rc);
-                else fb_list[atomicAdd(&ctl[2], 1)] = (uint16_t)((i << 6) | (2 * lane));
-                if (exact1) *(__nv_bfloat16*)(dst + 2) = round_mean(s1, 0.0f, cnt, rc);
-                else fb_list[atomicAdd(&ctl[2], 1)] = (uint16_t)((i << 6) | (2 * lane + 1));
+                const float rc = P.rcnt[i], cnt = P.cnt[i];
+                const uint32_t wpair = P.wpair[i];
+                uint32_t outw[4], bad = 0u;
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    // exponent fields; no carry: both halves stay below 2^16
+                    const uint32_t lim = (mlo[h] & 0x7f807f80u) + wpair;
+                    const uint32_t over = umax16x2(mhi[h] & 0x7f807f80u, lim) ^ lim;   // nonzero half: span too wide
+                    float q[2];
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        const float q1 = sum[2 * h + x] * rc;
+                        q[x] = fmaf(fmaf(-q1, cnt, sum[2 * h + x]), rc, q1);
+                    }
+                    outw[h] = pack2(q[0], q[1]);
+                    bad |= ((over & 0xffffu) ? 1u : 0u) << (2 * h);
+                    bad |= ((over >> 16) ? 1u : 0u) << (2 * h + 1);
+                }
+                // uncertified features (rare): the group sums each one again error-free
+                unsigned lanes = __ballot_sync(gmask, bad != 0u);
+                while (lanes) {
+                    const int src = __ffs(lanes) - 1;
+                    lanes &= lanes - 1u;
+                    uint32_t fb = __shfl_sync(gmask, bad, src);
+                    while (fb) {
+                        const int f = __ffs(fb) - 1;
+                        fb &= fb - 1u;
+                        const int feat = 8 * (src & 7) + f;
+                        const uint32_t fx = ((uint32_t)(feat >> 3) << 4) | ((uint32_t)(feat & 7) * 2u);
+                        float hi = 0.0f, lo = 0.0f;
+                        for (int e = e0 + gl; e < e1; e += 8)
+                            acc2(hi, lo, __uint_as_float((uint32_t)*(const uint16_t*)(Qb + ((uint32_t)toff_s[e] ^ fx)) << 16));
+#pragma unroll
+                        for (int o = 1; o < 8; o <<= 1) {
+                            const float oh = __shfl_xor_sync(gmask, hi, o), ol = __shfl_xor_sync(gmask, lo, o);
+                            float sh, se;
+                            two_sum(hi, oh, sh, se);
+                            hi = sh;
+                            lo += ol + se;
+                        }
+                        const uint32_t hb = __bfloat16_as_ushort(mean_to_bf16(hi, lo, cnt));
+                        const uint32_t sh = (f & 1) ? 16u : 0u, keep = ~(0xffffu << sh), put = hb << sh;
+                        const int h = f >> 1;
+                        const bool me = lane == src;
+                        outw[0] = me && h == 0 ? (outw[0] & keep) | put : outw[0];
+                        outw[1] = me && h == 1 ? (outw[1] & keep) | put : outw[1];
+                        outw[2] = me && h == 2 ? (outw[2] & keep) | put : outw[2];
+                        outw[3] = me && h == 3 ? (outw[3] & keep) | put : outw[3];
+                    }
+                }
+                *(uint4*)(sm + L.oQl + ((uint32_t)(i * 128 + (i & 7) * 16) ^ lx)) =
+                    make_uint4(outw[0], outw[1], outw[2], outw[3]);
             }
             __syncthreads();
-            const int nfb = ctl[2];
-            for (int x = tid; x < nfb; x += kThreads) {
-                const int i = fb_list[x] >> 6, f = fb_list[x] & 63;
-                const uint32_t fx = ((uint32_t)(f >> 3) << 4) | ((uint32_t)(f & 7) * 2u);
-                float hi = 0.0f, lo = 0.0f;
-                for (int e = P.tstart[i]; e < P.tstart[i + 1]; ++e)
-                    acc2(hi, lo, __uint_as_float((uint32_t)*(const uint16_t*)(Qb + ((uint32_t)P.toff[e] ^ fx)) << 16));
-                *(__nv_bfloat16*)(sm + L.oQl + ((uint32_t)(i * 128 + (i & 7) * 16) ^ fx)) = mean_to_bf16(hi, lo, P.cnt[i]);
-            }
-            __syncthreads();
-            if (tid == 0) ctl[2] = 0;
             if (P.Ql_keep)
                 for (int x = tid; x < m * 32; x += kThreads) {
                     const int i = x >> 5, fp = x & 31;
@@ -373,6 +651,11 @@ __global__ void __launch_bounds__(kThreads, 2)
 
         // ---------------- phase B: [K ; Q] . Q_l^T  -> scores and routes
         {
+            // score columns of keys N .. 8 NV - 1 hold NaN (the select's padding)
+            constexpr int NV = 4 * NV4;
+            for (int i = warp; i < m; i += kWarps)
+                for (int j = N + lane; j < 8 * NV; j += 32)
+                    S_s[i * L.sstr + (j / NV) * L.nvp + j % NV] = __int_as_float(0x7fc00000);
             uint32_t bq[4][4][2];   // Q_l as B operand: [n8 tile][k16 step][2]
 #pragma unroll
             for (int n = 0; n < 4; n += 2)
@@ -409,9 +692,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                         for (int h = 0; h < 2; ++h) {
                             const int j = r0 + g + 8 * h;
                             const int i = 8 * n + 2 * t;
+                            const int cj = (nvp_of(NV4) == 4 * NV4) ? j : (j / (4 * NV4)) * L.nvp + j % (4 * NV4);
                             if (j < N) {
-                                if (i < m) S_s[i * L.sstr + j] = acc[n][2 * h];
-                                if (i + 1 < m) S_s[(i + 1) * L.sstr + j] = acc[n][2 * h + 1];
+                                if (i < m) S_s[i * L.sstr + cj] = acc[n][2 * h];
+                                if (i + 1 < m) S_s[(i + 1) * L.sstr + cj] = acc[n][2 * h + 1];
                             }
                         }
                 } else {
@@ -445,152 +729,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         __syncthreads();
 
-        // ---------------- phase C: experts and numerators (warp per landmark)
-        for (int i = warp; i < m; i += kWarps) {
-            float* srow = S_s + i * L.sstr;
-            float v[NV];
-#pragma unroll
-            for (int u = 0; u < NV; ++u) {
-                const int j = lane + 32 * u;
-                v[u] = srow[j < N ? j : 0];   // a slot past N repeats key 0: max / min unchanged
+        // ---------------- phase C: experts and numerators (8-lane group per landmark)
+        {
+            const int ntask = (m + 3) >> 2;
+            for (int task = warp; task < ntask; task += kWarps) {
+                const int i = 4 * task + (lane >> 3);
+                if (i < m)
+                    select_landmark<NV4>(S_s + i * L.sstr, L.nvp, N, k, cs, idx_s + i * kSlots,
+                                         P.idx + ((size_t)head * m + i) * k);
             }
-            float mx = v[0], mn = v[0];
-#pragma unroll
-            for (int u = 1; u < NV; u += 2) {
-                const float b = u + 1 < NV ? v[u + 1] : v[u];
-                mx = max3(mx, v[u], b);
-                mn = min3(mn, v[u], b);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-            }
-            // monotone binning: a larger score never lands in a lower bin
-            const float range = mx - mn;
-            const float sc = range > 0.0f ? (float)kBins / range : 0.0f;
-            int bin[NV];
-#pragma unroll
-            for (int u = 0; u < NV; ++u) {
-                const int j = lane + 32 * u;
-                bin[u] = -1;
-                if (j < N) {
-                    bin[u] = min(kBins - 1, (int)((v[u] - mn) * sc));
-                    atomicAdd(&hist[bin[u]], 1);
-                }
-            }
-            __syncwarp();
-            // lane L holds bins 2L, 2L+1; suffix counts from the top bin down
-            const int2 hw = *(const int2*)(hist + 2 * lane);
-            *(int2*)(hist + 2 * lane) = make_int2(0, 0);   // each lane clears what it read
-            const int tot = hw.x + hw.y;
-            int suf = tot;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_down_sync(0xffffffffu, suf, o);
-                if (lane + o < 32) suf += y;
-            }
-            const int above = suf - tot;   // members of bins above 2L+1
-            const bool mine = above < k && suf >= k;
-            int bstar = 0, need = 0, cstar = 0;
-            if (mine) {
-                if (above + hw.y >= k) {
-                    bstar = 2 * lane + 1;
-                    need = k - above;
-                    cstar = hw.y;
-                } else {
-                    bstar = 2 * lane;
-                    need = k - above - hw.y;
-                    cstar = hw.x;
-                }
-            }
-            const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
-            bstar = __shfl_sync(0xffffffffu, bstar, src);
-            need = __shfl_sync(0xffffffffu, need, src);
-            cstar = __shfl_sync(0xffffffffu, cstar, src);
-            // boundary bin: take the `need` best of its `cstar` members
-            uint32_t bsel = 0;   // bit u: member lane + 32u is taken
-            if (need < cstar) {
-                if (cstar <= kCand) {
-                    // members to lanes 0 .. cstar-1, exact rank by (score desc, index asc)
-                    int base = 0, slot[NV];
-#pragma unroll
-                    for (int u = 0; u < NV; ++u) {
-                        const bool isb = bin[u] == bstar;
-                        const unsigned bal = __ballot_sync(0xffffffffu, isb);
-                        slot[u] = base + __popc(bal & ((1u << lane) - 1u));
-                        if (isb) cand[slot[u]] = make_float2(v[u], __int_as_float(lane + 32 * u));
-                        base += __popc(bal);
-                    }
-                    __syncwarp();
-                    const float2 me = cand[lane < cstar ? lane : 0];
-                    const int jm = __float_as_int(me.y);
-                    int rank = 0;
-                    for (int e = 0; e < cstar; ++e) {
-                        const float ve = __shfl_sync(0xffffffffu, me.x, e);
-                        const int je = __shfl_sync(0xffffffffu, jm, e);
-                        rank += (ve > me.x || (ve == me.x && je < jm)) ? 1 : 0;
-                    }
-                    const unsigned chosen = __ballot_sync(0xffffffffu, lane < cstar && rank < need);
-#pragma unroll
-                    for (int u = 0; u < NV; ++u)
-                        if (bin[u] == bstar && ((chosen >> slot[u]) & 1u)) bsel |= 1u << u;
-                    __syncwarp();
-                } else {
-                    // many members (degenerate scores): bisect the order key
-                    uint32_t key[NV];
-#pragma unroll
-                    for (int u = 0; u < NV; ++u) key[u] = order_key(v[u]);
-                    uint32_t T = 0;
-                    for (int b = 31; b >= 0; --b) {
-                        const uint32_t cand_t = T | (1u << b);
-                        int c = 0;
-#pragma unroll
-                        for (int u = 0; u < NV; ++u) c += (bin[u] == bstar && key[u] >= cand_t) ? 1 : 0;
-                        c = __reduce_add_sync(0xffffffffu, c);
-                        if (c >= need) T = cand_t;
-                    }
-                    int gt = 0;
-#pragma unroll
-                    for (int u = 0; u < NV; ++u) gt += (bin[u] == bstar && key[u] > T) ? 1 : 0;
-                    gt = __reduce_add_sync(0xffffffffu, gt);
-                    int eq_left = need - gt, base = 0;
-#pragma unroll
-                    for (int u = 0; u < NV; ++u) {
-                        const bool isb = bin[u] == bstar;
-                        const bool eq = isb && key[u] == T;
-                        const unsigned bal = __ballot_sync(0xffffffffu, eq);
-                        const int r = base + __popc(bal & ((1u << lane) - 1u));
-                        if ((isb && key[u] > T) || (eq && r < eq_left)) bsel |= 1u << u;
-                        base += __popc(bal);
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int u = 0; u < NV; ++u)
-                    if (bin[u] == bstar) bsel |= 1u << u;
-            }
-            // the expert in ascending key order
-            int pos = 0;
-            uint8_t* irow = idx_s + i * kSlots;
-#pragma unroll
-            for (int u = 0; u < NV; ++u) {
-                const bool sel = bin[u] > bstar || (bsel >> u & 1u);
-                const unsigned bal = __ballot_sync(0xffffffffu, sel);
-                if (sel) irow[pos + __popc(bal & ((1u << lane) - 1u))] = (uint8_t)(lane + 32 * u);
-                pos += __popc(bal);
-            }
-            // softmax numerators of the landmark row, bf16 as the MMA reads them,
-            // written over the row's own scores (every lane has read them)
-            __nv_bfloat16* prow = (__nv_bfloat16*)srow;
-            const float mb = mx * cs;
-#pragma unroll
-            for (int u = 0; u < NV; ++u) {
-                const int j = lane + 32 * u;
-                if (j < L.np16) prow[j] = __float2bfloat16_rn(j < N ? ex2(fmaf(v[u], cs, -mb)) : 0.0f);
-            }
-            __syncwarp();
-            if (lane < k) P.idx[((size_t)head * m + i) * k + lane] = irow[lane];
         }
         if (warp == kWarps - 1) {
             // bucket sort of the queries by route; tiles of up to kTile queries
@@ -795,16 +942,29 @@ static bool make_map(CUtensorMap* map, const void* base, int rows, int box_rows)
     return tma_map_bf16(map, base, fz::kD, (size_t)rows, fz::kD, box_rows);
 }
 
+// Entries of the pool's token table: the tokens of every landmark's bin.
+static int pool_tokens(const Shape& s) {
+    int n = 0;
+    for (int i = 0; i < s.m; ++i) {
+        const int r = i / s.pw, c = i % s.pw;
+        const int r0 = r * s.gh / s.ph, r1 = ((r + 1) * s.gh + s.ph - 1) / s.ph;
+        const int c0 = c * s.gw / s.pw, c1 = ((c + 1) * s.gw + s.pw - 1) / s.pw;
+        n += (r1 - r0) * (c1 - c0);
+    }
+    return n;
+}
+
 bool fused_supported(const Shape& s, mita_dtype_t dtype) {
     if (dtype != MITA_BF16 || s.d != fz::kD) return false;
     if (s.N > fz::kMaxN || s.m > fz::kSlots || s.k > fz::kSlots) return false;
-    return fz::make_layout(s.N, s.m).total <= fz::kMaxSmem;
+    const int ntok = pool_tokens(s);
+    return ntok <= fz::kTokMax && fz::make_layout(s.N, s.m, ntok).total <= fz::kMaxSmem;
 }
 
-template <int NV>
+template <int NV4>
 static cudaError_t launch_nv(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                              const CUtensorMap& mo, const fz::Params& prm, int device, cudaStream_t st) {
-    auto kern = fz::fused_kernel<NV>;
+    auto kern = fz::fused_kernel<NV4>;
     cudaError_t e = ensure_smem_attr((const void*)kern, prm.L.total);
     if (e != cudaSuccess) return e;
     int sms = 0;
@@ -827,7 +987,7 @@ cudaError_t run_fused(mita_plan_s* p, const void* Q, const void* K, const void* 
         return cudaErrorInvalidValue;
     fz::Params prm{};
     prm.s = s;
-    prm.L = fz::make_layout(s.N, s.m);
+    prm.L = fz::make_layout(s.N, s.m, pool_tokens(s));
     prm.Qg = (const unsigned char*)Q;
     prm.Kg = (const unsigned char*)K;
     prm.Vg = (const unsigned char*)V;
@@ -853,14 +1013,26 @@ cudaError_t run_fused(mita_plan_s* p, const void* Q, const void* K, const void* 
             }
         const int n = (r1 - r0) * (c1 - c0);
         prm.cnt[i] = (float)n;
+        prm.rcnt[i] = 1.0f / (float)n;
+        // a bin of n bf16 values sums exactly in fp32 when their exponents span
+        // at most win = 16 - ceil(log2 n) binades
         int lg = 0;
         while ((1 << lg) < n) ++lg;
-        prm.rcnt[i] = 1.0f / (float)n;
-        prm.win[i] = 16 - lg;
+        const int w = 128 * (16 - lg);
+        prm.wpair[i] = w > 0 ? ((uint32_t)w | ((uint32_t)w << 16)) : 0u;
     }
     prm.tstart[s.m] = (uint16_t)ntok;
+    prm.ntok = ntok;
+    {   // pool tasks: landmarks by bin size, largest first, four per task
+        int order[fz::kSlots];
+        for (int i = 0; i < s.m; ++i) order[i] = i;
+        std::stable_sort(order, order + s.m, [&](int a, int b) { return prm.cnt[a] > prm.cnt[b]; });
+        prm.ptasks = (s.m + 3) / 4;
+        for (int t = 0; t < fz::kWarps; ++t)
+            for (int g = 0; g < 4; ++g) prm.ptask[t][g] = 4 * t + g < s.m ? (uint8_t)order[4 * t + g] : 0xff;
+    }
     cudaError_t e;
-    switch ((s.N + 31) / 32) {
+    switch (fz::nv4_of(s.N)) {
         case 1: e = launch_nv<1>(mq, mk, mv, mo, prm, p->device, st); break;
         case 2: e = launch_nv<2>(mq, mk, mv, mo, prm, p->device, st); break;
         case 3: e = launch_nv<3>(mq, mk, mv, mo, prm, p->device, st); break;

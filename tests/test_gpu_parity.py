@@ -232,6 +232,54 @@ def test_landmarks_match_oracle(path):
             np.testing.assert_allclose(Vl[b, h], o["Vl"], rtol=0, atol=2 ** -7)
 
 
+def _midpoint_bins(seed):
+    """bf16 inputs on a 12 x 16 grid pooled to 4 x 4 bins of 12 tokens each:
+    features 0-15 hold integers below 256 whose bin sums are 12 k + 6 (the
+    exact mean k + 1/2 is a bf16 rounding midpoint: ties to even); features
+    16-31 the same with one token of each bin replaced by +-2^-20 (the exact
+    mean sits just off the midpoint and the values span 27 binades, past the
+    exact-fp32-sum window); features 32-63 N(0, 1)."""
+    w = W["deit_t"].scaled(B=1, H=2, N=192, gh=12, gw=16, ph=4, pw=4, m=16, k=16)
+    rng = np.random.default_rng(seed)
+    Q = rng.standard_normal((w.B, w.H, w.N, w.d))
+    for b in range(w.B):
+        for h in range(w.H):
+            for r in range(4):
+                for c in range(4):
+                    toks = [y * 16 + x for y in range(3 * r, 3 * r + 3) for x in range(4 * c, 4 * c + 4)]
+                    for f in range(32):
+                        k = int(rng.integers(128, 220))
+                        target = 12 * k + 6
+                        n = 12 if f < 16 else 11
+                        vals = np.full(n, target // n)
+                        vals[: target - vals.sum()] += 1
+                        rng.shuffle(vals)
+                        Q[b, h, toks[:n], f] = vals
+                        if f >= 16:
+                            Q[b, h, toks[11], f] = (2.0 ** -20) * (1 if rng.random() < 0.5 else -1)
+    Qt = torch.from_numpy(Q).to(torch.bfloat16)
+    assert torch.equal(Qt[..., :32].double(), torch.from_numpy(Q[..., :32]))   # exact in bf16
+    _, K, V = synth.make_inputs(w, seed=seed + 1)
+    return w, Qt.contiguous(), K, V
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_pool_rounding_at_midpoints_and_wide_spans(path):
+    """Q_l is the correctly rounded bin mean where it is hardest: exact
+    means on bf16 midpoints, and means a hair off a midpoint from bins whose
+    values span too many binades for an exact fp32 sum."""
+    import oracle
+    w, Q, K, V = _midpoint_bins(5)
+    _skip_unbuilt(w, path)
+    r = _run(w, Q, K, V, path, keep=True)
+    Ql = r["Ql"].cpu().double().numpy()
+    for b in range(w.B):
+        for h in range(w.H):
+            o = oracle.head(Q[b, h], K[b, h], V[b, h], w.grid, w.m, w.k, io=w.dtype, debug=True)
+            np.testing.assert_array_equal(Ql[b, h], o["Ql"])
+    compare_batch(w, Q, K, V, r["out"], r["idx"], r["route"], exact=False)
+
+
 EDGE = [
     # full attention + one pooled key: k = N, m = 1
     W["deit_t"].scaled(B=1, H=2, m=1, ph=1, pw=1, k=196),
