@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--backward", action="store_true",
                     help="time mita_backward (input gradients for an output gradient) instead of the forward")
     ap.add_argument("--no-soak", action="store_true", help="skip the untimed repeats that extend clock sampling")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the graph-timed forwards of the other workloads reported beside the main line")
     return ap.parse_args()
 
 
@@ -378,6 +380,54 @@ def long_sweep(args):
     return 0
 
 
+def measure_forward(mita, w, steps, dev, stream):
+    """The graph-timed forward of another workload with the main line's
+    method: rotating input sets above L2, the K steps captured once into one
+    CUDA graph and replayed between CUDA events.  Returns ms per step and the
+    roofline fraction of measured peak (the slower of HBM and tensor time)."""
+    Qc, Kc, Vc = synth.make_inputs(w)
+    set_bytes = 4 * Qc.numel() * Qc.element_size()
+    nsets = min(8, max(2, math.ceil(3 * L2_BYTES / set_bytes) + 1))
+    sets = []
+    for _ in range(nsets):
+        Q, K, V = Qc.to(dev), Kc.to(dev), Vc.to(dev)
+        sets.append((Q, K, V, torch.empty_like(Q), torch.empty(w.B, w.H, w.m, w.k, dtype=torch.int32, device=dev),
+                     torch.empty(w.B, w.H, w.N, dtype=torch.int32, device=dev)))
+    plan = mita.Plan.for_workload(w)
+    for i in range(3):
+        plan.forward(*sets[i % nsets], stream)
+    if plan.status() != mita.MITA_OK:
+        raise RuntimeError(f"{w.name}: device status {plan.status()}")
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
+        cs = torch.cuda.current_stream()
+        for i in range(steps):
+            plan.forward(*sets[i % nsets], cs)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if plan.status() != mita.MITA_OK:
+        raise RuntimeError(f"{w.name}: device status after the timed steps")
+    ms = e0.elapsed_time(e1) / steps
+    nbytes, flops = algorithmic(w)
+    pk = peaks()
+    t_hbm, t_tc = nbytes / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12)
+    out = {"workload": workload_desc(w), "path": plan.path, "ms_per_step": round(ms, 5),
+           "value": w.heads * w.N / (ms / 1000.0), "unit": "query-heads/s",
+           "roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor", "frac": round(max(t_hbm, t_tc) / (ms / 1000.0), 4)},
+           "steps": steps, "l2": f"inputs rotate over {nsets} buffer sets"}
+    plan.close()
+    del sets, g
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     args = parse()
     ws, rank, local = dist_setup()
@@ -567,6 +617,20 @@ def main():
     if graph_error:
         timing["graph_error"] = graph_error
 
+    # the other workloads' forwards, timed the same way,
+    # beside the main line (default run only)
+    others = None
+    if (not args.no_others and not args.backward and not args.routing_only and args.routes == 1
+            and args.path == "auto" and rank == 0):
+        others = {}
+        for name in ("deit_s", "deit_t", "hires56", "long1d"):
+            if name == args.workload:
+                continue
+            try:
+                others[name] = measure_forward(mita, synth.WORKLOADS[name], args.steps, dev, stream)
+            except Exception as exc:
+                others[name] = {"error": str(exc).splitlines()[0][:200]}
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.cpu_seconds, shared=not args.routing_only, routes=args.routes,
@@ -578,6 +642,7 @@ def main():
                 "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded generator, no dataset)",
                 "config": bench_config(w, ws, args.routes, variant_name(args)), "path": path,
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "timing": timing, "gpu_launches": launches,
+                "other_workloads": others,
                 "clocks": clocks, "achieved_tflops": round(tf, 2), "achieved_hbm_gbs": round(bw, 1),
                 "hbm_frac": round(hbm_frac, 4)}
         print(json.dumps(line))
