@@ -119,6 +119,7 @@ struct Params {
     float rcnt[kSlots];       // 1 / (tokens in the bin of landmark i)
     float cnt[kSlots];        // tokens in the bin of landmark i
     uint32_t wpair[kSlots];   // 128 win in both 16-bit halves: the exact-sum exponent span test
+    long long offset_cycles;  // start offset of the second CTA of each SM (0: none)
     int ntok;                 // entries of the token table
     int ptasks;               // pool tasks: four landmarks each, the largest bins first
     uint8_t ptask[kWarps][4]; // landmarks of pool task t (0xff: none)
@@ -517,6 +518,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_load_2d(uV, &mapV, 0, blockIdx.x * N, uBar);
     }
 
+    // The two CTAs of an SM run the same phases on equal heads; started
+    // together they stay in step and contend for the same units phase after
+    // phase.  The second CTA of each SM (blocks are placed breadth first)
+    // starts about a quarter of a head later, so that one CTA's selection and
+    // pooling overlap the other's tensor-core phases (measured at DeiT-S:
+    // 111.4 -> 109.7 us per forward; offsets of a tenth or a whole head gain
+    // nothing).
+    if (P.offset_cycles > 0 && (int)blockIdx.x >= (int)gridDim.x / 2) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < P.offset_cycles) {}
+    }
     const float cs = P.scale_log2;
     int it = 0;
     for (int head = blockIdx.x; head < BH; head += gridDim.x, ++it) {
@@ -973,7 +985,9 @@ static cudaError_t launch_nv(const CUtensorMap& mq, const CUtensorMap& mk, const
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int slots = sms * per_sm;
     const int grid = prm.s.BH() < slots ? prm.s.BH() : slots;
-    kern<<<grid, fz::kThreads, prm.L.total, st>>>(mq, mk, mv, mo, prm);
+    fz::Params p2 = prm;
+    p2.offset_cycles = grid > sms ? 50LL * prm.s.N : 0;   // ~a quarter of a head's time
+    kern<<<grid, fz::kThreads, prm.L.total, st>>>(mq, mk, mv, mo, p2);
     return cudaGetLastError();
 }
 
