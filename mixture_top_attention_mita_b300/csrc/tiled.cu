@@ -51,18 +51,28 @@ int max_tiles(const Shape& s) { return (s.N + qt_of(s.d) - 1) / qt_of(s.d) + s.m
 
 
 // ---------------------------------------------------------------- pool
-// Q_l (bf16): block per (landmark i, head bh), 128 threads.  Thread t sums the
+// Q_l (bf16): block per (landmark i, head bh), 128 threads; the block also
+// resets the landmark's row max, row min and query count for the kernels
+// after it (in place of three memsets).  Thread t sums the
 // 8 features of 16-byte group t % G (G = D / 8) over the bin's tokens
 // t / G, t / G + 128 / G, ... (one 16-byte load per token, four in flight),
 // each feature with TwoSum compensation; the 128 / G partial (hi, lo) pairs of
 // a feature are then combined the same way and the correctly rounded mean is
 // decided exactly against c times the midpoints (mean_to_bf16).
 template <int D>
-__global__ void __launch_bounds__(128) tl_pool(Shape s, const bf16* __restrict__ Q, bf16* __restrict__ Ql) {
+__global__ void __launch_bounds__(128) tl_pool(Shape s, const bf16* __restrict__ Q, bf16* __restrict__ Ql,
+                                               uint32_t* __restrict__ rowmax, uint32_t* __restrict__ rowmin,
+                                               int32_t* __restrict__ counts) {
     chain_wait_and_trigger();
     constexpr int G = D / 8, TL = 128 / G;   // feature groups, token lanes
     __shared__ float2 part[TL][D];
     const int i = blockIdx.x, bh = blockIdx.y, t = threadIdx.x, fg = t % G, tln = t / G;
+    if (t == 0) {
+        const size_t r = (size_t)bh * s.m + i;
+        rowmax[r] = 0u;             // below every score's order key
+        rowmin[r] = 0xffffffffu;    // above every score's order key
+        counts[r] = 0;
+    }
     int r0, r1, c0, c1;
     pool_bin(i / s.pw, s.gh, s.ph, r0, r1);
     pool_bin(i % s.pw, s.gw, s.pw, c0, c1);
@@ -596,14 +606,12 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
     bf16* Vl = (bf16*)p->Vl;
     uint32_t* rowmin = p->rowmax + (size_t)BH * s.m;
     cudaError_t err;
-    if ((err = cudaMemsetAsync(p->rowmax, 0, (size_t)BH * s.m * 4, st)) != cudaSuccess) return err;
-    if ((err = cudaMemsetAsync(rowmin, 0xff, (size_t)BH * s.m * 4, st)) != cudaSuccess) return err;
-    if ((err = cudaMemsetAsync(p->counts, 0, (size_t)BH * s.m * 4, st)) != cudaSuccess) return err;
     // launches overlap their predecessor's tail on short rows, where launch
     // latency is a visible share of the chain; on long rows (kernels of
     // hundreds of microseconds) the overlap measured slower and is off
     const bool chain = s.N <= kChainMaxN;
-    if ((err = launch_chained(chain, tl_pool<D>, dim3(s.m, BH), dim3(128), 0, st, s, Q, Ql)) != cudaSuccess)
+    if ((err = launch_chained(chain, tl_pool<D>, dim3(s.m, BH), dim3(128), 0, st, s, Q, Ql, p->rowmax, rowmin,
+                              p->counts)) != cudaSuccess)
         return err;
     const int ns = nsplit(s), G = head_group(s);
     for (int h0 = 0; h0 < BH; h0 += G) {
