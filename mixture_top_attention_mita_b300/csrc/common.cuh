@@ -137,7 +137,7 @@ struct mita_plan_s {
     uint32_t* rowmax;      // [2, BH, m] order keys of each landmark's largest, then smallest, raw score
     float* vpart;          // [head group, splits, m, d + 1] landmark-value partials
     int32_t* cursor;       // [BH, m]   bucket scatter cursors
-    int32_t* tiles;        // [BH, max tiles] attention tiles (expert << 16 | chunk)
+    int32_t* tiles;        // [BH, max tiles] int2 attention tiles (expert << 16 | queries, first position)
     int32_t* ntiles;       // [BH]
     uint64_t launches;     // kernels launched so far
 };

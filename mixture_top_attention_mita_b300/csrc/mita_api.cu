@@ -65,7 +65,7 @@ int ensure_tiled(mita_plan_s* p) {
     const size_t oRowmax = take(2 * BH * s.m * 4);   // row max, then row min
     const size_t oVpart = take(mita::tiled_part_bytes(s));
     const size_t oCursor = take(BH * s.m * 4);
-    const size_t oTiles = take(BH * (size_t)mita::tiled_max_tiles(s) * 4);
+    const size_t oTiles = take(BH * (size_t)mita::tiled_max_tiles(s) * 8);   // int2 per tile
     const size_t oNtiles = take(BH * 4);
     if ((rc = alloc_region(p, &p->ws_tiled, off)) != MITA_OK) return rc;
     char* b = (char*)p->ws_tiled;

@@ -20,7 +20,7 @@
 //   tc_route        q . Q_l^T per query tile, first argmax (the route), and
 //                   per-landmark query counts
 //   tl_bucket_off   per head: bucket offsets, cursors and the list of
-//                   (expert, 64-query chunk) attention tiles
+//                   attention tiles (expert, queries, first bucket position)
 //   tl_bucket_put   queries scattered to their bucket
 //   tl_attend       per tile: the 64 queries of one expert against the m
 //                   shared slots (Q_l, V_l) and the k routed slots (the
@@ -356,9 +356,10 @@ __global__ void tl_values_fin(Shape s, const float* __restrict__ part, int ns, b
 
 // ---------------------------------------------------------------- buckets
 // One warp per head: bucket offsets (exclusive scan of the counts), the
-// scatter cursors and the attention tile list (expert << 16 | chunk).
+// scatter cursors and the attention tile list: per tile (expert << 16 |
+// queries, first position in the head's bucketed query order).
 __global__ void tl_bucket_off(Shape s, const int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                              int32_t* __restrict__ cursor, int32_t* __restrict__ tiles,
+                              int32_t* __restrict__ cursor, int2* __restrict__ tiles,
                               int32_t* __restrict__ ntiles, int maxt, int qt) {
     chain_wait_and_trigger();
     const int bh = blockIdx.x, lane = threadIdx.x;
@@ -378,7 +379,8 @@ __global__ void tl_bucket_off(Shape s, const int32_t* __restrict__ counts, int32
             cursor[(size_t)bh * s.m + i] = carry + x - c;
             for (int e = 0; e < nt; ++e) {
                 const int tt = tcarry + y - nt + e;
-                if (tt < maxt) tiles[(size_t)bh * maxt + tt] = (i << 16) | e;
+                if (tt < maxt)
+                    tiles[(size_t)bh * maxt + tt] = make_int2((i << 16) | min(qt, c - e * qt), carry + x - c + e * qt);
             }
         }
         carry += __shfl_sync(0xffffffffu, x, 31);
@@ -419,8 +421,8 @@ template <int D, int QT>
 __global__ void __launch_bounds__(2 * QT, D == 64 ? 5 : 1)
     tl_attend(Shape s, const bf16* __restrict__ Q, const bf16* __restrict__ K, const bf16* __restrict__ V,
               const bf16* __restrict__ Ql, const bf16* __restrict__ Vl, const int32_t* __restrict__ idx,
-              const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm,
-              const int32_t* __restrict__ tiles, const int32_t* __restrict__ ntiles, int maxt,
+              const int32_t* __restrict__ perm, const int2* __restrict__ tiles,
+              const int32_t* __restrict__ ntiles, int maxt,
               bf16* __restrict__ out, float cs, int shared, int32_t* __restrict__ status) {
     chain_wait_and_trigger();
     constexpr int RB = 2 * D, CH = D / 8, KS = D / 16, NT = D / 8;
@@ -431,9 +433,8 @@ __global__ void __launch_bounds__(2 * QT, D == 64 ? 5 : 1)
     const int bh = blockIdx.y, tile = blockIdx.x;
     if (tile >= ntiles[bh]) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, t = lane & 3;
-    const int e = tiles[(size_t)bh * maxt + tile] >> 16, chunk = tiles[(size_t)bh * maxt + tile] & 0xffff;
-    const int qstart = offsets[(size_t)bh * (s.m + 1) + e] + chunk * QT;
-    const int nq = min(QT, offsets[(size_t)bh * (s.m + 1) + e + 1] - qstart);
+    const int2 td = tiles[(size_t)bh * maxt + tile];
+    const int e = td.x >> 16, nq = td.x & 0xffff, qstart = td.y;
     const int L = s.m + s.k, nblk = (L + 63) / 64;
     const int32_t* E = idx + ((size_t)bh * s.m + e) * s.k;
     const uint32_t uq = smem_u32(sm), ukv = uq + QT * RB;   // kv buffer b: K at ukv + b*2*64*RB, V after it
@@ -484,6 +485,7 @@ __global__ void __launch_bounds__(2 * QT, D == 64 ? 5 : 1)
 #pragma unroll
     for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
     float m0 = -INFINITY, m1 = -INFINITY;   // running max (raw logits) of rows g, g+8
+    const bool active = warp * 16 < nq;     // the warp's 16 rows hold at least one query
     for (int b = 0; b < nblk; ++b) {
         if (b + 1 < nblk) {
             stage(b + 1);
@@ -492,96 +494,100 @@ __global__ void __launch_bounds__(2 * QT, D == 64 ? 5 : 1)
             cp_async_wait<0>();
         }
         __syncthreads();
-        if (b == 0) {
+        if (active) {   // warps past the tile's queries only stage rows and wait
+            if (b == 0) {
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk)
+                    ldsm_x4(uq + swz<RB>(warp * 16 + arow, 2 * kk + (lane >> 4)), qa[kk][0], qa[kk][1], qa[kk][2],
+                            qa[kk][3]);
+            }
+            const uint32_t kb = ukv + (uint32_t)(b & 1) * 2u * 64u * RB, vb = kb + 64u * RB;
+            float sc[8][4];
+#pragma unroll
+            for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.0f;
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk)
-                ldsm_x4(uq + swz<RB>(warp * 16 + arow, 2 * kk + (lane >> 4)), qa[kk][0], qa[kk][1], qa[kk][2],
-                        qa[kk][3]);
-        }
-        const uint32_t kb = ukv + (uint32_t)(b & 1) * 2u * 64u * RB, vb = kb + 64u * RB;
-        float sc[8][4];
 #pragma unroll
-        for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.0f;
+                for (int np = 0; np < 4; ++np) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kb + swz<RB>(np * 16 + brow, 2 * kk + ((lane >> 3) & 1)), b0, b1, b2, b3);
+                    mma16816(sc[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+                    mma16816(sc[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+                }
+            if (b * 64 + 64 > L) {   // padding slots of the last block
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk)
+                for (int n = 0; n < 8; ++n)
 #pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(kb + swz<RB>(np * 16 + brow, 2 * kk + ((lane >> 3) & 1)), b0, b1, b2, b3);
-                mma16816(sc[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-                mma16816(sc[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+                    for (int x = 0; x < 4; ++x)
+                        if (b * 64 + 8 * n + 2 * t + (x & 1) >= L) sc[n][x] = -INFINITY;
             }
-        if (b * 64 + 64 > L) {   // padding slots of the last block
+            if (!shared && b * 64 < s.m) {   // routing only: the shared slots take no weight
 #pragma unroll
-            for (int n = 0; n < 8; ++n)
+                for (int n = 0; n < 8; ++n)
 #pragma unroll
-                for (int x = 0; x < 4; ++x)
-                    if (b * 64 + 8 * n + 2 * t + (x & 1) >= L) sc[n][x] = -INFINITY;
-        }
-        if (!shared && b * 64 < s.m) {   // routing only: the shared slots take no weight
+                    for (int x = 0; x < 4; ++x)
+                        if (b * 64 + 8 * n + 2 * t + (x & 1) < s.m) sc[n][x] = -INFINITY;
+            }
+            float bm0 = -INFINITY, bm1 = -INFINITY;
 #pragma unroll
-            for (int n = 0; n < 8; ++n)
+            for (int n = 0; n < 8; ++n) {
+                bm0 = fmaxf(bm0, fmaxf(sc[n][0], sc[n][1]));
+                bm1 = fmaxf(bm1, fmaxf(sc[n][2], sc[n][3]));
+            }
 #pragma unroll
-                for (int x = 0; x < 4; ++x)
-                    if (b * 64 + 8 * n + 2 * t + (x & 1) < s.m) sc[n][x] = -INFINITY;
-        }
-        float bm0 = -INFINITY, bm1 = -INFINITY;
+            for (int x = 1; x <= 2; x <<= 1) {
+                bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, x));
+                bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
+            }
+            const float n0 = fmaxf(m0, bm0), n1 = fmaxf(m1, bm1);
+            const float f0 = ex2((m0 - n0) * cs), f1 = ex2((m1 - n1) * cs);   // 0 on the first block
+            m0 = n0;
+            m1 = n1;
 #pragma unroll
-        for (int n = 0; n < 8; ++n) {
-            bm0 = fmaxf(bm0, fmaxf(sc[n][0], sc[n][1]));
-            bm1 = fmaxf(bm1, fmaxf(sc[n][2], sc[n][3]));
-        }
+            for (int n = 0; n < NT; ++n) {
+                o[n][0] *= f0;
+                o[n][1] *= f0;
+                o[n][2] *= f1;
+                o[n][3] *= f1;
+            }
+            osum[0] *= f0;
+            osum[1] *= f0;
+            osum[2] *= f1;
+            osum[3] *= f1;
+            const float mb0 = n0 * cs, mb1 = n1 * cs;
+            uint32_t pa[4][4];
 #pragma unroll
-        for (int x = 1; x <= 2; x <<= 1) {
-            bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, x));
-            bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
-        }
-        const float n0 = fmaxf(m0, bm0), n1 = fmaxf(m1, bm1);
-        const float f0 = ex2((m0 - n0) * cs), f1 = ex2((m1 - n1) * cs);   // 0 on the first block
-        m0 = n0;
-        m1 = n1;
+            for (int n = 0; n < 8; ++n) {
+                pa[n >> 1][(n & 1) * 2 + 0] = pack2(ex2(fmaf(sc[n][0], cs, -mb0)), ex2(fmaf(sc[n][1], cs, -mb0)));
+                pa[n >> 1][(n & 1) * 2 + 1] = pack2(ex2(fmaf(sc[n][2], cs, -mb1)), ex2(fmaf(sc[n][3], cs, -mb1)));
+            }
+            const int vrow = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-            o[n][0] *= f0;
-            o[n][1] *= f0;
-            o[n][2] *= f1;
-            o[n][3] *= f1;
-        }
-        osum[0] *= f0;
-        osum[1] *= f0;
-        osum[2] *= f1;
-        osum[3] *= f1;
-        const float mb0 = n0 * cs, mb1 = n1 * cs;
-        uint32_t pa[4][4];
+            for (int ks = 0; ks < 4; ++ks) {
+                mma16816(osum, pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], kOnes2, kOnes2);
 #pragma unroll
-        for (int n = 0; n < 8; ++n) {
-            pa[n >> 1][(n & 1) * 2 + 0] = pack2(ex2(fmaf(sc[n][0], cs, -mb0)), ex2(fmaf(sc[n][1], cs, -mb0)));
-            pa[n >> 1][(n & 1) * 2 + 1] = pack2(ex2(fmaf(sc[n][2], cs, -mb1)), ex2(fmaf(sc[n][3], cs, -mb1)));
-        }
-        const int vrow = (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            mma16816(osum, pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], kOnes2, kOnes2);
-#pragma unroll
-            for (int np = 0; np < NT / 2; ++np) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(vb + swz<RB>(ks * 16 + vrow, 2 * np + (lane >> 4)), b0, b1, b2, b3);
-                mma16816(o[2 * np], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], b0, b1);
-                mma16816(o[2 * np + 1], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], b2, b3);
+                for (int np = 0; np < NT / 2; ++np) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(vb + swz<RB>(ks * 16 + vrow, 2 * np + (lane >> 4)), b0, b1, b2, b3);
+                    mma16816(o[2 * np], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], b0, b1);
+                    mma16816(o[2 * np + 1], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], b2, b3);
+                }
             }
         }
         __syncthreads();   // this buffer is restaged two blocks later
     }
     // normalise; the rows go over the warp's own query rows, then out
-    const float inv0 = rcp(osum[0]), inv1 = rcp(osum[2]);
-    const int srow = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+    if (active) {
+        const float inv0 = rcp(osum[0]), inv1 = rcp(osum[2]);
+        const int srow = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-    for (int np = 0; np < NT / 2; ++np) {
-        const uint32_t r0 = pack2(o[2 * np][0] * inv0, o[2 * np][1] * inv0);
-        const uint32_t r1 = pack2(o[2 * np][2] * inv1, o[2 * np][3] * inv1);
-        const uint32_t r2 = pack2(o[2 * np + 1][0] * inv0, o[2 * np + 1][1] * inv0);
-        const uint32_t r3 = pack2(o[2 * np + 1][2] * inv1, o[2 * np + 1][3] * inv1);
-        stsm_x4(uq + swz<RB>(srow, 2 * np + (lane >> 4)), r0, r1, r2, r3);
+        for (int np = 0; np < NT / 2; ++np) {
+            const uint32_t r0 = pack2(o[2 * np][0] * inv0, o[2 * np][1] * inv0);
+            const uint32_t r1 = pack2(o[2 * np][2] * inv1, o[2 * np][3] * inv1);
+            const uint32_t r2 = pack2(o[2 * np + 1][0] * inv0, o[2 * np + 1][1] * inv0);
+            const uint32_t r3 = pack2(o[2 * np + 1][2] * inv1, o[2 * np + 1][3] * inv1);
+            stsm_x4(uq + swz<RB>(srow, 2 * np + (lane >> 4)), r0, r1, r2, r3);
+        }
     }
     __syncthreads();
     for (int x = tid; x < nq * CH; x += NTH) {
@@ -642,7 +648,7 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
     const int maxt = max_tiles(s);
     constexpr int QT = qt_of(D);
     if ((err = launch_chained(chain, tl_bucket_off, dim3(BH), dim3(32), 0, st, s, (const int32_t*)p->counts, p->offsets,
-                              p->cursor, p->tiles, p->ntiles, maxt, QT)) != cudaSuccess)
+                              p->cursor, (int2*)p->tiles, p->ntiles, maxt, QT)) != cudaSuccess)
         return err;
     if ((err = launch_chained(chain, tl_bucket_put, dim3((s.N + 255) / 256, BH), dim3(256), 0, st, s, (const int32_t*)route,
                               p->cursor, p->perm, p->status)) != cudaSuccess)
@@ -652,8 +658,8 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
         auto kern = tl_attend<D, QT>;
         ensure_smem_attr((const void*)kern, smem);
         if ((err = launch_chained(chain, kern, dim3(maxt, BH), dim3(2 * QT), smem, st, s, Q, K, V, (const bf16*)Ql,
-                                  (const bf16*)Vl, (const int32_t*)idx, (const int32_t*)p->offsets,
-                                  (const int32_t*)p->perm, (const int32_t*)p->tiles, (const int32_t*)p->ntiles, maxt,
+                                  (const bf16*)Vl, (const int32_t*)idx, (const int32_t*)p->perm,
+                                  (const int2*)p->tiles, (const int32_t*)p->ntiles, maxt,
                                   out, cs, p->routing_only ? 0 : 1, p->status)) != cudaSuccess)
             return err;
     }
