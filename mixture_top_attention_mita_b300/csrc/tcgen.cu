@@ -11,6 +11,8 @@
 //              next tile's numerators and V copy overlap the current MMAs).
 //   tc_route   q . Q_l^T for 128 queries against all landmarks; each thread
 //              owns one query and takes the first argmax (the route).
+//   tc_scores_route  both of the above for one tile of 128 tokens when m <= 128
+//              (S^T = K . Q_l^T and Q . Q_l^T side by side in tensor memory).
 // Step numbers refer to the operator of 36Kr / 新智元 "注意力也是FFN？",
 // section "用少量地标查询，同时构造全局概括与细节专家": scores are step 2,
 // landmark values step 4, routes step 5.
@@ -342,6 +344,128 @@ __global__ void __launch_bounds__(128) tc_route(const __grid_constant__ CUtensor
     if (warp == 0) tmem_free(tmem, (uint32_t)tcols);
 }
 
+// ---------------------------------------------------------------- scores and routes
+// Scores and routes of one tile of 128 tokens (m <= 128 landmarks): both
+// contractions take the token rows as M and the landmarks as N, against the
+// one Q_l tile, S^T = K . Q_l^T at tensor-memory column 0 and R = Q . Q_l^T at
+// column tcols / 2.  Thread t of the epilogue owns token n0 + t: it stores its
+// column of S (for each landmark the warp's 32 consecutive keys are one
+// 128-byte store), the warp's max and min of each landmark's scores (one
+// floating-point redux each) go into the block's row keys, and the thread takes the
+// first argmax of its query's logits (the route).  The block then adds its
+// row keys and route counts to the global ones.
+template <int D>
+__global__ void __launch_bounds__(128) tc_scores_route(const __grid_constant__ CUtensorMap mK,
+                                                       const __grid_constant__ CUtensorMap mQ,
+                                                       const __grid_constant__ CUtensorMap mQl, Shape s, int nb,
+                                                       int tcols, float* __restrict__ S, uint32_t* __restrict__ rowmax,
+                                                       uint32_t* __restrict__ rowmin, int32_t* __restrict__ route,
+                                                       int32_t* __restrict__ counts, int32_t* __restrict__ status) {
+    chain_wait_and_trigger();
+    constexpr int KC = D / 64;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ uint32_t tslot;
+    __shared__ __align__(8) uint64_t bars[2];
+    __shared__ uint32_t smax[128], smin[128];
+    __shared__ int hist[128];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (smem_u32(smem) & 1023u) {
+        if (tid == 0) atomicExch(status, (int)MITA_ERR_DEVICE);
+        return;
+    }
+    const int n0 = blockIdx.x * 128, bh = blockIdx.y, m = s.m, N = s.N;
+    const uint32_t sK = smem_u32(smem), sQ = sK + KC * kChunk, sB = sQ + KC * kChunk;
+    const uint32_t bchunk = (uint32_t)nb * 128u;   // bytes per 64-column chunk of the landmark tile
+    const uint32_t bar_ld = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[1]);
+    smax[tid] = 0u;
+    smin[tid] = 0xffffffffu;
+    hist[tid] = 0;
+    if (tid == 0) {
+        mbar_init(bar_ld, 1);
+        mbar_init(bar_mma, 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc(smem_u32(&tslot), (uint32_t)tcols);
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = tslot, tR = tmem + (uint32_t)(tcols / 2);
+    if (tid == 0) {
+        mbar_expect_tx(bar_ld, KC * (2 * kChunk + bchunk));
+        for (int kc = 0; kc < KC; ++kc) {
+            tma_load_2d(sK + kc * kChunk, &mK, kc * 64, bh * N + n0, bar_ld);
+            tma_load_2d(sQ + kc * kChunk, &mQ, kc * 64, bh * N + n0, bar_ld);
+            tma_load_2d(sB + kc * bchunk, &mQl, kc * 64, bh * m, bar_ld);
+        }
+        if (mbar_wait_bounded(bar_ld, 0)) {
+            fence_after();
+            const uint32_t idesc = idesc_bf16(128, nb, 0, 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t oa = (kk >> 2) * kChunk + (kk & 3) * 32;
+                const uint64_t db = desc_kmajor(sB + (kk >> 2) * bchunk + (kk & 3) * 32);
+                mma_bf16(tmem, desc_kmajor(sK + oa), db, idesc, kk > 0);
+                mma_bf16(tR, desc_kmajor(sQ + oa), db, idesc, kk > 0);
+            }
+            mma_commit(bar_mma);
+        }
+    }
+    if (!mbar_wait_bounded(bar_mma, 0)) {
+        if (lane == 0) atomicExch(status, (int)MITA_ERR_TIMEOUT);
+    } else {
+        fence_after();
+        const int n = n0 + warp * 32 + lane;
+        const bool live = n < N;
+        const uint32_t lanes = (uint32_t)(warp * 32) << 16;
+        float* scol = S + (size_t)bh * m * N + n;
+        for (int c0 = 0; c0 < nb; c0 += 32) {
+            float v[32];
+            tmem_ld32(tmem + lanes + c0, v);
+            float mine_hi = -INFINITY, mine_lo = INFINITY;   // lane j keeps landmark c0 + j's
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int c = c0 + j;
+                if (c < m) {   // block-uniform
+                    if (live) scol[(size_t)c * N] = v[j];
+                    float hi, lo;
+                    asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(hi) : "f"(live ? v[j] : -INFINITY));
+                    asm("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(lo) : "f"(live ? v[j] : INFINITY));
+                    mine_hi = lane == j ? hi : mine_hi;
+                    mine_lo = lane == j ? lo : mine_lo;
+                }
+            }
+            if (c0 + lane < m) {
+                atomicMax(&smax[c0 + lane], order_key(mine_hi));
+                atomicMin(&smin[c0 + lane], order_key(mine_lo));
+            }
+        }
+        float best = -INFINITY;
+        int arg = 0;
+        for (int c0 = 0; c0 < nb; c0 += 32) {
+            float v[32];
+            tmem_ld32(tR + lanes + c0, v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (c0 + j < m && v[j] > best) {   // ascending landmarks, strict: first argmax
+                    best = v[j];
+                    arg = c0 + j;
+                }
+        }
+        if (live) {
+            route[(size_t)bh * N + n] = arg;
+            atomicAdd(&hist[arg], 1);
+        }
+    }
+    fence_before();
+    __syncthreads();
+    if (tid < m) {
+        const size_t r = (size_t)bh * m + tid;
+        if (smax[tid] != 0u) atomicMax(&rowmax[r], smax[tid]);
+        if (smin[tid] != 0xffffffffu) atomicMin(&rowmin[r], smin[tid]);
+        if (hist[tid]) atomicAdd(&counts[r], hist[tid]);
+    }
+    if (warp == 0) tmem_free(tmem, (uint32_t)tcols);
+}
+
 }  // namespace tcg
 
 // ---------------------------------------------------------------- host side
@@ -419,6 +543,34 @@ static cudaError_t tc_route_t(const Shape& s, const void* Q, const void* Ql, int
                                     nb, tcols, route, counts, status);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t tc_scores_route_t(const Shape& s, const void* Ql, const void* K, const void* Q, float* S,
+                                     uint32_t* rowmax, uint32_t* rowmin, int32_t* route, int32_t* counts,
+                                     int32_t* status, cudaStream_t st, bool chain) {
+    const int nb = (s.m + 15) / 16 * 16;
+    int tcols = 32;
+    while (tcols < 2 * nb) tcols <<= 1;
+    CUtensorMap mk, mq, ml;
+    if (!map_rows(&mk, K, D, (size_t)s.BH() * s.N, 128) || !map_rows(&mq, Q, D, (size_t)s.BH() * s.N, 128) ||
+        !map_rows(&ml, Ql, D, (size_t)s.BH() * s.m, nb))
+        return cudaErrorInvalidValue;
+    const int smem = (D / 64) * (2 * (int)tcg::kChunk + nb * 128) + 1024;
+    ensure_smem_attr((const void*)tcg::tc_scores_route<D>, smem);
+    cudaError_t le = launch_chained(chain, tcg::tc_scores_route<D>, dim3((s.N + 127) / 128, s.BH()), dim3(128), smem, st,
+                                    mk, mq, ml, s, nb, tcols, S, rowmax, rowmin, route, counts, status);
+    if (le != cudaSuccess) return le;
+    return cudaGetLastError();
+}
+
+bool tc_scores_route_supported(const Shape& s) { return s.m <= 128; }
+
+cudaError_t tc_scores_route(const Shape& s, const void* Ql, const void* K, const void* Q, float* S, uint32_t* rowmax,
+                            uint32_t* rowmin, int32_t* route, int32_t* counts, int32_t* status, cudaStream_t st,
+                            bool chain) {
+    return s.d == 64 ? tc_scores_route_t<64>(s, Ql, K, Q, S, rowmax, rowmin, route, counts, status, st, chain)
+                     : tc_scores_route_t<128>(s, Ql, K, Q, S, rowmax, rowmin, route, counts, status, st, chain);
 }
 
 int tc_value_splits(const Shape& s) { return (s.N + tc_value_keys(s) - 1) / tc_value_keys(s); }

@@ -8,7 +8,8 @@
 //   tl_pool         Q_l, correctly rounded bin means (16-byte loads, TwoSum
 //                   partials per token lane combined error-free)
 //   tc_scores       S = Q_l . K^T (fp32, workspace) and each landmark's row
-//                   max and min
+//                   max and min (with the routes, tc_scores_route, when
+//                   m <= 128)
 //   tl_topk_bits    per landmark the k best keys (ties to the lower index):
 //                   a 2048-bin histogram over [min, max], an exact rank of the
 //                   boundary bin's members, the expert as a bitmap over the
@@ -620,14 +621,21 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
                               p->counts)) != cudaSuccess)
         return err;
     const int ns = nsplit(s), G = head_group(s);
+    // up to 128 landmarks: scores and routes from one kernel per token tile
+    const bool scores_route = tc_scores_route_supported(s) && G == BH;
     for (int h0 = 0; h0 < BH; h0 += G) {
         Shape sg = s;
         sg.B = 1;
         sg.H = min(G, BH - h0);
         const size_t mo = (size_t)h0 * s.m, no = (size_t)h0 * s.N;
-        if ((err = tc_scores(sg, Ql + mo * D, K + no * D, p->S, p->rowmax + mo, rowmin + mo, p->status, st, chain)) !=
-            cudaSuccess)
+        if (scores_route) {
+            if ((err = tc_scores_route(s, Ql, K, Q, p->S, p->rowmax, rowmin, route, p->counts, p->status, st, chain)) !=
+                cudaSuccess)
+                return err;
+        } else if ((err = tc_scores(sg, Ql + mo * D, K + no * D, p->S, p->rowmax + mo, rowmin + mo, p->status, st,
+                                    chain)) != cudaSuccess) {
             return err;
+        }
         if (s.N <= kBitsMaxN) {
             auto kern = s.N <= kShortRow ? tl_topk_bits<256> : tl_topk_bits<kNB>;
             if ((err = launch_chained(chain, kern, dim3(s.m, sg.H), dim3(kTB), 0, st, sg, (const float*)p->S,
@@ -644,7 +652,10 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
             return err;
         p->launches += 4;
     }
-    if ((err = tc_route(s, Q, Ql, route, p->counts, p->status, st, chain)) != cudaSuccess) return err;
+    if (!scores_route) {
+        if ((err = tc_route(s, Q, Ql, route, p->counts, p->status, st, chain)) != cudaSuccess) return err;
+        p->launches += 1;
+    }
     const int maxt = max_tiles(s);
     constexpr int QT = qt_of(D);
     if ((err = launch_chained(chain, tl_bucket_off, dim3(BH), dim3(32), 0, st, s, (const int32_t*)p->counts, p->offsets,
@@ -663,7 +674,7 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
                                   out, cs, p->routing_only ? 0 : 1, p->status)) != cudaSuccess)
             return err;
     }
-    p->launches += 5;
+    p->launches += 4;
     return cudaGetLastError();
 }
 
