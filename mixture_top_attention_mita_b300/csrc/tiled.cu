@@ -11,10 +11,12 @@
 //                   max and min (with the routes, tc_scores_route, when
 //                   m <= 128)
 //   tl_topk_bits    per landmark the k best keys (ties to the lower index):
-//                   a 2048-bin histogram over [min, max], an exact rank of the
-//                   boundary bin's members, the expert as a bitmap over the
-//                   row read out in key order (rows up to 64K keys; longer
-//                   rows use the staged path's radix select)
+//                   a 256- or 2048-bin histogram over [min, max], an exact
+//                   rank of the boundary bin's members, the expert as a bitmap
+//                   over the row read out in key order (rows up to 64K keys;
+//                   longer rows use the staged path's radix select; rows up
+//                   to 4096 keys: tl_topk_reg, the same with the row held in
+//                   registers)
 //   tc_values       split-K partial sums of exp(S / sqrt d - max) . V and of
 //                   the row sums, per split of 1024-4096 keys
 //   tl_values_fin   V_l = sum of partials / sum of row sums, bf16
@@ -341,6 +343,152 @@ __global__ void __launch_bounds__(kTB) tl_topk_bits(Shape s, const float* __rest
     }
 }
 
+// Rows up to kRegRowN keys (the 56x56 layer's 3136): the expert of
+// tl_topk_bits<256>, with thread t holding keys t, t + kTB, ... of the row in
+// registers.  The row is read once; the second pass recomputes each key's bin
+// (one fused multiply-add) from its register, and warp w's lanes hold the 32
+// consecutive keys of bitmap word 8u + w in register u.
+constexpr int kRegVPT = 16;
+constexpr int kRegRowN = kRegVPT * kTB;
+
+__global__ void __launch_bounds__(kTB, 6) tl_topk_reg(Shape s, const float* __restrict__ S,
+                                                   const uint32_t* __restrict__ rowmax,
+                                                   const uint32_t* __restrict__ rowmin, int32_t* __restrict__ idx) {
+    chain_wait_and_trigger();
+    constexpr int NB = 256;   // one bin per thread in the boundary search
+    __shared__ int hist[NB];
+    __shared__ uint32_t bits[kRegRowN / 32];
+    __shared__ float cval[kCandMax];
+    __shared__ int cidx[kCandMax];
+    __shared__ int wsum[kTB / 32];
+    __shared__ int sh[4];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int N = s.N, k = s.k, nw = (N + 31) >> 5;
+    const size_t r = (size_t)blockIdx.y * s.m + blockIdx.x;
+    const float* row = S + r * N;
+    const float mx = key_to_float(rowmax[r]), mn = key_to_float(rowmin[r]);
+    float sc = mx > mn ? (float)NB / (mx - mn) : 0.0f;
+    float off = -mn * sc;
+    if (!(fabsf(off) <= 3.0e38f)) sc = off = 0.0f;   // overflow: one bin, resolved by bisection
+    // a monotone function of the score; the conversion takes negatives to 0
+    auto bin_of = [&](float v) { return min(NB - 1, (int)fmaf(v, sc, off)); };
+    float v[kRegVPT];
+#pragma unroll
+    for (int u = 0; u < kRegVPT; ++u) {
+        const int j = tid + kTB * u;
+        v[u] = j < N ? __ldg(row + j) : 0.0f;
+    }
+    hist[tid] = 0;
+    for (int w = tid; w < nw; w += kTB) bits[w] = 0u;
+    if (tid == 0) sh[3] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kRegVPT; ++u)
+        if (tid + kTB * u < N) atomicAdd(&hist[bin_of(v[u])], 1);
+    __syncthreads();
+    {   // bin* holds the k-th best score: counts of the bins above, from the top down
+        const int c = hist[tid];
+        int all;
+        const int below = block_excl_scan(c, wsum, &all);
+        const int above = all - below - c;
+        if (above < k && above + c >= k) {
+            sh[0] = tid;
+            sh[1] = k - above;
+            sh[2] = c;
+        }
+    }
+    __syncthreads();
+    const int bstar = sh[0], need = sh[1], cstar = sh[2];
+    const bool take_all = need >= cstar;            // every member of bin* is in the expert
+    const bool listed = !take_all && cstar <= kCandMax;
+#pragma unroll
+    for (int u = 0; u < kRegVPT; ++u) {
+        const int j0 = kTB * u + 32 * warp;
+        if (j0 < N) {   // warp-uniform
+            const int j = j0 + lane;
+            const int b = j < N ? bin_of(v[u]) : -1;
+            const uint32_t sel = __ballot_sync(0xffffffffu, b > bstar || (take_all && b == bstar));
+            if (lane == 0) bits[j0 >> 5] = sel;
+            if (listed && b == bstar) {
+                const int p = atomicAdd(&sh[3], 1);
+                cval[p] = v[u];
+                cidx[p] = j;
+            }
+        }
+    }
+    __syncthreads();
+    if (listed) {
+        for (int p = tid; p < cstar; p += kTB) {
+            const float x = cval[p];
+            const int jp = cidx[p];
+            int rank = 0;
+            for (int q = 0; q < cstar; ++q) {
+                const float w = cval[q];
+                rank += (w > x || (w == x && cidx[q] < jp)) ? 1 : 0;
+            }
+            if (rank < need) atomicOr(&bits[jp >> 5], 1u << (jp & 31));
+        }
+        __syncthreads();
+    } else if (!take_all) {
+        // many members: the need-th best member's order key T by bisection, then
+        // members above T and, in key order, those equal to T until need is met
+        uint32_t T = 0u;
+        for (int bb = 31; bb >= 0; --bb) {
+            const uint32_t ct = T | (1u << bb);
+            int cnt = 0;
+#pragma unroll
+            for (int u = 0; u < kRegVPT; ++u)
+                cnt += (tid + kTB * u < N && bin_of(v[u]) == bstar && order_key(v[u]) >= ct) ? 1 : 0;
+            int total;
+            block_excl_scan(cnt, wsum, &total);
+            if (total >= need) T = ct;
+        }
+        int gt = 0;
+#pragma unroll
+        for (int u = 0; u < kRegVPT; ++u)
+            gt += (tid + kTB * u < N && bin_of(v[u]) == bstar && order_key(v[u]) > T) ? 1 : 0;
+        int gt_all;
+        block_excl_scan(gt, wsum, &gt_all);
+        if (warp == 0) {   // one warp, in key order: members above T, and the first ones equal to T
+            int eq_left = need - gt_all;
+            for (int w = 0; w < nw; ++w) {
+                const int j = 32 * w + lane;
+                bool above = false, eq = false;
+                if (j < N) {
+                    const float x = row[j];
+                    if (bin_of(x) == bstar) {
+                        const uint32_t kv = order_key(x);
+                        above = kv > T;
+                        eq = kv == T;
+                    }
+                }
+                const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
+                const int rr = __popc(eqm & ((1u << lane) - 1u));
+                const uint32_t add = __ballot_sync(0xffffffffu, above || (eq && rr < eq_left));
+                eq_left -= min(eq_left, __popc(eqm));
+                if (lane == 0) bits[w] |= add;
+            }
+        }
+        __syncthreads();
+    }
+    // the expert in ascending key order: thread t reads words [t*wpt, (t+1)*wpt)
+    const int wpt = (nw + kTB - 1) / kTB, w0 = min(nw, tid * wpt), w1 = min(nw, w0 + wpt);
+    int cnt = 0;
+    for (int w = w0; w < w1; ++w) cnt += __popc(bits[w]);
+    int total;
+    int pos = block_excl_scan(cnt, wsum, &total);
+    int32_t* out = idx + r * k;
+    for (int w = w0; w < w1; ++w) {
+        uint32_t b = bits[w];
+        while (b) {
+            const int x = __ffs(b) - 1;
+            b &= b - 1u;
+            if (pos < k) out[pos] = 32 * w + x;
+            ++pos;
+        }
+    }
+}
+
 // V_l[i] = (sum over splits of the partial row) / (sum of the partial row sums).
 template <int D>
 __global__ void tl_values_fin(Shape s, const float* __restrict__ part, int ns, bf16* __restrict__ Vl) {
@@ -637,7 +785,7 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
             return err;
         }
         if (s.N <= kBitsMaxN) {
-            auto kern = s.N <= kShortRow ? tl_topk_bits<256> : tl_topk_bits<kNB>;
+            auto kern = s.N <= kRegRowN ? tl_topk_reg : s.N <= kShortRow ? tl_topk_bits<256> : tl_topk_bits<kNB>;
             if ((err = launch_chained(chain, kern, dim3(s.m, sg.H), dim3(kTB), 0, st, sg, (const float*)p->S,
                                       (const uint32_t*)(p->rowmax + mo), (const uint32_t*)(rowmin + mo),
                                       idx + mo * s.k)) != cudaSuccess)
