@@ -16,6 +16,8 @@
 // Step numbers refer to the operator of 36Kr / 新智元 "注意力也是FFN？",
 // section "用少量地标查询，同时构造全局概括与细节专家": scores are step 2,
 // landmark values step 4, routes step 5.
+#include <algorithm>
+
 #include "tc_util.cuh"
 #include "tcgen.cuh"
 #include "host_cache.cuh"
@@ -495,17 +497,18 @@ static cudaError_t tc_scores_t(const Shape& s, const void* Ql, const void* K, fl
     return cudaGetLastError();
 }
 
-// Keys per landmark-values split: the longest of 1024, 2048, 4096 that still
-// gives at least two blocks per SM (measured: 64K-token rows 3366 / 3251 /
-// 3237 us per forward at 1024 / 2048 / 4096; the 56x56 layer needs 1024).
+// Keys per landmark-values split: the fewest whole 128-key tiles that let
+// every block of the launch run in one wave (two 512-thread blocks per SM),
+// with the row split as evenly as that allows.
 int tc_value_keys(const Shape& s) {
     int sms = 148;
     int dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long rows = (long long)((s.m + 127) / 128) * s.BH();
-    int kcv = 1024;
-    while (kcv < 4096 && rows * ((s.N + 2 * kcv - 1) / (2 * kcv)) >= 2LL * sms) kcv *= 2;
-    return kcv;
+    const long long tiles = (s.N + 127) / 128;
+    long long ns = (2LL * sms) / rows;
+    ns = std::max(1LL, std::min(ns, tiles));
+    return (int)(((tiles + ns - 1) / ns) * 128);
 }
 
 template <int D>
