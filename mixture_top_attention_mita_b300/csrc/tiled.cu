@@ -599,30 +599,39 @@ __global__ void __launch_bounds__(2 * QT, D == 64 ? 5 : 1)
         E_s[x] = j;
     }
     __syncthreads();
-    for (int x = tid; x < QT * CH; x += NTH) {
-        const int r = x / CH, c = x % CH;
-        cp_async16(uq + swz<RB>(r, c), Q + hoff + (size_t)rows_s[r] * D + 8 * c, 16u);
-    }
+    // thread t copies 16-byte chunk cc = t % CH of rows r0 + RS i (r0 = t / CH);
+    // RS is a multiple of 8, so the rows' swizzle term is the same for every
+    // i and the shared-memory offsets are soff + RS RB i
+    constexpr int RS = NTH / CH;   // rows per pass: 16 at d = 64, 8 at d = 128
+    static_assert(RS % 8 == 0, "rows per pass keep the swizzle term");
+    const int cc = tid % CH, r0 = tid / CH;
+    const uint32_t soff = swz<RB>(r0, cc);
+#pragma unroll
+    for (int i = 0; i < QT / RS; ++i)
+        cp_async16(uq + soff + (uint32_t)(i * RS * RB), Q + hoff + (size_t)rows_s[r0 + RS * i] * D + 8 * cc, 16u);
+    const bf16* qlb = Ql + (size_t)bh * s.m * D + 8 * cc;
+    const bf16* vlb = Vl + (size_t)bh * s.m * D + 8 * cc;
+    const bf16* kgb = K + hoff + 8 * cc;
+    const bf16* vgb = V + hoff + 8 * cc;
     auto stage = [&](int b) {
-        const uint32_t kb = ukv + (uint32_t)(b & 1) * 2u * 64u * RB, vb = kb + 64u * RB;
-        for (int x = tid; x < 64 * CH; x += NTH) {
-            const int r = x / CH, c = x % CH, slot = b * 64 + r;
-            const bf16 *ks, *vs;
+        const uint32_t kb = ukv + (uint32_t)(b & 1) * 2u * 64u * RB + soff, vb = kb + 64u * RB;
+#pragma unroll
+        for (int i = 0; i < 64 / RS; ++i) {
+            const int slot = b * 64 + r0 + RS * i;
+            const bf16 *ks = qlb, *vs = vlb;
             uint32_t nbytes = 16u;
             if (slot < s.m) {
-                ks = Ql + ((size_t)bh * s.m + slot) * D;
-                vs = Vl + ((size_t)bh * s.m + slot) * D;
+                ks = qlb + (size_t)slot * D;
+                vs = vlb + (size_t)slot * D;
             } else if (slot < L) {
-                const int j = E_s[slot - s.m];
-                ks = K + hoff + (size_t)j * D;
-                vs = V + hoff + (size_t)j * D;
+                const size_t j = (size_t)E_s[slot - s.m] * D;
+                ks = kgb + j;
+                vs = vgb + j;
             } else {
-                ks = Ql;
-                vs = Vl;
                 nbytes = 0u;   // zero rows past the last slot
             }
-            cp_async16(kb + swz<RB>(r, c), ks + 8 * c, nbytes);
-            cp_async16(vb + swz<RB>(r, c), vs + 8 * c, nbytes);
+            cp_async16(kb + (uint32_t)(i * RS * RB), ks, nbytes);
+            cp_async16(vb + (uint32_t)(i * RS * RB), vs, nbytes);
         }
         cp_async_commit();
     };
