@@ -17,6 +17,7 @@
 // section "用少量地标查询，同时构造全局概括与细节专家": scores are step 2,
 // landmark values step 4, routes step 5.
 #include <algorithm>
+#include <type_traits>
 
 #include "tc_util.cuh"
 #include "tcgen.cuh"
@@ -418,28 +419,37 @@ __global__ void __launch_bounds__(128) tc_scores_route(const __grid_constant__ C
         const int n = n0 + warp * 32 + lane;
         const bool live = n < N;
         const uint32_t lanes = (uint32_t)(warp * 32) << 16;
-        float* scol = S + (size_t)bh * m * N + n;
-        for (int c0 = 0; c0 < nb; c0 += 32) {
+        float* sp = S + (size_t)bh * m * N + n;   // advances one row of S per landmark
+        // one chunk of 32 landmarks; FULL: every token of the tile is in the
+        // row (block-uniform), so no lane needs masking
+        auto chunk = [&](int c0, auto full_t) {
+            constexpr bool FULL = decltype(full_t)::value;
             float v[32];
             tmem_ld32(tmem + lanes + c0, v);
+            const int cn = min(32, m - c0);
             float mine_hi = -INFINITY, mine_lo = INFINITY;   // lane j keeps landmark c0 + j's
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                const int c = c0 + j;
-                if (c < m) {   // block-uniform
-                    if (live) scol[(size_t)c * N] = v[j];
+                if (j < cn) {   // block-uniform
+                    if (FULL || live) *sp = v[j];
+                    sp += N;
+                    const float xh = FULL || live ? v[j] : -INFINITY, xl = FULL || live ? v[j] : INFINITY;
                     float hi, lo;
-                    asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(hi) : "f"(live ? v[j] : -INFINITY));
-                    asm("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(lo) : "f"(live ? v[j] : INFINITY));
+                    asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(hi) : "f"(xh));
+                    asm("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(lo) : "f"(xl));
                     mine_hi = lane == j ? hi : mine_hi;
                     mine_lo = lane == j ? lo : mine_lo;
                 }
             }
-            if (c0 + lane < m) {
+            if (lane < cn) {
                 atomicMax(&smax[c0 + lane], order_key(mine_hi));
                 atomicMin(&smin[c0 + lane], order_key(mine_lo));
             }
-        }
+        };
+        if (n0 + 128 <= N)
+            for (int c0 = 0; c0 < m; c0 += 32) chunk(c0, std::true_type{});
+        else
+            for (int c0 = 0; c0 < m; c0 += 32) chunk(c0, std::false_type{});
         float best = -INFINITY;
         int arg = 0;
         for (int c0 = 0; c0 < nb; c0 += 32) {
