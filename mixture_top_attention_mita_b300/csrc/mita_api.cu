@@ -276,7 +276,10 @@ int mita_backward(mita_plan_t p, const void* Q, const void* K, const void* V, co
         !aligned16(dV))
         return MITA_ERR_INVALID_ARG;
     if (p->routes_s > 1) return MITA_ERR_UNSUPPORTED;
-    const int rc = ensure_grad(p);
+    int rc = ensure_grad(p);
+    // the tiled path's row keys let the backward recompute the forward's
+    // scores and routes with its kernels
+    if (rc == MITA_OK) rc = ensure_tiled(p);
     if (rc != MITA_OK) return rc;
     if (mita::run_backward(p, Q, K, V, dOut, dQ, dK, dV, (cudaStream_t)stream) != cudaSuccess) return MITA_ERR_CUDA;
     note_launch(p, (cudaStream_t)stream);

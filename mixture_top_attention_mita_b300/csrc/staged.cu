@@ -17,6 +17,8 @@
 
 #include "common.cuh"
 #include "staged.cuh"
+#include "tcgen.cuh"
+#include "tiled.cuh"
 #include "host_cache.cuh"
 #include "launch.cuh"
 #include "mma_util.cuh"
@@ -1716,15 +1718,34 @@ static cudaError_t run_backward_t(mita_plan_s* p, const T* Q, const T* K, const 
     const size_t nbytes = (size_t)BH * s.N * D * sizeof(float);
     cudaError_t e;
     if ((e = cudaMemsetAsync(p->dQl, 0, (size_t)2 * BH * s.m * D * sizeof(float), st)) != cudaSuccess) return e;
-    // the forward's landmarks, scores, experts, landmark values and routes
-    pool_kernel<T><<<dim3(s.m, BH), D, 0, st>>>(s, Q, Ql);
-    scores_kernel<T><<<dim3((s.N + 127) / 128, (s.m + 31) / 32, BH), 256, 0, st>>>(s, Ql, K, p->S);
-    launch_topk(s, p->S, p->idx, st);
+    // the forward's landmarks, scores, experts, landmark values and routes; at
+    // bf16 with the tiled path's workspace (m <= 128), its pool and its
+    // one-kernel scores and routes (the same Q_l, scores and first argmax)
+    bool tiled_recompute = false;
+    if constexpr (std::is_same<T, __nv_bfloat16>::value)
+        tiled_recompute = p->rowmax != nullptr && tc_scores_route_supported(s);
+    if (tiled_recompute) {
+        uint32_t* rowmin = p->rowmax + (size_t)BH * s.m;
+        if ((e = tiled_pool(s, Q, Ql, p->rowmax, p->counts, st)) != cudaSuccess) return e;
+        if ((e = tc_scores_route(s, Ql, K, Q, p->S, p->rowmax, rowmin, p->route, p->counts, p->status, st, false)) !=
+            cudaSuccess)
+            return e;
+    } else {
+        pool_kernel<T><<<dim3(s.m, BH), D, 0, st>>>(s, Q, Ql);
+        scores_kernel<T><<<dim3((s.N + 127) / 128, (s.m + 31) / 32, BH), 256, 0, st>>>(s, Ql, K, p->S);
+        p->launches += 1;   // and the route kernel below
+    }
+    if (tiled_recompute && s.N > 256 && tiled_topk_supported(s)) {   // long rows: the register-resident select
+        if ((e = tiled_topk(s, p->S, p->rowmax, p->idx, st)) != cudaSuccess) return e;
+    } else {
+        launch_topk(s, p->S, p->idx, st);
+    }
     float* Vl32 = p->dVl + (size_t)BH * s.m * D;   // fp32 landmark values, then per-row {max S, sum w}
     float* stats = Vl32 + (size_t)BH * s.m * D;
     // key-split partial sums use dK as scratch before it is cleared
     p->launches += launch_values_rows<T, D>(s, p->S, V, Vl, Vl32, stats, dK, nbytes, st) - 1;
-    route_kernel<T, D><<<dim3((s.N + 127) / 128, BH), 128, 0, st>>>(s, Q, Ql, p->route, 1, nullptr);
+    if (!tiled_recompute)
+        route_kernel<T, D><<<dim3((s.N + 127) / 128, BH), 128, 0, st>>>(s, Q, Ql, p->route, 1, nullptr);
     if ((e = cudaMemsetAsync(dK, 0, nbytes, st)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(dV, 0, nbytes, st)) != cudaSuccess) return e;
     const int L = s.m + s.k;
@@ -1775,7 +1796,7 @@ static cudaError_t run_backward_t(mita_plan_s* p, const T* Q, const T* K, const 
     values_bwd_tile_kernel<T, D><<<dim3((s.N + kVrKeys - 1) / kVrKeys, BH), 256, vb_bytes, st>>>(
         s, p->S, stats, Vl32, K, V, Ql, p->dVl, dK, dV, p->dQl);
     pool_bwd_kernel<D><<<dim3((unsigned)((s.N * (D / 4) + 255) / 256), BH), 256, 0, st>>>(s, p->dQl, dQ);
-    p->launches += 7;
+    p->launches += 6;   // pool, scores (and routes), top-k, one value recompute, value backward, pool backward
     return cudaGetLastError();
 }
 

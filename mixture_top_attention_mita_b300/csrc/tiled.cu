@@ -847,6 +847,23 @@ size_t tiled_part_bytes(const Shape& s) {
 
 int tiled_max_tiles(const Shape& s) { return tl::max_tiles(s); }
 
+bool tiled_topk_supported(const Shape& s) { return s.N <= tl::kRegRowN; }
+
+cudaError_t tiled_topk(const Shape& s, const float* S, const uint32_t* rowmax, int32_t* idx, cudaStream_t st) {
+    const uint32_t* rowmin = rowmax + (size_t)s.BH() * s.m;
+    return launch_chained(false, tl::tl_topk_reg, dim3(s.m, s.BH()), dim3(tl::kTB), 0, st, s, S, rowmax, rowmin, idx);
+}
+
+cudaError_t tiled_pool(const Shape& s, const void* Q, void* Ql, uint32_t* rowmax, int32_t* counts, cudaStream_t st) {
+    using T = __nv_bfloat16;
+    uint32_t* rowmin = rowmax + (size_t)s.BH() * s.m;
+    if (s.d == 64)
+        return launch_chained(false, tl::tl_pool<64>, dim3(s.m, s.BH()), dim3(128), 0, st, s, (const T*)Q, (T*)Ql,
+                              rowmax, rowmin, counts);
+    return launch_chained(false, tl::tl_pool<128>, dim3(s.m, s.BH()), dim3(128), 0, st, s, (const T*)Q, (T*)Ql, rowmax,
+                          rowmin, counts);
+}
+
 cudaError_t run_tiled(mita_plan_s* p, const void* Q, const void* K, const void* V, void* out, int32_t* idx,
                       int32_t* route, cudaStream_t st) {
     using T = __nv_bfloat16;
