@@ -1726,7 +1726,13 @@ static cudaError_t run_backward_t(mita_plan_s* p, const T* Q, const T* K, const 
         tiled_recompute = p->rowmax != nullptr && tc_scores_route_supported(s);
     if (tiled_recompute) {
         uint32_t* rowmin = p->rowmax + (size_t)BH * s.m;
-        if ((e = tiled_pool(s, Q, Ql, p->rowmax, p->counts, st)) != cudaSuccess) return e;
+        if (s.N <= 32 * s.m) {   // bins of about 32 tokens or fewer: a block of D threads per landmark
+            pool_kernel<T><<<dim3(s.m, BH), D, 0, st>>>(s, Q, Ql);
+            if ((e = cudaMemsetAsync(p->rowmax, 0, (size_t)BH * s.m * 4, st)) != cudaSuccess) return e;
+            if ((e = cudaMemsetAsync(rowmin, 0xff, (size_t)BH * s.m * 4, st)) != cudaSuccess) return e;
+        } else if ((e = tiled_pool(s, Q, Ql, p->rowmax, p->counts, st)) != cudaSuccess) {
+            return e;
+        }
         if ((e = tc_scores_route(s, Ql, K, Q, p->S, p->rowmax, rowmin, p->route, p->counts, p->status, st, false)) !=
             cudaSuccess)
             return e;
