@@ -10,13 +10,13 @@
 //   tc_scores       S = Q_l . K^T (fp32, workspace) and each landmark's row
 //                   max and min (with the routes, tc_scores_route, when
 //                   m <= 128)
-//   tl_topk_bits    per landmark the k best keys (ties to the lower index):
-//                   a 256- or 2048-bin histogram over [min, max], an exact
-//                   rank of the boundary bin's members, the expert as a bitmap
-//                   over the row read out in key order (rows up to 64K keys;
-//                   longer rows use the staged path's radix select; rows up
-//                   to 4096 keys: tl_topk_reg, the same with the row held in
-//                   registers)
+//   tl_topk_reg     per landmark the k best keys (ties to the lower index),
+//                   rows up to 4096 keys held in registers: a 256-bin
+//                   histogram over [min, max], an exact rank of the boundary
+//                   bin's members, the expert as a bitmap over the row read
+//                   out in key order
+//   tl_topk_bits    the same from global memory with 2048 bins, rows up to
+//                   64K keys (longer rows use the staged path's radix select)
 //   tc_values       split-K partial sums of exp(S / sqrt d - max) . V and of
 //                   the row sums, per split of 1024-4096 keys
 //   tl_values_fin   V_l = sum of partials / sum of row sums, bf16
@@ -124,8 +124,7 @@ __global__ void __launch_bounds__(128) tl_pool(Shape s, const bf16* __restrict__
 
 // ---------------------------------------------------------------- top-k
 constexpr int kTB = 256;          // threads per top-k block
-constexpr int kNB = 2048;         // histogram bins (rows past kShortRow keys)
-constexpr int kShortRow = 4096;   // rows up to this many keys: 256 bins
+constexpr int kNB = 2048;         // histogram bins of tl_topk_bits (rows past 4096 keys)
 constexpr int kCandMax = 1024;    // boundary members ranked exactly
 
 // Block-wide exclusive prefix sum of one int per thread (kTB threads);
@@ -154,8 +153,8 @@ MITA_DEV int block_excl_scan(int x, int* wsum, int* total) {
 
 // Block per (landmark i, head bh), rows up to kBitsMaxN keys: the k keys
 // with the largest raw scores S[bh, i, :], ties to the lower key index, in
-// ascending order.  NB bins of equal width over [row min, row max] (256 on
-// rows up to kShortRow keys, 2048 beyond) find the bin
+// ascending order.  NB bins of equal width over [row min, row max] (2048 on
+// the rows past 4096 keys it is launched for) find the bin
 // bin* holding the k-th largest score; every pass over the row is coalesced.
 // Pass 1 builds the histogram; pass 2 marks the keys of the bins above bin* in a bitmap
 // over the row (one ballot word per 32 keys) and lists bin*'s members with
@@ -794,7 +793,7 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
             return err;
         }
         if (s.N <= kBitsMaxN) {
-            auto kern = s.N <= kRegRowN ? tl_topk_reg : s.N <= kShortRow ? tl_topk_bits<256> : tl_topk_bits<kNB>;
+            auto kern = s.N <= kRegRowN ? tl_topk_reg : tl_topk_bits<kNB>;
             if ((err = launch_chained(chain, kern, dim3(s.m, sg.H), dim3(kTB), 0, st, sg, (const float*)p->S,
                                       (const uint32_t*)(p->rowmax + mo), (const uint32_t*)(rowmin + mo),
                                       idx + mo * s.k)) != cudaSuccess)
