@@ -782,7 +782,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 perm_s[atomicAdd(&cnt_s[b], 1)] = (uint8_t)q;
             }
         }
-        __syncthreads();
+        // phase D's m16 tile mt = warp / 4 reads the numerators of landmarks
+        // 16 mt .. 16 mt + 15, written by the selects of warps 4 mt .. 4 mt + 3:
+        // each half of the warps waits for its own half only
+        asm volatile("bar.sync %0, 128;\n" ::"r"(1 + (warp >> 2)) : "memory");
 
         // ---------------- phase D: landmark values V_l = P . V / (P . 1)
         {

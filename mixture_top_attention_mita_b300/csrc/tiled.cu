@@ -566,7 +566,7 @@ __global__ void tl_bucket_put(Shape s, const int32_t* __restrict__ route, int32_
 // pairs (K, V rows of the expert's keys); 64-slot blocks are staged by
 // cp.async into a double buffer and folded in by an online softmax.
 template <int D, int QT>
-__global__ void __launch_bounds__(2 * QT, D == 64 ? 5 : 1)
+__global__ void __launch_bounds__(2 * QT, D == 64 ? 4 : 1)
     tl_attend(Shape s, const bf16* __restrict__ Q, const bf16* __restrict__ K, const bf16* __restrict__ V,
               const bf16* __restrict__ Ql, const bf16* __restrict__ Vl, const int32_t* __restrict__ idx,
               const int32_t* __restrict__ perm, const int2* __restrict__ tiles,
