@@ -17,6 +17,7 @@
 
 #include "common.cuh"
 #include "staged.cuh"
+#include "fused.cuh"
 #include "tcgen.cuh"
 #include "tiled.cuh"
 #include "host_cache.cuh"
@@ -656,12 +657,23 @@ static cudaError_t run_staged_t(mita_plan_s* p, const T* Q, const T* K, const T*
     const int BH = s.BH();
     T* Ql = (T*)p->Ql;
     T* Vl = (T*)p->Vl;
-    pool_kernel<T><<<dim3(s.m, BH), D, 0, st>>>(s, Q, Ql);
-    scores_kernel<T><<<dim3((s.N + 127) / 128, (s.m + 31) / 32, BH), 256, 0, st>>>(s, Ql, K, p->S);
-    launch_topk(s, p->S, idx, st);
-    // key-split partial sums (if any) use the output as scratch before the attention writes it
-    const int nv = launch_values_rows<T, D>(s, p->S, V, Vl, nullptr, nullptr, reinterpret_cast<float*>(out),
-                                            (size_t)BH * s.N * D * sizeof(T), st);
+    int nv = 0;
+    bool one_kernel = false;   // landmarks, experts and landmark values from the one-kernel path
+    if constexpr (std::is_same<T, __nv_bfloat16>::value)
+        one_kernel = p->routes_s > 1 && fused_supported(s, MITA_BF16);
+    if (one_kernel) {
+        // its output (one expert per query) is overwritten by the attention below
+        cudaError_t e = run_fused(p, Q, K, V, out, idx, route, 1, st);
+        if (e != cudaSuccess) return e;
+        nv = -3;   // run_fused counts its own launch; route, bucket and attention follow
+    } else {
+        pool_kernel<T><<<dim3(s.m, BH), D, 0, st>>>(s, Q, Ql);
+        scores_kernel<T><<<dim3((s.N + 127) / 128, (s.m + 31) / 32, BH), 256, 0, st>>>(s, Ql, K, p->S);
+        launch_topk(s, p->S, idx, st);
+        // key-split partial sums (if any) use the output as scratch before the attention writes it
+        nv = launch_values_rows<T, D>(s, p->S, V, Vl, nullptr, nullptr, reinterpret_cast<float*>(out),
+                                      (size_t)BH * s.N * D * sizeof(T), st);
+    }
     // s > 1: each query's landmark list goes into the score buffer, free once
     // the landmark values are done (BH x N x s <= BH x m x N entries)
     const int ns = p->routes_s > 1 ? p->routes_s : 1;
