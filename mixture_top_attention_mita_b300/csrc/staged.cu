@@ -1653,6 +1653,233 @@ __global__ void __launch_bounds__(256, D == 64 ? 3 : 1) values_bwd_tile_kernel(S
     }
 }
 
+// values_bwd_tile_kernel for bf16 I/O at d = 64 with its products on
+// mma.sync (m16n8k16, fp32 accumulation), per chunk of 32 landmark rows:
+// dP = dV_l . V_tile^T, then per element P (from the scores and the row's
+// max and sum) and dR = P (dP - dV_l . V_l) / sqrt d, then dV_tile += P^T
+// dV_l, dK_tile += dR^T Q_l and dQ_l += dR . K_tile.  The fp32 operands (dV_l,
+// P, dR) enter as bf16 pairs hi + lo (about 16 mantissa bits; the lo x lo
+// term of P^T dV_l is dropped).  Warp w keeps the dK and dV accumulators of
+// keys 16 (w % 4) .. + 15 and features 32 (w / 4) .. + 31 over all chunks;
+// the tile's rows are added once at the end.  Tiles are bf16 rows of 64 with
+// XOR-swizzled 16-byte chunks; rows past the landmarks or keys are zero.
+constexpr int kVmKeys = 64, kVmRows = 32;
+
+MITA_DEV void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(a - __low2float(h), b - __high2float(h));
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+__global__ void __launch_bounds__(256, 3)
+    values_bwd_mma_kernel(Shape s, const float* __restrict__ S, const float* __restrict__ stats,
+                          const float* __restrict__ Vl32, const __nv_bfloat16* __restrict__ K,
+                          const __nv_bfloat16* __restrict__ V, const __nv_bfloat16* __restrict__ Ql,
+                          const float* __restrict__ dVl, float* __restrict__ dK, float* __restrict__ dV,
+                          float* __restrict__ dQl) {
+    using namespace mx;
+    constexpr int D = 64, RB = 128;   // bytes per bf16 row of 64
+    extern __shared__ __align__(128) uint8_t vm_raw[];
+    uint8_t* Kt = vm_raw;             // [64 keys][64 features]
+    uint8_t* Vt = Kt + kVmKeys * RB;
+    uint8_t* Qc = Vt + kVmKeys * RB;  // [32 rows][64 features]: Q_l, dV_l hi, dV_l lo
+    uint8_t* Gh = Qc + kVmRows * RB;
+    uint8_t* Gl = Gh + kVmRows * RB;
+    uint8_t* Ph = Gl + kVmRows * RB;  // [32 rows][64 keys]: P hi, P lo, dR hi, dR lo
+    uint8_t* Pl = Ph + kVmRows * RB;
+    uint8_t* Rh = Pl + kVmRows * RB;
+    uint8_t* Rl = Rh + kVmRows * RB;
+    __shared__ float mx_s[kVmRows], den_s[kVmRows], dr_s[kVmRows];
+    const int j0 = blockIdx.x * kVmKeys, bh = blockIdx.y, tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int nk = min(kVmKeys, s.N - j0);
+    const size_t hoff = (size_t)bh * s.N * D;
+    const int g8 = lane >> 2, q2 = 2 * (lane & 3);
+    for (int u = tid; u < kVmKeys * 8; u += 256) {
+        const int r = u >> 3, c = u & 7;
+        const size_t o = hoff + (size_t)(j0 + (r < nk ? r : 0)) * D + 8 * c;
+        cp_async16(smem_u32(Kt + swz<RB>(r, c)), K + o, r < nk ? 16u : 0u);
+        cp_async16(smem_u32(Vt + swz<RB>(r, c)), V + o, r < nk ? 16u : 0u);
+    }
+    cp_async_commit();
+    const float scale = rsqrtf((float)D), c2 = scale * kLog2e;
+    float kacc[4][4], vacc[4][4];   // key tile w % 4, feature tiles 4 (w / 4) + n
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) kacc[n][v] = vacc[n][v] = 0.0f;
+    for (int i0 = 0; i0 < s.m; i0 += kVmRows) {
+        const int nr = min(kVmRows, s.m - i0);
+        if (i0 > 0) __syncthreads();   // the previous chunk's tiles consumed
+        for (int u = tid; u < kVmRows * 8; u += 256) {
+            const int r = u >> 3, c = u & 7;
+            const size_t o = ((size_t)bh * s.m + i0 + (r < nr ? r : 0)) * D + 8 * c;
+            cp_async16(smem_u32(Qc + swz<RB>(r, c)), Ql + o, r < nr ? 16u : 0u);
+            uint32_t hw[4] = {0u, 0u, 0u, 0u}, lw[4] = {0u, 0u, 0u, 0u};
+            if (r < nr) {
+                const float4 a = *reinterpret_cast<const float4*>(dVl + o);
+                const float4 b = *reinterpret_cast<const float4*>(dVl + o + 4);
+                split_bf16x2(a.x, a.y, hw[0], lw[0]);
+                split_bf16x2(a.z, a.w, hw[1], lw[1]);
+                split_bf16x2(b.x, b.y, hw[2], lw[2]);
+                split_bf16x2(b.z, b.w, hw[3], lw[3]);
+            }
+            *reinterpret_cast<uint4*>(Gh + swz<RB>(r, c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(Gl + swz<RB>(r, c)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+        cp_async_commit();
+        if (tid < kVmRows) {
+            const size_t so = (size_t)bh * s.m + i0 + tid;
+            mx_s[tid] = tid < nr ? stats[2 * so] : 0.0f;
+            den_s[tid] = tid < nr ? stats[2 * so + 1] : 1.0f;
+        }
+        for (int r = w; r < kVmRows; r += 8) {   // dV_l . V_l, the row's P . dP
+            float x = 0.0f;
+            if (r < nr) {
+                const size_t o = ((size_t)bh * s.m + i0 + r) * D;
+                for (int f = lane; f < D; f += 32) x = fmaf(dVl[o + f], Vl32[o + f], x);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+            if (lane == 0) dr_s[r] = x;
+        }
+        cp_async_wait<0>();
+        __syncthreads();
+        // dP = dV_l . V^T (warp w: row tile w % 2, key tiles 2 (w / 2), + 1), then P and dR
+        {
+            const int mt = w & 1, nt = 2 * (w >> 1);
+            float sv[2][2][2];   // the scores of this lane's elements, loaded before the products
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int r = mt * 16 + g8 + 8 * hh, key = (nt + n) * 8 + q2 + e;
+                        sv[n][hh][e] = r < nr && key < nk ? S[((size_t)bh * s.m + i0 + r) * s.N + j0 + key] : 0.0f;
+                    }
+            float p[2][4];
+#pragma unroll
+            for (int n = 0; n < 2; ++n) p[n][0] = p[n][1] = p[n][2] = p[n][3] = 0.0f;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                uint32_t ah[4], al[4], b0, b1, b2, b3;
+                const uint32_t ao = swz<RB>(mt * 16 + (lane & 15), 2 * kk + (lane >> 4));
+                ldsm_x4(smem_u32(Gh + ao), ah[0], ah[1], ah[2], ah[3]);
+                ldsm_x4(smem_u32(Gl + ao), al[0], al[1], al[2], al[3]);
+                ldsm_x4(smem_u32(Vt + swz<RB>(nt * 8 + (lane & 7) + ((lane >> 4) << 3), 2 * kk + ((lane >> 3) & 1))), b0,
+                        b1, b2, b3);
+                mma16816(p[0], ah[0], ah[1], ah[2], ah[3], b0, b1);
+                mma16816(p[0], al[0], al[1], al[2], al[3], b0, b1);
+                mma16816(p[1], ah[0], ah[1], ah[2], ah[3], b2, b3);
+                mma16816(p[1], al[0], al[1], al[2], al[3], b2, b3);
+            }
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int r = mt * 16 + g8 + 8 * hh, key = (nt + n) * 8 + q2;
+                    float pv[2], rv[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float pe = r < nr && key + e < nk ? exp2f((sv[n][hh][e] - mx_s[r]) * c2) / den_s[r] : 0.0f;
+                        pv[e] = pe;
+                        rv[e] = pe * (p[n][2 * hh + e] - dr_s[r]) * scale;
+                    }
+                    const uint32_t o = swz<RB>(r, key >> 3) + (uint32_t)(key & 7) * 2u;
+                    uint32_t h, l;
+                    split_bf16x2(pv[0], pv[1], h, l);
+                    *reinterpret_cast<uint32_t*>(Ph + o) = h;
+                    *reinterpret_cast<uint32_t*>(Pl + o) = l;
+                    split_bf16x2(rv[0], rv[1], h, l);
+                    *reinterpret_cast<uint32_t*>(Rh + o) = h;
+                    *reinterpret_cast<uint32_t*>(Rl + o) = l;
+                }
+        }
+        __syncthreads();
+        // dV += P^T dV_l, dK += dR^T Q_l (warp w: key tile w % 4, feature tiles 4 (w / 4) .. + 3)
+        {
+            const int mt = w & 3, n0 = 4 * (w >> 2);
+#pragma unroll
+            for (int kk = 0; kk < kVmRows / 16; ++kk) {
+                const int arow = kk * 16 + (lane & 7) + ((lane >> 4) << 3);
+                const int ach = 2 * mt + ((lane >> 3) & 1);
+                uint32_t ph[4], pl[4], rh[4], rl[4];
+                ldsm_x4_t(smem_u32(Ph + swz<RB>(arow, ach)), ph[0], ph[1], ph[2], ph[3]);
+                ldsm_x4_t(smem_u32(Pl + swz<RB>(arow, ach)), pl[0], pl[1], pl[2], pl[3]);
+                ldsm_x4_t(smem_u32(Rh + swz<RB>(arow, ach)), rh[0], rh[1], rh[2], rh[3]);
+                ldsm_x4_t(smem_u32(Rl + swz<RB>(arow, ach)), rl[0], rl[1], rl[2], rl[3]);
+#pragma unroll
+                for (int np = 0; np < 4; np += 2) {
+                    const int brow = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                    const int bch = n0 + np + (lane >> 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(smem_u32(Gh + swz<RB>(brow, bch)), b0, b1, b2, b3);
+                    mma16816(vacc[np], ph[0], ph[1], ph[2], ph[3], b0, b1);
+                    mma16816(vacc[np], pl[0], pl[1], pl[2], pl[3], b0, b1);
+                    mma16816(vacc[np + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
+                    mma16816(vacc[np + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
+                    ldsm_x4_t(smem_u32(Gl + swz<RB>(brow, bch)), b0, b1, b2, b3);
+                    mma16816(vacc[np], ph[0], ph[1], ph[2], ph[3], b0, b1);
+                    mma16816(vacc[np + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
+                    ldsm_x4_t(smem_u32(Qc + swz<RB>(brow, bch)), b0, b1, b2, b3);
+                    mma16816(kacc[np], rh[0], rh[1], rh[2], rh[3], b0, b1);
+                    mma16816(kacc[np], rl[0], rl[1], rl[2], rl[3], b0, b1);
+                    mma16816(kacc[np + 1], rh[0], rh[1], rh[2], rh[3], b2, b3);
+                    mma16816(kacc[np + 1], rl[0], rl[1], rl[2], rl[3], b2, b3);
+                }
+            }
+        }
+        // dQ_l += dR . K (warp w: row tile w % 2, feature tiles 2 (w / 2), + 1)
+        {
+            const int mt = w & 1, nt = 2 * (w >> 1);
+            float a[2][4];
+#pragma unroll
+            for (int n = 0; n < 2; ++n) a[n][0] = a[n][1] = a[n][2] = a[n][3] = 0.0f;
+#pragma unroll
+            for (int kk = 0; kk < kVmKeys / 16; ++kk) {
+                uint32_t rh[4], rl[4], b0, b1, b2, b3;
+                const uint32_t ao = swz<RB>(mt * 16 + (lane & 15), 2 * kk + (lane >> 4));
+                ldsm_x4(smem_u32(Rh + ao), rh[0], rh[1], rh[2], rh[3]);
+                ldsm_x4(smem_u32(Rl + ao), rl[0], rl[1], rl[2], rl[3]);
+                const int brow = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                ldsm_x4_t(smem_u32(Kt + swz<RB>(brow, nt + (lane >> 4))), b0, b1, b2, b3);
+                mma16816(a[0], rh[0], rh[1], rh[2], rh[3], b0, b1);
+                mma16816(a[0], rl[0], rl[1], rl[2], rl[3], b0, b1);
+                mma16816(a[1], rh[0], rh[1], rh[2], rh[3], b2, b3);
+                mma16816(a[1], rl[0], rl[1], rl[2], rl[3], b2, b3);
+            }
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int r = mt * 16 + g8 + 8 * hh;
+                    if (r < nr)
+                        atomicAdd(reinterpret_cast<float2*>(dQl + ((size_t)bh * s.m + i0 + r) * D + (nt + n) * 8 + q2),
+                                  make_float2(a[n][2 * hh], a[n][2 * hh + 1]));
+                }
+        }
+    }
+    // the tile's rows of dK and dV
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int key = (w & 3) * 16 + g8 + 8 * hh, f = (4 * (w >> 2) + n) * 8 + q2;
+            if (key >= nk) continue;
+            const size_t o = hoff + (size_t)(j0 + key) * D + f;
+            float2 k2 = *reinterpret_cast<float2*>(dK + o), v2 = *reinterpret_cast<float2*>(dV + o);
+            k2.x += kacc[n][2 * hh];
+            k2.y += kacc[n][2 * hh + 1];
+            v2.x += vacc[n][2 * hh];
+            v2.y += vacc[n][2 * hh + 1];
+            *reinterpret_cast<float2*>(dK + o) = k2;
+            *reinterpret_cast<float2*>(dV + o) = v2;
+        }
+}
+
+constexpr size_t values_bwd_mma_bytes() { return (size_t)(2 * kVmKeys + 7 * kVmRows) * 128; }
+
 template <int D>
 constexpr size_t values_bwd_tile_bytes() {
     return ((size_t)2 * kVrKeys * (D + 4) + 2 * kVrRows * (D + 4) + 2 * kVrRows * (kVrKeys + 8) + kVrRows) *
@@ -1809,10 +2036,19 @@ static cudaError_t run_backward_t(mita_plan_s* p, const T* Q, const T* K, const 
             s, Q, K, V, Ql, Vl, p->idx, p->route, dOut, dQ, dK, dV, p->dQl, p->dVl, shared, p->status);
         p->launches += 1;
     }
-    const size_t vb_bytes = values_bwd_tile_bytes<D>();
-    ensure_smem_attr((const void*)values_bwd_tile_kernel<T, D>, (int)vb_bytes);
-    values_bwd_tile_kernel<T, D><<<dim3((s.N + kVrKeys - 1) / kVrKeys, BH), 256, vb_bytes, st>>>(
-        s, p->S, stats, Vl32, K, V, Ql, p->dVl, dK, dV, p->dQl);
+    bool vmma = false;   // bf16 at d = 64: the landmark-value backward on mma.sync
+    if constexpr (D == 64 && std::is_same<T, __nv_bfloat16>::value) {
+        ensure_smem_attr((const void*)values_bwd_mma_kernel, (int)values_bwd_mma_bytes());
+        values_bwd_mma_kernel<<<dim3((s.N + kVmKeys - 1) / kVmKeys, BH), 256, values_bwd_mma_bytes(), st>>>(
+            s, p->S, stats, Vl32, K, V, Ql, p->dVl, dK, dV, p->dQl);
+        vmma = true;
+    }
+    if (!vmma) {
+        const size_t vb_bytes = values_bwd_tile_bytes<D>();
+        ensure_smem_attr((const void*)values_bwd_tile_kernel<T, D>, (int)vb_bytes);
+        values_bwd_tile_kernel<T, D><<<dim3((s.N + kVrKeys - 1) / kVrKeys, BH), 256, vb_bytes, st>>>(
+            s, p->S, stats, Vl32, K, V, Ql, p->dVl, dK, dV, p->dQl);
+    }
     pool_bwd_kernel<D><<<dim3((unsigned)((s.N * (D / 4) + 255) / 256), BH), 256, 0, st>>>(s, p->dQl, dQ);
     p->launches += 6;   // pool, scores (and routes), top-k, one value recompute, value backward, pool backward
     return cudaGetLastError();
