@@ -1914,9 +1914,11 @@ __global__ void __launch_bounds__(256) pool_bwd_kernel(Shape s, const float* __r
         for (int c = max(0, cc - 1); c <= min(s.pw - 1, cc + 1); ++c) {
             const int2 cr = rng[s.ph + c];
             if (x < cr.x || x >= cr.y) continue;
-            const float n = (float)((rr.y - rr.x) * (cr.y - cr.x));
+            // one correctly rounded reciprocal of the bin's size per bin, then products
+            const float rn = __frcp_rn((float)((rr.y - rr.x) * (cr.y - cr.x)));
             const float4 g = *reinterpret_cast<const float4*>(dQl + ((size_t)bh * s.m + r * s.pw + c) * D + c4);
-            acc.x += g.x / n; acc.y += g.y / n; acc.z += g.z / n; acc.w += g.w / n;
+            acc.x = fmaf(g.x, rn, acc.x); acc.y = fmaf(g.y, rn, acc.y);
+            acc.z = fmaf(g.z, rn, acc.z); acc.w = fmaf(g.w, rn, acc.w);
         }
     }
     float4* o = reinterpret_cast<float4*>(dQ + ((size_t)bh * s.N + t) * D + c4);
