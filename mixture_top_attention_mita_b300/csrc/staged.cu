@@ -1989,8 +1989,14 @@ static cudaError_t run_backward_t(mita_plan_s* p, const T* Q, const T* K, const 
     }
     float* Vl32 = p->dVl + (size_t)BH * s.m * D;   // fp32 landmark values, then per-row {max S, sum w}
     float* stats = Vl32 + (size_t)BH * s.m * D;
-    // key-split partial sums use dK as scratch before it is cleared
-    p->launches += launch_values_rows<T, D>(s, p->S, V, Vl, Vl32, stats, dK, nbytes, st) - 1;
+    if (tiled_recompute) {   // the tiled path's tensor-core landmark values, with the row stats
+        if ((e = tiled_values_stats(s, p->S, p->rowmax, V, p->vpart, Vl, Vl32, stats, p->status, st)) != cudaSuccess)
+            return e;
+        p->launches += 1;   // two launches in place of one
+    } else {
+        // key-split partial sums use dK as scratch before it is cleared
+        p->launches += launch_values_rows<T, D>(s, p->S, V, Vl, Vl32, stats, dK, nbytes, st) - 1;
+    }
     if (!tiled_recompute)
         route_kernel<T, D><<<dim3((s.N + 127) / 128, BH), 128, 0, st>>>(s, Q, Ql, p->route, 1, nullptr);
     if ((e = cudaMemsetAsync(dK, 0, nbytes, st)) != cudaSuccess) return e;

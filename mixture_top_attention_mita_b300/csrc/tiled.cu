@@ -502,6 +502,28 @@ __global__ void tl_values_fin(Shape s, const float* __restrict__ part, int ns, b
     Vl[((size_t)bh * s.m + i) * D + f] = __float2bfloat16_rn(num / den);
 }
 
+// As tl_values_fin, also keeping V_l in fp32 and each row's softmax stats
+// {max raw score, sum of the numerators} for the backward.
+template <int D>
+__global__ void tl_values_fin_stats(Shape s, const float* __restrict__ part, int ns, const uint32_t* __restrict__ rowmax,
+                                    bf16* __restrict__ Vl, float* __restrict__ Vl32, float* __restrict__ stats) {
+    const int i = blockIdx.x, bh = blockIdx.y, f = threadIdx.x;
+    const float* src = part + ((size_t)bh * ns * s.m + i) * (D + 1);
+    float num = 0.0f, den = 0.0f;
+    for (int sp = 0; sp < ns; ++sp) {
+        num += src[(size_t)sp * s.m * (D + 1) + f];
+        den += src[(size_t)sp * s.m * (D + 1) + D];
+    }
+    const size_t row = (size_t)bh * s.m + i;
+    const float y = num / den;
+    Vl[row * D + f] = __float2bfloat16_rn(y);
+    Vl32[row * D + f] = y;
+    if (f == 0) {
+        stats[2 * row] = key_to_float(rowmax[row]);
+        stats[2 * row + 1] = den;
+    }
+}
+
 // ---------------------------------------------------------------- buckets
 // One warp per head: bucket offsets (exclusive scan of the counts), the
 // scatter cursors and the attention tile list: per tile (expert << 16 |
@@ -847,6 +869,20 @@ size_t tiled_part_bytes(const Shape& s) {
 int tiled_max_tiles(const Shape& s) { return tl::max_tiles(s); }
 
 bool tiled_topk_supported(const Shape& s) { return s.N <= tl::kRegRowN; }
+
+cudaError_t tiled_values_stats(const Shape& s, const float* S, const uint32_t* rowmax, const void* V, float* part,
+                               void* Vl, float* Vl32, float* stats, int32_t* status, cudaStream_t st) {
+    const float cs = kLog2e / sqrtf((float)s.d);
+    cudaError_t err = tc_values(s, S, rowmax, V, part, cs, status, st, false);
+    if (err != cudaSuccess) return err;
+    const int ns = tl::nsplit(s);
+    using T = __nv_bfloat16;
+    if (s.d == 64)
+        return launch_chained(false, tl::tl_values_fin_stats<64>, dim3(s.m, s.BH()), dim3(64), 0, st, s,
+                              (const float*)part, ns, rowmax, (T*)Vl, Vl32, stats);
+    return launch_chained(false, tl::tl_values_fin_stats<128>, dim3(s.m, s.BH()), dim3(128), 0, st, s,
+                          (const float*)part, ns, rowmax, (T*)Vl, Vl32, stats);
+}
 
 cudaError_t tiled_topk(const Shape& s, const float* S, const uint32_t* rowmax, int32_t* idx, cudaStream_t st) {
     const uint32_t* rowmin = rowmax + (size_t)s.BH() * s.m;
