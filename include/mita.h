@@ -92,6 +92,32 @@ int mita_plan(mita_plan_t* plan, int B, int H, int N, int d, mita_grid_t grid,
 int mita_forward(mita_plan_t plan, const void* Q, const void* K, const void* V, void* out,
                  int32_t* expert_idx, int32_t* route, struct CUstream_st* stream);
 
+/* The forward of mita_forward() on tensors in HOST memory: Q, K, V, out,
+ * expert_idx and route have the layouts and types of mita_forward() but
+ * point to host memory (page-locked -- cudaMallocHost or cudaHostRegister --
+ * for the copies to overlap; pageable memory gives the same results with the
+ * copies serialised).  No alignment is required; expert_idx and route may be
+ * NULL.  The heads go through the device in 8 chunks, each a run of
+ * consecutive heads: while chunk c is copied to the device, chunk c - 1's
+ * forward runs on `stream` and chunk c - 2's results are copied back, on two
+ * copy streams the plan owns, so a call takes about as long as its larger
+ * copy direction.  The kernels, and so the results, are those of
+ * mita_forward() on the same path for a plan of the chunk's heads.
+ * Ordering: the copies to the device start once `stream` reaches this call,
+ * and `stream` passes the call's end only after the last result is in host
+ * memory, so synchronising `stream` (or an event recorded on it after the
+ * call) makes out, expert_idx and route readable; the host buffers must stay
+ * valid and unwritten until then.  The first call on a plan allocates two
+ * staging slots of device memory (about a quarter of Q, K, V and out
+ * together; MITA_ERR_OOM if that fails) and creates the copy streams
+ * (MITA_ERR_CUDA): make it before any stream capture.  Calls on one plan
+ * share the slots: order them on one stream.  Returns MITA_ERR_INVALID_ARG
+ * for a null Q, K, V or out, MITA_ERR_UNSUPPORTED where mita_forward()
+ * would, MITA_ERR_CUDA if a copy or launch fails to enqueue; data errors are
+ * reported by mita_get_status(), as for mita_forward(). */
+int mita_forward_host(mita_plan_t plan, const void* Q, const void* K, const void* V, void* out,
+                      int32_t* expert_idx, int32_t* route, struct CUstream_st* stream);
+
 /* Wait for the plan's last mita_forward() / mita_backward() launch and
  * return the device status word of the plan's kernels since the last call
  * (MITA_OK or MITA_ERR_DEVICE / MITA_ERR_TIMEOUT), then clear it.  It waits

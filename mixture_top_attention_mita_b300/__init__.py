@@ -23,7 +23,7 @@ PATH_AUTO, PATH_STAGED, PATH_FUSED, PATH_TILED = 0, 1, 2, 3
 PATH_NAMES = {PATH_STAGED: "staged", PATH_FUSED: "fused", PATH_TILED: "tiled"}
 
 # Every entry point declared in include/mita.h.
-EXPORTS = ("mita_plan", "mita_forward", "mita_backward", "mita_get_status", "mita_destroy", "mita_strerror",
+EXPORTS = ("mita_plan", "mita_forward", "mita_forward_host", "mita_backward", "mita_get_status", "mita_destroy", "mita_strerror",
            "mita_set_option", "mita_get_path", "mita_get_landmarks", "mita_workspace_bytes",
            "mita_launch_count", "mita_forward_noalloc", "mita_noalloc_scratch_bytes",
            "mita_testing_bucket", "mita_testing_wait")
@@ -54,6 +54,7 @@ def load(path: str | None = None):
     vp, i, ip = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int32)
     lib.mita_plan.argtypes = [ctypes.POINTER(vp), i, i, i, i, Grid, i, i, i]
     lib.mita_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.mita_forward_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
     lib.mita_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.mita_get_status.argtypes = [vp]
     lib.mita_destroy.argtypes = [vp]
@@ -139,6 +140,19 @@ class Plan:
         rc = self.lib.mita_forward(self.handle, _ptr(Q), _ptr(K), _ptr(V), _ptr(out), _ptr(expert_idx),
                                    _ptr(route), _stream_ptr(stream))
         _check(rc, "mita_forward")
+
+    def forward_host(self, Q, K, V, out, expert_idx=None, route=None, stream=None):
+        """Enqueue ``mita_forward_host`` on ``stream`` (default: torch's
+        current stream): the same forward on CPU tensors (page-locked for the
+        copies to overlap), streamed through the device in chunks of heads.
+        The results are in ``out``, ``expert_idx`` and ``route`` once the
+        stream has passed the call."""
+        for t in (Q, K, V, out, expert_idx, route):
+            if t is not None and (t.is_cuda or not t.is_contiguous()):
+                raise ValueError("forward_host takes contiguous CPU tensors")
+        rc = self.lib.mita_forward_host(self.handle, _ptr(Q), _ptr(K), _ptr(V), _ptr(out), _ptr(expert_idx),
+                                        _ptr(route), _stream_ptr(stream))
+        _check(rc, "mita_forward_host")
 
     def backward(self, Q, K, V, dOut, dQ, dK, dV, stream=None):
         """Enqueue ``mita_backward``: input gradients dQ, dK, dV (fp32 CUDA

@@ -140,4 +140,13 @@ struct mita_plan_s {
     int32_t* tiles;        // [BH, max tiles] int2 attention tiles (expert << 16 | queries, first position)
     int32_t* ntiles;       // [BH]
     uint64_t launches;     // kernels launched so far
+    // mita_forward_host only: device staging for two chunks of heads (Q, K,
+    // V, out, experts, routes and, where the tiled path applies, its value
+    // partials), the two copy streams, and the events that order the chunks
+    // across those streams and the caller's
+    void* ws_host;
+    size_t host_slot_bytes;
+    int host_heads;        // heads per chunk
+    cudaStream_t h2d, d2h;
+    cudaEvent_t ev_start, ev_in[2], ev_comp[2], ev_out[2];
 };

@@ -2,6 +2,7 @@
 // choice and dispatch.  The operator and every argument are described in
 // include/mita.h.
 #include <stdlib.h>
+#include <algorithm>
 #include <string.h>
 
 #include "common.cuh"
@@ -98,6 +99,75 @@ int ensure_path(mita_plan_s* p) {
     return MITA_OK;
 }
 
+// ---------------------------------------------------------------- host forward
+// mita_forward_host streams the heads through the device in kHostChunks
+// chunks, two staging slots deep.
+constexpr int kHostChunks = 8;
+
+size_t io_size(const mita_plan_s* p) { return p->dtype == MITA_BF16 ? 2 : 4; }
+
+// Byte offsets of one staging slot: Q, K, V and out of `hc` heads, then
+// their experts and routes, then (tiled-capable shapes) value partials sized
+// for the larger of the two chunk shapes a call uses.
+struct HostSlot {
+    size_t q, k, v, o, idx, route, part, bytes;
+};
+
+mita::Shape chunk_shape(const mita::Shape& s, int heads) {
+    mita::Shape c = s;
+    c.B = 1;
+    c.H = heads;
+    return c;
+}
+
+HostSlot host_slot(const mita_plan_s* p, int hc) {
+    const mita::Shape& s = p->s;
+    HostSlot L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+    const size_t act = (size_t)hc * s.N * s.d * io_size(p);
+    L.q = take(act);
+    L.k = take(act);
+    L.v = take(act);
+    L.o = take(act);
+    L.idx = take((size_t)hc * s.m * s.k * 4);
+    L.route = take((size_t)hc * s.N * 4);
+    size_t part = 0;
+    if (mita::tiled_supported(s, p->dtype)) {
+        const int BH = s.BH(), last = BH - (BH - 1) / hc * hc;
+        part = std::max(mita::tiled_part_bytes(chunk_shape(s, hc)), mita::tiled_part_bytes(chunk_shape(s, last)));
+    }
+    L.part = take(part);
+    L.bytes = off;
+    return L;
+}
+
+// The copy streams and events on the plan's device, then the two staging
+// slots (one allocation), on the first mita_forward_host() call.
+int ensure_host(mita_plan_s* p) {
+    if (p->ws_host) return MITA_OK;
+    if (!p->ev_out[1]) {
+        int prev = 0;
+        cudaGetDevice(&prev);
+        cudaSetDevice(p->device);
+        bool ok = (p->h2d || cudaStreamCreateWithFlags(&p->h2d, cudaStreamNonBlocking) == cudaSuccess) &&
+                  (p->d2h || cudaStreamCreateWithFlags(&p->d2h, cudaStreamNonBlocking) == cudaSuccess);
+        cudaEvent_t* evs[7] = {&p->ev_start, &p->ev_in[0], &p->ev_in[1], &p->ev_comp[0],
+                               &p->ev_comp[1], &p->ev_out[0], &p->ev_out[1]};
+        for (int i = 0; ok && i < 7; ++i)
+            ok = *evs[i] || cudaEventCreateWithFlags(evs[i], cudaEventDisableTiming) == cudaSuccess;
+        cudaSetDevice(prev);
+        if (!ok) {
+            cudaGetLastError();
+            return MITA_ERR_CUDA;
+        }
+    }
+    const int BH = p->s.BH();
+    p->host_heads = (BH + kHostChunks - 1) / kHostChunks;
+    p->host_slot_bytes = host_slot(p, p->host_heads).bytes;
+    return alloc_region(p, &p->ws_host, 2 * p->host_slot_bytes);
+}
+
 void free_plan(mita_plan_s* p) {
     int prev = 0;
     cudaGetDevice(&prev);
@@ -107,8 +177,15 @@ void free_plan(mita_plan_s* p) {
     if (p->ws_S) cudaFree(p->ws_S);
     if (p->ws_tiled) cudaFree(p->ws_tiled);
     if (p->ws_grad) cudaFree(p->ws_grad);
+    if (p->ws_host) cudaFree(p->ws_host);
     if (p->done) cudaEventDestroy(p->done);
     if (p->aux) cudaStreamDestroy(p->aux);
+    if (p->h2d) cudaStreamDestroy(p->h2d);
+    if (p->d2h) cudaStreamDestroy(p->d2h);
+    cudaEvent_t evs[7] = {p->ev_start, p->ev_in[0], p->ev_in[1], p->ev_comp[0], p->ev_comp[1], p->ev_out[0],
+                          p->ev_out[1]};
+    for (cudaEvent_t e : evs)
+        if (e) cudaEventDestroy(e);
     cudaSetDevice(prev);
     free(p);
 }
@@ -129,6 +206,24 @@ void note_launch(mita_plan_s* p, cudaStream_t st) {
     }
     p->done_valid = cudaEventRecord(p->done, st) == cudaSuccess;
     if (!p->done_valid) cudaGetLastError();
+}
+
+// The path a forward takes, or -status when the plan cannot run it.
+int forward_path(const mita_plan_s* p) {
+    const int path = resolve_path(p);
+    if (path != MITA_PATH_STAGED && p->routes_s > 1) return -MITA_ERR_UNSUPPORTED;
+    if (path == MITA_PATH_FUSED && !mita::fused_supported(p->s, p->dtype)) return -MITA_ERR_UNSUPPORTED;
+    if (path == MITA_PATH_TILED && !p->rowmax) return -MITA_ERR_UNSUPPORTED;
+    if (path == MITA_PATH_STAGED && !p->S) return -MITA_ERR_UNSUPPORTED;
+    return path;
+}
+
+// Enqueue the forward of plan p's heads on `path` (device pointers).
+cudaError_t run_path(mita_plan_s* p, int path, const void* Q, const void* K, const void* V, void* out, int32_t* idx,
+                     int32_t* rt, cudaStream_t st) {
+    if (path == MITA_PATH_FUSED) return mita::run_fused(p, Q, K, V, out, idx, rt, p->keep_landmarks, st);
+    if (path == MITA_PATH_TILED) return mita::run_tiled(p, Q, K, V, out, idx, rt, st);
+    return mita::run_staged(p, Q, K, V, out, idx, rt, st);
 }
 
 }  // namespace
@@ -250,20 +345,74 @@ int mita_forward(mita_plan_t p, const void* Q, const void* K, const void* V, voi
     int32_t* idx = expert_idx ? expert_idx : p->idx;
     int32_t* rt = route ? route : p->route;
     cudaStream_t st = (cudaStream_t)stream;
-    cudaError_t err;
-    const int path = resolve_path(p);
-    if (path != MITA_PATH_STAGED && p->routes_s > 1) return MITA_ERR_UNSUPPORTED;
-    if (path == MITA_PATH_FUSED) {
-        if (!mita::fused_supported(p->s, p->dtype)) return MITA_ERR_UNSUPPORTED;
-        err = mita::run_fused(p, Q, K, V, out, idx, rt, p->keep_landmarks, st);
-    } else if (path == MITA_PATH_TILED) {
-        if (!p->rowmax) return MITA_ERR_UNSUPPORTED;
-        err = mita::run_tiled(p, Q, K, V, out, idx, rt, st);
-    } else {
-        if (!p->S) return MITA_ERR_UNSUPPORTED;
-        err = mita::run_staged(p, Q, K, V, out, idx, rt, st);
+    const int path = forward_path(p);
+    if (path < 0) return -path;
+    if (run_path(p, path, Q, K, V, out, idx, rt, st) != cudaSuccess) return MITA_ERR_CUDA;
+    note_launch(p, st);
+    p->landmarks_valid = p->keep_landmarks || path != MITA_PATH_FUSED;
+    return MITA_OK;
+}
+
+int mita_forward_host(mita_plan_t p, const void* Q, const void* K, const void* V, void* out, int32_t* expert_idx,
+                      int32_t* route, struct CUstream_st* stream) {
+    if (!p || !Q || !K || !V || !out) return MITA_ERR_INVALID_ARG;
+    const int path = forward_path(p);
+    if (path < 0) return -path;
+    int rc = ensure_host(p);
+    if (rc != MITA_OK) return rc;
+    const mita::Shape& s = p->s;
+    const size_t e = io_size(p);
+    const int BH = s.BH(), hc = p->host_heads, nc = (BH + hc - 1) / hc;
+    const HostSlot L = host_slot(p, hc);
+    cudaStream_t st = (cudaStream_t)stream;
+    // the copies in wait for the caller's stream position at this call (and
+    // so for the previous call's last copy out); chunk c reuses the slot of
+    // chunk c - 2 once that chunk's results have left it
+#define MITA_CK(x)                              \
+    do {                                        \
+        if ((x) != cudaSuccess) {               \
+            cudaGetLastError();                 \
+            return MITA_ERR_CUDA;               \
+        }                                       \
+    } while (0)
+    MITA_CK(cudaEventRecord(p->ev_start, st));
+    MITA_CK(cudaStreamWaitEvent(p->h2d, p->ev_start, 0));
+    MITA_CK(cudaStreamWaitEvent(p->d2h, p->ev_start, 0));
+    mita_plan_s sub = *p;
+    for (int c = 0; c < nc; ++c) {
+        const int slot = c & 1, h0 = c * hc, nh = std::min(hc, BH - h0);
+        char* base = (char*)p->ws_host + slot * p->host_slot_bytes;
+        const size_t act = (size_t)nh * s.N * s.d * e, aoff = (size_t)h0 * s.N * s.d * e;
+        const size_t ib = (size_t)nh * s.m * s.k * 4, ioff = (size_t)h0 * s.m * s.k * 4;
+        const size_t rb = (size_t)nh * s.N * 4, roff = (size_t)h0 * s.N * 4;
+        if (c >= 2) MITA_CK(cudaStreamWaitEvent(p->h2d, p->ev_out[slot], 0));
+        MITA_CK(cudaMemcpyAsync(base + L.q, (const char*)Q + aoff, act, cudaMemcpyHostToDevice, p->h2d));
+        MITA_CK(cudaMemcpyAsync(base + L.k, (const char*)K + aoff, act, cudaMemcpyHostToDevice, p->h2d));
+        MITA_CK(cudaMemcpyAsync(base + L.v, (const char*)V + aoff, act, cudaMemcpyHostToDevice, p->h2d));
+        MITA_CK(cudaEventRecord(p->ev_in[slot], p->h2d));
+        MITA_CK(cudaStreamWaitEvent(st, p->ev_in[slot], 0));
+        // the chunk as a plan of its own over the same workspace: landmarks
+        // at the chunk's place, value partials in the slot
+        sub.s = chunk_shape(s, nh);
+        sub.Ql = (char*)p->Ql + (size_t)h0 * s.m * s.d * e;
+        sub.Vl = (char*)p->Vl + (size_t)h0 * s.m * s.d * e;
+        if (L.part) sub.vpart = (float*)(base + L.part);
+        sub.launches = 0;
+        const cudaError_t err = run_path(&sub, path, base + L.q, base + L.k, base + L.v, base + L.o,
+                                         (int32_t*)(base + L.idx), (int32_t*)(base + L.route), st);
+        p->launches += sub.launches;
+        MITA_CK(err);
+        MITA_CK(cudaEventRecord(p->ev_comp[slot], st));
+        MITA_CK(cudaStreamWaitEvent(p->d2h, p->ev_comp[slot], 0));
+        MITA_CK(cudaMemcpyAsync((char*)out + aoff, base + L.o, act, cudaMemcpyDeviceToHost, p->d2h));
+        if (expert_idx)
+            MITA_CK(cudaMemcpyAsync((char*)expert_idx + ioff, base + L.idx, ib, cudaMemcpyDeviceToHost, p->d2h));
+        if (route) MITA_CK(cudaMemcpyAsync((char*)route + roff, base + L.route, rb, cudaMemcpyDeviceToHost, p->d2h));
+        MITA_CK(cudaEventRecord(p->ev_out[slot], p->d2h));
     }
-    if (err != cudaSuccess) return MITA_ERR_CUDA;
+    // the copies out run in order: the last one's event covers them all
+    MITA_CK(cudaStreamWaitEvent(st, p->ev_out[(nc - 1) & 1], 0));
+#undef MITA_CK
     note_launch(p, st);
     p->landmarks_valid = p->keep_landmarks || path != MITA_PATH_FUSED;
     return MITA_OK;
