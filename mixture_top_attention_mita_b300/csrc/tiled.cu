@@ -15,8 +15,11 @@
 //                   histogram over [min, max], an exact rank of the boundary
 //                   bin's members, the expert as a bitmap over the row read
 //                   out in key order
-//   tl_topk_bits    the same from global memory with 2048 bins, rows up to
-//                   64K keys (longer rows use the staged path's radix select)
+//   tl_topk_cb      the same for rows up to 64K keys (N a multiple of 4)
+//                   with 2048 bins, the row read once: each key's coarse bin
+//                   kept as a byte in shared memory for the second pass
+//   tl_topk_bits    the same reading the row twice (other lengths up to
+//                   64K keys; longer rows use the staged path's radix select)
 //   tc_values       split-K partial sums of exp(S / sqrt d - max) . V and of
 //                   the row sums, per split of 1024-4096 keys
 //   tl_values_fin   V_l = sum of partials / sum of row sums, bf16
@@ -127,8 +130,9 @@ constexpr int kTB = 256;          // threads per top-k block
 constexpr int kNB = 2048;         // histogram bins of tl_topk_bits (rows past 4096 keys)
 constexpr int kCandMax = 1024;    // boundary members ranked exactly
 
-// Block-wide exclusive prefix sum of one int per thread (kTB threads);
+// Block-wide exclusive prefix sum of one int per thread (NT threads);
 // *total receives the block total.
+template <int NT = kTB>
 MITA_DEV int block_excl_scan(int x, int* wsum, int* total) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     int incl = x;
@@ -142,7 +146,7 @@ MITA_DEV int block_excl_scan(int x, int* wsum, int* total) {
     __syncthreads();
     int base = 0, tot = 0;
 #pragma unroll
-    for (int u = 0; u < kTB / 32; ++u) {
+    for (int u = 0; u < NT / 32; ++u) {
         const int v = wsum[u];
         base += u < w ? v : 0;
         tot += v;
@@ -341,6 +345,202 @@ __global__ void __launch_bounds__(kTB) tl_topk_bits(Shape s, const float* __rest
         }
     }
 }
+
+// Rows of 4097 .. kBitsMaxN keys, N a multiple of 4: the select of
+// tl_topk_bits with the row read from memory once.  Pass 1 builds the
+// histogram of kCNB fine bins and keeps each key's coarse bin (fine bin / 8)
+// as one byte in shared memory (N bytes); pass 2 decides every key from its
+// byte and reads back from the score matrix only the keys of the coarse bin
+// that holds bin* (a few dozen per row on these inputs, still in L2).  Two
+// blocks of kCT threads per SM: one streams its row while the other works
+// from shared memory.
+constexpr int kCT = 512;
+constexpr int kCNB = 2048;
+
+__global__ void __launch_bounds__(kCT, 2) tl_topk_cb(Shape s, const float* __restrict__ S,
+                                                  const uint32_t* __restrict__ rowmax,
+                                                  const uint32_t* __restrict__ rowmin, int32_t* __restrict__ idx) {
+    chain_wait_and_trigger();
+    constexpr int BPT = kCNB / kCT;   // bins per thread in the boundary search
+    extern __shared__ __align__(16) unsigned char cbin_raw[];   // coarse bin of every key
+    __shared__ int hist[kCNB];
+    __shared__ uint32_t bits[kBitsMaxN / 32];
+    __shared__ float cval[kCandMax];
+    __shared__ int cidx[kCandMax];
+    __shared__ int wsum[kCT / 32];
+    __shared__ int sh[4];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int N = s.N, k = s.k, nw = (N + 31) >> 5, n4 = N >> 2;
+    const size_t r = (size_t)blockIdx.y * s.m + blockIdx.x;
+    const float* row = S + r * N;
+    uint32_t* cb4 = (uint32_t*)cbin_raw;   // four keys' coarse bins per word
+    const float mx = key_to_float(rowmax[r]), mn = key_to_float(rowmin[r]);
+    const float range = mx - mn;
+    const float sc = range > 0.0f ? (float)kCNB / range : 0.0f;
+    auto bin_of = [&](float v) { return min(kCNB - 1, (int)((v - mn) * sc)); };
+    for (int b = tid; b < kCNB; b += kCT) hist[b] = 0;
+    for (int w = tid; w < nw; w += kCT) bits[w] = 0u;
+    if (tid == 0) sh[3] = 0;
+    __syncthreads();
+    auto put4 = [&](int j, const float4& a) {
+        const int b0 = bin_of(a.x), b1 = bin_of(a.y), b2 = bin_of(a.z), b3 = bin_of(a.w);
+        atomicAdd(&hist[b0], 1);
+        atomicAdd(&hist[b1], 1);
+        atomicAdd(&hist[b2], 1);
+        atomicAdd(&hist[b3], 1);
+        cb4[j] = (uint32_t)(b0 >> 3) | ((uint32_t)(b1 >> 3) << 8) | ((uint32_t)(b2 >> 3) << 16) |
+                 ((uint32_t)(b3 >> 3) << 24);
+    };
+    {   // pass 1: 16-byte loads, kU in flight per thread
+        constexpr int kU = 8;
+        const float4* row4 = (const float4*)row;
+        int j = tid;
+        for (; j + (kU - 1) * kCT < n4; j += kU * kCT) {
+            float4 a[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) a[u] = __ldg(row4 + j + u * kCT);
+#pragma unroll
+            for (int u = 0; u < kU; ++u) put4(j + u * kCT, a[u]);
+        }
+        for (; j < n4; j += kCT) put4(j, __ldg(row4 + j));
+    }
+    __syncthreads();
+    {   // thread t holds bins [BPT t, BPT t + BPT); counts of bins above, from the top down
+        int c[BPT], tot = 0;
+#pragma unroll
+        for (int u = 0; u < BPT; ++u) { c[u] = hist[BPT * tid + u]; tot += c[u]; }
+        int all;
+        const int below = block_excl_scan<kCT>(tot, wsum, &all);
+        const int above = all - below - tot;
+        if (above < k && above + tot >= k) {
+            int run = above;
+#pragma unroll
+            for (int u = BPT - 1; u >= 0; --u) {
+                if (run < k && run + c[u] >= k) {
+                    sh[0] = BPT * tid + u;
+                    sh[1] = k - run;
+                    sh[2] = c[u];
+                }
+                run += c[u];
+            }
+        }
+    }
+    __syncthreads();
+    const int bstar = sh[0], need = sh[1], cstar = sh[2];
+    const bool take_all = need >= cstar;            // every member of bin* is in the expert
+    const bool listed = !take_all && cstar <= kCandMax;
+    const uint32_t cstar8 = (uint32_t)bstar >> 3;
+    // pass 2: warp w's lanes hold the 128 consecutive keys of bitmap words
+    // 4c .. 4c + 3 (c = w, w + 16, ...), four keys a lane; the keys of bin*'s
+    // coarse bin are read back for their fine bin
+    for (int c = warp; 32 * c < n4; c += kCT / 32) {
+        const int q = 32 * c + lane;
+        uint32_t nib = 0u;
+        if (q < n4) {
+            const uint32_t cbw = cb4[q];
+            float v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = ((cbw >> (8 * u)) & 0xffu) == cstar8 ? row[4 * q + u] : 0.0f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t cb = (cbw >> (8 * u)) & 0xffu;
+                bool sel = cb > cstar8;
+                if (cb == cstar8) {
+                    const int b = bin_of(v[u]);
+                    sel = b > bstar || (take_all && b == bstar);
+                    if (listed && b == bstar) {
+                        const int p = atomicAdd(&sh[3], 1);
+                        cval[p] = v[u];
+                        cidx[p] = 4 * q + u;
+                    }
+                }
+                nib |= (sel ? 1u : 0u) << u;
+            }
+        }
+        uint32_t word = nib << (4 * (lane & 7));
+        word |= __shfl_xor_sync(0xffffffffu, word, 1);
+        word |= __shfl_xor_sync(0xffffffffu, word, 2);
+        word |= __shfl_xor_sync(0xffffffffu, word, 4);
+        const int wi = 4 * c + (lane >> 3);
+        if ((lane & 7) == 0 && wi < nw) bits[wi] = word;
+    }
+    __syncthreads();
+    if (listed) {
+        for (int p = tid; p < cstar; p += kCT) {
+            const float x = cval[p];
+            const int jp = cidx[p];
+            int rank = 0;
+            for (int q = 0; q < cstar; ++q) {
+                const float w = cval[q];
+                rank += (w > x || (w == x && cidx[q] < jp)) ? 1 : 0;
+            }
+            if (rank < need) atomicOr(&bits[jp >> 5], 1u << (jp & 31));
+        }
+        __syncthreads();
+    } else if (!take_all) {
+        // many members (ties, flat rows): the need-th best member's order key T
+        // by bisection over the row, then members above T and, in key order,
+        // those equal to T until need is met
+        uint32_t T = 0u;
+        for (int bb = 31; bb >= 0; --bb) {
+            const uint32_t ct = T | (1u << bb);
+            int cnt = 0;
+            for (int j = tid; j < N; j += kCT) {
+                const float v = row[j];
+                cnt += (bin_of(v) == bstar && order_key(v) >= ct) ? 1 : 0;
+            }
+            int total;
+            block_excl_scan<kCT>(cnt, wsum, &total);
+            if (total >= need) T = ct;
+        }
+        int gt = 0;
+        for (int j = tid; j < N; j += kCT) {
+            const float v = row[j];
+            gt += (bin_of(v) == bstar && order_key(v) > T) ? 1 : 0;
+        }
+        int gt_all;
+        block_excl_scan<kCT>(gt, wsum, &gt_all);
+        if (warp == 0) {
+            int eq_left = need - gt_all;
+            for (int w = 0; w < nw; ++w) {
+                const int j = 32 * w + lane;
+                bool above = false, eq = false;
+                if (j < N) {
+                    const float v = row[j];
+                    if (bin_of(v) == bstar) {
+                        const uint32_t kv = order_key(v);
+                        above = kv > T;
+                        eq = kv == T;
+                    }
+                }
+                const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
+                const int rr = __popc(eqm & ((1u << lane) - 1u));
+                const uint32_t add = __ballot_sync(0xffffffffu, above || (eq && rr < eq_left));
+                eq_left -= min(eq_left, __popc(eqm));
+                if (lane == 0) bits[w] |= add;
+            }
+        }
+        __syncthreads();
+    }
+    // the expert in ascending key order: thread t reads words [t*wpt, (t+1)*wpt)
+    const int wpt = (nw + kCT - 1) / kCT, w0 = min(nw, tid * wpt), w1 = min(nw, w0 + wpt);
+    int cnt = 0;
+    for (int w = w0; w < w1; ++w) cnt += __popc(bits[w]);
+    int total;
+    int pos = block_excl_scan<kCT>(cnt, wsum, &total);
+    int32_t* out = idx + r * k;
+    for (int w = w0; w < w1; ++w) {
+        uint32_t b = bits[w];
+        while (b) {
+            const int x = __ffs(b) - 1;
+            b &= b - 1u;
+            if (pos < k) out[pos] = 32 * w + x;
+            ++pos;
+        }
+    }
+}
+
+size_t topk_cb_smem(int N) { return ((size_t)N + 15) / 16 * 16; }
 
 // Rows up to kRegRowN keys (the 56x56 layer's 3136): the expert of
 // tl_topk_bits<256>, with thread t holding keys t, t + kTB, ... of the row in
@@ -814,7 +1014,14 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
                                     chain)) != cudaSuccess) {
             return err;
         }
-        if (s.N <= kBitsMaxN) {
+        if (s.N > kRegRowN && s.N <= kBitsMaxN && (s.N & 3) == 0) {
+            const size_t smem = topk_cb_smem(s.N);
+            if ((err = ensure_smem_attr((const void*)tl_topk_cb, smem)) != cudaSuccess) return err;
+            if ((err = launch_chained(chain, tl_topk_cb, dim3(s.m, sg.H), dim3(kCT), smem, st, sg, (const float*)p->S,
+                                      (const uint32_t*)(p->rowmax + mo), (const uint32_t*)(rowmin + mo),
+                                      idx + mo * s.k)) != cudaSuccess)
+                return err;
+        } else if (s.N <= kBitsMaxN) {
             auto kern = s.N <= kRegRowN ? tl_topk_reg : tl_topk_bits<kNB>;
             if ((err = launch_chained(chain, kern, dim3(s.m, sg.H), dim3(kTB), 0, st, sg, (const float*)p->S,
                                       (const uint32_t*)(p->rowmax + mo), (const uint32_t*)(rowmin + mo),
