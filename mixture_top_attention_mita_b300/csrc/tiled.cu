@@ -375,9 +375,12 @@ __global__ void __launch_bounds__(kCT, 2) tl_topk_cb(Shape s, const float* __res
     const float* row = S + r * N;
     uint32_t* cb4 = (uint32_t*)cbin_raw;   // four keys' coarse bins per word
     const float mx = key_to_float(rowmax[r]), mn = key_to_float(rowmin[r]);
-    const float range = mx - mn;
-    const float sc = range > 0.0f ? (float)kCNB / range : 0.0f;
-    auto bin_of = [&](float v) { return min(kCNB - 1, (int)((v - mn) * sc)); };
+    float sc = mx > mn ? (float)kCNB / (mx - mn) : 0.0f;
+    float off = -mn * sc;
+    if (!(fabsf(off) <= 3.0e38f)) sc = off = 0.0f;   // overflow: one bin, resolved by bisection
+    // a monotone function of the score; the unsigned conversion takes
+    // negatives and NaN to 0
+    auto bin_of = [&](float v) { return (int)min((unsigned)(kCNB - 1), __float2uint_rz(fmaf(v, sc, off))); };
     for (int b = tid; b < kCNB; b += kCT) hist[b] = 0;
     for (int w = tid; w < nw; w += kCT) bits[w] = 0u;
     if (tid == 0) sh[3] = 0;
@@ -429,32 +432,33 @@ __global__ void __launch_bounds__(kCT, 2) tl_topk_cb(Shape s, const float* __res
     const int bstar = sh[0], need = sh[1], cstar = sh[2];
     const bool take_all = need >= cstar;            // every member of bin* is in the expert
     const bool listed = !take_all && cstar <= kCandMax;
-    const uint32_t cstar8 = (uint32_t)bstar >> 3;
+    const uint32_t c4 = ((uint32_t)bstar >> 3) * 0x01010101u;   // bin*'s coarse bin in every byte
     // pass 2: warp w's lanes hold the 128 consecutive keys of bitmap words
-    // 4c .. 4c + 3 (c = w, w + 16, ...), four keys a lane; the keys of bin*'s
-    // coarse bin are read back for their fine bin
+    // 4c .. 4c + 3 (c = w, w + 16, ...), four keys (one word of bytes) a
+    // lane, compared four at a time; the keys of bin*'s coarse bin (rare) are
+    // read back for their fine bin
     for (int c = warp; 32 * c < n4; c += kCT / 32) {
         const int q = 32 * c + lane;
         uint32_t nib = 0u;
         if (q < n4) {
             const uint32_t cbw = cb4[q];
-            float v[4];
+            // one bit per byte above bin*'s coarse bin, gathered into bits 24 .. 27
+            nib = (((__vcmpgtu4(cbw, c4) & 0x01010101u) * 0x01020408u) >> 24) & 0xfu;
+            const uint32_t eq = __vcmpeq4(cbw, c4);
+            if (eq) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = ((cbw >> (8 * u)) & 0xffu) == cstar8 ? row[4 * q + u] : 0.0f;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t cb = (cbw >> (8 * u)) & 0xffu;
-                bool sel = cb > cstar8;
-                if (cb == cstar8) {
-                    const int b = bin_of(v[u]);
-                    sel = b > bstar || (take_all && b == bstar);
-                    if (listed && b == bstar) {
-                        const int p = atomicAdd(&sh[3], 1);
-                        cval[p] = v[u];
-                        cidx[p] = 4 * q + u;
+                for (int u = 0; u < 4; ++u) {
+                    if ((eq >> (8 * u)) & 1u) {
+                        const float v = row[4 * q + u];
+                        const int b = bin_of(v);
+                        if (b > bstar || (take_all && b == bstar)) nib |= 1u << u;
+                        if (listed && b == bstar) {
+                            const int p = atomicAdd(&sh[3], 1);
+                            cval[p] = v;
+                            cidx[p] = 4 * q + u;
+                        }
                     }
                 }
-                nib |= (sel ? 1u : 0u) << u;
             }
         }
         uint32_t word = nib << (4 * (lane & 7));
