@@ -1,9 +1,12 @@
 // tcgen05 kernels of the tiled MiTA path (sm_103a): the dense contractions
 // run on the fifth-generation tensor cores with operands staged by TMA and
 // fp32 accumulators in tensor memory.
-//   tc_scores  S = Q_l . K^T per (128 landmarks x 128 keys) tile; each thread
-//              of the epilogue owns one landmark row: it stores the row's
-//              scores and folds them into the row max and min.
+//   tc_scores  S = Q_l . K^T: for m <= 256 the scores half of
+//              tc_scores_route below (tokens as M, every store 128
+//              consecutive bytes of one row); beyond, per (128 landmarks x
+//              128 keys) tile with each epilogue thread owning one landmark
+//              row, storing the row's scores and folding them into the row
+//              max and min.
 //   tc_values  split-K partials of V_l: numerators exp(S / sqrt d - max) are
 //              computed from S straight into a 128-byte swizzled K-major A
 //              tile, V comes by TMA as an M/N-major B tile, and the MMAs of a
@@ -351,13 +354,14 @@ __global__ void __launch_bounds__(128) tc_route(const __grid_constant__ CUtensor
 // Scores and routes of one tile of 128 tokens (m <= 128 landmarks): both
 // contractions take the token rows as M and the landmarks as N, against the
 // one Q_l tile, S^T = K . Q_l^T at tensor-memory column 0 and R = Q . Q_l^T at
-// column tcols / 2.  Thread t of the epilogue owns token n0 + t: it stores its
+// column tcols / 2 (ROUTE), or the scores alone for up to 256 landmarks
+// (!ROUTE; the routes then come from tc_route).  Thread t of the epilogue owns token n0 + t: it stores its
 // column of S (for each landmark the warp's 32 consecutive keys are one
 // 128-byte store), the warp's max and min of each landmark's scores (one
 // floating-point redux each) go into the block's row keys, and the thread takes the
 // first argmax of its query's logits (the route).  The block then adds its
 // row keys and route counts to the global ones.
-template <int D>
+template <int D, bool ROUTE>
 __global__ void __launch_bounds__(128) tc_scores_route(const __grid_constant__ CUtensorMap mK,
                                                        const __grid_constant__ CUtensorMap mQ,
                                                        const __grid_constant__ CUtensorMap mQl, Shape s, int nb,
@@ -369,20 +373,23 @@ __global__ void __launch_bounds__(128) tc_scores_route(const __grid_constant__ C
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ uint32_t tslot;
     __shared__ __align__(8) uint64_t bars[2];
-    __shared__ uint32_t smax[128], smin[128];
-    __shared__ int hist[128];
+    constexpr int kML = ROUTE ? 128 : 256;   // landmarks a block takes
+    __shared__ uint32_t smax[kML], smin[kML];
+    __shared__ int hist[ROUTE ? 128 : 1];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (smem_u32(smem) & 1023u) {
         if (tid == 0) atomicExch(status, (int)MITA_ERR_DEVICE);
         return;
     }
     const int n0 = blockIdx.x * 128, bh = blockIdx.y, m = s.m, N = s.N;
-    const uint32_t sK = smem_u32(smem), sQ = sK + KC * kChunk, sB = sQ + KC * kChunk;
+    const uint32_t sK = smem_u32(smem), sQ = sK + KC * kChunk, sB = ROUTE ? sQ + KC * kChunk : sQ;
     const uint32_t bchunk = (uint32_t)nb * 128u;   // bytes per 64-column chunk of the landmark tile
     const uint32_t bar_ld = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[1]);
-    smax[tid] = 0u;
-    smin[tid] = 0xffffffffu;
-    hist[tid] = 0;
+    for (int e = tid; e < kML; e += 128) {
+        smax[e] = 0u;
+        smin[e] = 0xffffffffu;
+    }
+    if (ROUTE) hist[tid] = 0;
     if (tid == 0) {
         mbar_init(bar_ld, 1);
         mbar_init(bar_mma, 1);
@@ -393,10 +400,10 @@ __global__ void __launch_bounds__(128) tc_scores_route(const __grid_constant__ C
     fence_after();
     const uint32_t tmem = tslot, tR = tmem + (uint32_t)(tcols / 2);
     if (tid == 0) {
-        mbar_expect_tx(bar_ld, KC * (2 * kChunk + bchunk));
+        mbar_expect_tx(bar_ld, KC * ((ROUTE ? 2 : 1) * kChunk + bchunk));
         for (int kc = 0; kc < KC; ++kc) {
             tma_load_2d(sK + kc * kChunk, &mK, kc * 64, bh * N + n0, bar_ld);
-            tma_load_2d(sQ + kc * kChunk, &mQ, kc * 64, bh * N + n0, bar_ld);
+            if (ROUTE) tma_load_2d(sQ + kc * kChunk, &mQ, kc * 64, bh * N + n0, bar_ld);
             tma_load_2d(sB + kc * bchunk, &mQl, kc * 64, bh * m, bar_ld);
         }
         if (mbar_wait_bounded(bar_ld, 0)) {
@@ -407,7 +414,7 @@ __global__ void __launch_bounds__(128) tc_scores_route(const __grid_constant__ C
                 const uint32_t oa = (kk >> 2) * kChunk + (kk & 3) * 32;
                 const uint64_t db = desc_kmajor(sB + (kk >> 2) * bchunk + (kk & 3) * 32);
                 mma_bf16(tmem, desc_kmajor(sK + oa), db, idesc, kk > 0);
-                mma_bf16(tR, desc_kmajor(sQ + oa), db, idesc, kk > 0);
+                if (ROUTE) mma_bf16(tR, desc_kmajor(sQ + oa), db, idesc, kk > 0);
             }
             mma_commit(bar_mma);
         }
@@ -450,30 +457,32 @@ __global__ void __launch_bounds__(128) tc_scores_route(const __grid_constant__ C
             for (int c0 = 0; c0 < m; c0 += 32) chunk(c0, std::true_type{});
         else
             for (int c0 = 0; c0 < m; c0 += 32) chunk(c0, std::false_type{});
-        float best = -INFINITY;
-        int arg = 0;
-        for (int c0 = 0; c0 < nb; c0 += 32) {
-            float v[32];
-            tmem_ld32(tR + lanes + c0, v);
+        if (ROUTE) {
+            float best = -INFINITY;
+            int arg = 0;
+            for (int c0 = 0; c0 < nb; c0 += 32) {
+                float v[32];
+                tmem_ld32(tR + lanes + c0, v);
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (c0 + j < m && v[j] > best) {   // ascending landmarks, strict: first argmax
-                    best = v[j];
-                    arg = c0 + j;
-                }
-        }
-        if (live) {
-            route[(size_t)bh * N + n] = arg;
-            atomicAdd(&hist[arg], 1);
+                for (int j = 0; j < 32; ++j)
+                    if (c0 + j < m && v[j] > best) {   // ascending landmarks, strict: first argmax
+                        best = v[j];
+                        arg = c0 + j;
+                    }
+            }
+            if (live) {
+                route[(size_t)bh * N + n] = arg;
+                atomicAdd(&hist[arg], 1);
+            }
         }
     }
     fence_before();
     __syncthreads();
-    if (tid < m) {
-        const size_t r = (size_t)bh * m + tid;
-        if (smax[tid] != 0u) atomicMax(&rowmax[r], smax[tid]);
-        if (smin[tid] != 0xffffffffu) atomicMin(&rowmin[r], smin[tid]);
-        if (hist[tid]) atomicAdd(&counts[r], hist[tid]);
+    for (int e = tid; e < m; e += 128) {
+        const size_t r = (size_t)bh * m + e;
+        if (smax[e] != 0u) atomicMax(&rowmax[r], smax[e]);
+        if (smin[e] != 0xffffffffu) atomicMin(&rowmin[r], smin[e]);
+        if (ROUTE && hist[e]) atomicAdd(&counts[r], hist[e]);
     }
     if (warp == 0) tmem_free(tmem, (uint32_t)tcols);
 }
@@ -560,21 +569,31 @@ static cudaError_t tc_route_t(const Shape& s, const void* Q, const void* Ql, int
     return cudaGetLastError();
 }
 
-template <int D>
+// ROUTE: scores and routes (m <= 128); else the scores alone (m <= 256), Q
+// and the route arguments unused.
+template <int D, bool ROUTE>
 static cudaError_t tc_scores_route_t(const Shape& s, const void* Ql, const void* K, const void* Q, float* S,
                                      uint32_t* rowmax, uint32_t* rowmin, int32_t* route, int32_t* counts,
                                      int32_t* status, cudaStream_t st, bool chain) {
     const int nb = (s.m + 15) / 16 * 16;
     int tcols = 32;
-    while (tcols < 2 * nb) tcols <<= 1;
+    while (tcols < (ROUTE ? 2 : 1) * nb) tcols <<= 1;
     CUtensorMap mk, mq, ml;
-    if (!map_rows(&mk, K, D, (size_t)s.BH() * s.N, 128) || !map_rows(&mq, Q, D, (size_t)s.BH() * s.N, 128) ||
-        !map_rows(&ml, Ql, D, (size_t)s.BH() * s.m, nb))
+    if (!map_rows(&mk, K, D, (size_t)s.BH() * s.N, 128) || !map_rows(&ml, Ql, D, (size_t)s.BH() * s.m, nb))
         return cudaErrorInvalidValue;
-    const int smem = (D / 64) * (2 * (int)tcg::kChunk + nb * 128) + 1024;
-    ensure_smem_attr((const void*)tcg::tc_scores_route<D>, smem);
-    cudaError_t le = launch_chained(chain, tcg::tc_scores_route<D>, dim3((s.N + 127) / 128, s.BH()), dim3(128), smem, st,
-                                    mk, mq, ml, s, nb, tcols, S, rowmax, rowmin, route, counts, status);
+    if (ROUTE && !map_rows(&mq, Q, D, (size_t)s.BH() * s.N, 128)) return cudaErrorInvalidValue;
+    if (!ROUTE) mq = mk;   // not read
+    // scores alone: at most 512 / tcols blocks a SM (the 512 tensor-memory
+    // columns); the shared-memory request keeps a further block, which would
+    // only wait in its allocation, off the SM (228 KB of shared memory a SM).
+    // With the routes the smaller request measures faster (56x56: 193.0
+    // against 194.5 us with the cap).
+    const int smem0 = (D / 64) * ((ROUTE ? 2 : 1) * (int)tcg::kChunk + nb * 128) + 1024;
+    const int smem = ROUTE ? smem0 : std::max(smem0, 233472 / (512 / tcols + 1));
+    auto kern = tcg::tc_scores_route<D, ROUTE>;
+    ensure_smem_attr((const void*)kern, smem);
+    cudaError_t le = launch_chained(chain, kern, dim3((s.N + 127) / 128, s.BH()), dim3(128), smem, st, mk, mq, ml, s,
+                                    nb, tcols, S, rowmax, rowmin, route, counts, status);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
@@ -584,14 +603,19 @@ bool tc_scores_route_supported(const Shape& s) { return s.m <= 128; }
 cudaError_t tc_scores_route(const Shape& s, const void* Ql, const void* K, const void* Q, float* S, uint32_t* rowmax,
                             uint32_t* rowmin, int32_t* route, int32_t* counts, int32_t* status, cudaStream_t st,
                             bool chain) {
-    return s.d == 64 ? tc_scores_route_t<64>(s, Ql, K, Q, S, rowmax, rowmin, route, counts, status, st, chain)
-                     : tc_scores_route_t<128>(s, Ql, K, Q, S, rowmax, rowmin, route, counts, status, st, chain);
+    return s.d == 64 ? tc_scores_route_t<64, true>(s, Ql, K, Q, S, rowmax, rowmin, route, counts, status, st, chain)
+                     : tc_scores_route_t<128, true>(s, Ql, K, Q, S, rowmax, rowmin, route, counts, status, st, chain);
 }
 
 int tc_value_splits(const Shape& s) { return (s.N + tc_value_keys(s) - 1) / tc_value_keys(s); }
 
 cudaError_t tc_scores(const Shape& s, const void* Ql, const void* K, float* S, uint32_t* rowmax, uint32_t* rowmin,
                       int32_t* status, cudaStream_t st, bool chain) {
+    if (s.m <= 256)   // token-major tiles: every store is 128 consecutive bytes of one row
+        return s.d == 64 ? tc_scores_route_t<64, false>(s, Ql, K, nullptr, S, rowmax, rowmin, nullptr, nullptr,
+                                                        status, st, chain)
+                         : tc_scores_route_t<128, false>(s, Ql, K, nullptr, S, rowmax, rowmin, nullptr, nullptr,
+                                                         status, st, chain);
     return s.d == 64 ? tc_scores_t<64>(s, Ql, K, S, rowmax, rowmin, status, st, chain)
                      : tc_scores_t<128>(s, Ql, K, S, rowmax, rowmin, status, st, chain);
 }
