@@ -1964,7 +1964,7 @@ static cudaError_t run_backward_t(mita_plan_s* p, const T* Q, const T* K, const 
     // one-kernel scores and routes (the same Q_l, scores and first argmax)
     bool tiled_recompute = false;
     if constexpr (std::is_same<T, __nv_bfloat16>::value)
-        tiled_recompute = p->rowmax != nullptr && tc_scores_route_supported(s);
+        tiled_recompute = p->rowmax != nullptr && s.m <= 128 && tc_scores_route_supported(s);
     if (tiled_recompute) {
         uint32_t* rowmin = p->rowmax + (size_t)BH * s.m;
         if (s.N <= 32 * s.m) {   // bins of about 32 tokens or fewer: a block of D threads per landmark

@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(128) tc_scores_route(const __grid_constant__ C
     __shared__ __align__(8) uint64_t bars[2];
     constexpr int kML = ROUTE ? 128 : 256;   // landmarks a block takes
     __shared__ uint32_t smax[kML], smin[kML];
-    __shared__ int hist[ROUTE ? 128 : 1];
+    __shared__ int hist[kML];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (smem_u32(smem) & 1023u) {
         if (tid == 0) atomicExch(status, (int)MITA_ERR_DEVICE);
@@ -389,7 +389,8 @@ __global__ void __launch_bounds__(128) tc_scores_route(const __grid_constant__ C
         smax[e] = 0u;
         smin[e] = 0xffffffffu;
     }
-    if (ROUTE) hist[tid] = 0;
+    const bool seq = !ROUTE && route != nullptr;   // routes after the scores, same columns
+    for (int e = tid; e < kML; e += 128) hist[e] = 0;
     if (tid == 0) {
         mbar_init(bar_ld, 1);
         mbar_init(bar_mma, 1);
@@ -417,15 +418,41 @@ __global__ void __launch_bounds__(128) tc_scores_route(const __grid_constant__ C
                 if (ROUTE) mma_bf16(tR, desc_kmajor(sQ + oa), db, idesc, kk > 0);
             }
             mma_commit(bar_mma);
+            // the key tile's slot takes the query tile once the MMAs have read it
+            if (seq && mbar_wait_bounded(bar_mma, 0)) {
+                mbar_expect_tx(bar_ld, KC * kChunk);
+                for (int kc = 0; kc < KC; ++kc) tma_load_2d(sK + kc * kChunk, &mQ, kc * 64, bh * N + n0, bar_ld);
+            }
         }
     }
-    if (!mbar_wait_bounded(bar_mma, 0)) {
+    const int n = n0 + warp * 32 + lane;
+    const bool live = n < N;
+    const uint32_t lanes = (uint32_t)(warp * 32) << 16;
+    // first argmax over the landmarks of this thread's query logits at
+    // tensor-memory column tr (ascending landmarks, strict compare)
+    auto take_route = [&](uint32_t tr) {
+        float best = -INFINITY;
+        int arg = 0;
+        for (int c0 = 0; c0 < nb; c0 += 32) {
+            float v[32];
+            tmem_ld32(tr + lanes + c0, v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (c0 + j < m && v[j] > best) {
+                    best = v[j];
+                    arg = c0 + j;
+                }
+        }
+        if (live) {
+            route[(size_t)bh * N + n] = arg;
+            atomicAdd(&hist[arg], 1);
+        }
+    };
+    const bool ok = mbar_wait_bounded(bar_mma, 0);
+    if (!ok) {
         if (lane == 0) atomicExch(status, (int)MITA_ERR_TIMEOUT);
     } else {
         fence_after();
-        const int n = n0 + warp * 32 + lane;
-        const bool live = n < N;
-        const uint32_t lanes = (uint32_t)(warp * 32) << 16;
         float* sp = S + (size_t)bh * m * N + n;   // advances one row of S per landmark
         // one chunk of 32 landmarks; FULL: every token of the tile is in the
         // row (block-uniform), so no lane needs masking
@@ -457,32 +484,41 @@ __global__ void __launch_bounds__(128) tc_scores_route(const __grid_constant__ C
             for (int c0 = 0; c0 < m; c0 += 32) chunk(c0, std::true_type{});
         else
             for (int c0 = 0; c0 < m; c0 += 32) chunk(c0, std::false_type{});
-        if (ROUTE) {
-            float best = -INFINITY;
-            int arg = 0;
-            for (int c0 = 0; c0 < nb; c0 += 32) {
-                float v[32];
-                tmem_ld32(tR + lanes + c0, v);
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (c0 + j < m && v[j] > best) {   // ascending landmarks, strict: first argmax
-                        best = v[j];
-                        arg = c0 + j;
-                    }
-            }
-            if (live) {
-                route[(size_t)bh * N + n] = arg;
-                atomicAdd(&hist[arg], 1);
-            }
-        }
+        if (ROUTE) take_route(tR);
     }
     fence_before();
+    if (seq) {
+        // every score read from tensor memory: R = Q . Q_l^T into the same columns
+        const bool all_ok = __syncthreads_and(ok);
+        if (all_ok && tid == 0) {
+            fence_after();
+            if (mbar_wait_bounded(bar_ld, 1)) {
+                const uint32_t idesc = idesc_bf16(128, nb, 0, 0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t oa = (kk >> 2) * kChunk + (kk & 3) * 32;
+                    mma_bf16(tmem, desc_kmajor(sK + oa), desc_kmajor(sB + (kk >> 2) * bchunk + (kk & 3) * 32), idesc,
+                             kk > 0);
+                }
+                mma_commit(bar_mma);
+            }
+        }
+        if (all_ok) {
+            if (!mbar_wait_bounded(bar_mma, 1)) {
+                if (lane == 0) atomicExch(status, (int)MITA_ERR_TIMEOUT);
+            } else {
+                fence_after();
+                take_route(tmem);
+            }
+        }
+        fence_before();
+    }
     __syncthreads();
     for (int e = tid; e < m; e += 128) {
         const size_t r = (size_t)bh * m + e;
         if (smax[e] != 0u) atomicMax(&rowmax[r], smax[e]);
         if (smin[e] != 0xffffffffu) atomicMin(&rowmin[r], smin[e]);
-        if (ROUTE && hist[e]) atomicAdd(&counts[r], hist[e]);
+        if ((ROUTE || seq) && hist[e]) atomicAdd(&counts[r], hist[e]);
     }
     if (warp == 0) tmem_free(tmem, (uint32_t)tcols);
 }
@@ -569,8 +605,9 @@ static cudaError_t tc_route_t(const Shape& s, const void* Q, const void* Ql, int
     return cudaGetLastError();
 }
 
-// ROUTE: scores and routes (m <= 128); else the scores alone (m <= 256), Q
-// and the route arguments unused.
+// ROUTE: scores and routes side by side (m <= 128); else the scores (m <=
+// 256) and, when route is given, the routes after them in the same
+// tensor-memory columns.
 template <int D, bool ROUTE>
 static cudaError_t tc_scores_route_t(const Shape& s, const void* Ql, const void* K, const void* Q, float* S,
                                      uint32_t* rowmax, uint32_t* rowmin, int32_t* route, int32_t* counts,
@@ -581,8 +618,11 @@ static cudaError_t tc_scores_route_t(const Shape& s, const void* Ql, const void*
     CUtensorMap mk, mq, ml;
     if (!map_rows(&mk, K, D, (size_t)s.BH() * s.N, 128) || !map_rows(&ml, Ql, D, (size_t)s.BH() * s.m, nb))
         return cudaErrorInvalidValue;
-    if (ROUTE && !map_rows(&mq, Q, D, (size_t)s.BH() * s.N, 128)) return cudaErrorInvalidValue;
-    if (!ROUTE) mq = mk;   // not read
+    if (route != nullptr) {
+        if (!map_rows(&mq, Q, D, (size_t)s.BH() * s.N, 128)) return cudaErrorInvalidValue;
+    } else {
+        mq = mk;   // not read
+    }
     // scores alone: at most 512 / tcols blocks a SM (the 512 tensor-memory
     // columns); the shared-memory request keeps a further block, which would
     // only wait in its allocation, off the SM (228 KB of shared memory a SM).
@@ -598,11 +638,15 @@ static cudaError_t tc_scores_route_t(const Shape& s, const void* Ql, const void*
     return cudaGetLastError();
 }
 
-bool tc_scores_route_supported(const Shape& s) { return s.m <= 128; }
+bool tc_scores_route_supported(const Shape& s) { return s.m <= 256; }
 
 cudaError_t tc_scores_route(const Shape& s, const void* Ql, const void* K, const void* Q, float* S, uint32_t* rowmax,
                             uint32_t* rowmin, int32_t* route, int32_t* counts, int32_t* status, cudaStream_t st,
                             bool chain) {
+    if (s.m > 128)   // 256 tensor-memory columns for the scores, then the routes in the same ones
+        return s.d == 64 ? tc_scores_route_t<64, false>(s, Ql, K, Q, S, rowmax, rowmin, route, counts, status, st, chain)
+                         : tc_scores_route_t<128, false>(s, Ql, K, Q, S, rowmax, rowmin, route, counts, status, st,
+                                                         chain);
     return s.d == 64 ? tc_scores_route_t<64, true>(s, Ql, K, Q, S, rowmax, rowmin, route, counts, status, st, chain)
                      : tc_scores_route_t<128, true>(s, Ql, K, Q, S, rowmax, rowmin, route, counts, status, st, chain);
 }

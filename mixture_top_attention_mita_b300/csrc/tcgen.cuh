@@ -12,7 +12,7 @@ cudaError_t tc_scores(const Shape& s, const void* Ql, const void* K, float* S, u
 cudaError_t tc_values(const Shape& s, const float* S, const uint32_t* rowmax, const void* V, float* part,
                       float cs, int32_t* status, cudaStream_t st, bool chain);
 int tc_value_splits(const Shape& s);
-// Both of the above in one launch (m <= 128): raw scores with each row's max
+// Scores and routes in one launch (m <= 256): raw scores with each row's max
 // and min, and every query's route with the per-landmark counts (added).
 bool tc_scores_route_supported(const Shape& s);
 cudaError_t tc_scores_route(const Shape& s, const void* Ql, const void* K, const void* Q, float* S, uint32_t* rowmax,
