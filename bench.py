@@ -62,6 +62,9 @@ def parse():
     ap.add_argument("--no-soak", action="store_true", help="skip the untimed repeats that extend clock sampling")
     ap.add_argument("--no-others", action="store_true",
                     help="skip the graph-timed forwards of the other workloads reported beside the main line")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch B (smaller cases for profiler captures)")
+    ap.add_argument("--heads", type=int, default=None, help="override the workload's head count H")
     return ap.parse_args()
 
 
@@ -432,6 +435,9 @@ def main():
     args = parse()
     ws, rank, local = dist_setup()
     w = synth.WORKLOADS[args.workload]
+    if args.batch is not None or args.heads is not None:
+        B, H = args.batch or w.B, args.heads or w.H
+        w = w.scaled(name=f"{w.name}_B{B}_H{H}", B=B, H=H)
     if args.impl == "reference":
         return run_reference(args, w, ws, rank)
     if args.long_sweep:

@@ -9,7 +9,7 @@
 //                   partials per token lane combined error-free)
 //   tc_scores       S = Q_l . K^T (fp32, workspace) and each landmark's row
 //                   max and min (with the routes, tc_scores_route, when
-//                   m <= 128)
+//                   m <= 256)
 //   tl_topk_reg     per landmark the k best keys (ties to the lower index),
 //                   rows up to 4096 keys held in registers: a 256-bin
 //                   histogram over [min, max], an exact rank of the boundary
@@ -24,7 +24,7 @@
 //                   the row sums, per split of 1024-4096 keys
 //   tl_values_fin   V_l = sum of partials / sum of row sums, bf16
 //   tc_route        q . Q_l^T per query tile, first argmax (the route), and
-//                   per-landmark query counts
+//                   per-landmark query counts (m > 256 only)
 //   tl_bucket_off   per head: bucket offsets, cursors and the list of
 //                   attention tiles (expert, queries, first bucket position)
 //   tl_bucket_put   queries scattered to their bucket
