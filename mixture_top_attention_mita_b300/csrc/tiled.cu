@@ -547,13 +547,16 @@ __global__ void __launch_bounds__(kCT, 2) tl_topk_cb(Shape s, const float* __res
 size_t topk_cb_smem(int N) { return ((size_t)N + 15) / 16 * 16; }
 
 // Rows up to kRegRowN keys (the 56x56 layer's 3136): the expert of
-// tl_topk_bits<256>, with thread t holding keys t, t + kTB, ... of the row in
-// registers.  The row is read once; the second pass recomputes each key's bin
-// (one fused multiply-add) from its register, and warp w's lanes hold the 32
-// consecutive keys of bitmap word 8u + w in register u.
+// tl_topk_bits with 256 bins, with thread t holding keys t, t + kTB, ... of
+// the row in registers.  The row is read once; the second pass recomputes
+// each key's bin (one fused multiply-add) from its register, and warp w's
+// lanes hold the 32 consecutive keys of bitmap word 8u + w in register u.
+// VPT = ceil(N / kTB) keys a thread: every thread's first VPT - 1 keys are in
+// the row, so only the last one is checked.
 constexpr int kRegVPT = 16;
 constexpr int kRegRowN = kRegVPT * kTB;
 
+template <int VPT>
 __global__ void __launch_bounds__(kTB, 6) tl_topk_reg(Shape s, const float* __restrict__ S,
                                                    const uint32_t* __restrict__ rowmax,
                                                    const uint32_t* __restrict__ rowmin, int32_t* __restrict__ idx) {
@@ -575,19 +578,18 @@ __global__ void __launch_bounds__(kTB, 6) tl_topk_reg(Shape s, const float* __re
     if (!(fabsf(off) <= 3.0e38f)) sc = off = 0.0f;   // overflow: one bin, resolved by bisection
     // a monotone function of the score; the conversion takes negatives to 0
     auto bin_of = [&](float v) { return min(NB - 1, (int)fmaf(v, sc, off)); };
-    float v[kRegVPT];
+    // key u of this thread is in the row (only the last can fall past it)
+    auto in_row = [&](int u) { return u < VPT - 1 || tid + kTB * u < N; };
+    float v[VPT];
 #pragma unroll
-    for (int u = 0; u < kRegVPT; ++u) {
-        const int j = tid + kTB * u;
-        v[u] = j < N ? __ldg(row + j) : 0.0f;
-    }
+    for (int u = 0; u < VPT; ++u) v[u] = in_row(u) ? __ldg(row + tid + kTB * u) : 0.0f;
     hist[tid] = 0;
     for (int w = tid; w < nw; w += kTB) bits[w] = 0u;
     if (tid == 0) sh[3] = 0;
     __syncthreads();
 #pragma unroll
-    for (int u = 0; u < kRegVPT; ++u)
-        if (tid + kTB * u < N) atomicAdd(&hist[bin_of(v[u])], 1);
+    for (int u = 0; u < VPT; ++u)
+        if (in_row(u)) atomicAdd(&hist[bin_of(v[u])], 1);
     __syncthreads();
     {   // bin* holds the k-th best score: counts of the bins above, from the top down
         const int c = hist[tid];
@@ -604,13 +606,14 @@ __global__ void __launch_bounds__(kTB, 6) tl_topk_reg(Shape s, const float* __re
     const int bstar = sh[0], need = sh[1], cstar = sh[2];
     const bool take_all = need >= cstar;            // every member of bin* is in the expert
     const bool listed = !take_all && cstar <= kCandMax;
+    const int bsel = take_all ? bstar - 1 : bstar;   // keys of bins above bsel are in the expert
 #pragma unroll
-    for (int u = 0; u < kRegVPT; ++u) {
+    for (int u = 0; u < VPT; ++u) {
         const int j0 = kTB * u + 32 * warp;
-        if (j0 < N) {   // warp-uniform
+        if (u < VPT - 1 || j0 < N) {   // warp-uniform
             const int j = j0 + lane;
-            const int b = j < N ? bin_of(v[u]) : -1;
-            const uint32_t sel = __ballot_sync(0xffffffffu, b > bstar || (take_all && b == bstar));
+            const int b = in_row(u) ? bin_of(v[u]) : -1;
+            const uint32_t sel = __ballot_sync(0xffffffffu, b > bsel);
             if (lane == 0) bits[j0 >> 5] = sel;
             if (listed && b == bstar) {
                 const int p = atomicAdd(&sh[3], 1);
@@ -640,16 +643,16 @@ __global__ void __launch_bounds__(kTB, 6) tl_topk_reg(Shape s, const float* __re
             const uint32_t ct = T | (1u << bb);
             int cnt = 0;
 #pragma unroll
-            for (int u = 0; u < kRegVPT; ++u)
-                cnt += (tid + kTB * u < N && bin_of(v[u]) == bstar && order_key(v[u]) >= ct) ? 1 : 0;
+            for (int u = 0; u < VPT; ++u)
+                cnt += (in_row(u) && bin_of(v[u]) == bstar && order_key(v[u]) >= ct) ? 1 : 0;
             int total;
             block_excl_scan(cnt, wsum, &total);
             if (total >= need) T = ct;
         }
         int gt = 0;
 #pragma unroll
-        for (int u = 0; u < kRegVPT; ++u)
-            gt += (tid + kTB * u < N && bin_of(v[u]) == bstar && order_key(v[u]) > T) ? 1 : 0;
+        for (int u = 0; u < VPT; ++u)
+            gt += (in_row(u) && bin_of(v[u]) == bstar && order_key(v[u]) > T) ? 1 : 0;
         int gt_all;
         block_excl_scan(gt, wsum, &gt_all);
         if (warp == 0) {   // one warp, in key order: members above T, and the first ones equal to T
@@ -690,6 +693,16 @@ __global__ void __launch_bounds__(kTB, 6) tl_topk_reg(Shape s, const float* __re
             ++pos;
         }
     }
+}
+
+// tl_topk_reg for N <= kRegRowN keys with VPT = ceil(N / kTB).
+template <int VPT = kRegVPT>
+cudaError_t launch_topk_reg(bool chain, const Shape& s, dim3 grid, cudaStream_t st, const float* S,
+                            const uint32_t* rowmax, const uint32_t* rowmin, int32_t* idx) {
+    if constexpr (VPT > 1) {
+        if ((s.N + kTB - 1) / kTB < VPT) return launch_topk_reg<VPT - 1>(chain, s, grid, st, S, rowmax, rowmin, idx);
+    }
+    return launch_chained(chain, tl_topk_reg<VPT>, grid, dim3(kTB), 0, st, s, S, rowmax, rowmin, idx);
 }
 
 // V_l[i] = (sum over splits of the partial row) / (sum of the partial row sums).
@@ -1025,11 +1038,15 @@ cudaError_t run_t(mita_plan_s* p, const bf16* Q, const bf16* K, const bf16* V, b
                                       (const uint32_t*)(p->rowmax + mo), (const uint32_t*)(rowmin + mo),
                                       idx + mo * s.k)) != cudaSuccess)
                 return err;
+        } else if (s.N <= kRegRowN) {
+            if ((err = launch_topk_reg(chain, sg, dim3(s.m, sg.H), st, (const float*)p->S,
+                                       (const uint32_t*)(p->rowmax + mo), (const uint32_t*)(rowmin + mo),
+                                       idx + mo * s.k)) != cudaSuccess)
+                return err;
         } else if (s.N <= kBitsMaxN) {
-            auto kern = s.N <= kRegRowN ? tl_topk_reg : tl_topk_bits<kNB>;
-            if ((err = launch_chained(chain, kern, dim3(s.m, sg.H), dim3(kTB), 0, st, sg, (const float*)p->S,
-                                      (const uint32_t*)(p->rowmax + mo), (const uint32_t*)(rowmin + mo),
-                                      idx + mo * s.k)) != cudaSuccess)
+            if ((err = launch_chained(chain, tl_topk_bits<kNB>, dim3(s.m, sg.H), dim3(kTB), 0, st, sg,
+                                      (const float*)p->S, (const uint32_t*)(p->rowmax + mo),
+                                      (const uint32_t*)(rowmin + mo), idx + mo * s.k)) != cudaSuccess)
                 return err;
         } else {   // rows past the bitmap: the staged path's radix select
             if ((err = staged_topk(sg, p->S, idx + mo * s.k, st, chain)) != cudaSuccess) return err;
@@ -1097,7 +1114,7 @@ cudaError_t tiled_values_stats(const Shape& s, const float* S, const uint32_t* r
 
 cudaError_t tiled_topk(const Shape& s, const float* S, const uint32_t* rowmax, int32_t* idx, cudaStream_t st) {
     const uint32_t* rowmin = rowmax + (size_t)s.BH() * s.m;
-    return launch_chained(false, tl::tl_topk_reg, dim3(s.m, s.BH()), dim3(tl::kTB), 0, st, s, S, rowmax, rowmin, idx);
+    return tl::launch_topk_reg(false, s, dim3(s.m, s.BH()), st, S, rowmax, rowmin, idx);
 }
 
 cudaError_t tiled_pool(const Shape& s, const void* Q, void* Ql, uint32_t* rowmax, int32_t* counts, cudaStream_t st) {
