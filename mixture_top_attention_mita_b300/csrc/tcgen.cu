@@ -455,16 +455,17 @@ __global__ void __launch_bounds__(128) tc_scores_route(const __grid_constant__ C
         fence_after();
         float* sp = S + (size_t)bh * m * N + n;   // advances one row of S per landmark
         // one chunk of 32 landmarks; FULL: every token of the tile is in the
-        // row (block-uniform), so no lane needs masking
-        auto chunk = [&](int c0, auto full_t) {
-            constexpr bool FULL = decltype(full_t)::value;
+        // row (block-uniform), so no lane needs masking; ALL: all 32
+        // landmarks of the chunk exist, so no landmark is checked
+        auto chunk = [&](int c0, auto full_t, auto all_t) {
+            constexpr bool FULL = decltype(full_t)::value, ALL = decltype(all_t)::value;
             float v[32];
             tmem_ld32(tmem + lanes + c0, v);
-            const int cn = min(32, m - c0);
+            const int cn = ALL ? 32 : min(32, m - c0);
             float mine_hi = -INFINITY, mine_lo = INFINITY;   // lane j keeps landmark c0 + j's
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                if (j < cn) {   // block-uniform
+                if (ALL || j < cn) {   // block-uniform
                     if (FULL || live) *sp = v[j];
                     sp += N;
                     const float xh = FULL || live ? v[j] : -INFINITY, xl = FULL || live ? v[j] : INFINITY;
@@ -480,10 +481,14 @@ __global__ void __launch_bounds__(128) tc_scores_route(const __grid_constant__ C
                 atomicMin(&smin[c0 + lane], order_key(mine_lo));
             }
         };
-        if (n0 + 128 <= N)
-            for (int c0 = 0; c0 < m; c0 += 32) chunk(c0, std::true_type{});
-        else
-            for (int c0 = 0; c0 < m; c0 += 32) chunk(c0, std::false_type{});
+        const int mfull = m & ~31;   // landmarks in whole chunks of 32
+        if (n0 + 128 <= N) {
+            for (int c0 = 0; c0 < mfull; c0 += 32) chunk(c0, std::true_type{}, std::true_type{});
+            if (mfull < m) chunk(mfull, std::true_type{}, std::false_type{});
+        } else {
+            for (int c0 = 0; c0 < mfull; c0 += 32) chunk(c0, std::false_type{}, std::true_type{});
+            if (mfull < m) chunk(mfull, std::false_type{}, std::false_type{});
+        }
         if (ROUTE) take_route(tR);
     }
     fence_before();

@@ -83,6 +83,11 @@ __global__ void __launch_bounds__(128) tl_pool(Shape s, const bf16* __restrict__
     pool_bin(i / s.pw, s.gh, s.ph, r0, r1);
     pool_bin(i % s.pw, s.gw, s.pw, c0, c1);
     const int w = c1 - c0, cnt = (r1 - r0) * w;
+    // token e of the bin is at row e / w, column e % w: the quotient as
+    // floor((e + 1/2) / w) in fp32, exact while e < 2^21 (the fraction of
+    // (e + 1/2) / w stays 1 / (2 w) from an integer, above the product's
+    // relative error of 2^-22); bins hold at most 65536 tokens here
+    const float rw = 1.0f / (float)w;
     const bf16* q = Q + (size_t)bh * s.N * D + fg * 8;
     float hi[8], lo[8];
 #pragma unroll
@@ -94,7 +99,8 @@ __global__ void __launch_bounds__(128) tl_pool(Shape s, const bf16* __restrict__
             const int e = e0 + u * TL;
             v[u] = make_uint4(0u, 0u, 0u, 0u);
             if (e < cnt) {
-                const int y = r0 + e / w, x = c0 + e % w;
+                const int yq = __float2int_rz(((float)e + 0.5f) * rw);
+                const int y = r0 + yq, x = c0 + (e - yq * w);
                 v[u] = *(const uint4*)(q + (size_t)(y * s.gw + x) * D);
             }
         }
