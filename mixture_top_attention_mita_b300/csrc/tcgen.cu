@@ -124,11 +124,14 @@ __global__ void __launch_bounds__(128) tc_scores(const __grid_constant__ CUtenso
 }
 
 // ---------------------------------------------------------------- landmark values
-// 512 threads: thread t builds the numerators of landmark row t % 128 for
-// keys [32 (t / 128), + 32) of each 128-key tile, with the next tile's scores
-// already loaded into registers; warps w, w + 4 (w < 4) read the same
-// tensor-memory lanes and split the D output columns.
-template <int D, bool VEC>
+// 512 threads, TPR of them a landmark row: thread t builds the numerators of
+// row t % RPB (RPB = 512 / TPR rows) for keys [KPT (t / RPB), + KPT) of each
+// 128-key tile (KPT = 128 / TPR), with the next tile's scores already loaded
+// into registers.  TPR = 4 covers the 128 rows of the MMA tile; TPR = 8
+// (few landmarks) puts every thread on the first 64 rows.
+// Warps w, w + 4 (w < 4) read the same tensor-memory lanes and split the D
+// output columns.
+template <int D, bool VEC, int TPR>
 __global__ void __launch_bounds__(512) tc_values(const __grid_constant__ CUtensorMap mV, Shape s,
                                                  const float* __restrict__ S, const uint32_t* __restrict__ rowmax,
                                                  float* __restrict__ part, float cs, int kcv,
@@ -163,7 +166,8 @@ __global__ void __launch_bounds__(512) tc_values(const __grid_constant__ CUtenso
     __syncthreads();
     fence_after();
     const uint32_t tmem = tslot;
-    const int r = tid & 127, q = tid >> 7, i = i0 + r;
+    constexpr int RPB = 512 / TPR, KPT = 128 / TPR;   // rows a pass, keys a thread
+    const int r = tid % RPB, q = tid / RPB, i = i0 + r;
     const bool live = i < s.m;
     const float mb = live ? key_to_float(rowmax[(size_t)bh * s.m + i]) * cs : 0.0f;
     const float* srow = S + ((size_t)bh * s.m + (live ? i : 0)) * s.N;
@@ -175,32 +179,43 @@ __global__ void __launch_bounds__(512) tc_values(const __grid_constant__ CUtenso
         for (int kc = 0; kc < KC; ++kc)
             tma_load_2d(base + st * STAGE + PBYTES + kc * kChunk, &mV, kc * 64, bh * s.N + jb0 + 128 * t, v_full(st));
     };
-    // this thread's 32 scores of tile t
-    auto load_s = [&](int t, float (&x)[32]) {
-        const int j = jb0 + 128 * t + 32 * q;
-        if (VEC && live && j + 32 <= je) {
+    // this thread's KPT scores of tile t
+    auto load_s = [&](int t, float (&x)[KPT]) {
+        const int j = jb0 + 128 * t + KPT * q;
+        if (VEC && live && j + KPT <= je) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < KPT / 4; ++c) {
                 const float4 a = __ldg((const float4*)(srow + j + 4 * c));
                 x[4 * c] = a.x; x[4 * c + 1] = a.y; x[4 * c + 2] = a.z; x[4 * c + 3] = a.w;
             }
         } else {
 #pragma unroll
-            for (int u = 0; u < 32; ++u) x[u] = (live && j + u < je) ? __ldg(srow + j + u) : -INFINITY;
+            for (int u = 0; u < KPT; ++u) x[u] = (live && j + u < je) ? __ldg(srow + j + u) : -INFINITY;
         }
+    };
+    // 16-byte piece c of this thread's numerators: piece pc of row r in chunk ch of the A tile
+    auto piece_addr = [&](int st, int c) {
+        const int pg = q * (KPT / 8) + c, ch = pg >> 3, pc = pg & 7;
+        return smem + st * STAGE + ch * kChunk + r * 128 + ((pc ^ (r & 7)) << 4);
     };
     if (tid == 0) {
         issue_v(0);
         if (ntile > 1) issue_v(1);
     }
     if (!live) {   // padding rows: zero numerators in both stages, written once
-        for (int st = 0; st < 2; ++st) {
-            unsigned char* prow = smem + st * STAGE + (q >> 1) * kChunk + r * 128;
+        for (int st = 0; st < 2; ++st)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) *(uint4*)(prow + ((4 * (q & 1) + c) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+            for (int c = 0; c < KPT / 8; ++c) *(uint4*)piece_addr(st, c) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (RPB < 128) {   // rows RPB .. 127 of the A tile hold no landmark: zero in both stages
+        constexpr int kPieces = (128 - RPB) * 16;   // 16-byte pieces a stage
+        for (int x = tid; x < 2 * kPieces; x += 512) {
+            const int st = x / kPieces, y = x % kPieces, rr = RPB + y / 16, pg = y % 16;
+            *(uint4*)(smem + st * STAGE + (pg >> 3) * kChunk + rr * 128 + (((pg & 7) ^ (rr & 7)) << 4)) =
+                make_uint4(0u, 0u, 0u, 0u);
         }
     }
-    float x[32];
+    float x[KPT];
     if (live) load_s(0, x);
     for (int t = 0; t < ntile; ++t) {
         const int st = t & 1;
@@ -209,12 +224,11 @@ __global__ void __launch_bounds__(512) tc_values(const __grid_constant__ CUtenso
             if (!mbar_wait_bounded(mma_done(st), ((t - 2) >> 1) & 1)) ok = false;
             if (tid == 0 && ok) issue_v(t);
         }
-        // numerators of row r, keys 32 q .. 32 q + 31 of the tile: 16-byte pieces
-        // 4 (q & 1) .. + 3 of row r in chunk q / 2 of the A tile
+        // numerators of row r, keys KPT q .. KPT q + KPT - 1 of the tile
         if (live) {
-        uint32_t w[16];
+        uint32_t w[KPT / 2];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
+        for (int u = 0; u < KPT / 2; ++u) {
             float p0, p1;
             asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(p0) : "f"(fmaf(x[2 * u], cs, -mb)));
             asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(p1) : "f"(fmaf(x[2 * u + 1], cs, -mb)));
@@ -223,12 +237,9 @@ __global__ void __launch_bounds__(512) tc_values(const __grid_constant__ CUtenso
             w[u] = *reinterpret_cast<const uint32_t*>(&pp);
         }
         if (t + 1 < ntile) load_s(t + 1, x);   // in flight while the stores and the MMAs proceed
-        unsigned char* prow = smem + st * STAGE + (q >> 1) * kChunk + r * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int piece = 4 * (q & 1) + c;
-            *(uint4*)(prow + ((piece ^ (r & 7)) << 4)) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-        }
+        for (int c = 0; c < KPT / 8; ++c)
+            *(uint4*)piece_addr(st, c) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
         }
         fence_async_smem();   // the numerators are read next by the tensor core
         __syncthreads();
@@ -265,7 +276,12 @@ __global__ void __launch_bounds__(512) tc_values(const __grid_constant__ CUtenso
 #pragma unroll
                 for (int j = 0; j < 32; ++j) dst[cbase + c0 + j] = v[j];
         }
-        if (warp < 4 && li < s.m) dst[D] = rsum[lr] + rsum[lr + 128] + rsum[lr + 256] + rsum[lr + 384];
+        if (warp < 4 && li < s.m) {
+            float den = 0.0f;
+#pragma unroll
+            for (int u = 0; u < TPR; ++u) den += rsum[lr + RPB * u];
+            dst[D] = den;
+        }
     }
     fence_before();
     __syncthreads();
@@ -581,15 +597,14 @@ static cudaError_t tc_values_t(const Shape& s, const float* S, const uint32_t* r
     const int smem = 2 * (2 * (int)tcg::kChunk + (D / 64) * (int)tcg::kChunk) + 1024;
     const int kcv = tc_value_keys(s);
     const dim3 grid((s.N + kcv - 1) / kcv, (s.m + 127) / 128, s.BH());
-    if (s.N % 4 == 0) {
-        ensure_smem_attr((const void*)tcg::tc_values<D, true>, smem);
-        cudaError_t le = launch_chained(chain, tcg::tc_values<D, true>, grid, dim3(512), smem, st, mv, s, S, rowmax, part, cs, kcv, status);
-        if (le != cudaSuccess) return le;
-    } else {
-        ensure_smem_attr((const void*)tcg::tc_values<D, false>, smem);
-        cudaError_t le = launch_chained(chain, tcg::tc_values<D, false>, grid, dim3(512), smem, st, mv, s, S, rowmax, part, cs, kcv, status);
-        if (le != cudaSuccess) return le;
-    }
+    // eight threads a landmark row for at most 32 landmarks (DeiT-S backward
+    // recompute 963.6 -> 947.7 us); at 49 landmarks (56x56) four measure
+    // faster (177.9 against 179.3 us)
+    auto kern = s.N % 4 == 0 ? (s.m <= 32 ? tcg::tc_values<D, true, 8> : tcg::tc_values<D, true, 4>)
+                             : (s.m <= 32 ? tcg::tc_values<D, false, 8> : tcg::tc_values<D, false, 4>);
+    ensure_smem_attr((const void*)kern, smem);
+    cudaError_t le = launch_chained(chain, kern, grid, dim3(512), smem, st, mv, s, S, rowmax, part, cs, kcv, status);
+    if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
 
