@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(512) tc_values(const __grid_constant__ CUtenso
 #pragma unroll
             for (int c = 0; c < KPT / 8; ++c) *(uint4*)piece_addr(st, c) = make_uint4(0u, 0u, 0u, 0u);
     }
-    if (RPB < 128) {   // rows RPB .. 127 of the A tile hold no landmark: zero in both stages
+    if constexpr (RPB < 128) {   // rows RPB .. 127 of the A tile hold no landmark: zero in both stages
         constexpr int kPieces = (128 - RPB) * 16;   // 16-byte pieces a stage
         for (int x = tid; x < 2 * kPieces; x += 512) {
             const int st = x / kPieces, y = x % kPieces, rr = RPB + y / 16, pg = y % 16;
