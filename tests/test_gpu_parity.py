@@ -336,6 +336,9 @@ EDGE_MORE = [
     W["long1d"].scaled(B=1, H=2, N=4096, gw=4096, pw=256, m=256, k=100),
     # d = 64 on the tiled path with k at its limit
     W["hires56"].scaled(B=1, H=1, N=1024, gh=32, gw=32, ph=4, pw=4, m=16, k=512),
+    # rows past 4096 keys whose length is not a multiple of 4: the tiled
+    # path's two-read histogram select (the one-read select takes N % 4 == 0)
+    W["long1d"].scaled(B=1, H=2, N=5002, gw=5002, pw=24, m=24, k=77, gen="iid"),
 ]
 
 
