@@ -39,3 +39,19 @@ def test_reference_arm_prints_one_contract_line():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_rescaled_workload_is_named_for_its_sizes():
+    """--batch / --heads (smaller cases for profiler captures) give the
+    workload a name of its own, so a DRAM-traffic record taken on the full
+    workload is never reported for it."""
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "deit_t", "--batch", "1",
+                        "--heads", "2", "--steps", "1", "--warmup", "1", "--cpu-seconds", "1"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads([ln for ln in r.stdout.splitlines() if ln.startswith("{")][0])
+    wl = d["config"]["workload"]
+    assert wl.startswith("deit_t_B1_H2:") and "B=1 H=2" in wl
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.traffic_from_profiles("mita_fused", "deit_t_B1_H2") is None
