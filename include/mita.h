@@ -97,8 +97,9 @@ int mita_forward(mita_plan_t plan, const void* Q, const void* K, const void* V, 
  * point to host memory (page-locked -- cudaMallocHost or cudaHostRegister --
  * for the copies to overlap; pageable memory gives the same results with the
  * copies serialised).  No alignment is required; expert_idx and route may be
- * NULL.  The heads go through the device in 8 chunks, each a run of
- * consecutive heads: while chunk c is copied to the device, chunk c - 1's
+ * NULL.  The heads go through the device in at most 8 chunks (B*H / 8
+ * heads each, rounded up), each a run of consecutive heads: while chunk c is
+ * copied to the device, chunk c - 1's
  * forward runs on `stream` and chunk c - 2's results are copied back, on two
  * copy streams the plan owns, so a call takes about as long as its larger
  * copy direction.  The kernels, and so the results, are those of
@@ -108,9 +109,11 @@ int mita_forward(mita_plan_t plan, const void* Q, const void* K, const void* V, 
  * memory, so synchronising `stream` (or an event recorded on it after the
  * call) makes out, expert_idx and route readable; the host buffers must stay
  * valid and unwritten until then.  The first call on a plan allocates two
- * staging slots of device memory (about a quarter of Q, K, V and out
- * together; MITA_ERR_OOM if that fails) and creates the copy streams
- * (MITA_ERR_CUDA): make it before any stream capture.  Calls on one plan
+ * staging slots of device memory (each one chunk's Q, K, V, out, experts and
+ * routes, plus the tiled path's value partials for a chunk: about a quarter
+ * of Q, K, V and out together at 8 chunks; MITA_ERR_OOM if that fails) and
+ * creates the copy streams and their events (MITA_ERR_CUDA): make it before
+ * any stream capture.  Calls on one plan
  * share the slots: order them on one stream.  Returns MITA_ERR_INVALID_ARG
  * for a null Q, K, V or out, MITA_ERR_UNSUPPORTED where mita_forward()
  * would, MITA_ERR_CUDA if a copy or launch fails to enqueue; data errors are
